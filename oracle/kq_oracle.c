@@ -1,0 +1,346 @@
+/*
+ * KroQuant MXFP4 activation quantizer -- CPU reference ("oracle").
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file; only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark use it.  It shares no code, header, table or constant
+ * generator with the CUDA library.
+ *
+ * Source of every step: "KroQuant: Kronecker-Structured Block Transforms for
+ * Efficient Post-Training Quantization of Diffusion Transformers"
+ * (arXiv 2607.21446v1), cited below as [KQ] with the section / equation.
+ *
+ * Arithmetic is IEEE fp64 throughout.  bf16 activations and fp32 factor
+ * entries convert to fp64 exactly.  Nothing here is blocked, fused or
+ * reordered beyond what the definitions state: the Kronecker block is
+ * expanded entry by entry (eq. 12), applied as a dense 32x32 row-vector
+ * product (eq. 4, K1's A_tile @ K), and each 32-element block is then
+ * quantized on its own (Sec. 3.1, MXFP4 per the OCP MX format named in
+ * Sec. 4.1 "Data format").
+ *
+ * Readings taken where the pages are silent (each also listed in the design doc):
+ *   - shared exponent e = floor(log2 amax) - 2 (2 = emax of E2M1), clamped to
+ *     the E8M0 range [-127, 127]; amax == 0 gives e = -127;
+ *   - e2m1 rounding is round-to-nearest, ties to the even code, with
+ *     saturation to +-6; the sign of y is kept, also for a zero magnitude;
+ *   - packing: byte k of a row holds code 2k in bits 0-3 and code 2k+1 in
+ *     bits 4-7.
+ *
+ * Parity: every function here is pinned by tests that do not use it as
+ * their own reference (closed forms, a brute-force twin, library routines).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define KQO_EXPORT __attribute__((visibility("default")))
+
+/* --- input conversion ---------------------------------------------------- */
+
+static double bf16_bits_to_f64(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;     /* bf16 is the top half of an fp32 */
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+KQO_EXPORT double kqo_bf16_to_f64(uint16_t h) { return bf16_bits_to_f64(h); }
+
+/* --- [KQ] Sec. 3.2, eq. (6): unit-|det| LU factor ----------------------------
+ * lu = {a, b, c}; G = [[1,0],[c,1]] . [[a,b],[0,u22]] with
+ *   u22 = -1/a  (det_sign = -1, the paper's form, eq. 6)
+ *   u22 = +1/a  (det_sign = +1, the unit-determinant form of the workloads).
+ * G is written row-major: G[0]=G00, G[1]=G01, G[2]=G10, G[3]=G11.
+ */
+KQO_EXPORT void kqo_lu_to_factor(const double lu[3], int det_sign, double G[4])
+{
+    double a = lu[0], b = lu[1], c = lu[2];
+    double u22 = (det_sign < 0 ? -1.0 : 1.0) / a;
+    /* L . U, entry by entry (the zero products of the triangular factors
+     * are left out) */
+    G[0] = a;              /* 1*a + 0*0   */
+    G[1] = b;              /* 1*b + 0*u22 */
+    G[2] = c * a;          /* c*a + 1*0   */
+    G[3] = c * b + u22;    /* c*b + 1*u22 */
+}
+
+/* --- [KQ] Sec. 3.5.1, eq. (12): entry-wise Kronecker expansion ---------------
+ * K[r][c] = prod_{k=1..5} G_k[ bit_{5-k}(r), bit_{5-k}(c) ]
+ * G holds the five factors G_1..G_5 as [5][2][2] row-major; G_1 pairs with
+ * bit 4 (the most significant bit) of the row and column index.
+ */
+KQO_EXPORT void kqo_expand_block(const double *G, double *K)
+{
+    for (int r = 0; r < 32; ++r)
+        for (int c = 0; c < 32; ++c) {
+            double p = 1.0;
+            for (int k = 1; k <= 5; ++k) {
+                int bit = 5 - k;
+                int rb = (r >> bit) & 1, cb = (c >> bit) & 1;
+                p *= G[(k - 1) * 4 + rb * 2 + cb];
+            }
+            K[r * 32 + c] = p;
+        }
+}
+
+/* Closed-form normalised Walsh-Hadamard block ([KQ] Sec. 3.2, "Hadamard
+ * initialization"): H32[r][c] = (-1)^popcount(r & c) / sqrt(32). */
+KQO_EXPORT void kqo_hadamard_block(double *K)
+{
+    double s = 1.0 / sqrt(32.0);
+    for (int r = 0; r < 32; ++r)
+        for (int c = 0; c < 32; ++c)
+            K[r * 32 + c] = (__builtin_popcount((unsigned)(r & c)) & 1) ? -s : s;
+}
+
+/* --- [KQ] eq. (4) with K1's orientation A_tile @ K (Sec. 3.5.1) --------------
+ * y[i][32j + c] = sum_r a[i][32j + r] * K_j[r][c]
+ * bound[i][32j + c] = sum_r |a[i][32j + r] * K_j[r][c]|   (error scale)
+ * Kall holds nb dense blocks [nb][32][32].
+ */
+static void apply_dense_blocks(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                               const double *Kall, double *y, double *bound)
+{
+    int64_t nb = d / 32;
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < m; ++i) {
+        double a[32];
+        for (int64_t j = 0; j < nb; ++j) {
+            const double *K = Kall + j * 1024;
+            for (int r = 0; r < 32; ++r)
+                a[r] = bf16_bits_to_f64(A[i * lda + j * 32 + r]);
+            for (int c = 0; c < 32; ++c) {
+                double acc = 0.0, mag = 0.0;
+                for (int r = 0; r < 32; ++r) {
+                    double t = a[r] * K[r * 32 + c];
+                    acc += t;
+                    mag += fabs(t);
+                }
+                y[i * d + j * 32 + c] = acc;
+                if (bound) bound[i * d + j * 32 + c] = mag;
+            }
+        }
+    }
+}
+
+/* Any dense per-block matrices Kall [nb][32][32] (used for the weight side
+ * W T^{-T} of eq. 1, whose blocks are K_j^{-T}). */
+KQO_EXPORT void kqo_transform_dense(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                    const double *Kall, double *y, double *bound)
+{
+    apply_dense_blocks(A, m, d, lda, Kall, y, bound);
+}
+
+/* KroQuant transform: factors [nb][5][2][2] (fp64), one set per 32-block
+ * (eq. 4: T = diag(K^(1), ..., K^(nb)), eq. 5: K = G1 (x) ... (x) G5).
+ * Kscratch must hold nb*1024 doubles. */
+KQO_EXPORT void kqo_transform_kron(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                   const double *factors, double *Kscratch,
+                                   double *y, double *bound)
+{
+    int64_t nb = d / 32;
+    for (int64_t j = 0; j < nb; ++j)
+        kqo_expand_block(factors + j * 20, Kscratch + j * 1024);
+    apply_dense_blocks(A, m, d, lda, Kscratch, y, bound);
+}
+
+/* Fixed block-Hadamard baseline ([KQ] Sec. 4.3, Table 2 "Hadamard (32x32)"). */
+KQO_EXPORT void kqo_transform_hadamard(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                       double *Kscratch, double *y, double *bound)
+{
+    int64_t nb = d / 32;
+    kqo_hadamard_block(Kscratch);
+    for (int64_t j = 1; j < nb; ++j)
+        memcpy(Kscratch + j * 1024, Kscratch, 1024 * sizeof(double));
+    apply_dense_blocks(A, m, d, lda, Kscratch, y, bound);
+}
+
+/* Diagonal (per-channel scaling, SmoothQuant-style) baseline:
+ * T = diag(s), y = a * s[c]  ([KQ] Sec. 4.4, the "Scale" kernel). */
+KQO_EXPORT void kqo_transform_diag(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                   const double *s, double *y, double *bound)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t c = 0; c < d; ++c) {
+            double t = bf16_bits_to_f64(A[i * lda + c]) * s[c];
+            y[i * d + c] = t;
+            if (bound) bound[i * d + c] = fabs(t);
+        }
+}
+
+/* Identity transform: the bare quantizer ("Q4", [KQ] Tables 3 and 4). */
+KQO_EXPORT void kqo_transform_identity(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                       double *y, double *bound)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t c = 0; c < d; ++c) {
+            double t = bf16_bits_to_f64(A[i * lda + c]);
+            y[i * d + c] = t;
+            if (bound) bound[i * d + c] = fabs(t);
+        }
+}
+
+/* --- MXFP4 block quantizer ([KQ] Sec. 3.1; OCP MX, Sec. 4.1) --------------- */
+
+/* E8M0 shared exponent: e = floor(log2 amax) - 2, clamped to [-127, 127]. */
+KQO_EXPORT int kqo_e8m0_exponent(double amax)
+{
+    if (!(amax > 0.0)) return -127;
+    int ex;
+    frexp(amax, &ex);               /* amax = f * 2^ex, f in [0.5, 1) */
+    int e = (ex - 1) - 2;           /* floor(log2 amax) = ex - 1 */
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+/* e2m1 magnitude grid, code order: {0, .5, 1, 1.5, 2, 3, 4, 6}. */
+KQO_EXPORT double kqo_e2m1_value(uint8_t code)
+{
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    double v = mag[code & 7];
+    return (code & 8) ? -v : v;
+}
+
+/* e2m1 encode: round to nearest on the e2m1 grid, ties to the even code
+ * (even mantissa bit), saturate at 6, keep the sign bit of v.
+ * Between binades the grid spacing is 0.5 on [0,2), 1 on [2,4), 2 on [4,6];
+ * rint() (round half to even) on the spacing gives the nearest grid point,
+ * and an even multiple there is an even code. */
+KQO_EXPORT uint8_t kqo_encode_e2m1(double v)
+{
+    uint8_t sign = signbit(v) ? 8 : 0;
+    double a = fabs(v);
+    double q;
+    if (a > 6.0) {
+        q = 6.0;
+    } else {
+        double step = (a < 2.0) ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+        q = rint(a / step) * step;
+    }
+    uint8_t mag;
+    int twice = (int)(q * 2.0);
+    switch (twice) {
+    case 0: mag = 0; break;    /* 0   */
+    case 1: mag = 1; break;    /* 0.5 */
+    case 2: mag = 2; break;    /* 1   */
+    case 3: mag = 3; break;    /* 1.5 */
+    case 4: mag = 4; break;    /* 2   */
+    case 6: mag = 5; break;    /* 3   */
+    case 8: mag = 6; break;    /* 4   */
+    default: mag = 7; break;   /* 6   */
+    }
+    return (uint8_t)(sign | mag);
+}
+
+/* Scale-factor byte position.
+ * layout 0: row-major [m][nb].
+ * layout 1: the 128x4 tiled layout of block-scaled MMA operands -- tiles of
+ *   128 rows x 4 block-columns, 512 bytes each, tiles ordered row-tile major;
+ *   inside a tile, row i and block-column kb sit at
+ *   (i % 32) * 16 + ((i % 128) / 32) * 4 + (kb % 4). */
+KQO_EXPORT int64_t kqo_sf_offset(int64_t i, int64_t kb, int64_t nb, int layout)
+{
+    if (layout == 0) return i * nb + kb;
+    int64_t ncb = (nb + 3) / 4;
+    int64_t tile = (i / 128) * ncb + kb / 4;
+    return tile * 512 + (i % 32) * 16 + ((i % 128) / 32) * 4 + (kb % 4);
+}
+
+KQO_EXPORT int64_t kqo_sf_bytes(int64_t m, int64_t nb, int layout)
+{
+    if (layout == 0) return m * nb;
+    return ((m + 127) / 128) * ((nb + 3) / 4) * 512;
+}
+
+/* Flags for the comparison rules (bit mask per element):
+ *   1: |v| within 1e-3 relative of a rounding midpoint
+ *   2: the block's amax within 1e-3 relative of a power of two
+ *   4: sign of a zero code not decided: |y| <= 2^-16 * bound and the
+ *      magnitude rounds to 0. */
+static const double kMidpoints[7] = {0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0};
+
+/* Quantize y [m][d] (fp64) into packed codes q [m][ldq] and scales sf. */
+KQO_EXPORT void kqo_quantize(const double *y, const double *bound, int64_t m, int64_t d,
+                             uint8_t *q, int64_t ldq, uint8_t *sf, int layout,
+                             uint8_t *flags)
+{
+    int64_t nb = d / 32;
+    if (layout == 1) memset(sf, 0, (size_t)kqo_sf_bytes(m, nb, layout));
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < m; ++i) {
+        for (int64_t j = 0; j < nb; ++j) {
+            const double *yb = y + i * d + j * 32;
+            double amax = 0.0;
+            for (int c = 0; c < 32; ++c)
+                if (fabs(yb[c]) > amax) amax = fabs(yb[c]);
+            int e = kqo_e8m0_exponent(amax);
+            sf[kqo_sf_offset(i, j, nb, layout)] = (uint8_t)(e + 127);
+            int edge = 0;
+            if (amax > 0.0) {
+                int ex;
+                double f = frexp(amax, &ex);      /* f in [0.5, 1) */
+                edge = (f - 0.5 <= 1e-3 * 0.5) || (1.0 - f <= 1e-3 * 1.0);
+            }
+            uint8_t codes[32];
+            for (int c = 0; c < 32; ++c) {
+                double v = ldexp(yb[c], -e);      /* y / 2^e, exact */
+                codes[c] = kqo_encode_e2m1(v);
+                if (flags) {
+                    uint8_t fl = edge ? 2 : 0;
+                    double av = fabs(v);
+                    for (int k = 0; k < 7; ++k)
+                        if (fabs(av - kMidpoints[k]) <= 1e-3 * kMidpoints[k]) fl |= 1;
+                    if (bound && (codes[c] & 7) == 0 &&
+                        fabs(yb[c]) <= ldexp(bound[i * d + j * 32 + c], -16))
+                        fl |= 4;
+                    flags[i * d + j * 32 + c] = fl;
+                }
+            }
+            for (int k = 0; k < 16; ++k)
+                q[i * ldq + j * 16 + k] = (uint8_t)(codes[2 * k] | (codes[2 * k + 1] << 4));
+        }
+    }
+}
+
+/* Dequantize: value(code) * 2^(sf - 127). */
+KQO_EXPORT void kqo_dequantize(const uint8_t *q, int64_t ldq, const uint8_t *sf, int layout,
+                               int64_t m, int64_t d, double *out)
+{
+    int64_t nb = d / 32;
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t c = 0; c < d; ++c) {
+            uint8_t byte = q[i * ldq + c / 2];
+            uint8_t code = (c & 1) ? (byte >> 4) : (byte & 15);
+            int e = (int)sf[kqo_sf_offset(i, c / 32, nb, layout)] - 127;
+            out[i * d + c] = ldexp(kqo_e2m1_value(code), e);
+        }
+}
+
+/* Packed codes of the fp32 bit patterns first, first+1, ..., first+count-1
+ * taken as values v with scale 2^0 (count even): the expected output of the
+ * device encoder under an exhaustive sweep. */
+KQO_EXPORT void kqo_encode_f32_range(uint32_t first, int64_t count, uint8_t *packed)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t k = 0; k < count / 2; ++k) {
+        uint8_t c[2];
+        for (int t = 0; t < 2; ++t) {
+            uint32_t u = first + (uint32_t)(2 * k + t);
+            float f;
+            memcpy(&f, &u, sizeof f);
+            c[t] = kqo_encode_e2m1((double)f);
+        }
+        packed[k] = (uint8_t)(c[0] | (c[1] << 4));
+    }
+}
+
+KQO_EXPORT void kqo_encode_e2m1_array(const double *v, int64_t n, uint8_t *codes)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t k = 0; k < n; ++k) codes[k] = kqo_encode_e2m1(v[k]);
+}

@@ -1,0 +1,47 @@
+"""Planted mistakes: each test compiles a copy of the C oracle with one
+plausible mistake and checks that the pins reject it.  This shows the pins
+are strong enough to catch that class of error in the oracle itself.
+The mistakes are planted only in temporary copies of the oracle, on the CPU.
+"""
+import pytest
+
+import test_oracle_pins as pins
+from oracle import kq_oracle
+
+# (name, original text, mutated text, pins that must fail)
+MUTANTS = [
+    ("ties_away_from_zero", "q = rint(a / step) * step;", "q = round(a / step) * step;",
+     [pins.test_e2m1_rounding_golden, pins.test_worked_block]),
+    ("reversed_bit_order", "int bit = 5 - k;", "int bit = k - 1;",
+     [pins.test_orientation_and_bit_order, pins.test_expand_matches_nested_kron]),
+    ("transposed_factor", "p *= G[(k - 1) * 4 + rb * 2 + cb];",
+     "p *= G[(k - 1) * 4 + cb * 2 + rb];",
+     [pins.test_orientation_and_bit_order, pins.test_expand_matches_nested_kron]),
+    ("scale_offset_by_one", "int e = (ex - 1) - 2;", "int e = (ex - 1) - 1;",
+     [pins.test_e8m0_edges, pins.test_worked_block]),
+    ("sf_tile_rows_swapped", "return tile * 512 + (i % 32) * 16 + ((i % 128) / 32) * 4 + (kb % 4);",
+     "return tile * 512 + (i % 32) * 4 + ((i % 128) / 32) * 16 + (kb % 4);",
+     [pins.test_sf_blocked_offsets_golden]),
+    ("nibbles_swapped", "(uint8_t)(codes[2 * k] | (codes[2 * k + 1] << 4))",
+     "(uint8_t)(codes[2 * k + 1] | (codes[2 * k] << 4))",
+     [pins.test_worked_block]),
+    ("zero_sign_dropped", "uint8_t sign = signbit(v) ? 8 : 0;", "uint8_t sign = (v < 0) ? 8 : 0;",
+     [pins.test_e2m1_rounding_golden, pins.test_worked_block]),
+    ("dropped_last_term", "for (int r = 0; r < 32; ++r) {\n                    double t",
+     "for (int r = 0; r < 31; ++r) {\n                    double t",
+     [pins.test_orientation_and_bit_order, pins.bruteforce_small_case]),
+    ("hadamard_sign", "? -s : s;", "? s : -s;", [pins.test_hadamard_closed_form]),
+    ("lu_wrong_entry", "G[3] = c * b + u22;", "G[3] = c * a + u22;",
+     [pins.test_lu_factor_determinants]),
+]
+
+
+@pytest.mark.parametrize("name,orig,mut,must_fail", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, oracle_lib, name, orig, mut, must_fail):
+    src = kq_oracle.source_text()
+    assert src.count(orig) == 1, f"mutation anchor for {name} not found exactly once"
+    path = kq_oracle.build_variant(src.replace(orig, mut), str(tmp_path / f"lib_{name}.so"))
+    with kq_oracle.swapped_library(path):
+        for pin in must_fail:
+            with pytest.raises(AssertionError):
+                pin(kq_oracle)
