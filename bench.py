@@ -1,0 +1,473 @@
+#!/usr/bin/env python3
+"""Throughput of the KroQuant MXFP4 activation quantizer on one GB300 (or N,
+one process per GPU, weak scaling).
+
+A step quantizes the FLUX.1-schnell-shaped layer pair of "KroQuant:
+Kronecker-Structured Block Transforms for Efficient Post-Training
+Quantization of Diffusion Transformers" (Sec. 4.1 models, Table 4 widths):
+m = 4608 tokens (4096 image + 512 text) at d = 3072 and at d = 12288 (the
+FFN-down input), bf16 activations with outlier channels (synthetic: per-token
+lognormal(0, 0.7) x N(0, 1), 1 % of channels x U[30, 300]) and random
+unit-determinant LU Kronecker factors per layer, quantized to MXFP4 with the
+scale factors in the 128x4 tiled layout of block-scaled MMA.
+
+Metric: GB/s moved = m * d * (2 + 1/2 + 1/32) bytes / time (bf16 read, packed
+FP4 and E8M0 written), and the fraction of the measured HBM copy bandwidth.
+Four input/output sets rotate so that no step reads data a recent step left
+in L2 (~710 MB footprint against a 126 MB L2).
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded
+row sample of the same workload and prints the same line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KroQuant MXFP4 quantizer GB/s and % HBM peak; speedup vs diag-scale quantizer"
+LAYERS = (("flux_3072", 4608, 3072), ("flux_ffn_down", 4608, 12288))
+DOMINANT = 1                        # the d = 12288 launch dominates the step
+SETS = 4
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algo_bytes(m: int, d: int) -> float:
+    """bf16 read + packed E2M1 written + one E8M0 byte per 32 elements."""
+    return m * d * 2 + m * d / 2 + m * d / 32
+
+
+STEP_BYTES = sum(algo_bytes(m, d) for _, m, d in LAYERS)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--variant", choices=("butterfly", "mma"), default="butterfly")
+    ap.add_argument("--no-baselines", action="store_true",
+                    help="skip the diagonal / Hadamard / bare-quantizer side measurements")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU time budget of the oracle baseline sample")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------- distributed --
+
+class Dist:
+    def __init__(self, use_cuda: bool):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if use_cuda else "gloo"
+            if use_cuda:
+                import torch
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            if self.pg.get_backend() == "nccl":
+                import torch
+                self.pg.barrier(device_ids=[torch.cuda.current_device()])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        return self._reduce(x, "max")
+
+    def sum(self, x: float) -> float:
+        return self._reduce(x, "sum")
+
+    def _reduce(self, x: float, op: str) -> float:
+        if self.pg is None:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX if op == "max" else self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ helpers --
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("w4a4_mxfp4_activation_gb300/csrc/kq_quant.cu",
+                "w4a4_mxfp4_activation_gb300/csrc/kq_device.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 4 and parts[0] == workload and parts[1] == kernel_source_hash():
+                    return float(parts[3])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of the benchmarked GPU while alive."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        mhz, mx, reasons = [], [], set()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            if self.uuid and self.uuid not in f[0] and f[0] not in self.uuid:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def device_uuid(dev) -> str | None:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def cpu_oracle_rate(rows_per_layer: int, seed: int = 0):
+    """Times the oracle (transform + quantize, fp64, OpenMP over host cores)
+    on the first rows of both layers; returns (GB/s, seconds, bytes)."""
+    import numpy as np
+    from oracle import kq_oracle as O
+    from w4a4_mxfp4_activation_gb300 import synth
+    inputs = []
+    for i, (_, m, d) in enumerate(LAYERS):
+        r = min(rows_per_layer, m)
+        A = synth.activations(r, d, synth.SEED_A + 3 + seed, "flux")
+        lu = synth.lu_params(d // 32, synth.SEED_FACTORS + 3 + i)
+        F = O.lu_to_factors(lu.astype(np.float64), +1).astype(np.float32).astype(np.float64)
+        inputs.append((A, d, F, r))
+    t0 = time.perf_counter()
+    nbytes = 0.0
+    for A, d, F, r in inputs:
+        y, bound = O.transform(A, d, "kron", F)
+        O.quantize(y, bound, O.SF_BLOCKED_128x4)
+        nbytes += algo_bytes(r, d)
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, dt, nbytes
+
+
+def cpu_cores() -> int:
+    n = os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n and n.isdigit() else (os.cpu_count() or 1)
+
+
+def cpu_baseline(budget_s: float):
+    _, t16, _ = cpu_oracle_rate(16)
+    rows = max(16, min(LAYERS[0][1], int(16 * budget_s / max(t16, 1e-3))))
+    rate, dt, _ = cpu_oracle_rate(rows)
+    return {"value": round(rate, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"first {rows} rows of each FLUX layer (m=4608, d=3072 and 12288), "
+                      f"{dt:.1f} s of CPU work"}
+
+
+def run_reference(args, dist: Dist):
+    if dist.rank != 0:
+        return
+    W, K = args.warmup, args.steps
+    _, t16, _ = cpu_oracle_rate(16)
+    per_step = 90.0 / max(K + W, 1)
+    rows = max(1, min(LAYERS[0][1], int(16 * per_step / max(t16, 1e-6))))
+    for w in range(W):
+        cpu_oracle_rate(rows, seed=w)
+    total_t, total_b = 0.0, 0.0
+    for k in range(K):
+        _, dt, nb = cpu_oracle_rate(rows, seed=k)
+        total_t += dt
+        total_b += nb
+    value = total_b / total_t / 1e9
+    line = {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": K, "warmup": W, "ms_per_step": round(1e3 * total_t / K, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": "flux_layer_pair_row_sample", "m": 4608, "d": [3072, 12288],
+                       "rows_per_layer_per_step": rows, "transform": "kroquant",
+                       "sf_layout": "blocked_128x4"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_cores(),
+                             "kind": "oracle",
+                             "sample": f"first {rows} rows of each FLUX layer per step"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU --
+
+def run_ours(args, dist: Dist):
+    import numpy as np
+    import torch
+    from w4a4_mxfp4_activation_gb300 import kq, synth
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.Stream(device=dev)
+    layout = kq.KQ_SF_BLOCKED_128x4
+    variant = kq.VARIANT_BUTTERFLY if args.variant == "butterfly" else kq.VARIANT_MMA
+
+    # ---- inputs resident in HBM: SETS rotating sets per layer
+    A, Q, SF, F, KX = [], [], [], [], []
+    host_A = []
+    for li, (_, m, d) in enumerate(LAYERS):
+        bits = synth.activations(m, d, synth.SEED_A + 3 + 100 * dist.rank + li, "flux")
+        host = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        host_A.append(host)
+        base = host.to(dev)
+        A.append([torch.roll(base, shifts=137 * s, dims=0).contiguous() for s in range(SETS)])
+        Q.append([torch.empty((m, d // 2), dtype=torch.uint8, device=dev) for _ in range(SETS)])
+        SF.append([torch.empty(kq.kq_sf_bytes(m, d, layout), dtype=torch.uint8, device=dev)
+                   for _ in range(SETS)])
+        fac = kq.kq_lu_to_factors(synth.lu_params(d // 32, synth.SEED_FACTORS + 3 + li), +1)
+        F.append(torch.from_numpy(fac).to(dev))
+        KX.append(kq.kq_expand_blocks(F[-1], kq.KQ_K_BF16X3) if variant == kq.VARIANT_MMA else None)
+    torch.cuda.synchronize()
+
+    def launch(kind, li, s):
+        _, m, d = LAYERS[li]
+        if kind == "kroquant":
+            kq.kq_quantize_mxfp4(A[li][s], d, factors=F[li] if variant == 0 else None,
+                                 K_expanded=KX[li], layout=layout, q=Q[li][s], sf=SF[li][s],
+                                 variant=variant, stream=stream)
+        elif kind == "diag":
+            kq.kq_smooth_quantize_mxfp4(A[li][s], DIAG[li], d, layout=layout, q=Q[li][s],
+                                        sf=SF[li][s], stream=stream)
+        elif kind == "hadamard":
+            kq.kq_hadamard_quantize_mxfp4(A[li][s], d, layout=layout, q=Q[li][s], sf=SF[li][s],
+                                          stream=stream)
+        else:
+            kq.kq_quantize_mxfp4(A[li][s], d, layout=layout, q=Q[li][s], sf=SF[li][s],
+                                 stream=stream)
+
+    DIAG = [torch.from_numpy(synth.smooth_scales(d)).to(dev) for _, _, d in LAYERS]
+
+    def graphs_for(kind):
+        """One CUDA graph per (set, layer): a single kernel launch each."""
+        g = [[None] * len(LAYERS) for _ in range(SETS)]
+        with torch.cuda.stream(stream):
+            for s in range(SETS):
+                for li in range(len(LAYERS)):
+                    launch(kind, li, s)              # warm the launch path before capture
+            stream.synchronize()
+            for s in range(SETS):
+                for li in range(len(LAYERS)):
+                    gr = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gr, stream=stream):
+                        launch(kind, li, s)
+                    g[s][li] = gr
+        stream.synchronize()
+        return g
+
+    def timed(kind, steps, warmup, per_launch=False, sampler=False):
+        g = graphs_for(kind)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(steps)] if per_launch else []
+        clock = ClockSampler(device_uuid(dev)) if sampler else None
+        with torch.cuda.stream(stream):
+            for w in range(warmup):
+                for li in range(len(LAYERS)):
+                    g[w % SETS][li].replay()
+            stream.synchronize()
+            dist.barrier()
+            torch.cuda.synchronize()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for k in range(steps):
+                s = k % SETS
+                for li in range(len(LAYERS)):
+                    if per_launch and li == DOMINANT:
+                        pairs[k][0].record(stream)
+                        g[s][li].replay()
+                        pairs[k][1].record(stream)
+                    else:
+                        g[s][li].replay()
+            t1.record(stream)
+            stream.synchronize()
+            clocks = clock.stop() if clock is not None else None
+            dist.barrier()
+            torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1)
+        launch_ms = [a.elapsed_time(b) for a, b in pairs]
+        return ms, launch_ms, clocks
+
+    W, K = args.warmup, args.steps
+    ms, launch_ms, clocks = timed("kroquant", K, W, per_launch=True, sampler=True)
+    ms_max = dist.max(ms)
+    total_bytes = dist.sum(STEP_BYTES * K)
+    value = total_bytes / (ms_max * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+
+    dom_m, dom_d = LAYERS[DOMINANT][1], LAYERS[DOMINANT][2]
+    dom_ms = statistics.mean(launch_ms) if launch_ms else float("nan")
+    achieved = algo_bytes(dom_m, dom_d) / (dom_ms * 1e-3) / 1e9
+    workload = f"kq_quantize_mxfp4 {args.variant} m={dom_m} d={dom_d}"
+    traffic = recorded_traffic(f"flux_ffn_down_{args.variant}")
+
+    # ---- side measurements: the baselines built alongside
+    baselines = {}
+    if not args.no_baselines:
+        nb_steps = max(3, min(K, 4000))
+        for kind in ("diag", "hadamard", "identity"):
+            bms, _, _ = timed(kind, nb_steps, 3)
+            baselines[kind] = round(STEP_BYTES * nb_steps / (dist.max(bms) * 1e-3) / 1e9, 2)
+
+    # ---- end to end through the public call with host buffers
+    e2e_steps = max(3, min(K, 100))
+    host_q = [torch.empty(Q[li][0].shape, dtype=torch.uint8).pin_memory() for li in range(2)]
+    host_sf = [torch.empty(SF[li][0].shape, dtype=torch.uint8).pin_memory() for li in range(2)]
+    h2d = sum(h.numel() * 2 for h in host_A)
+    d2h = sum(t.numel() for t in host_q) + sum(t.numel() for t in host_sf)
+    with torch.cuda.stream(stream):
+        def e2e_step(s):
+            for li in range(len(LAYERS)):
+                A[li][s].copy_(host_A[li], non_blocking=True)
+                launch("kroquant", li, s)
+                host_q[li].copy_(Q[li][s], non_blocking=True)
+                host_sf[li].copy_(SF[li][s], non_blocking=True)
+        for w in range(3):
+            e2e_step(w % SETS)
+        stream.synchronize()
+        dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(e2e_steps):
+            e2e_step(k % SETS)
+        e1.record(stream)
+        stream.synchronize()
+    e2e_ms = dist.max(e0.elapsed_time(e1))
+    e2e_value = dist.sum(STEP_BYTES * e2e_steps) / (e2e_ms * 1e-3) / 1e9
+
+    cpu = cpu_baseline(args.cpu_seconds) if dist.rank == 0 and dist.world == 1 else None
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
+            "steps": K, "warmup": W, "ms_per_step": round(ms_max / K, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "flux_layer_pair", "m": 4608, "d": [3072, 12288],
+                       "transform": f"kroquant_{args.variant}", "input": "bf16",
+                       "output": "mxfp4 (e2m1 codes + e8m0 scales, 128x4 tiled)",
+                       "l2": f"{SETS} rotating input/output sets, "
+                             f"{SETS * STEP_BYTES / 1e6:.0f} MB footprint > L2",
+                       "launch": "one CUDA graph per layer launch", "parallelism":
+                           f"replicas x{dist.world} (rows independent, no exchange)"},
+            "hbm_frac": round(value / dist.world / peak, 4),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "kernel": workload, "launch_ms": round(dom_ms, 5),
+                         "peak_source": peak_src},
+            "vs_diag_scale": round(value / dist.world / baselines["diag"], 4)
+            if baselines.get("diag") else None,
+            "baselines_gbs": baselines,
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": K * len(LAYERS),
+            "clocks": clocks,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        dist = Dist(use_cuda=False) if int(os.environ.get("WORLD_SIZE", "1")) > 1 else Dist(False)
+        try:
+            run_reference(args, dist)
+        finally:
+            dist.close()
+        return
+    import torch
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}), flush=True)
+        sys.exit(1)
+    dist = Dist(use_cuda=True)
+    torch.cuda.set_device(dist.local)
+    from w4a4_mxfp4_activation_gb300 import build
+    build.build()
+    try:
+        run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+/*
+ * kq.h -- C ABI of the GB300 (sm_103a) KroQuant MXFP4 activation quantizer.
+ *
+ * What it computes ("KroQuant: Kronecker-Structured Block Transforms for
+ * Efficient Post-Training Quantization of Diffusion Transformers",
+ * arXiv 2607.21446v1, cited below as [KQ]):
+ *   - eq. (4): T = diag(K_1, ..., K_nb) is block diagonal with 32x32 blocks;
+ *   - eq. (5): K_j = G1 (x) G2 (x) G3 (x) G4 (x) G5, five 2x2 factors;
+ *   - eq. (12): K_j[r][c] = prod_k G_k[bit_{5-k}(r)][bit_{5-k}(c)], so G1
+ *     acts on bit 4 (most significant) of the channel index within a block;
+ *   - Sec. 3.5.1 (K1, "A_tile @ K"): every row a of A is transformed as the
+ *     row vector y = a . K_j per 32-channel block j;
+ *   - Sec. 3.1 and 4.1: y is quantized to MXFP4 -- per 32-element block one
+ *     E8M0 scale 2^e with e = floor(log2 amax) - 2 (clamped to [-127, 127],
+ *     e = -127 when amax = 0) and 32 FP4 E2M1 codes of y / 2^e, rounded to
+ *     nearest with ties to even, saturated to +-6, sign kept (also -0).
+ *
+ * Data layout.
+ *   A       bf16 bit patterns, row-major [m][lda], lda >= d.
+ *   q       packed E2M1 codes, row-major [m][ldq] bytes, ldq >= d/2; byte k
+ *           of a row holds code 2k in bits 0-3 and code 2k+1 in bits 4-7
+ *           (code = sign << 3 | E2M1 magnitude index 0..7).
+ *   sf      E8M0 scale bytes (e + 127), nb = d/32 per row, either
+ *           KQ_SF_ROWMAJOR [m][nb], or KQ_SF_BLOCKED_128x4, the tiled layout
+ *           that block-scaled MMA reads: tiles of 128 rows x 4 block-columns,
+ *           512 bytes each, tiles in row-tile-major order; inside a tile the
+ *           scale of (row i, block kb) sits at
+ *           (i % 32) * 16 + ((i % 128) / 32) * 4 + (kb % 4).  Rows are padded
+ *           to a multiple of 128 and block-columns to a multiple of 4; the
+ *           library writes 0x00 into the padding.  kq_sf_bytes() gives the size.
+ *   factors fp32 raw 2x2 entries [nb][5][2][2]: factor k of block j is
+ *           factors[((j*5 + k)*2 + r)*2 + c] = G_{k+1}[r][c].  Any raw
+ *           entries are accepted (both determinant-sign conventions of the
+ *           LU form, eq. 6, and the Hadamard factor of Sec. 3.2).
+ *
+ * Ownership and execution.  The caller allocates and owns every buffer.
+ * Entry points taking a cudaStream_t validate their arguments on the host,
+ * then enqueue work on that stream and return without synchronizing;
+ * results are valid once the stream reaches that point.  They never
+ * allocate, free or synchronize.  Device-pointer arguments must be device
+ * (or managed) memory of the current device.
+ *
+ * Errors.  Argument checks run before anything is enqueued; a failed check
+ * returns its status and enqueues nothing.  A launch failure reported by the
+ * CUDA runtime returns KQ_ERR_CUDA.  m = 0 is a valid no-op (KQ_OK).
+ * A kernel that finds its data pipeline stalled for longer than about one
+ * second stops waiting and writes the E8M0 NaN byte 0xFF as the scale of
+ * every block it could not finish (finite inputs never produce 0xFF).
+ */
+#ifndef KQ_H
+#define KQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define KQ_API __attribute__((visibility("default")))
+#else
+#define KQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kq_status {
+    KQ_OK = 0,
+    KQ_ERR_NULL = 1,        /* a required pointer is NULL */
+    KQ_ERR_SHAPE = 2,       /* m < 0, d <= 0, d % 32 != 0, lda < d, ldq < d/2, nb <= 0 */
+    KQ_ERR_ALIGN = 3,       /* a pointer or leading dimension breaks the alignment rules */
+    KQ_ERR_LAYOUT = 4,      /* unknown kq_sf_layout / kq_kfmt / variant / sign value */
+    KQ_ERR_CUDA = 5,        /* the CUDA runtime or driver reported an error */
+    KQ_ERR_UNSUPPORTED = 6  /* the current device is not sm_103 (GB300) */
+} kq_status;
+
+typedef enum kq_sf_layout {
+    KQ_SF_ROWMAJOR = 0,
+    KQ_SF_BLOCKED_128x4 = 1
+} kq_sf_layout;
+
+typedef enum kq_kfmt {
+    KQ_K_FP32 = 0,      /* dense K_j, fp32 row-major [nb][32][32] */
+    KQ_K_BF16X3 = 1     /* K_j as three bf16 terms hi + mid + lo, in the operand
+                           order of the tensor-core variant (opaque) */
+} kq_kfmt;
+
+/* Alignment rules shared by the quantizer entry points:
+ *   A, q, sf, y_debug, factors, s, K_expanded: 16-byte aligned;
+ *   lda % 8 == 0 (16-byte row pitch), ldq % 16 == 0. */
+
+/*
+ * kq_quantize_mxfp4 -- the KroQuant online activation quantizer.
+ * [KQ] eq. (4), (5), (12); Sec. 3.5 (one pass: transform, then the fused
+ * MXFP4 quantizer); Sec. 3.1 / 4.1 (MXFP4).
+ *   A          device, bf16 [m][lda] (read only)
+ *   m, d, lda  rows, channels (d % 32 == 0), row pitch in elements
+ *   factors    device, fp32 [d/32][5][2][2] raw factor entries, or NULL
+ *   K_expanded device, output of kq_expand_blocks(..., KQ_K_BF16X3, ...), or
+ *              NULL.  With factors != NULL the five 2x2 factors are applied
+ *              as an in-register butterfly; with factors == NULL and
+ *              K_expanded != NULL the dense blocks run on the tensor cores;
+ *              with both NULL the transform is the identity (the bare
+ *              quantizer, "Q4" of [KQ] Tables 3 and 4).
+ *   q, ldq     device, packed codes [m][ldq] (written)
+ *   sf         device, scales in sf_layout (written; kq_sf_bytes() bytes)
+ *   y_debug    device fp32 [m][d] or NULL: if given, receives y = a . K_j
+ *              exactly as it enters the quantizer (for verification)
+ *   stream     CUDA stream (0 = legacy default stream)
+ */
+KQ_API kq_status kq_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                            const float *factors, const void *K_expanded,
+                            uint8_t *q, int64_t ldq, uint8_t *sf, kq_sf_layout sf_layout,
+                            float *y_debug, cudaStream_t stream);
+
+/*
+ * kq_smooth_quantize_mxfp4 -- diagonal-scale baseline: T = diag(s),
+ * y[i][c] = a[i][c] * s[c], then the same MXFP4 quantizer ([KQ] Sec. 4.4,
+ * "Scale", per-channel scaling of SmoothQuant; a SmoothQuant user passes
+ * s = 1/gamma with gamma of Appendix D.2).
+ *   s  device fp32 [d]; other arguments as kq_quantize_mxfp4.
+ */
+KQ_API kq_status kq_smooth_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                   const float *s, uint8_t *q, int64_t ldq, uint8_t *sf,
+                                   kq_sf_layout sf_layout, float *y_debug, cudaStream_t stream);
+
+/*
+ * kq_hadamard_quantize_mxfp4 -- fixed block-Hadamard baseline: every K_j is
+ * the normalised 32-point Walsh-Hadamard matrix H32 / sqrt(32) (Sylvester
+ * order, H32[r][c] = (-1)^popcount(r & c)), [KQ] Sec. 3.2 "Hadamard
+ * initialization" and Table 2 "Hadamard (32x32)".  Arguments as
+ * kq_quantize_mxfp4.
+ */
+KQ_API kq_status kq_hadamard_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                     uint8_t *q, int64_t ldq, uint8_t *sf,
+                                     kq_sf_layout sf_layout, float *y_debug, cudaStream_t stream);
+
+/*
+ * kq_expand_blocks -- [KQ] Sec. 3.5.1 K1 ("each 32x32 block K_j is
+ * materialized"): expand the raw factors into dense blocks by eq. (12),
+ * computed in fp64 and then rounded to the requested format.
+ *   factors  device fp32 [nb][5][2][2]
+ *   nb       number of 32-channel blocks (> 0)
+ *   fmt      KQ_K_FP32 (row-major [nb][32][32] fp32) or KQ_K_BF16X3
+ *   K_out    device, kq_expanded_bytes(nb, fmt) bytes, 16-byte aligned
+ */
+KQ_API kq_status kq_expand_blocks(const float *factors, int64_t nb, kq_kfmt fmt, void *K_out,
+                           cudaStream_t stream);
+
+/* Bytes kq_expand_blocks writes for nb blocks in format fmt (0 if invalid). */
+KQ_API size_t kq_expanded_bytes(int64_t nb, kq_kfmt fmt);
+
+/*
+ * kq_dequantize -- MXFP4 decode: out[i][c] = e2m1(code) * 2^(sf - 127),
+ * exact in fp32 (OCP MX element x shared scale; [KQ] Sec. 3.1, Q_b returns
+ * the dequantized matrix).
+ *   q, ldq, sf, sf_layout  as written by the quantizers (device)
+ *   m, d                   shape of the quantized matrix
+ *   out                    device fp32 [m][d] (16-byte aligned)
+ */
+KQ_API kq_status kq_dequantize(const uint8_t *q, int64_t ldq, const uint8_t *sf,
+                        kq_sf_layout sf_layout, int64_t m, int64_t d, float *out,
+                        cudaStream_t stream);
+
+/* Bytes of the scale array for an m x d matrix (padded for the blocked
+ * layout); 0 if the arguments are invalid. */
+KQ_API size_t kq_sf_bytes(int64_t m, int64_t d, kq_sf_layout sf_layout);
+
+/* Static, never-NULL description of a status code. */
+KQ_API const char *kq_status_string(kq_status status);
+
+/*
+ * Host helpers (host memory, synchronous, no CUDA calls).
+ *
+ * kq_lu_to_factors -- [KQ] eq. (6): lu [nb][5][3] = (a, b, c) per factor,
+ *   G = [[1, 0], [c, 1]] . [[a, b], [0, det_sign / a]], evaluated in fp64 and
+ *   rounded once to fp32 into factors [nb][5][2][2].  det_sign = -1 is the
+ *   paper's form (det G = -1), +1 the unit-determinant form.  a == 0 gives
+ *   KQ_ERR_SHAPE.
+ */
+KQ_API kq_status kq_lu_to_factors(const float *lu, int64_t nb, int det_sign, float *factors);
+
+/*
+ * kq_invert_transpose_factors -- factors of K_j^{-T} = (x)_k G_k^{-T}
+ *   ([KQ] Sec. 3.2: the inverse of a Kronecker product is the Kronecker
+ *   product of the inverses; eq. (1): the weights take W T^{-T}).  Each 2x2
+ *   inverse-transpose is evaluated in fp64 and rounded once to fp32.  A
+ *   singular factor gives KQ_ERR_SHAPE.  Feed the result to
+ *   kq_quantize_mxfp4 to quantize the rows of W T^{-T}.
+ */
+KQ_API kq_status kq_invert_transpose_factors(const float *factors, int64_t nb, float *out);
+
+/*
+ * Verification and benchmarking hooks.
+ *
+ * kq_quantize_mxfp4_variant -- kq_quantize_mxfp4 with the block-transform
+ *   implementation chosen explicitly: variant 0 = in-register butterfly
+ *   from the raw factors (needs factors), 1 = tensor-core mma.sync on the
+ *   pre-expanded blocks (needs K_expanded), 2 = identity.
+ */
+KQ_API kq_status kq_quantize_mxfp4_variant(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                    const float *factors, const void *K_expanded,
+                                    uint8_t *q, int64_t ldq, uint8_t *sf,
+                                    kq_sf_layout sf_layout, float *y_debug, int variant,
+                                    cudaStream_t stream);
+
+/*
+ * kq_test_encode_e2m1 -- runs the quantizers' E2M1 encoder on the fp32 bit
+ *   patterns first, first+1, ..., first+count-1 with the scale fixed at 2^0
+ *   (v = y), writing count/2 packed bytes (code of the even pattern in bits
+ *   0-3).  count must be a multiple of 8; out is device memory, 16-byte
+ *   aligned.  Used for the exhaustive rounding check.
+ */
+KQ_API kq_status kq_test_encode_e2m1(uint32_t first, int64_t count, uint8_t *out, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KQ_H */

@@ -1,0 +1,146 @@
+"""C-ABI library on the host (no GPU): it loads, exports every function that
+``include/kq.h`` declares, its host helpers agree with the oracle, and its
+argument checks reject bad calls before touching CUDA."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+from w4a4_mxfp4_activation_gb300 import kq, synth
+
+HEADER = os.path.join(ROOT, "include", "kq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from w4a4_mxfp4_activation_gb300 import build
+    build.build()
+    return kq.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"KQ_API\s+[\w\s\*]+?\b(kq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for required in ("kq_expand_blocks", "kq_quantize_mxfp4", "kq_smooth_quantize_mxfp4",
+                     "kq_hadamard_quantize_mxfp4", "kq_dequantize"):
+        assert required in names
+    assert set(names) == set(kq.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert kq.status_string(s)
+    assert kq.status_string(99) == "unknown status"
+
+
+def test_sf_bytes_matches_oracle(L, oracle_lib):
+    for m in (0, 1, 127, 128, 129, 4608):
+        for d in (32, 1152, 2240, 5600, 12288):
+            for layout in (0, 1):
+                assert kq.kq_sf_bytes(m, d, layout) == oracle_lib.sf_bytes(m, d // 32, layout)
+    assert kq.kq_sf_bytes(4, 33, 0) == 0 and kq.kq_sf_bytes(-1, 32, 0) == 0
+    assert kq.kq_sf_bytes(4, 32, 7) == 0
+
+
+def test_expanded_bytes(L):
+    assert kq.kq_expanded_bytes(36, kq.KQ_K_FP32) == 36 * 4096
+    assert kq.kq_expanded_bytes(36, kq.KQ_K_BF16X3) == 36 * 6144
+    assert kq.kq_expanded_bytes(0, kq.KQ_K_FP32) == 0
+
+
+@pytest.mark.parametrize("sign", [-1, 1])
+def test_lu_to_factors_matches_oracle_bitwise(L, oracle_lib, sign):
+    """Library helper and oracle both evaluate eq. (6) in fp64 and round once
+    to fp32: the entries must be identical."""
+    lu = synth.lu_params(384, 2003)
+    got = kq.kq_lu_to_factors(lu, sign)
+    ref = oracle_lib.lu_to_factors(lu.astype(np.float64), sign).astype(np.float32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_invert_transpose_factors(L):
+    F = kq.kq_lu_to_factors(synth.lu_params(20, 5), 1)
+    Finv = kq.kq_invert_transpose_factors(F)
+    for j in range(20):
+        for k in range(5):
+            ref = np.linalg.inv(F[j, k].astype(np.float64)).T
+            assert np.allclose(Finv[j, k], ref, rtol=2 ** -23, atol=0)
+    with pytest.raises(kq.KqError):
+        kq.kq_invert_transpose_factors(np.zeros((1, 5, 2, 2), np.float32))
+
+
+def test_lu_to_factors_rejects(L):
+    with pytest.raises(kq.KqError):
+        kq.kq_lu_to_factors(np.zeros((1, 5, 3), np.float32), 1)   # a = 0
+    with pytest.raises(kq.KqError):
+        kq.kq_lu_to_factors(synth.lu_params(1, 0), 2)             # bad sign
+
+
+# --- argument checks: each call fails validation before any CUDA call ----------------
+
+FAKE = 1 << 20          # a 16-byte aligned, never dereferenced address
+
+
+def _q(L, A=FAKE, m=4, d=64, lda=64, f=FAKE, K=None, q=FAKE, ldq=32, sf=FAKE, layout=0, y=None,
+       variant=None):
+    if variant is None:
+        return L.kq_quantize_mxfp4(A, m, d, lda, f, K, q, ldq, sf, layout, y, None)
+    return L.kq_quantize_mxfp4_variant(A, m, d, lda, f, K, q, ldq, sf, layout, y, variant, None)
+
+
+def test_quantize_argument_checks(L):
+    assert _q(L, d=48) == 2                       # d % 32
+    assert _q(L, d=0) == 2
+    assert _q(L, m=-1) == 2
+    assert _q(L, lda=32) == 2                     # lda < d
+    assert _q(L, ldq=16) == 2                     # ldq < d/2
+    assert _q(L, layout=5) == 4
+    assert _q(L, A=None) == 1
+    assert _q(L, q=None) == 1
+    assert _q(L, sf=None) == 1
+    assert _q(L, A=FAKE + 2) == 3                 # A misaligned
+    assert _q(L, q=FAKE + 8) == 3
+    assert _q(L, lda=68) == 3                     # row pitch not 16-byte multiple
+    assert _q(L, ldq=40) == 3
+    assert _q(L, y=FAKE + 4) == 3
+    assert _q(L, f=FAKE + 4) == 3                 # factors misaligned
+    assert _q(L, m=0) == 0                        # empty: no-op
+    assert _q(L, m=0, A=None, q=None, sf=None) == 0
+    assert _q(L, variant=3) == 4
+    assert _q(L, variant=1, K=None) == 1
+    assert _q(L, variant=0, f=None) == 1
+
+
+def test_baseline_argument_checks(L):
+    assert L.kq_smooth_quantize_mxfp4(FAKE, 4, 64, 64, None, FAKE, 32, FAKE, 0, None, None) == 1
+    assert L.kq_smooth_quantize_mxfp4(FAKE, 4, 64, 64, FAKE + 4, FAKE, 32, FAKE, 0, None, None) == 3
+    assert L.kq_smooth_quantize_mxfp4(FAKE, 4, 60, 64, FAKE, FAKE, 32, FAKE, 0, None, None) == 2
+    assert L.kq_hadamard_quantize_mxfp4(FAKE, 4, 64, 64, FAKE, 32, None, 0, None, None) == 1
+    assert L.kq_hadamard_quantize_mxfp4(FAKE, 0, 64, 64, FAKE, 32, FAKE, 0, None, None) == 0
+
+
+def test_aux_argument_checks(L):
+    assert L.kq_dequantize(FAKE, 32, FAKE, 0, 4, 63, FAKE, None) == 2
+    assert L.kq_dequantize(None, 32, FAKE, 0, 4, 64, FAKE, None) == 1
+    assert L.kq_dequantize(FAKE, 32, FAKE, 2, 4, 64, FAKE, None) == 4
+    assert L.kq_dequantize(FAKE, 32, FAKE, 0, 4, 64, FAKE + 4, None) == 3
+    assert L.kq_expand_blocks(FAKE, 0, 0, FAKE, None) == 2
+    assert L.kq_expand_blocks(FAKE, 4, 9, FAKE, None) == 4
+    assert L.kq_expand_blocks(None, 4, 0, FAKE, None) == 1
+    assert L.kq_test_encode_e2m1(0, 7, FAKE, None) == 2
+    assert L.kq_test_encode_e2m1(0xFFFFFFF8, 16, FAKE, None) == 2
+    assert L.kq_test_encode_e2m1(0, 0, None, None) == 0

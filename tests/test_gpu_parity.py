@@ -1,0 +1,385 @@
+"""GPU parity: the CUDA quantizers, called through the C ABI, against the CPU
+oracle on seeded synthetic inputs (comparison rules in ``parity.py``).
+
+Workloads: stand-ins for the DiT layers of "KroQuant: Kronecker-Structured
+Block Transforms for Efficient Post-Training Quantization of Diffusion
+Transformers" (Sec. 4.1; Tables 3-4 shapes): the 256 x 1152 correctness case,
+PixArt-Sigma (4096 x 1152 / 4608), SANA (4096 x 2240 / 5600), FLUX.1-schnell
+(4608 x 3072 / 12288) and the m x d sweep.
+"""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from conftest import build_c_helper, read_golden
+import parity
+from oracle import kq_oracle as O
+from w4a4_mxfp4_activation_gb300 import kq, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from w4a4_mxfp4_activation_gb300 import build
+    build.build()
+    kq.lib()
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def to_bf16(bits):
+    return dev(bits.view(np.int16)).view(torch.bfloat16)
+
+
+def np_(t):
+    return t.cpu().numpy()
+
+
+def lib_factors(nb, seed, sign=+1):
+    """Raw fp32 factors through the library helper (GPU side) and the
+    oracle's own fp64 entries from the same LU parameters."""
+    lu = synth.lu_params(nb, seed)
+    return kq.kq_lu_to_factors(lu, sign), O.lu_to_factors(lu.astype(np.float64), sign) \
+        .astype(np.float32).astype(np.float64)
+
+
+def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None, q=None, sf=None):
+    A = to_bf16(A_bits)
+    if kind == "kron":
+        return kq.kq_quantize_mxfp4(A, d, factors=dev(param_gpu), layout=layout, y_debug=y_debug,
+                                    variant=variant, q=q, sf=sf)
+    if kind == "identity":
+        return kq.kq_quantize_mxfp4(A, d, layout=layout, y_debug=y_debug, q=q, sf=sf)
+    if kind == "diag":
+        return kq.kq_smooth_quantize_mxfp4(A, dev(param_gpu), d, layout=layout, y_debug=y_debug,
+                                           q=q, sf=sf)
+    if kind == "hadamard":
+        return kq.kq_hadamard_quantize_mxfp4(A, d, layout=layout, y_debug=y_debug, q=q, sf=sf)
+    raise ValueError(kind)
+
+
+def params_for(kind, nb, d, seed):
+    """(gpu param, oracle param) for a transform kind."""
+    if kind == "kron":
+        return lib_factors(nb, seed)
+    if kind == "diag":
+        s = synth.smooth_scales(d)
+        return s, s.astype(np.float64)
+    return None, None
+
+
+# ------------------------------------------------------------------ encoder --
+
+def test_encoder_exhaustive_fp32(tmp_path):
+    """P4g: every finite fp32 bit pattern through the kernels' E2M1 encoder
+    (scale 2^0) equals the table scan (nearest magnitude, ties to the even
+    code, |v| > 6 -> 6, sign kept) -- also pins the nibble order."""
+    pin = ctypes.CDLL(build_c_helper(tmp_path, "pin_e2m1_table_scan"))
+    pin.pin_table_scan_packed.argtypes = [ctypes.c_uint64, ctypes.c_uint64,
+                                          ctypes.POINTER(ctypes.c_double), ctypes.c_void_p]
+    grid = {int(r[0]): float(r[1]) for r in read_golden("e2m1_grid.txt")}
+    mag = np.array([grid[k] for k in range(8)], np.float64)
+    magp = mag.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+    chunk = 1 << 28
+    out = torch.empty(chunk // 2, dtype=torch.uint8, device="cuda")
+    exp = np.empty(chunk // 2, np.uint8)
+    per_exp = 1 << 22                                # bytes per fp32 exponent value
+    for first in range(0, 1 << 32, chunk):
+        kq.kq_test_encode_e2m1(first, chunk, out)
+        got = np_(out)
+        pin.pin_table_scan_packed(first, chunk, magp, exp.ctypes.data)
+        for r in range(chunk // 2 // per_exp):
+            if (((first >> 23) + r) & 0xFF) == 0xFF:
+                continue                             # inf / NaN patterns: out of contract
+            g, e = got[r * per_exp:(r + 1) * per_exp], exp[r * per_exp:(r + 1) * per_exp]
+            if not np.array_equal(g, e):
+                k = int(np.argmax(g != e))
+                raise AssertionError(f"encoder mismatch at pattern 0x{first + 2 * (r * per_exp + k):08x}:"
+                                     f" got {g[k]:#04x}, want {e[k]:#04x}")
+
+
+def test_worked_block_bare_quantizer():
+    """Hand-derived block through the identity transform (bit-exact)."""
+    g = {r[0]: r[1:] for r in read_golden("worked_block.txt")}
+    y = np.array([float(v) for v in g["y"]])
+    bits = synth.f64_to_bf16_bits(y[None, :])
+    assert np.array_equal(synth.bf16_bits_to_f32(bits)[0].astype(np.float64), y)
+    q, sf, _ = run_kind("identity", bits, 32, 0)
+    codes = [int(c) for c in g["codes"]]
+    assert int(np_(sf)[0]) == int(g["scale"][0])
+    assert list(np_(q)[0]) == [codes[2 * k] | (codes[2 * k + 1] << 4) for k in range(16)]
+
+
+# ------------------------------------------------------------- configs 0-3 --
+
+CASES = synth.CONFIG0 + synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3
+
+
+@pytest.mark.parametrize("name,m,d,model,cfg", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("kind", ["kron", "diag", "hadamard", "identity"])
+def test_config_parity(name, m, d, model, cfg, kind):
+    """Configs 0-3 at full size, both scale layouts (flux shapes compare a
+    seeded sample of rows, always including the first and last tiles)."""
+    nb = d // 32
+    A_bits = synth.activations(m, d, synth.SEED_A + cfg, model)
+    pg, po = params_for(kind, nb, d, synth.SEED_FACTORS + cfg)
+    rows = None
+    if m * d > 30_000_000:
+        rng = np.random.default_rng(cfg)
+        rows = np.unique(np.concatenate([np.arange(130), np.arange(m - 130, m),
+                                         rng.choice(m, 700, replace=False)]))
+    for layout in (0, 1):
+        q, sf, y = run_kind(kind, A_bits, d, layout, pg)
+        res = parity.check(A_bits, d, kind, po, layout, np_(q), np_(sf), np_(y), rows)
+        # the production launch (no debug output) writes the same bytes
+        q2, sf2, _ = run_kind(kind, A_bits, d, layout, pg, y_debug=False)
+        assert torch.equal(q, q2) and torch.equal(sf, sf2)
+        print(name, kind, layout, res)
+
+
+def test_hadamard_factors_config0():
+    """Config 0's second run: every factor the Hadamard initial factor; the
+    KroQuant kernel and the fixed block-Hadamard kernel both match the
+    oracle, and each other outside the oracle's flags."""
+    m, d = 256, 1152
+    nb = d // 32
+    A_bits = synth.activations(m, d, synth.SEED_A, "gauss_outlier8")
+    F = synth.hadamard_factors(nb)
+    qk, sfk, yk = run_kind("kron", A_bits, d, 0, F)
+    parity.check(A_bits, d, "kron", F.astype(np.float64), 0, np_(qk), np_(sfk), np_(yk))
+    qh, sfh, yh = run_kind("hadamard", A_bits, d, 0)
+    _, _, flags = O.quantize(*O.transform(A_bits, d, "hadamard"), O.SF_ROWMAJOR)
+    ck, ch = parity.unpack(np_(qk), d), parity.unpack(np_(qh), d)
+    strict = flags == 0
+    assert np.array_equal(ck[strict], ch[strict])
+
+
+# ------------------------------------------------------------------ E(T) --
+
+@pytest.mark.parametrize("factor_kind", ["random", "hadamard"])
+def test_layer_error_config0(factor_kind):
+    """eq. (2): ||Q(AT) Q(W T^{-T})^T - A W^T||_F from the GPU quantizer and
+    dequantizer matches the oracle to 1e-3 relative."""
+    m, d, o = 256, 1152, 1152
+    nb = d // 32
+    A_bits = synth.activations(m, d, synth.SEED_A, "gauss_outlier8")
+    W_bits = synth.weights(o, d)
+    if factor_kind == "random":
+        Fg, Fo = lib_factors(nb, synth.SEED_FACTORS)
+    else:
+        Fg = synth.hadamard_factors(nb)
+        Fo = Fg.astype(np.float64)
+    FgT = kq.kq_invert_transpose_factors(Fg)
+    qa, sfa, _ = run_kind("kron", A_bits, d, 0, Fg, y_debug=False)
+    qw, sfw, _ = run_kind("kron", W_bits, d, 0, FgT, y_debug=False)
+    Aq = np_(kq.kq_dequantize(qa, sfa, m, d)).astype(np.float64)
+    Wq = np_(kq.kq_dequantize(qw, sfw, o, d)).astype(np.float64)
+    a = synth.bf16_bits_to_f32(A_bits).astype(np.float64)
+    w = synth.bf16_bits_to_f32(W_bits).astype(np.float64)
+    e_gpu = np.linalg.norm(Aq @ Wq.T - a @ w.T)
+    e_ref, ref = O.layer_error(A_bits, W_bits, d, Fo)
+    assert abs(e_gpu - e_ref) <= 1e-3 * e_ref, (e_gpu, e_ref)
+    assert e_ref < ref
+
+
+@pytest.mark.parametrize("name,m,d,model,cfg", synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3,
+                         ids=[c[0] for c in synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3])
+def test_layer_error_configs(name, m, d, model, cfg):
+    """E(T) on configs 1-3: first 512 rows of A, a weight of o = min(d, 3072)
+    output channels."""
+    m, o = 512, min(d, 3072)
+    nb = d // 32
+    A_bits = synth.activations(m, d, synth.SEED_A + cfg, model)
+    W_bits = synth.weights(o, d, seed=synth.SEED_W + cfg)
+    Fg, Fo = lib_factors(nb, synth.SEED_FACTORS + cfg)
+    qa, sfa, _ = run_kind("kron", A_bits, d, 1, Fg, y_debug=False)
+    qw, sfw, _ = run_kind("kron", W_bits, d, 1, kq.kq_invert_transpose_factors(Fg), y_debug=False)
+    Aq = np_(kq.kq_dequantize(qa, sfa, m, d, layout=1)).astype(np.float64)
+    Wq = np_(kq.kq_dequantize(qw, sfw, o, d, layout=1)).astype(np.float64)
+    a = synth.bf16_bits_to_f32(A_bits).astype(np.float64)
+    w = synth.bf16_bits_to_f32(W_bits).astype(np.float64)
+    e_gpu = np.linalg.norm(Aq @ Wq.T - a @ w.T)
+    e_ref, _ = O.layer_error(A_bits, W_bits, d, Fo, layout=1)
+    assert abs(e_gpu - e_ref) <= 1e-3 * e_ref, (e_gpu, e_ref)
+
+
+# ------------------------------------------------------------ config 4 --
+
+SWEEP = [(m, d) for m in synth.SWEEP_M for d in synth.SWEEP_D]
+
+
+@pytest.mark.parametrize("m,d", SWEEP, ids=[f"{m}x{d}" for m, d in SWEEP])
+def test_sweep_parity(m, d):
+    """Config 4: 4 layers' factor sets per point; KroQuant, diagonal and
+    Hadamard quantizers; large points compare a seeded row sample."""
+    nb = d // 32
+    A_bits = synth.activations(m, d, synth.SEED_A + 4, "flux")
+    rng = np.random.default_rng(m + d)
+    rows = None
+    if m * d > 20_000_000:
+        rows = np.unique(np.concatenate([np.arange(128), np.arange(m - 128, m),
+                                         rng.choice(m, 400, replace=False)]))
+    for layer in range(4):
+        Fg, Fo = lib_factors(nb, synth.SEED_FACTORS + 4 + layer)
+        q, sf, y = run_kind("kron", A_bits, d, layer % 2, Fg)
+        parity.check(A_bits, d, "kron", Fo, layer % 2, np_(q), np_(sf), np_(y), rows)
+    s = synth.smooth_scales(d)
+    q, sf, y = run_kind("diag", A_bits, d, 1, s)
+    parity.check(A_bits, d, "diag", s.astype(np.float64), 1, np_(q), np_(sf), np_(y), rows)
+    q, sf, y = run_kind("hadamard", A_bits, d, 0)
+    parity.check(A_bits, d, "hadamard", None, 0, np_(q), np_(sf), np_(y), rows)
+
+
+# ------------------------------------------------------------ edge cases --
+
+EDGE_SHAPES = [(1, 32), (7, 96), (127, 160), (129, 64), (200, 5600), (3, 2240), (300, 1152)]
+
+
+@pytest.mark.parametrize("m,d", EDGE_SHAPES, ids=[f"{m}x{d}" for m, d in EDGE_SHAPES])
+@pytest.mark.parametrize("kind", ["kron", "diag", "hadamard", "identity"])
+def test_ragged_shapes_with_pitches_and_canaries(m, d, kind):
+    """Ragged m and d (partial tiles and block-columns), lda > d, ldq > d/2,
+    and guard bytes around every output that must stay untouched."""
+    nb = d // 32
+    lda, ldq = d + 64, d // 2 + 32
+    A_bits = synth.activations(m, d, 77 + m, "pixart", lda=lda)
+    pg, po = params_for(kind, nb, d, 55 + d)
+    for layout in (0, 1):
+        sfb = kq.kq_sf_bytes(m, d, layout)
+        q_store = torch.full((m + 2, ldq), 0xA5, dtype=torch.uint8, device="cuda")
+        sf_store = torch.full((sfb + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+        q = q_store[1:m + 1]
+        sf = sf_store[16:16 + sfb]
+        qq, ssf, y = run_kind(kind, A_bits, d, layout, pg, q=q, sf=sf)
+        qs = np_(q_store)
+        assert (qs[0] == 0xA5).all() and (qs[m + 1] == 0xA5).all()
+        assert (qs[1:m + 1, d // 2:] == 0xA5).all(), "row padding of q overwritten"
+        ss = np_(sf_store)
+        assert (ss[:16] == 0xA5).all() and (ss[16 + sfb:] == 0xA5).all()
+        parity.check(np.ascontiguousarray(A_bits[:, :d]), d, kind, po, layout, np_(q)[:, :d // 2],
+                     np_(sf), np_(y))
+        if layout == 1:
+            # padding of the tiled layout is written as zero
+            full = np.zeros(sfb, bool)
+            rows = np.arange(m)
+            i, kb = np.meshgrid(rows, np.arange(nb), indexing="ij")
+            ncb = (nb + 3) // 4
+            off = ((i // 128) * ncb + kb // 4) * 512 + (i % 32) * 16 + ((i % 128) // 32) * 4 + kb % 4
+            full[off.ravel()] = True
+            assert (np_(sf)[~full] == 0).all()
+
+
+def test_special_values():
+    """Zeros, negative zeros, bf16 subnormals, the largest bf16 values and
+    exact midpoints through the bare quantizer and the Kronecker kernel."""
+    rows = []
+    rows.append(np.zeros(32))
+    rows.append(-np.zeros(32))
+    rows.append(np.ldexp(np.arange(32) - 16.0, -133))        # subnormal bf16
+    rows.append(np.ldexp(np.linspace(-1, 1, 32), -126))
+    rows.append(np.full(32, 3.3e38) * np.where(np.arange(32) % 2, 1, -1))
+    rows.append(np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0] * 4) * 2.0 ** 40)
+    rows.append(np.concatenate([[1e-30], np.zeros(31)]))
+    y = np.stack(rows)
+    bits = synth.f64_to_bf16_bits(y)
+    q, sf, yd = run_kind("identity", bits, 32, 0)
+    parity.check(bits, 32, "identity", None, 0, np_(q), np_(sf), np_(yd))
+    # the special rows pass through the identity exactly: no flags needed
+    codes = parity.unpack(np_(q), 32)
+    assert (codes[0] == 0).all() and (codes[1] == 8).all() and (np_(sf)[:2] == 0).all()
+    Fg, Fo = lib_factors(1, 3)
+    q, sf, yd = run_kind("kron", bits, 32, 0, Fg)
+    parity.check(bits, 32, "kron", Fo, 0, np_(q), np_(sf), np_(yd))
+
+
+def test_raw_factor_interface():
+    """Arbitrary raw 2x2 entries (no determinant constraint) and both LU
+    sign conventions."""
+    m, d = 300, 640
+    nb = d // 32
+    A_bits = synth.activations(m, d, 9, "sana")
+    F = synth.random_factors(nb, 12, scale=0.8)
+    q, sf, y = run_kind("kron", A_bits, d, 1, F)
+    parity.check(A_bits, d, "kron", F.astype(np.float64), 1, np_(q), np_(sf), np_(y))
+    Fg, Fo = lib_factors(nb, 13, sign=-1)
+    q, sf, y = run_kind("kron", A_bits, d, 0, Fg)
+    parity.check(A_bits, d, "kron", Fo, 0, np_(q), np_(sf), np_(y))
+
+
+def test_empty_input_is_noop():
+    A = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    q, sf, _ = kq.kq_quantize_mxfp4(A, 64, layout=0)
+    assert q.shape[0] == 0
+
+
+# ------------------------------------------------------- dequant, expand --
+
+def test_dequantize_exact():
+    """P9: the dequantizer equals the oracle's value(code) * 2^e exactly, for
+    both layouts (including the padded tiles)."""
+    m, d = 333, 1152
+    A_bits = synth.activations(m, d, 21, "flux")
+    Fg, _ = lib_factors(d // 32, 21)
+    for layout in (0, 1):
+        q, sf, _ = run_kind("kron", A_bits, d, layout, Fg, y_debug=False)
+        out = np_(kq.kq_dequantize(q, sf, m, d, layout=layout)).astype(np.float64)
+        ref = O.dequantize(np_(q), np_(sf), layout, m, d)
+        assert np.array_equal(out, ref)
+        assert np.array_equal(np.signbit(out), np.signbit(ref))
+
+
+def test_expand_blocks_fp32():
+    """K1's dense blocks: the device product (fp64, then fp32) equals the
+    oracle's eq. (12) expansion rounded to fp32, bit for bit."""
+    nb = 70
+    Fg, Fo = lib_factors(nb, 31)
+    out = kq.kq_expand_blocks(dev(Fg), kq.KQ_K_FP32)
+    K = np_(out).view(np.float32).reshape(nb, 32, 32)
+    ref = O.expand_blocks(Fg.astype(np.float64)).astype(np.float32)
+    assert np.array_equal(K.view(np.uint32), ref.view(np.uint32))
+
+
+def test_blocked_layout_against_library_gemm():
+    """P8: the packed codes and the 128x4 scale tiles, handed to the
+    library's block-scaled MXFP4 GEMM (torch._scaled_mm), give the fp64
+    product of our own dequantized operands.  Skipped if this torch/cuBLAS
+    build has no MXFP4 GEMM."""
+    if not hasattr(torch, "float4_e2m1fn_x2") or not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("torch has no float4_e2m1fn_x2 / float8_e8m0fnu")
+    m, d, o = 256, 1152, 384
+    A_bits = synth.activations(m, d, 41, "pixart")
+    W_bits = synth.weights(o, d, seed=42, std=1.0)
+    Fg, _ = lib_factors(d // 32, 43)
+    qa, sfa, _ = run_kind("kron", A_bits, d, 1, Fg, y_debug=False)
+    qw, sfw, _ = run_kind("identity", W_bits, d, 1, None, y_debug=False)
+    nbp = -(-(d // 32) // 4) * 4
+    sa, sw = sfa.view(torch.float8_e8m0fnu), sfw.view(torch.float8_e8m0fnu)
+    out, errors = None, []
+    for shape_a, shape_w in (((-1,), (-1,)), ((-(-m // 128) * 128, nbp), (-(-o // 128) * 128, nbp))):
+        try:
+            out = torch._scaled_mm(qa.view(torch.float4_e2m1fn_x2),
+                                   qw.view(torch.float4_e2m1fn_x2).t(),
+                                   sa.reshape(shape_a), sw.reshape(shape_w),
+                                   out_dtype=torch.float32)
+            break
+        except (RuntimeError, TypeError, NotImplementedError, ValueError) as e:
+            errors.append(str(e)[:160])
+    if out is None:
+        pytest.skip(f"no MXFP4 block-scaled GEMM here: {errors}")
+    torch.cuda.synchronize()
+    Aq = np_(kq.kq_dequantize(qa, sfa, m, d, layout=1)).astype(np.float64)
+    Wq = np_(kq.kq_dequantize(qw, sfw, o, d, layout=1)).astype(np.float64)
+    ref = Aq @ Wq.T
+    got = np_(out).astype(np.float64)
+    scale = np.abs(Aq) @ np.abs(Wq).T
+    assert np.all(np.abs(got - ref) <= 1e-5 * scale + 1e-30), float(
+        (np.abs(got - ref) / (scale + 1e-30)).max())

@@ -1,0 +1,226 @@
+// Device-side building blocks of the KroQuant MXFP4 quantizer (sm_103a).
+//
+// Hand-written PTX for the Blackwell data path: mbarrier pipeline waits with
+// a time limit, 2-D TMA tile loads (cp.async.bulk.tensor), the fp32 -> E2M1
+// conversion (cvt.rn.satfinite.e2m1x2.f32) and packed fp32x2 arithmetic.
+//
+// MXFP4 rule ("KroQuant: Kronecker-Structured Block Transforms for Efficient
+// Post-Training Quantization of Diffusion Transformers", Sec. 3.1 and 4.1,
+// OCP MX v1.0): per 32-element block, e = floor(log2 amax) - 2 clamped to
+// [-127, 127], scale byte e + 127, codes = E2M1(y / 2^e) with round to
+// nearest even and saturation.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+namespace kq {
+
+// A wait that has not completed after this many nanoseconds gives up.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier ---------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes the initialised barriers visible to the async (TMA) proxy.
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Returns false if
+// it has not completed within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// ---- TMA ----------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2-D tiled load of the box at element coordinates (x, y) into shared memory,
+// completing `bytes` of transaction count on the barrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t x,
+                                            int32_t y, uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read exactly once (the activations): evict first.
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ---- loads / stores -------------------------------------------------------------
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float4 ldg_nc_f4(const float *p)
+{
+    float4 v;
+    asm("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p));
+    return v;
+}
+
+// Streaming 16-byte store (written once, not re-read by this kernel).
+__device__ __forceinline__ void stg128_cs(void *p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void stg_f4(float *p, float4 v)
+{
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+
+// ---- bf16 -> fp32 -------------------------------------------------------------------
+
+// A 32-bit word holds two bf16 values, element 2t in the low half.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// ---- MXFP4 epilogue -----------------------------------------------------------------
+
+// E8M0 byte of a block from its amax (>= 0, finite): with E the biased fp32
+// exponent field, floor(log2 amax) = E - 127 for normal amax, so
+// e + 127 = E - 2; zero, subnormal and E <= 2 amax all clamp to byte 0
+// (e = -127).  The largest finite amax gives 252 (e = 125).
+__device__ __forceinline__ uint32_t e8m0_byte(float amax)
+{
+    const int E = static_cast<int>(__float_as_uint(amax) >> 23);
+    return static_cast<uint32_t>(max(E - 2, 0));
+}
+
+// 2^-e as fp32 for scale byte b (e = b - 127): exponent field 254 - b, which
+// stays in [2, 254] for b in [0, 252], so the multiply y * 2^-e is exact.
+__device__ __forceinline__ float inv_scale(uint32_t byte)
+{
+    return __uint_as_float((254u - byte) << 23);
+}
+
+// Eight fp32 values -> eight E2M1 codes packed in a word, value 0 in bits 0-3.
+// cvt.rn.satfinite.e2m1x2.f32 d, a, b puts a in the high nibble of d and b in
+// the low nibble.
+__device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v3, float v4,
+                                           float v5, float v6, float v7)
+{
+    uint32_t out;
+    asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
+        "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
+        : "=r"(out)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
+    return out;
+}
+
+// Quantizes one 32-element block held as 16 float2 (y[2t], y[2t+1]).
+// Returns the packed codes (16 bytes) and writes the scale byte.
+__device__ __forceinline__ uint4 quantize_block(const float2 (&Y)[16], uint32_t &byte_out)
+{
+    float m0 = fmaxf(fabsf(Y[0].x), fabsf(Y[0].y));
+    float m1 = fmaxf(fabsf(Y[1].x), fabsf(Y[1].y));
+    float m2 = fmaxf(fabsf(Y[2].x), fabsf(Y[2].y));
+    float m3 = fmaxf(fabsf(Y[3].x), fabsf(Y[3].y));
+#pragma unroll
+    for (int t = 4; t < 16; t += 4) {
+        m0 = fmaxf(m0, fmaxf(fabsf(Y[t + 0].x), fabsf(Y[t + 0].y)));
+        m1 = fmaxf(m1, fmaxf(fabsf(Y[t + 1].x), fabsf(Y[t + 1].y)));
+        m2 = fmaxf(m2, fmaxf(fabsf(Y[t + 2].x), fabsf(Y[t + 2].y)));
+        m3 = fmaxf(m3, fmaxf(fabsf(Y[t + 3].x), fabsf(Y[t + 3].y)));
+    }
+    const float amax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+    const uint32_t byte = e8m0_byte(amax);
+    const float s = inv_scale(byte);
+    const float2 s2 = make_float2(s, s);
+    float2 V[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) V[t] = __fmul2_rn(Y[t], s2);
+    uint4 q;
+    q.x = e2m1x8(V[0].x, V[0].y, V[1].x, V[1].y, V[2].x, V[2].y, V[3].x, V[3].y);
+    q.y = e2m1x8(V[4].x, V[4].y, V[5].x, V[5].y, V[6].x, V[6].y, V[7].x, V[7].y);
+    q.z = e2m1x8(V[8].x, V[8].y, V[9].x, V[9].y, V[10].x, V[10].y, V[11].x, V[11].y);
+    q.w = e2m1x8(V[12].x, V[12].y, V[13].x, V[13].y, V[14].x, V[14].y, V[15].x, V[15].y);
+    byte_out = byte;
+    return q;
+}
+
+// Byte position of a scale in the 128x4 tiled layout of block-scaled MMA.
+__device__ __forceinline__ int64_t sf_blocked_offset(int64_t row, int64_t kb, int64_t ncb)
+{
+    const int64_t tile = (row >> 7) * ncb + (kb >> 2);
+    return tile * 512 + (row & 31) * 16 + ((row & 127) >> 5) * 4 + (kb & 3);
+}
+
+}  // namespace kq

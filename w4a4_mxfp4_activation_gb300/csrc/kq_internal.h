@@ -1,0 +1,62 @@
+// Internal declarations shared by the translation units of the library.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kq.h"
+
+namespace kq {
+
+enum Transform : int {
+    kKron = 0,      // five 2x2 factors per block, in-register butterfly
+    kDiag = 1,      // y = a * s[c]
+    kHadamard = 2,  // y = a . H32 / sqrt(32)
+    kIdentity = 3   // y = a
+};
+
+// Arguments of the TMA-fed quantizer kernels.
+struct QuantParams {
+    int64_t m;          // rows
+    int64_t m_rows;     // rows the grid covers (m, or m padded to 128 for the blocked layout)
+    int64_t d;          // channels
+    int64_t nb;         // d / 32
+    int64_t ncol_tiles; // ceil(nb / 4)
+    int64_t nrow_tiles; // ceil(m_rows / BR)
+    int64_t ntiles;
+    const float *factors;  // kKron: [nb][5][2][2]
+    const float *s;        // kDiag: [d]
+    uint8_t *q;
+    int64_t ldq;
+    uint8_t *sf;
+    int sf_layout;
+    int64_t ncb;        // ceil(nb / 4), for the blocked layout
+    float *y_debug;     // [m][d] or null
+};
+
+// Per-device facts the launchers need.
+struct DeviceInfo {
+    int sm_count;
+    bool supported;  // compute capability 10.3
+};
+
+kq_status device_info(DeviceInfo &info);
+kq_status make_tensor_map_2d_bf16(CUtensorMap *map, const void *base, int64_t rows, int64_t cols,
+                                  int64_t ld_elems, uint32_t box_cols, uint32_t box_rows);
+kq_status check_launch();
+
+kq_status launch_quant_tma(Transform t, const uint16_t *A, int64_t lda, const QuantParams &p,
+                           cudaStream_t stream);
+kq_status launch_quant_mma(const uint16_t *A, int64_t lda, const void *K_expanded,
+                           const QuantParams &p, cudaStream_t stream);
+
+kq_status validate_quant_args(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                              const uint8_t *q, int64_t ldq, const uint8_t *sf,
+                              kq_sf_layout layout, const float *y_debug);
+void fill_quant_params(QuantParams &p, int64_t m, int64_t d, int64_t rows_per_tile, uint8_t *q,
+                       int64_t ldq, uint8_t *sf, kq_sf_layout layout, float *y_debug);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace kq
