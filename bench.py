@@ -60,6 +60,11 @@ def parse_args():
                     help="skip the diagonal / Hadamard / bare-quantizer side measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU time budget of the oracle baseline sample")
+    ap.add_argument("--profile", choices=("kroquant", "diag", "hadamard", "identity"),
+                    help="profiling case for ncu: run one quantizer a few times and exit")
+    ap.add_argument("--m", type=int, default=9216, help="rows of the profiling case")
+    ap.add_argument("--d", type=int, default=12288, help="channels of the profiling case")
+    ap.add_argument("--launches", type=int, default=3, help="launches of the profiling case")
     return ap.parse_args()
 
 
@@ -446,8 +451,42 @@ def run_ours(args, dist: Dist):
         print(json.dumps(line), flush=True)
 
 
+def run_profile_case(args):
+    """A few launches of one quantizer on one synthetic layer (for ncu)."""
+    import numpy as np
+    import torch
+    from w4a4_mxfp4_activation_gb300 import kq, synth
+    m, d = args.m, args.d
+    bits = synth.activations(m, d, synth.SEED_A + 3, "flux")
+    A = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    F = torch.from_numpy(kq.kq_lu_to_factors(synth.lu_params(d // 32, 7), +1)).cuda()
+    s = torch.from_numpy(synth.smooth_scales(d)).cuda()
+    layout = kq.KQ_SF_BLOCKED_128x4
+    q = torch.empty((m, d // 2), dtype=torch.uint8, device="cuda")
+    sf = torch.empty(kq.kq_sf_bytes(m, d, layout), dtype=torch.uint8, device="cuda")
+    KX = kq.kq_expand_blocks(F, kq.KQ_K_BF16X3) if args.variant == "mma" else None
+    for _ in range(args.launches):
+        if args.profile == "kroquant":
+            kq.kq_quantize_mxfp4(A, d, factors=F if KX is None else None, K_expanded=KX,
+                                 layout=layout, q=q, sf=sf,
+                                 variant=kq.VARIANT_MMA if KX is not None else None)
+        elif args.profile == "diag":
+            kq.kq_smooth_quantize_mxfp4(A, s, d, layout=layout, q=q, sf=sf)
+        elif args.profile == "hadamard":
+            kq.kq_hadamard_quantize_mxfp4(A, d, layout=layout, q=q, sf=sf)
+        else:
+            kq.kq_quantize_mxfp4(A, d, layout=layout, q=q, sf=sf)
+    torch.cuda.synchronize()
+    print(f"profile case done: {args.profile} m={m} d={d} launches={args.launches}")
+
+
 def main():
     args = parse_args()
+    if args.profile:
+        from w4a4_mxfp4_activation_gb300 import build
+        build.build()
+        run_profile_case(args)
+        return
     if args.impl == "reference":
         dist = Dist(use_cuda=False) if int(os.environ.get("WORLD_SIZE", "1")) > 1 else Dist(False)
         try:

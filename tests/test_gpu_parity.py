@@ -296,9 +296,14 @@ def test_special_values():
     # the special rows pass through the identity exactly: no flags needed
     codes = parity.unpack(np_(q), 32)
     assert (codes[0] == 0).all() and (codes[1] == 8).all() and (np_(sf)[:2] == 0).all()
+    # the Kronecker transform may grow values by up to sum_r |K_rc|; keep y
+    # inside the fp32 range (larger y is outside the contract)
+    y_k = y.copy()
+    y_k[4] /= 2.0 ** 8
+    bits_k = synth.f64_to_bf16_bits(y_k)
     Fg, Fo = lib_factors(1, 3)
-    q, sf, yd = run_kind("kron", bits, 32, 0, Fg)
-    parity.check(bits, 32, "kron", Fo, 0, np_(q), np_(sf), np_(yd))
+    q, sf, yd = run_kind("kron", bits_k, 32, 0, Fg)
+    parity.check(bits_k, 32, "kron", Fo, 0, np_(q), np_(sf), np_(yd))
 
 
 def test_raw_factor_interface():
@@ -364,22 +369,29 @@ def test_blocked_layout_against_library_gemm():
     nbp = -(-(d // 32) // 4) * 4
     sa, sw = sfa.view(torch.float8_e8m0fnu), sfw.view(torch.float8_e8m0fnu)
     out, errors = None, []
-    for shape_a, shape_w in (((-1,), (-1,)), ((-(-m // 128) * 128, nbp), (-(-o // 128) * 128, nbp))):
-        try:
-            out = torch._scaled_mm(qa.view(torch.float4_e2m1fn_x2),
-                                   qw.view(torch.float4_e2m1fn_x2).t(),
-                                   sa.reshape(shape_a), sw.reshape(shape_w),
-                                   out_dtype=torch.float32)
+    for shape_a, shape_w in (((-(-m // 128) * 128, nbp), (-(-o // 128) * 128, nbp)),
+                             ((-1,), (-1,))):
+        for out_dtype in (torch.bfloat16, torch.float32):
+            try:
+                out = torch._scaled_mm(qa.view(torch.float4_e2m1fn_x2),
+                                       qw.view(torch.float4_e2m1fn_x2).t(),
+                                       sa.reshape(shape_a), sw.reshape(shape_w),
+                                       out_dtype=out_dtype)
+                break
+            except (RuntimeError, TypeError, NotImplementedError, ValueError) as e:
+                errors.append(str(e)[-300:])
+        if out is not None:
             break
-        except (RuntimeError, TypeError, NotImplementedError, ValueError) as e:
-            errors.append(str(e)[:160])
     if out is None:
         pytest.skip(f"no MXFP4 block-scaled GEMM here: {errors}")
     torch.cuda.synchronize()
     Aq = np_(kq.kq_dequantize(qa, sfa, m, d, layout=1)).astype(np.float64)
     Wq = np_(kq.kq_dequantize(qw, sfw, o, d, layout=1)).astype(np.float64)
     ref = Aq @ Wq.T
-    got = np_(out).astype(np.float64)
+    got = out.float().cpu().numpy().astype(np.float64)
     scale = np.abs(Aq) @ np.abs(Wq).T
-    assert np.all(np.abs(got - ref) <= 1e-5 * scale + 1e-30), float(
+    tol = 1e-5 if out.dtype == torch.float32 else 2 ** -7
+    assert np.all(np.abs(got - ref) <= tol * scale + 1e-30), float(
         (np.abs(got - ref) / (scale + 1e-30)).max())
+    assert np.linalg.norm(got - ref) <= (1e-6 if out.dtype == torch.float32 else 1e-2) * \
+        np.linalg.norm(ref)

@@ -44,9 +44,11 @@ __device__ __forceinline__ void mbar_fence_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Release arrive: this thread's earlier shared-memory reads of the guarded
+// buffer happen before the arrival is observed.
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
@@ -114,7 +116,8 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
+                 : "r"(addr)
+                 : "memory");
     return v;
 }
 

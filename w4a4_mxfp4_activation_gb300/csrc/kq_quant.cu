@@ -208,12 +208,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint4 w[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) w[k] = lds128(rowaddr + ((((h << 2) | k) ^ (r & 7)) << 4));
-            if (g + kConsumerWarps >= BR / 8) mbar_arrive(bar_empty + 8 * s);
+            const bool last = g + kConsumerWarps >= BR / 8;
 
             const int64_t row = rt * BR + r;
             if (j >= p.nb) {
                 // block-column padding of the tiled scale layout
                 if (p.sf_layout != KQ_SF_ROWMAJOR) store_scale(p, row, j, 0u);
+                if (last) mbar_arrive(bar_empty + 8 * s);
                 continue;
             }
             float2 Y[16];
@@ -236,6 +237,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             const uint4 codes = quantize_block(Y, byte);
             if (row < p.m) stg128_cs(p.q + row * p.ldq + j * 16, codes);
             store_scale(p, row, j, byte);
+            // Release the stage only after this item's results are stored:
+            // the stores consume the loaded words, so the reads are complete.
+            if (last) mbar_arrive(bar_empty + 8 * s);
         }
     }
 }
