@@ -284,7 +284,6 @@ def run_ours(args, dist: Dist):
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.Stream(device=dev)
     layout = kq.KQ_SF_BLOCKED_128x4
-    variant = kq.VARIANT_BUTTERFLY if args.variant == "butterfly" else kq.VARIANT_MMA
 
     # ---- inputs resident in HBM: SETS rotating sets per layer
     A, Q, SF, F, KX = [], [], [], [], []
@@ -300,15 +299,19 @@ def run_ours(args, dist: Dist):
                    for _ in range(SETS)])
         fac = kq.kq_lu_to_factors(synth.lu_params(d // 32, synth.SEED_FACTORS + 3 + li), +1)
         F.append(torch.from_numpy(fac).to(dev))
-        KX.append(kq.kq_expand_blocks(F[-1], kq.KQ_K_BF16X3) if variant == kq.VARIANT_MMA else None)
+        KX.append(kq.kq_expand_blocks(F[-1], kq.KQ_K_BF16X3))
     torch.cuda.synchronize()
 
     def launch(kind, li, s):
         _, m, d = LAYERS[li]
         if kind == "kroquant":
-            kq.kq_quantize_mxfp4(A[li][s], d, factors=F[li] if variant == 0 else None,
-                                 K_expanded=KX[li], layout=layout, q=Q[li][s], sf=SF[li][s],
-                                 variant=variant, stream=stream)
+            kind = args.variant
+        if kind == "butterfly":
+            kq.kq_quantize_mxfp4(A[li][s], d, factors=F[li], layout=layout, q=Q[li][s],
+                                 sf=SF[li][s], variant=kq.VARIANT_BUTTERFLY, stream=stream)
+        elif kind == "mma":
+            kq.kq_quantize_mxfp4(A[li][s], d, K_expanded=KX[li], layout=layout, q=Q[li][s],
+                                 sf=SF[li][s], variant=kq.VARIANT_MMA, stream=stream)
         elif kind == "diag":
             kq.kq_smooth_quantize_mxfp4(A[li][s], DIAG[li], d, layout=layout, q=Q[li][s],
                                         sf=SF[li][s], stream=stream)
@@ -388,9 +391,11 @@ def run_ours(args, dist: Dist):
     baselines = {}
     if not args.no_baselines:
         nb_steps = max(3, min(K, 4000))
-        for kind in ("diag", "hadamard", "identity"):
+        other = "mma" if args.variant == "butterfly" else "butterfly"
+        for kind in (other, "diag", "hadamard", "identity"):
             bms, _, _ = timed(kind, nb_steps, 3)
-            baselines[kind] = round(STEP_BYTES * nb_steps / (dist.max(bms) * 1e-3) / 1e9, 2)
+            name = f"kroquant_{kind}" if kind in ("mma", "butterfly") else kind
+            baselines[name] = round(STEP_BYTES * nb_steps / (dist.max(bms) * 1e-3) / 1e9, 2)
 
     # ---- end to end through the public call with host buffers
     e2e_steps = max(3, min(K, 100))

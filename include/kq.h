@@ -81,8 +81,11 @@ typedef enum kq_sf_layout {
 
 typedef enum kq_kfmt {
     KQ_K_FP32 = 0,      /* dense K_j, fp32 row-major [nb][32][32] */
-    KQ_K_BF16X3 = 1     /* K_j as three bf16 terms hi + mid + lo, in the operand
-                           order of the tensor-core variant (opaque) */
+    KQ_K_BF16X3 = 1     /* operand records of the tensor-core variant (opaque,
+                           1552 bytes per block): K_j = G1 (x) K'_j with
+                           K'_j = G2 (x) G3 (x) G4 (x) G5 expanded to its dense
+                           16x16 block as three bf16 terms hi + mid + lo in
+                           mma fragment order, plus G1 in fp32 */
 } kq_kfmt;
 
 /* Alignment rules shared by the quantizer entry points:
@@ -99,7 +102,9 @@ typedef enum kq_kfmt {
  *   K_expanded device, output of kq_expand_blocks(..., KQ_K_BF16X3, ...), or
  *              NULL.  With factors != NULL the five 2x2 factors are applied
  *              as an in-register butterfly; with factors == NULL and
- *              K_expanded != NULL the dense blocks run on the tensor cores;
+ *              K_expanded != NULL the pre-expanded blocks run on the tensor
+ *              cores (mma.sync: the dense 16x16 G2..G5 part in bf16 terms,
+ *              then the G1 stage in fp32);
  *              with both NULL the transform is the identity (the bare
  *              quantizer, "Q4" of [KQ] Tables 3 and 4).
  *   q, ldq     device, packed codes [m][ldq] (written)
@@ -141,7 +146,8 @@ KQ_API kq_status kq_hadamard_quantize_mxfp4(const uint16_t *A, int64_t m, int64_
  * computed in fp64 and then rounded to the requested format.
  *   factors  device fp32 [nb][5][2][2]
  *   nb       number of 32-channel blocks (> 0)
- *   fmt      KQ_K_FP32 (row-major [nb][32][32] fp32) or KQ_K_BF16X3
+ *   fmt      KQ_K_FP32 (row-major [nb][32][32] fp32) or KQ_K_BF16X3 (the
+ *            tensor-core operand records consumed by kq_quantize_mxfp4)
  *   K_out    device, kq_expanded_bytes(nb, fmt) bytes, 16-byte aligned
  */
 KQ_API kq_status kq_expand_blocks(const float *factors, int64_t nb, kq_kfmt fmt, void *K_out,

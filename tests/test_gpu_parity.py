@@ -54,6 +54,10 @@ def lib_factors(nb, seed, sign=+1):
 
 def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None, q=None, sf=None):
     A = to_bf16(A_bits)
+    if kind == "kron_mma":
+        records = kq.kq_expand_blocks(dev(param_gpu), kq.KQ_K_BF16X3)
+        return kq.kq_quantize_mxfp4(A, d, K_expanded=records, layout=layout, y_debug=y_debug,
+                                    q=q, sf=sf)
     if kind == "kron":
         return kq.kq_quantize_mxfp4(A, d, factors=dev(param_gpu), layout=layout, y_debug=y_debug,
                                     variant=variant, q=q, sf=sf)
@@ -67,9 +71,13 @@ def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None
     raise ValueError(kind)
 
 
+def oracle_kind(kind):
+    return "kron" if kind == "kron_mma" else kind
+
+
 def params_for(kind, nb, d, seed):
     """(gpu param, oracle param) for a transform kind."""
-    if kind == "kron":
+    if kind in ("kron", "kron_mma"):
         return lib_factors(nb, seed)
     if kind == "diag":
         s = synth.smooth_scales(d)
@@ -125,7 +133,7 @@ CASES = synth.CONFIG0 + synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3
 
 
 @pytest.mark.parametrize("name,m,d,model,cfg", CASES, ids=[c[0] for c in CASES])
-@pytest.mark.parametrize("kind", ["kron", "diag", "hadamard", "identity"])
+@pytest.mark.parametrize("kind", ["kron", "kron_mma", "diag", "hadamard", "identity"])
 def test_config_parity(name, m, d, model, cfg, kind):
     """Configs 0-3 at full size, both scale layouts (flux shapes compare a
     seeded sample of rows, always including the first and last tiles)."""
@@ -139,11 +147,28 @@ def test_config_parity(name, m, d, model, cfg, kind):
                                          rng.choice(m, 700, replace=False)]))
     for layout in (0, 1):
         q, sf, y = run_kind(kind, A_bits, d, layout, pg)
-        res = parity.check(A_bits, d, kind, po, layout, np_(q), np_(sf), np_(y), rows)
+        res = parity.check(A_bits, d, oracle_kind(kind), po, layout, np_(q), np_(sf), np_(y), rows)
         # the production launch (no debug output) writes the same bytes
         q2, sf2, _ = run_kind(kind, A_bits, d, layout, pg, y_debug=False)
         assert torch.equal(q, q2) and torch.equal(sf, sf2)
         print(name, kind, layout, res)
+
+
+def test_mma_matches_butterfly_outside_flags():
+    """The tensor-core and the butterfly implementations of the same
+    transform agree on every unflagged code (both are checked against the
+    oracle elsewhere)."""
+    m, d = 4096, 4608
+    A_bits = synth.activations(m, d, synth.SEED_A + 1, "pixart")
+    Fg, Fo = lib_factors(d // 32, synth.SEED_FACTORS + 1)
+    qb, sfb, _ = run_kind("kron", A_bits, d, 1, Fg, y_debug=False)
+    qm, sfm, _ = run_kind("kron_mma", A_bits, d, 1, Fg, y_debug=False)
+    rows = np.arange(0, m, 7)
+    _, _, flags = O.quantize(*O.transform(np.ascontiguousarray(A_bits[rows]), d, "kron", Fo),
+                             O.SF_ROWMAJOR)
+    strict = flags == 0
+    cb, cm = parity.unpack(np_(qb)[rows], d), parity.unpack(np_(qm)[rows], d)
+    assert np.array_equal(cb[strict], cm[strict])
 
 
 def test_hadamard_factors_config0():
@@ -230,7 +255,8 @@ def test_sweep_parity(m, d):
                                          rng.choice(m, 400, replace=False)]))
     for layer in range(4):
         Fg, Fo = lib_factors(nb, synth.SEED_FACTORS + 4 + layer)
-        q, sf, y = run_kind("kron", A_bits, d, layer % 2, Fg)
+        kind = "kron" if layer < 2 else "kron_mma"
+        q, sf, y = run_kind(kind, A_bits, d, layer % 2, Fg)
         parity.check(A_bits, d, "kron", Fo, layer % 2, np_(q), np_(sf), np_(y), rows)
     s = synth.smooth_scales(d)
     q, sf, y = run_kind("diag", A_bits, d, 1, s)
@@ -245,7 +271,7 @@ EDGE_SHAPES = [(1, 32), (7, 96), (127, 160), (129, 64), (200, 5600), (3, 2240), 
 
 
 @pytest.mark.parametrize("m,d", EDGE_SHAPES, ids=[f"{m}x{d}" for m, d in EDGE_SHAPES])
-@pytest.mark.parametrize("kind", ["kron", "diag", "hadamard", "identity"])
+@pytest.mark.parametrize("kind", ["kron", "kron_mma", "diag", "hadamard", "identity"])
 def test_ragged_shapes_with_pitches_and_canaries(m, d, kind):
     """Ragged m and d (partial tiles and block-columns), lda > d, ldq > d/2,
     and guard bytes around every output that must stay untouched."""
@@ -265,8 +291,8 @@ def test_ragged_shapes_with_pitches_and_canaries(m, d, kind):
         assert (qs[1:m + 1, d // 2:] == 0xA5).all(), "row padding of q overwritten"
         ss = np_(sf_store)
         assert (ss[:16] == 0xA5).all() and (ss[16 + sfb:] == 0xA5).all()
-        parity.check(np.ascontiguousarray(A_bits[:, :d]), d, kind, po, layout, np_(q)[:, :d // 2],
-                     np_(sf), np_(y))
+        parity.check(np.ascontiguousarray(A_bits[:, :d]), d, oracle_kind(kind), po, layout,
+                     np_(q)[:, :d // 2], np_(sf), np_(y))
         if layout == 1:
             # padding of the tiled layout is written as zero
             full = np.zeros(sfb, bool)
@@ -302,8 +328,9 @@ def test_special_values():
     y_k[4] /= 2.0 ** 8
     bits_k = synth.f64_to_bf16_bits(y_k)
     Fg, Fo = lib_factors(1, 3)
-    q, sf, yd = run_kind("kron", bits_k, 32, 0, Fg)
-    parity.check(bits_k, 32, "kron", Fo, 0, np_(q), np_(sf), np_(yd))
+    for kind in ("kron", "kron_mma"):
+        q, sf, yd = run_kind(kind, bits_k, 32, 0, Fg)
+        parity.check(bits_k, 32, "kron", Fo, 0, np_(q), np_(sf), np_(yd))
 
 
 def test_raw_factor_interface():
@@ -313,8 +340,9 @@ def test_raw_factor_interface():
     nb = d // 32
     A_bits = synth.activations(m, d, 9, "sana")
     F = synth.random_factors(nb, 12, scale=0.8)
-    q, sf, y = run_kind("kron", A_bits, d, 1, F)
-    parity.check(A_bits, d, "kron", F.astype(np.float64), 1, np_(q), np_(sf), np_(y))
+    for kind in ("kron", "kron_mma"):
+        q, sf, y = run_kind(kind, A_bits, d, 1, F)
+        parity.check(A_bits, d, "kron", F.astype(np.float64), 1, np_(q), np_(sf), np_(y))
     Fg, Fo = lib_factors(nb, 13, sign=-1)
     q, sf, y = run_kind("kron", A_bits, d, 0, Fg)
     parity.check(A_bits, d, "kron", Fo, 0, np_(q), np_(sf), np_(y))

@@ -160,7 +160,7 @@ __global__ void dequant_kernel(const uint8_t *__restrict__ q, int64_t ldq,
 }
 
 // Dense K_j by eq. (12), one thread per entry, product in fp64.
-__global__ void expand_kernel(const float *__restrict__ factors, int64_t nb, int fmt,
+__global__ void expand_kernel(const float *__restrict__ factors, int64_t nb,
                               void *__restrict__ out)
 {
     const int64_t n = nb * 1024;
@@ -175,20 +175,7 @@ __global__ void expand_kernel(const float *__restrict__ factors, int64_t nb, int
             const int bit = 4 - t;
             k *= static_cast<double>(f[t * 4 + ((r >> bit) & 1) * 2 + ((c >> bit) & 1)]);
         }
-        if (fmt == KQ_K_FP32) {
-            static_cast<float *>(out)[idx] = static_cast<float>(k);
-        } else {
-            // three bf16 terms hi + mid + lo; term t of block j at
-            // [j][t][r][c] (row-major per term)
-            const __nv_bfloat16 hi = __double2bfloat16(k);
-            const double r1 = k - static_cast<double>(__bfloat162float(hi));
-            const __nv_bfloat16 mid = __double2bfloat16(r1);
-            const __nv_bfloat16 lo = __double2bfloat16(r1 - static_cast<double>(__bfloat162float(mid)));
-            __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(out) + j * 3072 + r * 32 + c;
-            o[0] = hi;
-            o[1024] = mid;
-            o[2048] = lo;
-        }
+        static_cast<float *>(out)[idx] = static_cast<float>(k);
     }
 }
 
@@ -323,8 +310,8 @@ kq_status kq_expand_blocks(const float *factors, int64_t nb, kq_kfmt fmt, void *
     DeviceInfo info;
     kq_status st = device_info(info);
     if (st != KQ_OK) return st;
-    expand_kernel<<<grid_for(nb * 1024, 256), 256, 0, stream>>>(factors, nb, static_cast<int>(fmt),
-                                                                K_out);
+    if (fmt == KQ_K_BF16X3) return launch_mma_records(factors, nb, K_out, stream);
+    expand_kernel<<<grid_for(nb * 1024, 256), 256, 0, stream>>>(factors, nb, K_out);
     return check_launch();
 }
 
