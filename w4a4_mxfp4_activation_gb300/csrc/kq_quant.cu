@@ -38,12 +38,31 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;
 
-template <int BR, int STAGES>
+// Per-block parameter bytes a tile stages next to its activations.
+template <int T>
+__host__ __device__ constexpr int param_bytes_per_block()
+{
+    return T == kKron ? 80 : (T == kDiag ? 128 : 0);   // 5 factors / 32 scales
+}
+
+// Shared-memory stride between the staged parameters of the tile's blocks.
+// The two blocks a quarter-warp reads must not start 128 bytes apart (same
+// banks): the 32 scales of the diagonal kernel sit 144 bytes apart.
+template <int T>
+__host__ __device__ constexpr int param_stride()
+{
+    return T == kDiag ? 144 : param_bytes_per_block<T>();
+}
+
+template <int T, int BR, int STAGES>
 struct TileCfg {
     static constexpr int kBoxBytes = BR * 128;           // BR rows x 64 bf16
-    static constexpr int kStageBytes = 2 * kBoxBytes;    // 128 channels
+    static constexpr int kABytes = 2 * kBoxBytes;        // 128 channels
+    static constexpr int kParamBytes = param_bytes_per_block<T>() > 0 ? 1024 : 0;
+    static constexpr int kStageBytes = kABytes + kParamBytes;
     static constexpr int kSmemBytes = STAGES * kStageBytes + 1024 + 2 * STAGES * 8;
     static_assert(BR % 8 == 0 && BR <= 256, "box rows");
+    static_assert(4 * param_stride<T>() <= kParamBytes, "parameter area");
 };
 
 __device__ __forceinline__ float2 swap2(float2 a) { return make_float2(a.y, a.x); }
@@ -73,23 +92,29 @@ __device__ __forceinline__ void butterfly_inpair(float2 (&Y)[16], float4 g)
     for (int t = 0; t < 16; ++t) Y[t] = __ffma2_rn(swap2(Y[t]), d1, __fmul2_rn(Y[t], d0));
 }
 
+__device__ __forceinline__ float4 lds_f4(uint32_t addr)
+{
+    const uint4 v = lds128(addr);
+    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                       __uint_as_float(v.w));
+}
+
+// `prm`: shared-memory address of this block's staged parameters.
 template <int T>
-__device__ __forceinline__ void apply_transform(float2 (&Y)[16], const QuantParams &p, int64_t j)
+__device__ __forceinline__ void apply_transform(float2 (&Y)[16], uint32_t prm)
 {
     if constexpr (T == kKron) {
-        const float *f = p.factors + j * 20;
-        const float4 g1 = ldg_nc_f4(f), g2 = ldg_nc_f4(f + 4), g3 = ldg_nc_f4(f + 8);
-        const float4 g4 = ldg_nc_f4(f + 12), g5 = ldg_nc_f4(f + 16);
+        const float4 g1 = lds_f4(prm), g2 = lds_f4(prm + 16), g3 = lds_f4(prm + 32);
+        const float4 g4 = lds_f4(prm + 48), g5 = lds_f4(prm + 64);
         butterfly_inpair(Y, g5);      // G5: bit 0
         butterfly_cross<1>(Y, g4);    // G4: bit 1
         butterfly_cross<2>(Y, g3);    // G3: bit 2
         butterfly_cross<4>(Y, g2);    // G2: bit 3
         butterfly_cross<8>(Y, g1);    // G1: bit 4
     } else if constexpr (T == kDiag) {
-        const float *s = p.s + j * 32;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const float4 v = ldg_nc_f4(s + 4 * k);
+            const float4 v = lds_f4(prm + 16 * k);
             Y[2 * k] = __fmul2_rn(Y[2 * k], make_float2(v.x, v.y));
             Y[2 * k + 1] = __fmul2_rn(Y[2 * k + 1], make_float2(v.z, v.w));
         }
@@ -145,7 +170,7 @@ template <int T, int BR, int STAGES>
 __global__ void __launch_bounds__(kThreads, 2)
     quant_tma_kernel(const __grid_constant__ CUtensorMap tmA, const QuantParams p)
 {
-    using Cfg = TileCfg<BR, STAGES>;
+    using Cfg = TileCfg<T, BR, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;   // 128B-swizzle atoms: 1 KB
     const uint32_t bar_full = base + STAGES * Cfg::kStageBytes;
@@ -173,11 +198,28 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (it >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1u)) break;
             const int64_t rt = tile / p.ncol_tiles, ct = tile % p.ncol_tiles;
             const uint32_t dst = base + s * Cfg::kStageBytes;
-            mbar_arrive_expect_tx(bar_full + 8 * s, Cfg::kStageBytes);
+            uint32_t pbytes = 0;
+            const void *psrc = nullptr;
+            if constexpr (param_bytes_per_block<T>() > 0) {
+                const int64_t left = p.nb - ct * 4;
+                pbytes = static_cast<uint32_t>((left < 4 ? left : 4) * param_bytes_per_block<T>());
+                psrc = (T == kKron) ? static_cast<const void *>(p.factors + ct * 4 * 20)
+                                    : static_cast<const void *>(p.s + ct * 4 * 32);
+            }
+            mbar_arrive_expect_tx(bar_full + 8 * s, Cfg::kABytes + pbytes);
             tma_load_2d(dst, &tmA, static_cast<int32_t>(ct * 128), static_cast<int32_t>(rt * BR),
                         bar_full + 8 * s, pol);
             tma_load_2d(dst + Cfg::kBoxBytes, &tmA, static_cast<int32_t>(ct * 128 + 64),
                         static_cast<int32_t>(rt * BR), bar_full + 8 * s, pol);
+            if constexpr (param_stride<T>() == param_bytes_per_block<T>()) {
+                if (pbytes) bulk_load(dst + Cfg::kABytes, psrc, pbytes, bar_full + 8 * s);
+            } else {
+                // one copy per block into its padded slot
+                const uint32_t per = param_bytes_per_block<T>();
+                for (uint32_t off = 0, b = 0; off < pbytes; off += per, ++b)
+                    bulk_load(dst + Cfg::kABytes + b * param_stride<T>(),
+                              static_cast<const uint8_t *>(psrc) + off, per, bar_full + 8 * s);
+            }
         }
         // Do not leave while loads into this CTA's shared memory may be in
         // flight: wait (bounded) for the last ring's worth of them.
@@ -201,6 +243,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int64_t rt = tile / p.ncol_tiles, ct = tile % p.ncol_tiles;
         const int64_t j = ct * 4 + box * 2 + h;
         const uint32_t stage = base + s * Cfg::kStageBytes + box * Cfg::kBoxBytes;
+        const uint32_t prm = base + s * Cfg::kStageBytes + Cfg::kABytes +
+                             (box * 2 + h) * param_stride<T>();
 #pragma unroll 1
         for (int g = cw; g < BR / 8; g += kConsumerWarps) {
             const int r = g * 8 + rhi * 4 + rlo;
@@ -225,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 Y[4 * k + 2] = make_float2(bf16_lo(w[k].z), bf16_hi(w[k].z));
                 Y[4 * k + 3] = make_float2(bf16_lo(w[k].w), bf16_hi(w[k].w));
             }
-            apply_transform<T>(Y, p, j);
+            apply_transform<T>(Y, prm);
             if (p.y_debug != nullptr && row < p.m) {
                 float *yd = p.y_debug + row * p.d + j * 32;
 #pragma unroll
@@ -256,7 +300,7 @@ struct KernelSlot {
 template <int T, int BR, int STAGES>
 kq_status launch_one(const CUtensorMap &map, QuantParams p, int sm_count, cudaStream_t stream)
 {
-    using Cfg = TileCfg<BR, STAGES>;
+    using Cfg = TileCfg<T, BR, STAGES>;
     auto kern = quant_tma_kernel<T, BR, STAGES>;
     static KernelSlot slot;
     int dev = 0;
