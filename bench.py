@@ -55,7 +55,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=40000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--variant", choices=("butterfly", "mma"), default="butterfly")
+    ap.add_argument("--variant", choices=("butterfly", "mma", "umma"), default="butterfly")
     ap.add_argument("--no-baselines", action="store_true",
                     help="skip the diagonal / Hadamard / bare-quantizer side measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -312,6 +312,9 @@ def run_ours(args, dist: Dist):
         elif kind == "mma":
             kq.kq_quantize_mxfp4(A[li][s], d, K_expanded=KX[li], layout=layout, q=Q[li][s],
                                  sf=SF[li][s], variant=kq.VARIANT_MMA, stream=stream)
+        elif kind == "umma":
+            kq.kq_quantize_mxfp4(A[li][s], d, K_expanded=KX[li], layout=layout, q=Q[li][s],
+                                 sf=SF[li][s], variant=kq.VARIANT_UMMA, stream=stream)
         elif kind == "diag":
             kq.kq_smooth_quantize_mxfp4(A[li][s], DIAG[li], d, layout=layout, q=Q[li][s],
                                         sf=SF[li][s], stream=stream)
@@ -391,10 +394,10 @@ def run_ours(args, dist: Dist):
     baselines = {}
     if not args.no_baselines:
         nb_steps = max(3, min(K, 4000))
-        other = "mma" if args.variant == "butterfly" else "butterfly"
-        for kind in (other, "diag", "hadamard", "identity"):
+        others = [v for v in ("butterfly", "mma", "umma") if v != args.variant]
+        for kind in (*others, "diag", "hadamard", "identity"):
             bms, _, _ = timed(kind, nb_steps, 3)
-            name = f"kroquant_{kind}" if kind in ("mma", "butterfly") else kind
+            name = f"kroquant_{kind}" if kind in ("mma", "butterfly", "umma") else kind
             baselines[name] = round(STEP_BYTES * nb_steps / (dist.max(bms) * 1e-3) / 1e9, 2)
 
     # ---- end to end through the public call with host buffers
@@ -469,12 +472,13 @@ def run_profile_case(args):
     layout = kq.KQ_SF_BLOCKED_128x4
     q = torch.empty((m, d // 2), dtype=torch.uint8, device="cuda")
     sf = torch.empty(kq.kq_sf_bytes(m, d, layout), dtype=torch.uint8, device="cuda")
-    KX = kq.kq_expand_blocks(F, kq.KQ_K_BF16X3) if args.variant == "mma" else None
+    KX = kq.kq_expand_blocks(F, kq.KQ_K_BF16X3) if args.variant in ("mma", "umma") else None
+    variant = {"butterfly": kq.VARIANT_BUTTERFLY, "mma": kq.VARIANT_MMA,
+               "umma": kq.VARIANT_UMMA}[args.variant]
     for _ in range(args.launches):
         if args.profile == "kroquant":
             kq.kq_quantize_mxfp4(A, d, factors=F if KX is None else None, K_expanded=KX,
-                                 layout=layout, q=q, sf=sf,
-                                 variant=kq.VARIANT_MMA if KX is not None else None)
+                                 layout=layout, q=q, sf=sf, variant=variant)
         elif args.profile == "diag":
             kq.kq_smooth_quantize_mxfp4(A, s, d, layout=layout, q=q, sf=sf)
         elif args.profile == "hadamard":

@@ -81,11 +81,12 @@ typedef enum kq_sf_layout {
 
 typedef enum kq_kfmt {
     KQ_K_FP32 = 0,      /* dense K_j, fp32 row-major [nb][32][32] */
-    KQ_K_BF16X3 = 1     /* operand records of the tensor-core variant (opaque,
-                           1552 bytes per block): K_j = G1 (x) K'_j with
+    KQ_K_BF16X3 = 1     /* operand records of the tensor-core variants (opaque,
+                           2 x 1552 bytes per block): K_j = G1 (x) K'_j with
                            K'_j = G2 (x) G3 (x) G4 (x) G5 expanded to its dense
-                           16x16 block as three bf16 terms hi + mid + lo in
-                           mma fragment order, plus G1 in fp32 */
+                           16x16 block as three bf16 terms hi + mid + lo, once
+                           in the tcgen05 shared-memory operand layout and once
+                           in mma.sync fragment order, each with G1 in fp32 */
 } kq_kfmt;
 
 /* Alignment rules shared by the quantizer entry points:
@@ -103,8 +104,8 @@ typedef enum kq_kfmt {
  *              NULL.  With factors != NULL the five 2x2 factors are applied
  *              as an in-register butterfly; with factors == NULL and
  *              K_expanded != NULL the pre-expanded blocks run on the tensor
- *              cores (mma.sync: the dense 16x16 G2..G5 part in bf16 terms,
- *              then the G1 stage in fp32);
+ *              cores (tcgen05.mma with TMEM accumulators: the dense 16x16
+ *              G2..G5 part in bf16 terms, then the G1 stage in fp32);
  *              with both NULL the transform is the identity (the bare
  *              quantizer, "Q4" of [KQ] Tables 3 and 4).
  *   q, ldq     device, packed codes [m][ldq] (written)
@@ -201,8 +202,10 @@ KQ_API kq_status kq_invert_transpose_factors(const float *factors, int64_t nb, f
  *
  * kq_quantize_mxfp4_variant -- kq_quantize_mxfp4 with the block-transform
  *   implementation chosen explicitly: variant 0 = in-register butterfly
- *   from the raw factors (needs factors), 1 = tensor-core mma.sync on the
- *   pre-expanded blocks (needs K_expanded), 2 = identity.
+ *   from the raw factors (needs factors), 1 = warp-level mma.sync on the
+ *   pre-expanded operand records (needs K_expanded), 2 = identity,
+ *   3 = tcgen05 tensor cores with TMEM accumulators on the pre-expanded
+ *   operand records (needs K_expanded).
  */
 KQ_API kq_status kq_quantize_mxfp4_variant(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
                                     const float *factors, const void *K_expanded,

@@ -58,7 +58,7 @@ def test_sf_bytes_matches_oracle(L, oracle_lib):
 
 def test_expanded_bytes(L):
     assert kq.kq_expanded_bytes(36, kq.KQ_K_FP32) == 36 * 4096
-    assert kq.kq_expanded_bytes(36, kq.KQ_K_BF16X3) == 36 * 1552
+    assert kq.kq_expanded_bytes(36, kq.KQ_K_BF16X3) == 36 * 2 * 1552
     assert kq.kq_expanded_bytes(0, kq.KQ_K_FP32) == 0
 
 
@@ -120,7 +120,8 @@ def test_quantize_argument_checks(L):
     assert _q(L, f=FAKE + 4) == 3                 # factors misaligned
     assert _q(L, m=0) == 0                        # empty: no-op
     assert _q(L, m=0, A=None, q=None, sf=None) == 0
-    assert _q(L, variant=3) == 4
+    assert _q(L, variant=4) == 4
+    assert _q(L, variant=3, K=None) == 1
     assert _q(L, variant=1, K=None) == 1
     assert _q(L, variant=0, f=None) == 1
 

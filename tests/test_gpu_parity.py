@@ -54,10 +54,11 @@ def lib_factors(nb, seed, sign=+1):
 
 def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None, q=None, sf=None):
     A = to_bf16(A_bits)
-    if kind == "kron_mma":
+    if kind in ("kron_umma", "kron_mma"):
         records = kq.kq_expand_blocks(dev(param_gpu), kq.KQ_K_BF16X3)
+        variant = kq.VARIANT_UMMA if kind == "kron_umma" else kq.VARIANT_MMA
         return kq.kq_quantize_mxfp4(A, d, K_expanded=records, layout=layout, y_debug=y_debug,
-                                    q=q, sf=sf)
+                                    variant=variant, q=q, sf=sf)
     if kind == "kron":
         return kq.kq_quantize_mxfp4(A, d, factors=dev(param_gpu), layout=layout, y_debug=y_debug,
                                     variant=variant, q=q, sf=sf)
@@ -72,12 +73,12 @@ def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None
 
 
 def oracle_kind(kind):
-    return "kron" if kind == "kron_mma" else kind
+    return "kron" if kind in ("kron_mma", "kron_umma") else kind
 
 
 def params_for(kind, nb, d, seed):
     """(gpu param, oracle param) for a transform kind."""
-    if kind in ("kron", "kron_mma"):
+    if kind in ("kron", "kron_mma", "kron_umma"):
         return lib_factors(nb, seed)
     if kind == "diag":
         s = synth.smooth_scales(d)
@@ -133,7 +134,7 @@ CASES = synth.CONFIG0 + synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3
 
 
 @pytest.mark.parametrize("name,m,d,model,cfg", CASES, ids=[c[0] for c in CASES])
-@pytest.mark.parametrize("kind", ["kron", "kron_mma", "diag", "hadamard", "identity"])
+@pytest.mark.parametrize("kind", ["kron", "kron_mma", "kron_umma", "diag", "hadamard", "identity"])
 def test_config_parity(name, m, d, model, cfg, kind):
     """Configs 0-3 at full size, both scale layouts (flux shapes compare a
     seeded sample of rows, always including the first and last tiles)."""
@@ -255,7 +256,7 @@ def test_sweep_parity(m, d):
                                          rng.choice(m, 400, replace=False)]))
     for layer in range(4):
         Fg, Fo = lib_factors(nb, synth.SEED_FACTORS + 4 + layer)
-        kind = "kron" if layer < 2 else "kron_mma"
+        kind = ("kron", "kron_umma", "kron_mma", "kron_umma")[layer]
         q, sf, y = run_kind(kind, A_bits, d, layer % 2, Fg)
         parity.check(A_bits, d, "kron", Fo, layer % 2, np_(q), np_(sf), np_(y), rows)
     s = synth.smooth_scales(d)
@@ -271,7 +272,7 @@ EDGE_SHAPES = [(1, 32), (7, 96), (127, 160), (129, 64), (200, 5600), (3, 2240), 
 
 
 @pytest.mark.parametrize("m,d", EDGE_SHAPES, ids=[f"{m}x{d}" for m, d in EDGE_SHAPES])
-@pytest.mark.parametrize("kind", ["kron", "kron_mma", "diag", "hadamard", "identity"])
+@pytest.mark.parametrize("kind", ["kron", "kron_mma", "kron_umma", "diag", "hadamard", "identity"])
 def test_ragged_shapes_with_pitches_and_canaries(m, d, kind):
     """Ragged m and d (partial tiles and block-columns), lda > d, ldq > d/2,
     and guard bytes around every output that must stay untouched."""
@@ -328,7 +329,7 @@ def test_special_values():
     y_k[4] /= 2.0 ** 8
     bits_k = synth.f64_to_bf16_bits(y_k)
     Fg, Fo = lib_factors(1, 3)
-    for kind in ("kron", "kron_mma"):
+    for kind in ("kron", "kron_mma", "kron_umma"):
         q, sf, yd = run_kind(kind, bits_k, 32, 0, Fg)
         parity.check(bits_k, 32, "kron", Fo, 0, np_(q), np_(sf), np_(yd))
 
@@ -340,7 +341,7 @@ def test_raw_factor_interface():
     nb = d // 32
     A_bits = synth.activations(m, d, 9, "sana")
     F = synth.random_factors(nb, 12, scale=0.8)
-    for kind in ("kron", "kron_mma"):
+    for kind in ("kron", "kron_mma", "kron_umma"):
         q, sf, y = run_kind(kind, A_bits, d, 1, F)
         parity.check(A_bits, d, "kron", F.astype(np.float64), 1, np_(q), np_(sf), np_(y))
     Fg, Fo = lib_factors(nb, 13, sign=-1)

@@ -75,6 +75,22 @@ kq_status make_tensor_map_2d_bf16(CUtensorMap *map, const void *base, int64_t ro
     return r == CUDA_SUCCESS ? KQ_OK : KQ_ERR_CUDA;
 }
 
+kq_status make_tensor_map_2d_u8(CUtensorMap *map, void *base, int64_t rows, int64_t cols,
+                                int64_t ld_bytes, uint32_t box_cols, uint32_t box_rows,
+                                CUtensorMapSwizzle swizzle)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr) return KQ_ERR_CUDA;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_bytes)};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KQ_OK : KQ_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------------------
 // argument checks (host only; nothing is enqueued when they fail)
 
@@ -222,19 +238,20 @@ kq_status kq_quantize_mxfp4_variant(const uint16_t *A, int64_t m, int64_t d, int
                                     int64_t ldq, uint8_t *sf, kq_sf_layout sf_layout,
                                     float *y_debug, int variant, cudaStream_t stream)
 {
-    if (variant < 0 || variant > 2) return KQ_ERR_LAYOUT;
+    if (variant < 0 || variant > 3) return KQ_ERR_LAYOUT;
     kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
     if (st != KQ_OK) return st;
     if (variant == 0 && factors == nullptr) return KQ_ERR_NULL;
-    if (variant == 1 && K_expanded == nullptr) return KQ_ERR_NULL;
+    if ((variant == 1 || variant == 3) && K_expanded == nullptr) return KQ_ERR_NULL;
     if (variant == 0 && !aligned16(factors)) return KQ_ERR_ALIGN;
-    if (variant == 1 && !aligned16(K_expanded)) return KQ_ERR_ALIGN;
+    if ((variant == 1 || variant == 3) && !aligned16(K_expanded)) return KQ_ERR_ALIGN;
     if (m == 0) return KQ_OK;
     DeviceInfo info;
     if ((st = device_info(info)) != KQ_OK) return st;
     QuantParams p;
     fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
     if (variant == 1) return launch_quant_mma(A, lda, K_expanded, p, stream);
+    if (variant == 3) return launch_quant_umma(A, lda, K_expanded, p, stream);
     if (variant == 0) {
         p.factors = factors;
         return launch_quant_tma(kKron, A, lda, p, stream);
@@ -247,7 +264,7 @@ kq_status kq_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda
                             uint8_t *sf, kq_sf_layout sf_layout, float *y_debug,
                             cudaStream_t stream)
 {
-    const int variant = factors != nullptr ? 0 : (K_expanded != nullptr ? 1 : 2);
+    const int variant = factors != nullptr ? 0 : (K_expanded != nullptr ? 3 : 2);
     return kq_quantize_mxfp4_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout,
                                      y_debug, variant, stream);
 }

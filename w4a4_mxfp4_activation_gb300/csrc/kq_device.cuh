@@ -70,6 +70,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// try_wait that may suspend the thread (up to the hint, in ns) until the
+// phase completes, so that waiting threads do not keep polling the barrier.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(100000u)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false if
 // it has not completed within kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
@@ -77,7 +92,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity)) return true;
         if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
@@ -112,6 +127,47 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// 2-D tiled store of a shared-memory box to global memory at element
+// coordinates (x, y); out-of-range parts of the box are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int32_t x, int32_t y,
+                                             uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until at most N committed bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until every committed bulk group has completed.
+__device__ __forceinline__ void bulk_wait_group_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA, tensor cores).
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Barrier over `count` threads (whole warps) with id `id` (1..15).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // L2 policy for data read exactly once (the activations): evict first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
@@ -130,6 +186,19 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
                  : "r"(addr)
                  : "memory");
     return v;
+}
+
+__device__ __forceinline__ float4 lds_f4(uint32_t addr)
+{
+    const uint4 v = lds128(addr);
+    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                       __uint_as_float(v.w));
+}
+
+// Entry [r][c] of a 2x2 factor held as (g00, g01, g10, g11).
+__device__ __forceinline__ float sel2x2(float4 g, int r, int c)
+{
+    return r ? (c ? g.w : g.z) : (c ? g.y : g.x);
 }
 
 __device__ __forceinline__ float4 ldg_nc_f4(const float *p)
@@ -229,6 +298,29 @@ __device__ __forceinline__ uint4 quantize_block(const float2 (&Y)[16], uint32_t 
     byte_out = byte;
     return q;
 }
+
+// Row-major walk over (row tile, column tile) pairs: first, first + step,
+// first + 2 step, ... with tile = rt * ncol + ct, without 64-bit division in
+// the loop.  The walk ends when rt reaches the number of row tiles.
+struct TileWalk {
+    int rt, ct;
+    int ncol, step_rt, step_ct;
+    __device__ __forceinline__ TileWalk(int64_t first, int64_t step, int64_t ncol_)
+        : rt(static_cast<int>(first / ncol_)), ct(static_cast<int>(first % ncol_)),
+          ncol(static_cast<int>(ncol_)), step_rt(static_cast<int>(step / ncol_)),
+          step_ct(static_cast<int>(step % ncol_))
+    {
+    }
+    __device__ __forceinline__ void next()
+    {
+        ct += step_ct;
+        rt += step_rt;
+        if (ct >= ncol) {
+            ct -= ncol;
+            ++rt;
+        }
+    }
+};
 
 // Byte position of a scale in the 128x4 tiled layout of block-scaled MMA.
 __device__ __forceinline__ int64_t sf_blocked_offset(int64_t row, int64_t kb, int64_t ncb)

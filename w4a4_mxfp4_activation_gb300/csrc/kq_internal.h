@@ -44,6 +44,9 @@ struct DeviceInfo {
 kq_status device_info(DeviceInfo &info);
 kq_status make_tensor_map_2d_bf16(CUtensorMap *map, const void *base, int64_t rows, int64_t cols,
                                   int64_t ld_elems, uint32_t box_cols, uint32_t box_rows);
+kq_status make_tensor_map_2d_u8(CUtensorMap *map, void *base, int64_t rows, int64_t cols,
+                                int64_t ld_bytes, uint32_t box_cols, uint32_t box_rows,
+                                CUtensorMapSwizzle swizzle);
 kq_status check_launch();
 
 kq_status launch_quant_tma(Transform t, const uint16_t *A, int64_t lda, const QuantParams &p,
@@ -51,6 +54,8 @@ kq_status launch_quant_tma(Transform t, const uint16_t *A, int64_t lda, const Qu
 kq_status launch_quant_mma(const uint16_t *A, int64_t lda, const void *K_expanded,
                            const QuantParams &p, cudaStream_t stream);
 kq_status launch_mma_records(const float *factors, int64_t nb, void *out, cudaStream_t stream);
+kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expanded,
+                            const QuantParams &p, cudaStream_t stream);
 
 // Bytes of one block's operand record for the tensor-core variant.
 constexpr int64_t kMmaRecordBytes = 1552;

@@ -127,11 +127,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_prefetch_desc(&tmA);
         const uint64_t pol = l2_policy_evict_first();
         int64_t it = 0;
-        for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++it) {
+        for (TileWalk tw(blockIdx.x, gridDim.x, p.ncol_tiles); tw.rt < p.nrow_tiles; tw.next(), ++it) {
             const int s = static_cast<int>(it % STAGES);
             const uint32_t ph = static_cast<uint32_t>((it / STAGES) & 1);
             if (it >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1u)) break;
-            const int64_t rt = tile / p.ncol_tiles, ct = tile % p.ncol_tiles;
+            const int64_t rt = tw.rt, ct = tw.ct;
             const uint32_t dst = base + s * Cfg::kStageBytes;
             const int64_t left = p.nb - ct * 4;
             const int64_t nrec = left < 4 ? left : 4;
@@ -159,14 +159,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int lm_row = ((lane >> 3) & 1) * 8 + (lane & 7);
     const int lm_kc = lane >> 4;
     int64_t it = 0;
-    for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++it) {
+    for (TileWalk tw(blockIdx.x, gridDim.x, p.ncol_tiles); tw.rt < p.nrow_tiles; tw.next(), ++it) {
         const int s = static_cast<int>(it % STAGES);
         const uint32_t ph = static_cast<uint32_t>((it / STAGES) & 1);
+        const int64_t rt = tw.rt, ct = tw.ct;
         if (!mbar_wait(bar_full + 8 * s, ph)) {
-            fail_items_m<BR>(p, tile, warp, lane);
+            fail_items_m<BR>(p, rt * p.ncol_tiles + ct, warp, lane);
             return;
         }
-        const int64_t rt = tile / p.ncol_tiles, ct = tile % p.ncol_tiles;
         const int64_t j = ct * 4 + b;
         const uint32_t stage = base + s * Cfg::kStageBytes;
         if (j >= p.nb) {
@@ -347,6 +347,36 @@ __global__ void mma_records_kernel(const float *__restrict__ factors, int64_t nb
     }
 }
 
+// Records of the tcgen05 variant: per block, the three bf16 terms of
+// K'^T (n = output channel, k = input channel, both 0..15) in the
+// no-swizzle K-major operand layout -- 8 x 16-byte core matrices, core
+// (n / 8, k / 8) at (n / 8) * 256 + (k / 8) * 128, row n % 8 at 16 B,
+// element k % 8 at 2 B; 512 B per term -- then G1 (fp32) at byte 1536.
+__global__ void umma_records_kernel(const float *__restrict__ factors, int64_t nb,
+                                    uint8_t *__restrict__ out)
+{
+    constexpr int kWords = 3 * 16 * 8 + 4;
+    const int64_t n = nb * kWords;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t j = idx / kWords;
+        const int w = static_cast<int>(idx % kWords);
+        const float *f = factors + j * 20;
+        uint8_t *rec = out + j * kRecordBytes;
+        if (w >= 3 * 16 * 8) {                    // G1 entries
+            reinterpret_cast<uint32_t *>(rec + 1536)[w - 384] = __float_as_uint(f[w - 384]);
+            continue;
+        }
+        const int t = w / 128, ncol = (w / 8) % 16, kp = w % 8;
+        const int k0 = 2 * kp;
+        const uint16_t e0 = bf16_term(kron_tail(f, k0, ncol), t);
+        const uint16_t e1 = bf16_term(kron_tail(f, k0 + 1, ncol), t);
+        const int off = t * 512 + (ncol >> 3) * 256 + (k0 >> 3) * 128 + (ncol & 7) * 16 + (k0 & 7) * 2;
+        *reinterpret_cast<uint32_t *>(rec + off) = static_cast<uint32_t>(e0) |
+                                                   (static_cast<uint32_t>(e1) << 16);
+    }
+}
+
 }  // namespace
 
 kq_status launch_quant_mma(const uint16_t *A, int64_t lda, const void *K_expanded,
@@ -359,15 +389,22 @@ kq_status launch_quant_mma(const uint16_t *A, int64_t lda, const void *K_expande
     CUtensorMap map;
     st = make_tensor_map_2d_bf16(&map, A, p.m, p.d, lda, 64, BR);
     if (st != KQ_OK) return st;
-    return launch_mma<BR, 4>(map, p, static_cast<const uint8_t *>(K_expanded), info.sm_count,
-                             stream);
+    // the mma.sync records follow the nb tcgen05 records
+    return launch_mma<BR, 4>(map, p,
+                             static_cast<const uint8_t *>(K_expanded) + p.nb * kRecordBytes,
+                             info.sm_count, stream);
 }
 
+// K_expanded (KQ_K_BF16X3) = [nb tcgen05 records][nb mma.sync records].
 kq_status launch_mma_records(const float *factors, int64_t nb, void *out, cudaStream_t stream)
 {
+    uint8_t *o = static_cast<uint8_t *>(out);
+    const int64_t work_u = nb * (3 * 16 * 8 + 4);
+    umma_records_kernel<<<static_cast<int>(std::min<int64_t>((work_u + 255) / 256, 4096)), 256, 0,
+                          stream>>>(factors, nb, o);
     const int64_t work = nb * (32 * 12 + 4);
-    const int grid = static_cast<int>(std::min<int64_t>((work + 255) / 256, 4096));
-    mma_records_kernel<<<grid, 256, 0, stream>>>(factors, nb, static_cast<uint8_t *>(out));
+    mma_records_kernel<<<static_cast<int>(std::min<int64_t>((work + 255) / 256, 4096)), 256, 0,
+                         stream>>>(factors, nb, o + nb * kRecordBytes);
     return check_launch();
 }
 

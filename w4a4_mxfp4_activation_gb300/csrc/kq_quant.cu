@@ -92,13 +92,6 @@ __device__ __forceinline__ void butterfly_inpair(float2 (&Y)[16], float4 g)
     for (int t = 0; t < 16; ++t) Y[t] = __ffma2_rn(swap2(Y[t]), d1, __fmul2_rn(Y[t], d0));
 }
 
-__device__ __forceinline__ float4 lds_f4(uint32_t addr)
-{
-    const uint4 v = lds128(addr);
-    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                       __uint_as_float(v.w));
-}
-
 // `prm`: shared-memory address of this block's staged parameters.
 template <int T>
 __device__ __forceinline__ void apply_transform(float2 (&Y)[16], uint32_t prm)
@@ -192,11 +185,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_prefetch_desc(&tmA);
         const uint64_t pol = l2_policy_evict_first();
         int64_t it = 0;
-        for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++it) {
+        for (TileWalk tw(blockIdx.x, gridDim.x, p.ncol_tiles); tw.rt < p.nrow_tiles; tw.next(), ++it) {
             const int s = static_cast<int>(it % STAGES);
             const uint32_t ph = static_cast<uint32_t>((it / STAGES) & 1);
             if (it >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1u)) break;
-            const int64_t rt = tile / p.ncol_tiles, ct = tile % p.ncol_tiles;
+            const int64_t rt = tw.rt, ct = tw.ct;
             const uint32_t dst = base + s * Cfg::kStageBytes;
             uint32_t pbytes = 0;
             const void *psrc = nullptr;
@@ -233,14 +226,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int cw = warp;
     const int h = lane & 1, rlo = (lane >> 1) & 3, box = (lane >> 3) & 1, rhi = (lane >> 4) & 1;
     int64_t it = 0;
-    for (int64_t tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x, ++it) {
+    for (TileWalk tw(blockIdx.x, gridDim.x, p.ncol_tiles); tw.rt < p.nrow_tiles; tw.next(), ++it) {
         const int s = static_cast<int>(it % STAGES);
         const uint32_t ph = static_cast<uint32_t>((it / STAGES) & 1);
+        const int64_t rt = tw.rt, ct = tw.ct;
         if (!mbar_wait(bar_full + 8 * s, ph)) {
-            fail_items<BR>(p, tile, lane, cw);
+            fail_items<BR>(p, rt * p.ncol_tiles + ct, lane, cw);
             return;
         }
-        const int64_t rt = tile / p.ncol_tiles, ct = tile % p.ncol_tiles;
         const int64_t j = ct * 4 + box * 2 + h;
         const uint32_t stage = base + s * Cfg::kStageBytes + box * Cfg::kBoxBytes;
         const uint32_t prm = base + s * Cfg::kStageBytes + Cfg::kABytes +

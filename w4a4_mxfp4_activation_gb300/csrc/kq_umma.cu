@@ -1,0 +1,410 @@
+// KroQuant quantizer with the block transform on the 5th-generation tensor
+// cores (tcgen05.mma, accumulators in TMEM), sm_103a.
+//
+// "KroQuant: Kronecker-Structured Block Transforms for Efficient Post-
+// Training Quantization of Diffusion Transformers", eq. (5) and (12): with
+// K_j = G1 (x) K'_j and K'_j = G2 (x) G3 (x) G4 (x) G5 (16 x 16), the row
+// transform of a 32-channel block splits over its two 16-channel halves:
+//     Z_h = a_h . K'_j,   y_0 = G1[0][0] Z_0 + G1[1][0] Z_1,
+//                         y_1 = G1[0][1] Z_0 + G1[1][1] Z_1.
+// The 16x16 products run as tcgen05.mma (bf16 operands, fp32 accumulation in
+// TMEM) against K'_j pre-expanded once per layer by kq_expand_blocks as three
+// bf16 terms hi + mid + lo (exact to about 2^-24 relative; the activations
+// are exact in bf16).  The three terms sit side by side along N: one
+// M = 128, N = 48, K = 16 MMA per (block, half) reads its A slice from shared
+// memory once, and the epilogue adds the three partial products.  (Issuing
+// one N = 16 MMA per term re-reads A three times; measured on GB300 that
+// made the tensor-core reads of A the bottleneck.)
+// The G1 stage and the MXFP4 encoding run on the CUDA cores after the
+// accumulators are read back with tcgen05.ld (one thread = one row of a
+// 32-channel block, all 32 values in registers).
+//
+// Roles in a CTA (one CTA per SM, persistent over tiles of 128 rows x 64
+// channels = 2 blocks = one 128B-swizzled TMA box):
+//   warp 0      TMA producer: the A box + one bulk copy of the tile's two
+//               operand records (1552 B each: the three 16x16 bf16 terms in
+//               the no-swizzle K-major layout and G1) into a STAGES-deep
+//               shared-memory ring;
+//   warp 1      owns the TMEM allocation (2 accumulator buffers x 192
+//               columns); one lane issues the 4 MMAs of the tile and commits
+//               them to the ring's empty barrier and to the accumulator's full
+//               barrier;
+//   warps 2-17  epilogue, two groups of 8 warps taking alternate tiles (and
+//               accumulator buffers): warp w reads TMEM lanes 32 (w % 4)..+31
+//               (rows) of one block, sums the terms, applies G1 and quantizes;
+//               the codes of the tile go to a shared staging buffer (32-byte
+//               swizzle) and leave with one TMA store of 128 rows x 32 bytes
+//               (a thread owns a row, so direct 16-byte stores from a warp
+//               would touch 32 rows and clog the memory pipe).
+// Every wait is bounded in time; a timed-out epilogue writes the E8M0 NaN
+// byte 0xFF as the scale of the blocks it could not finish.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "kq_device.cuh"
+#include "kq_internal.h"
+
+namespace kq {
+namespace {
+
+constexpr int kEpiWarps = 16;
+constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kThreadsU = (2 + kEpiWarps) * 32;
+constexpr int kBR = 128;                       // rows per tile (= MMA M)
+constexpr int kBlockCols = 96;                 // per block: 2 halves x 3 terms x 16
+constexpr int kAccCols = 2 * kBlockCols;       // fp32 columns per accumulator buffer
+constexpr int kTmemCols = 512;                 // 2 buffers (384 columns), power of two
+
+template <int STAGES>
+struct UCfg {
+    static constexpr int kABytes = kBR * 128;                 // 128 rows x 64 bf16 = 16 KB
+    static constexpr int kBOff = kABytes;                     // operand records
+    static constexpr int kRecBytes = 1552;                    // 3 terms + G1
+    static constexpr int kStageBytes = kABytes + 4096;        // 2 records, padded: 20 KB
+    // after the ring: barriers + TMEM base (1 KB), 1 KB spare, code staging
+    // for the TMA stores: 2 groups x 2 buffers x 128 rows x 32 B
+    static constexpr int kBarOff = STAGES * kStageBytes;
+    static constexpr int kStgOff = kBarOff + 2048;
+    static constexpr int kStgBytes = kBR * 32;
+    static constexpr int kSmemBytes = kStgOff + 4 * kStgBytes + 1024;   // + alignment slack
+    static_assert(kStageBytes % 1024 == 0, "stage alignment");
+};
+
+// ---- tcgen05 wrappers ---------------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: start address, leading / stride byte
+// offsets (16-byte units), descriptor version 1, swizzle mode (0 none, 2 128B).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swizzle)
+{
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+           (static_cast<uint64_t>(lbo >> 4) << 16) | (static_cast<uint64_t>(sbo >> 4) << 32) |
+           (1ull << 46) | (static_cast<uint64_t>(swizzle) << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = 48 (three 16-column terms), M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((48u >> 3) << 17) |
+                            ((128u >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void store_scale_u(const QuantParams &p, int64_t row, int64_t j,
+                                              uint32_t byte)
+{
+    if (p.sf_layout == KQ_SF_ROWMAJOR) {
+        if (row < p.m) p.sf[row * p.nb + j] = static_cast<uint8_t>(byte);
+    } else {
+        p.sf[sf_blocked_offset(row, j, p.ncb)] = static_cast<uint8_t>(byte);
+    }
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(kThreadsU, 1)
+    quant_umma_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmQ, const QuantParams p,
+                      const uint8_t *__restrict__ records)
+{
+    using Cfg = UCfg<STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+    const uint32_t bar = base + Cfg::kBarOff;
+    const uint32_t bar_full = bar;                        // [STAGES]
+    const uint32_t bar_empty = bar + 8 * STAGES;          // [STAGES]
+    const uint32_t bar_acc_full = bar + 16 * STAGES;      // [2]
+    const uint32_t bar_acc_empty = bar_acc_full + 16;     // [2]
+    const uint32_t tmem_slot = bar_acc_empty + 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(bar_acc_full + 8 * a, 1);        // MMA commit
+            mbar_init(bar_acc_empty + 8 * a, kEpiThreads / 2);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    uint32_t tmem_base;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(tmem_base) : "r"(tmem_slot) : "memory");
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            const uint64_t pol = l2_policy_evict_first();
+            int64_t it = 0;
+            for (TileWalk tw(blockIdx.x, gridDim.x, p.ncol_tiles); tw.rt < p.nrow_tiles;
+                 tw.next(), ++it) {
+                const int s = static_cast<int>(it % STAGES);
+                const uint32_t ph = static_cast<uint32_t>((it / STAGES) & 1);
+                if (it >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1u)) break;
+                const int64_t rt = tw.rt, ct = tw.ct;
+                const uint32_t dst = base + s * Cfg::kStageBytes;
+                const int64_t left = p.nb - ct * 2;     // < 1 on padding tiles
+                const uint32_t rbytes = static_cast<uint32_t>(
+                    (left < 0 ? 0 : (left < 2 ? left : 2)) * Cfg::kRecBytes);
+                mbar_arrive_expect_tx(bar_full + 8 * s, Cfg::kABytes + rbytes);
+                tma_load_2d(dst, &tmA, static_cast<int32_t>(ct * 64),
+                            static_cast<int32_t>(rt * kBR), bar_full + 8 * s, pol);
+                if (rbytes)
+                    bulk_load(dst + Cfg::kBOff, records + ct * 2 * Cfg::kRecBytes, rbytes,
+                              bar_full + 8 * s);
+            }
+            for (int64_t k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
+                (void)mbar_wait(bar_full + 8 * static_cast<int>(k % STAGES),
+                                static_cast<uint32_t>((k / STAGES) & 1));
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        int64_t it = 0;
+        bool ok = true;
+        for (TileWalk tw(blockIdx.x, gridDim.x, p.ncol_tiles); tw.rt < p.nrow_tiles && ok;
+             tw.next(), ++it) {
+            const int s = static_cast<int>(it % STAGES);
+            const int a = static_cast<int>(it & 1);
+            const int64_t ct = tw.ct;
+            const int64_t left = p.nb - ct * 2;
+            const int nblk = static_cast<int>(left < 0 ? 0 : (left < 2 ? left : 2));
+            bool w = mbar_wait(bar_full + 8 * s, static_cast<uint32_t>((it / STAGES) & 1));
+            if (w && it >= 2)
+                w = mbar_wait(bar_acc_empty + 8 * a, static_cast<uint32_t>(((it >> 1) & 1) ^ 1));
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            const uint32_t stage = base + s * Cfg::kStageBytes;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t d0 = tmem_base + a * kAccCols;
+                for (int b = 0; b < nblk; ++b)
+                    for (int h = 0; h < 2; ++h)
+                        umma_bf16(d0 + b * kBlockCols + h * 48,
+                                  smem_desc(stage + 64 * b + 32 * h, 16, 1024, 2),
+                                  smem_desc(stage + Cfg::kBOff + b * Cfg::kRecBytes, 128, 256, 0),
+                                  0u);
+                umma_commit(bar_empty + 8 * s);          // ring stage free once the MMAs read it
+                umma_commit(bar_acc_full + 8 * a);       // accumulators ready
+            }
+            __syncwarp();
+        }
+        // Wait (bounded) for the MMAs of the last tiles before releasing TMEM.
+        for (int64_t k = (it > 2 ? it - 2 : 0); k < it; ++k)
+            (void)mbar_wait(bar_acc_full + 8 * static_cast<int>(k & 1),
+                            static_cast<uint32_t>((k >> 1) & 1));
+    } else {
+        // ---------------- epilogue ----------------
+        const int e = warp - 2;
+        const int grp = e >> 3;               // takes tiles (and buffers) with it % 2 == grp
+        const int b = (e >> 2) & 1;           // block of the tile
+        const int qtr = warp & 3;             // TMEM lane quarter this warp may access
+        const bool leader = (e & 7) == 0 && lane == 0;
+        const int r = qtr * 32 + lane;        // row within the tile
+        int64_t it = grp;
+        bool ok = true;
+        for (TileWalk tw(blockIdx.x + grp * static_cast<int64_t>(gridDim.x),
+                         2 * static_cast<int64_t>(gridDim.x), p.ncol_tiles);
+             tw.rt < p.nrow_tiles; tw.next(), it += 2) {
+            const int a = grp;
+            const int64_t rt = tw.rt, ct = tw.ct;
+            const int64_t j = ct * 2 + b;
+            const int64_t row = rt * kBR + r;
+            const uint32_t stg = base + Cfg::kStgOff + (grp * 2 + ((it >> 1) & 1)) * Cfg::kStgBytes;
+            // G1 of this block: the fp32 entries at byte 1536 of its operand record
+            float4 g1 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < p.nb)
+                g1 = ldg_nc_f4(reinterpret_cast<const float *>(records + j * Cfg::kRecBytes + 1536));
+            if (ok) ok = __all_sync(0xffffffffu,
+                                    mbar_wait(bar_acc_full + 8 * a, static_cast<uint32_t>((it >> 1) & 1)));
+            uint4 codes = make_uint4(0u, 0u, 0u, 0u);
+            if (ok) {
+                tc_fence_after();
+                float2 Y[16];
+                if (j < p.nb) {
+                    // columns: half 0 terms 0..2, half 1 terms 0..2 (16 each)
+                    const uint32_t tb = tmem_base + (static_cast<uint32_t>(qtr * 32) << 16) +
+                                        a * kAccCols + b * kBlockCols;
+                    uint32_t rr[32];
+                    float z0[16], z1[16];
+                    tmem_ld32(tb, rr);           // Z0^hi, Z0^mid
+#pragma unroll
+                    for (int n = 0; n < 16; ++n)
+                        z0[n] = __uint_as_float(rr[n]) + __uint_as_float(rr[16 + n]);
+                    tmem_ld32(tb + 32, rr);      // Z0^lo, Z1^hi
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        z0[n] += __uint_as_float(rr[n]);
+                        z1[n] = __uint_as_float(rr[16 + n]);
+                    }
+                    tmem_ld32(tb + 64, rr);      // Z1^mid, Z1^lo
+#pragma unroll
+                    for (int n = 0; n < 16; ++n)
+                        z1[n] = (z1[n] + __uint_as_float(rr[n])) + __uint_as_float(rr[16 + n]);
+                    tc_fence_before();
+                    mbar_arrive(bar_acc_empty + 8 * a);
+                    // G1 stage: y_0 = g00 Z_0 + g10 Z_1, y_1 = g01 Z_0 + g11 Z_1
+                    const float2 a00 = make_float2(g1.x, g1.x), a01 = make_float2(g1.y, g1.y);
+                    const float2 a10 = make_float2(g1.z, g1.z), a11 = make_float2(g1.w, g1.w);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const float2 zz0 = make_float2(z0[2 * t], z0[2 * t + 1]);
+                        const float2 zz1 = make_float2(z1[2 * t], z1[2 * t + 1]);
+                        Y[t] = __ffma2_rn(zz1, a10, __fmul2_rn(zz0, a00));
+                        Y[8 + t] = __ffma2_rn(zz1, a11, __fmul2_rn(zz0, a01));
+                    }
+                    if (p.y_debug != nullptr && row < p.m) {
+                        float *yd = p.y_debug + row * p.d + j * 32;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            stg_f4(yd + 4 * k, make_float4(Y[2 * k].x, Y[2 * k].y, Y[2 * k + 1].x,
+                                                           Y[2 * k + 1].y));
+                    }
+                    uint32_t byte;
+                    codes = quantize_block(Y, byte);
+                    store_scale_u(p, row, j, byte);
+                } else {
+                    tc_fence_before();
+                    mbar_arrive(bar_acc_empty + 8 * a);
+                    if (p.sf_layout != KQ_SF_ROWMAJOR) store_scale_u(p, row, j, 0u);
+                }
+            } else if (j < p.nb && row < p.m_rows) {
+                store_scale_u(p, row, j, 0xFFu);
+            }
+            // Codes -> staging buffer -> one TMA store per tile.  Every thread of
+            // the group passes both barriers on every tile, whatever happened above.
+            if (leader) bulk_wait_group_read<1>();        // this buffer's previous store has read it
+            named_barrier(1 + grp, kEpiThreads / 2);
+            sts128(stg + r * 32 + ((b ^ ((r >> 2) & 1)) << 4), codes);
+            fence_proxy_async_smem();
+            named_barrier(1 + grp, kEpiThreads / 2);
+            if (leader) {
+                if (ct * 2 < p.nb)      // padding tiles of the scale layout have no codes
+                    tma_store_2d(&tmQ, static_cast<int32_t>(ct * 32),
+                                 static_cast<int32_t>(rt * kBR), stg);
+                bulk_commit_group();
+            }
+        }
+        if (leader) bulk_wait_group_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+struct USlot {
+    std::once_flag once[64];
+    int occupancy[64] = {};
+    cudaError_t err[64] = {};
+};
+
+template <int STAGES>
+kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, QuantParams p,
+                      const uint8_t *records, int sm_count, cudaStream_t stream)
+{
+    using Cfg = UCfg<STAGES>;
+    auto kern = quant_umma_kernel<STAGES>;
+    static USlot slot;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
+    std::call_once(slot.once[dev], [&] {
+        slot.err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg::kSmemBytes);
+        if (slot.err[dev] == cudaSuccess)
+            slot.err[dev] = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &slot.occupancy[dev], kern, kThreadsU, Cfg::kSmemBytes);
+    });
+    if (slot.err[dev] != cudaSuccess || slot.occupancy[dev] < 1) return KQ_ERR_CUDA;
+    // tiles of 64 channels (one TMA box); the tiled scale layout also needs
+    // its padding block-columns (up to a multiple of 4) visited and zeroed
+    p.ncol_tiles = p.sf_layout == KQ_SF_ROWMAJOR ? (p.nb + 1) / 2 : 2 * p.ncb;
+    p.nrow_tiles = (p.m_rows + kBR - 1) / kBR;
+    p.ntiles = p.nrow_tiles * p.ncol_tiles;
+    if (p.ntiles == 0) return KQ_OK;
+    // one CTA per SM: each holds 256 of the SM's 512 TMEM columns
+    const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, sm_count));
+    kern<<<grid, kThreadsU, Cfg::kSmemBytes, stream>>>(map, mapq, p, records);
+    return check_launch();
+}
+
+}  // namespace
+
+kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expanded,
+                            const QuantParams &p, cudaStream_t stream)
+{
+    DeviceInfo info;
+    kq_status st = device_info(info);
+    if (st != KQ_OK) return st;
+    CUtensorMap map, mapq;
+    st = make_tensor_map_2d_bf16(&map, A, p.m, p.d, lda, 64, kBR);
+    if (st != KQ_OK) return st;
+    st = make_tensor_map_2d_u8(&mapq, p.q, p.m, p.d / 2, p.ldq, 32, kBR,
+                               CU_TENSOR_MAP_SWIZZLE_32B);
+    if (st != KQ_OK) return st;
+    return launch_umma<8>(map, mapq, p, static_cast<const uint8_t *>(K_expanded), info.sm_count,
+                          stream);
+}
+
+}  // namespace kq

@@ -27,6 +27,7 @@ KQ_K_BF16X3 = 1
 VARIANT_BUTTERFLY = 0
 VARIANT_MMA = 1
 VARIANT_IDENTITY = 2
+VARIANT_UMMA = 3
 
 EXPORTS = (
     "kq_quantize_mxfp4", "kq_smooth_quantize_mxfp4", "kq_hadamard_quantize_mxfp4",
