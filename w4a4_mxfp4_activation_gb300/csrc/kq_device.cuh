@@ -287,16 +287,16 @@ __device__ __forceinline__ uint4 quantize_block(const float2 (&Y)[16], uint32_t 
     const uint32_t byte = e8m0_byte(amax);
     const float s = inv_scale(byte);
     const float2 s2 = make_float2(s, s);
-    float2 V[16];
+    // scale and encode eight values at a time (keeps few values live)
+    uint32_t w[4];
 #pragma unroll
-    for (int t = 0; t < 16; ++t) V[t] = __fmul2_rn(Y[t], s2);
-    uint4 q;
-    q.x = e2m1x8(V[0].x, V[0].y, V[1].x, V[1].y, V[2].x, V[2].y, V[3].x, V[3].y);
-    q.y = e2m1x8(V[4].x, V[4].y, V[5].x, V[5].y, V[6].x, V[6].y, V[7].x, V[7].y);
-    q.z = e2m1x8(V[8].x, V[8].y, V[9].x, V[9].y, V[10].x, V[10].y, V[11].x, V[11].y);
-    q.w = e2m1x8(V[12].x, V[12].y, V[13].x, V[13].y, V[14].x, V[14].y, V[15].x, V[15].y);
+    for (int k = 0; k < 4; ++k) {
+        const float2 v0 = __fmul2_rn(Y[4 * k], s2), v1 = __fmul2_rn(Y[4 * k + 1], s2);
+        const float2 v2 = __fmul2_rn(Y[4 * k + 2], s2), v3 = __fmul2_rn(Y[4 * k + 3], s2);
+        w[k] = e2m1x8(v0.x, v0.y, v1.x, v1.y, v2.x, v2.y, v3.x, v3.y);
+    }
     byte_out = byte;
-    return q;
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Row-major walk over (row tile, column tile) pairs: first, first + step,

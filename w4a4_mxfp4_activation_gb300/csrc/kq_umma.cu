@@ -25,11 +25,12 @@
 //               operand records (1552 B each: the three 16x16 bf16 terms in
 //               the no-swizzle K-major layout and G1) into a STAGES-deep
 //               shared-memory ring;
-//   warp 1      owns the TMEM allocation (2 accumulator buffers x 192
-//               columns); one lane issues the 4 MMAs of the tile and commits
-//               them to the ring's empty barrier and to the accumulator's full
-//               barrier;
-//   warps 2-17  epilogue, two groups of 8 warps taking alternate tiles (and
+//   warps 1-2   MMA issuers, one per accumulator buffer (2 x 192 TMEM columns,
+//               allocated by warp 1): warp 1 + m takes the CTA's tiles with
+//               it % 2 == m, so two tiles are in flight through the tensor
+//               core; one lane issues the tile's 4 MMAs and commits them to the
+//               ring's empty barrier and to the accumulator's full barrier;
+//   warps 3-18  epilogue, two groups of 8 warps taking alternate tiles (and
 //               accumulator buffers): warp w reads TMEM lanes 32 (w % 4)..+31
 //               (rows) of one block, sums the terms, applies G1 and quantizes;
 //               the codes of the tile go to a shared staging buffer (32-byte
@@ -51,7 +52,9 @@ namespace {
 
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreadsU = (2 + kEpiWarps) * 32;
+constexpr int kMmaWarps = 2;                   // one per accumulator buffer
+constexpr int kFirstEpiWarp = 1 + kMmaWarps;
+constexpr int kThreadsU = (kFirstEpiWarp + kEpiWarps) * 32;
 constexpr int kBR = 128;                       // rows per tile (= MMA M)
 constexpr int kBlockCols = 96;                 // per block: 2 halves x 3 terms x 16
 constexpr int kAccCols = 2 * kBlockCols;       // fp32 columns per accumulator buffer
@@ -135,6 +138,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
         : "memory");
+}
+
+// Waits until this thread's earlier tcgen05.ld results are in registers.
+__device__ __forceinline__ void tmem_wait_ld()
+{
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
@@ -155,7 +163,7 @@ __device__ __forceinline__ void store_scale_u(const QuantParams &p, int64_t row,
     }
 }
 
-template <int STAGES>
+template <int STAGES, bool DEBUG>
 __global__ void __launch_bounds__(kThreadsU, 1)
     quant_umma_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmQ, const QuantParams p,
@@ -217,14 +225,15 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                 (void)mbar_wait(bar_full + 8 * static_cast<int>(k % STAGES),
                                 static_cast<uint32_t>((k / STAGES) & 1));
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        int64_t it = 0;
+    } else if (warp < kFirstEpiWarp) {
+        // ---------------- MMA issuers ----------------
+        const int a = warp - 1;               // accumulator buffer; tiles with it % 2 == a
+        int64_t it = a;
         bool ok = true;
-        for (TileWalk tw(blockIdx.x, gridDim.x, p.ncol_tiles); tw.rt < p.nrow_tiles && ok;
-             tw.next(), ++it) {
+        for (TileWalk tw(blockIdx.x + a * static_cast<int64_t>(gridDim.x),
+                         2 * static_cast<int64_t>(gridDim.x), p.ncol_tiles);
+             tw.rt < p.nrow_tiles && ok; tw.next(), it += 2) {
             const int s = static_cast<int>(it % STAGES);
-            const int a = static_cast<int>(it & 1);
             const int64_t ct = tw.ct;
             const int64_t left = p.nb - ct * 2;
             const int nblk = static_cast<int>(left < 0 ? 0 : (left < 2 ? left : 2));
@@ -247,13 +256,12 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             }
             __syncwarp();
         }
-        // Wait (bounded) for the MMAs of the last tiles before releasing TMEM.
-        for (int64_t k = (it > 2 ? it - 2 : 0); k < it; ++k)
-            (void)mbar_wait(bar_acc_full + 8 * static_cast<int>(k & 1),
-                            static_cast<uint32_t>((k >> 1) & 1));
+        // Wait (bounded) for this warp's last MMAs before TMEM is released.
+        if (it >= 2)
+            (void)mbar_wait(bar_acc_full + 8 * a, static_cast<uint32_t>(((it - 2) >> 1) & 1));
     } else {
         // ---------------- epilogue ----------------
-        const int e = warp - 2;
+        const int e = warp - kFirstEpiWarp;
         const int grp = e >> 3;               // takes tiles (and buffers) with it % 2 == grp
         const int b = (e >> 2) & 1;           // block of the tile
         const int qtr = warp & 3;             // TMEM lane quarter this warp may access
@@ -261,15 +269,16 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int r = qtr * 32 + lane;        // row within the tile
         int64_t it = grp;
         bool ok = true;
-        for (TileWalk tw(blockIdx.x + grp * static_cast<int64_t>(gridDim.x),
-                         2 * static_cast<int64_t>(gridDim.x), p.ncol_tiles);
-             tw.rt < p.nrow_tiles; tw.next(), it += 2) {
+        TileWalk tw(blockIdx.x + grp * static_cast<int64_t>(gridDim.x),
+                    2 * static_cast<int64_t>(gridDim.x), p.ncol_tiles);
+        for (; tw.rt < p.nrow_tiles; tw.next(), it += 2) {
             const int a = grp;
-            const int64_t rt = tw.rt, ct = tw.ct;
-            const int64_t j = ct * 2 + b;
-            const int64_t row = rt * kBR + r;
+            const int rt = tw.rt, ct = tw.ct;
+            const int j = ct * 2 + b;
+            const int row = rt * kBR + r;
             const uint32_t stg = base + Cfg::kStgOff + (grp * 2 + ((it >> 1) & 1)) * Cfg::kStgBytes;
-            // G1 of this block: the fp32 entries at byte 1536 of its operand record
+            // G1 of this block: the fp32 entries at byte 1536 of its operand
+            // record (issued before the accumulator wait, which hides its latency)
             float4 g1 = make_float4(0.f, 0.f, 0.f, 0.f);
             if (j < p.nb)
                 g1 = ldg_nc_f4(reinterpret_cast<const float *>(records + j * Cfg::kRecBytes + 1536));
@@ -286,16 +295,19 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                     uint32_t rr[32];
                     float z0[16], z1[16];
                     tmem_ld32(tb, rr);           // Z0^hi, Z0^mid
+                    tmem_wait_ld();
 #pragma unroll
                     for (int n = 0; n < 16; ++n)
                         z0[n] = __uint_as_float(rr[n]) + __uint_as_float(rr[16 + n]);
                     tmem_ld32(tb + 32, rr);      // Z0^lo, Z1^hi
+                    tmem_wait_ld();
 #pragma unroll
                     for (int n = 0; n < 16; ++n) {
                         z0[n] += __uint_as_float(rr[n]);
                         z1[n] = __uint_as_float(rr[16 + n]);
                     }
                     tmem_ld32(tb + 64, rr);      // Z1^mid, Z1^lo
+                    tmem_wait_ld();
 #pragma unroll
                     for (int n = 0; n < 16; ++n)
                         z1[n] = (z1[n] + __uint_as_float(rr[n])) + __uint_as_float(rr[16 + n]);
@@ -311,8 +323,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                         Y[t] = __ffma2_rn(zz1, a10, __fmul2_rn(zz0, a00));
                         Y[8 + t] = __ffma2_rn(zz1, a11, __fmul2_rn(zz0, a01));
                     }
-                    if (p.y_debug != nullptr && row < p.m) {
-                        float *yd = p.y_debug + row * p.d + j * 32;
+                    if (DEBUG && row < p.m) {
+                        float *yd = p.y_debug + static_cast<int64_t>(row) * p.d + j * 32;
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
                             stg_f4(yd + 4 * k, make_float4(Y[2 * k].x, Y[2 * k].y, Y[2 * k + 1].x,
@@ -360,12 +372,12 @@ struct USlot {
     cudaError_t err[64] = {};
 };
 
-template <int STAGES>
+template <int STAGES, bool DEBUG>
 kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, QuantParams p,
                       const uint8_t *records, int sm_count, cudaStream_t stream)
 {
     using Cfg = UCfg<STAGES>;
-    auto kern = quant_umma_kernel<STAGES>;
+    auto kern = quant_umma_kernel<STAGES, DEBUG>;
     static USlot slot;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
@@ -403,8 +415,9 @@ kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expand
     st = make_tensor_map_2d_u8(&mapq, p.q, p.m, p.d / 2, p.ldq, 32, kBR,
                                CU_TENSOR_MAP_SWIZZLE_32B);
     if (st != KQ_OK) return st;
-    return launch_umma<8>(map, mapq, p, static_cast<const uint8_t *>(K_expanded), info.sm_count,
-                          stream);
+    const uint8_t *rec = static_cast<const uint8_t *>(K_expanded);
+    if (p.y_debug != nullptr) return launch_umma<8, true>(map, mapq, p, rec, info.sm_count, stream);
+    return launch_umma<8, false>(map, mapq, p, rec, info.sm_count, stream);
 }
 
 }  // namespace kq
