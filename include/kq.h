@@ -82,11 +82,12 @@ typedef enum kq_sf_layout {
 typedef enum kq_kfmt {
     KQ_K_FP32 = 0,      /* dense K_j, fp32 row-major [nb][32][32] */
     KQ_K_BF16X3 = 1     /* operand records of the tensor-core variants (opaque,
-                           2 x 1552 bytes per block): K_j = G1 (x) K'_j with
-                           K'_j = G2 (x) G3 (x) G4 (x) G5 expanded to its dense
-                           16x16 block as three bf16 terms hi + mid + lo, once
-                           in the tcgen05 shared-memory operand layout and once
-                           in mma.sync fragment order, each with G1 in fp32 */
+                           6144 + 1552 bytes per block), each a three-term bf16
+                           split hi + mid + lo: first nb tcgen05 records (the
+                           dense 32x32 K_j in the shared-memory operand
+                           layout), then nb mma.sync records (K'_j = G2 (x) G3
+                           (x) G4 (x) G5 as a 16x16 block in fragment order,
+                           plus G1 in fp32) */
 } kq_kfmt;
 
 /* Alignment rules shared by the quantizer entry points:

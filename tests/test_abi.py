@@ -58,7 +58,7 @@ def test_sf_bytes_matches_oracle(L, oracle_lib):
 
 def test_expanded_bytes(L):
     assert kq.kq_expanded_bytes(36, kq.KQ_K_FP32) == 36 * 4096
-    assert kq.kq_expanded_bytes(36, kq.KQ_K_BF16X3) == 36 * 2 * 1552
+    assert kq.kq_expanded_bytes(36, kq.KQ_K_BF16X3) == 36 * (6144 + 1552)
     assert kq.kq_expanded_bytes(0, kq.KQ_K_FP32) == 0
 
 

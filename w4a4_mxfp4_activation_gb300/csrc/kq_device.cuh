@@ -250,6 +250,15 @@ __device__ __forceinline__ float inv_scale(uint32_t byte)
     return __uint_as_float((254u - byte) << 23);
 }
 
+// max(a, b, c) in one instruction (3-input max.f32; a NaN input is ignored
+// like fmaxf does).
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Eight fp32 values -> eight E2M1 codes packed in a word, value 0 in bits 0-3.
 // cvt.rn.satfinite.e2m1x2.f32 d, a, b puts a in the high nibble of d and b in
 // the low nibble.
@@ -272,18 +281,17 @@ __device__ __forceinline__ uint32_t e2m1x8(float v0, float v1, float v2, float v
 // Returns the packed codes (16 bytes) and writes the scale byte.
 __device__ __forceinline__ uint4 quantize_block(const float2 (&Y)[16], uint32_t &byte_out)
 {
-    float m0 = fmaxf(fabsf(Y[0].x), fabsf(Y[0].y));
-    float m1 = fmaxf(fabsf(Y[1].x), fabsf(Y[1].y));
-    float m2 = fmaxf(fabsf(Y[2].x), fabsf(Y[2].y));
-    float m3 = fmaxf(fabsf(Y[3].x), fabsf(Y[3].y));
+    // four independent chains of 3-input maxima over |y|
+    float m[4];
 #pragma unroll
-    for (int t = 4; t < 16; t += 4) {
-        m0 = fmaxf(m0, fmaxf(fabsf(Y[t + 0].x), fabsf(Y[t + 0].y)));
-        m1 = fmaxf(m1, fmaxf(fabsf(Y[t + 1].x), fabsf(Y[t + 1].y)));
-        m2 = fmaxf(m2, fmaxf(fabsf(Y[t + 2].x), fabsf(Y[t + 2].y)));
-        m3 = fmaxf(m3, fmaxf(fabsf(Y[t + 3].x), fabsf(Y[t + 3].y)));
+    for (int c = 0; c < 4; ++c) {
+        const float2 p0 = Y[4 * c], p1 = Y[4 * c + 1], p2 = Y[4 * c + 2], p3 = Y[4 * c + 3];
+        float t = fmax3(fabsf(p0.x), fabsf(p0.y), fabsf(p1.x));
+        t = fmax3(t, fabsf(p1.y), fabsf(p2.x));
+        t = fmax3(t, fabsf(p2.y), fabsf(p3.x));
+        m[c] = fmaxf(t, fabsf(p3.y));
     }
-    const float amax = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+    const float amax = fmax3(fmaxf(m[0], m[1]), m[2], m[3]);
     const uint32_t byte = e8m0_byte(amax);
     const float s = inv_scale(byte);
     const float2 s2 = make_float2(s, s);

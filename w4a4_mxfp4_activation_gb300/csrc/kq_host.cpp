@@ -7,6 +7,7 @@
 #include <cstdint>
 
 #include "kq.h"
+#include "kq_records.h"
 
 extern "C" {
 
@@ -38,7 +39,8 @@ size_t kq_expanded_bytes(int64_t nb, kq_kfmt fmt)
 {
     if (nb <= 0) return 0;
     if (fmt == KQ_K_FP32) return static_cast<size_t>(nb) * 32 * 32 * 4;
-    if (fmt == KQ_K_BF16X3) return static_cast<size_t>(nb) * 2 * 1552;   // two record sets
+    if (fmt == KQ_K_BF16X3)      // two record sets
+        return static_cast<size_t>(nb) * (kq::kUmmaRecordBytes + kq::kMmaRecordBytes);
     return 0;
 }
 

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "kq.h"
+#include "kq_records.h"
 
 namespace kq {
 
@@ -56,9 +57,6 @@ kq_status launch_quant_mma(const uint16_t *A, int64_t lda, const void *K_expande
 kq_status launch_mma_records(const float *factors, int64_t nb, void *out, cudaStream_t stream);
 kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expanded,
                             const QuantParams &p, cudaStream_t stream);
-
-// Bytes of one block's operand record for the tensor-core variant.
-constexpr int64_t kMmaRecordBytes = 1552;
 
 kq_status validate_quant_args(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
                               const uint8_t *q, int64_t ldq, const uint8_t *sf,

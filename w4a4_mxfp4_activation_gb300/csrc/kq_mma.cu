@@ -42,7 +42,7 @@
 namespace kq {
 namespace {
 
-constexpr int kRecordBytes = 1552;
+constexpr int kRecordBytes = static_cast<int>(kMmaRecordBytes);
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;
@@ -347,31 +347,31 @@ __global__ void mma_records_kernel(const float *__restrict__ factors, int64_t nb
     }
 }
 
-// Records of the tcgen05 variant: per block, the three bf16 terms of
-// K'^T (n = output channel, k = input channel, both 0..15) in the
-// no-swizzle K-major operand layout -- 8 x 16-byte core matrices, core
-// (n / 8, k / 8) at (n / 8) * 256 + (k / 8) * 128, row n % 8 at 16 B,
-// element k % 8 at 2 B; 512 B per term -- then G1 (fp32) at byte 1536.
+// Records of the tcgen05 variant: per block, the dense K_j = G1 (x) K'_j
+// (entries in fp64, eq. 12) as three bf16 terms, arranged as the B operands
+// of the block's two K = 16 steps.  Step h (input channels 16 h .. 16 h + 15)
+// occupies bytes [3072 h, 3072 h + 3072): B^T with n = 32 t + c (term t,
+// output channel c) and k = input channel - 16 h, in the no-swizzle K-major
+// layout -- 8 x 16-byte core matrices, core (n / 8, k / 8) at
+// (n / 8) * 256 + (k / 8) * 128, row n % 8 at 16 B, element k % 8 at 2 B.
 __global__ void umma_records_kernel(const float *__restrict__ factors, int64_t nb,
                                     uint8_t *__restrict__ out)
 {
-    constexpr int kWords = 3 * 16 * 8 + 4;
+    constexpr int kWords = static_cast<int>(kUmmaRecordBytes / 4);   // element pairs
     const int64_t n = nb * kWords;
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t j = idx / kWords;
         const int w = static_cast<int>(idx % kWords);
         const float *f = factors + j * 20;
-        uint8_t *rec = out + j * kRecordBytes;
-        if (w >= 3 * 16 * 8) {                    // G1 entries
-            reinterpret_cast<uint32_t *>(rec + 1536)[w - 384] = __float_as_uint(f[w - 384]);
-            continue;
-        }
-        const int t = w / 128, ncol = (w / 8) % 16, kp = w % 8;
-        const int k0 = 2 * kp;
-        const uint16_t e0 = bf16_term(kron_tail(f, k0, ncol), t);
-        const uint16_t e1 = bf16_term(kron_tail(f, k0 + 1, ncol), t);
-        const int off = t * 512 + (ncol >> 3) * 256 + (k0 >> 3) * 128 + (ncol & 7) * 16 + (k0 & 7) * 2;
+        uint8_t *rec = out + j * kUmmaRecordBytes;
+        const int h = w / 768, nn = (w / 8) % 96, kp = w % 8;
+        const int t = nn / 32, c = nn % 32, k0 = 2 * kp, r0 = 16 * h + k0;
+        // K_j[r][c] = G1[bit4(r)][bit4(c)] * K'_j[r % 16][c % 16]
+        const double g0 = static_cast<double>(f[((r0 >> 4) & 1) * 2 + ((c >> 4) & 1)]);
+        const uint16_t e0 = bf16_term(g0 * kron_tail(f, r0 & 15, c & 15), t);
+        const uint16_t e1 = bf16_term(g0 * kron_tail(f, (r0 + 1) & 15, c & 15), t);
+        const int off = h * 3072 + (nn >> 3) * 256 + (k0 >> 3) * 128 + (nn & 7) * 16 + (k0 & 7) * 2;
         *reinterpret_cast<uint32_t *>(rec + off) = static_cast<uint32_t>(e0) |
                                                    (static_cast<uint32_t>(e1) << 16);
     }
@@ -391,7 +391,7 @@ kq_status launch_quant_mma(const uint16_t *A, int64_t lda, const void *K_expande
     if (st != KQ_OK) return st;
     // the mma.sync records follow the nb tcgen05 records
     return launch_mma<BR, 4>(map, p,
-                             static_cast<const uint8_t *>(K_expanded) + p.nb * kRecordBytes,
+                             static_cast<const uint8_t *>(K_expanded) + p.nb * kUmmaRecordBytes,
                              info.sm_count, stream);
 }
 
@@ -399,12 +399,12 @@ kq_status launch_quant_mma(const uint16_t *A, int64_t lda, const void *K_expande
 kq_status launch_mma_records(const float *factors, int64_t nb, void *out, cudaStream_t stream)
 {
     uint8_t *o = static_cast<uint8_t *>(out);
-    const int64_t work_u = nb * (3 * 16 * 8 + 4);
+    const int64_t work_u = nb * (kUmmaRecordBytes / 4);
     umma_records_kernel<<<static_cast<int>(std::min<int64_t>((work_u + 255) / 256, 4096)), 256, 0,
                           stream>>>(factors, nb, o);
     const int64_t work = nb * (32 * 12 + 4);
     mma_records_kernel<<<static_cast<int>(std::min<int64_t>((work + 255) / 256, 4096)), 256, 0,
-                         stream>>>(factors, nb, o + nb * kRecordBytes);
+                         stream>>>(factors, nb, o + nb * kUmmaRecordBytes);
     return check_launch();
 }
 

@@ -2,28 +2,28 @@
 // cores (tcgen05.mma, accumulators in TMEM), sm_103a.
 //
 // "KroQuant: Kronecker-Structured Block Transforms for Efficient Post-
-// Training Quantization of Diffusion Transformers", eq. (5) and (12): with
-// K_j = G1 (x) K'_j and K'_j = G2 (x) G3 (x) G4 (x) G5 (16 x 16), the row
-// transform of a 32-channel block splits over its two 16-channel halves:
-//     Z_h = a_h . K'_j,   y_0 = G1[0][0] Z_0 + G1[1][0] Z_1,
-//                         y_1 = G1[0][1] Z_0 + G1[1][1] Z_1.
-// The 16x16 products run as tcgen05.mma (bf16 operands, fp32 accumulation in
-// TMEM) against K'_j pre-expanded once per layer by kq_expand_blocks as three
-// bf16 terms hi + mid + lo (exact to about 2^-24 relative; the activations
-// are exact in bf16).  The three terms sit side by side along N: one
-// M = 128, N = 48, K = 16 MMA per (block, half) reads its A slice from shared
-// memory once, and the epilogue adds the three partial products.  (Issuing
-// one N = 16 MMA per term re-reads A three times; measured on GB300 that
-// made the tensor-core reads of A the bottleneck.)
-// The G1 stage and the MXFP4 encoding run on the CUDA cores after the
-// accumulators are read back with tcgen05.ld (one thread = one row of a
-// 32-channel block, all 32 values in registers).
+// Training Quantization of Diffusion Transformers", eq. (5) and (12): the
+// row transform y = a . K_j of a 32-channel block runs as tcgen05.mma (bf16
+// operands, fp32 accumulation in TMEM) against the dense 32 x 32 K_j =
+// G1 (x) G2 (x) G3 (x) G4 (x) G5, expanded once per layer by kq_expand_blocks
+// (entries in fp64) as three bf16 terms hi + mid + lo (exact to about 2^-24
+// relative; the activations are exact in bf16).  The three terms sit side by
+// side along N: per block two M = 128, N = 96, K = 16 MMAs (one per
+// 16-channel input half, accumulating) read each A slice from shared memory
+// once, and the epilogue adds the three partial results.  (One MMA per term
+// would re-read A three times; measured on GB300, the tensor core's reads of
+// A then became the bottleneck.  Keeping G1 out of the operands and applying
+// it on the CUDA cores was measured too: the epilogue, not the tensor core,
+// limits this kernel, so the whole transform goes to the tensor core.)
+// The MXFP4 encoding runs on the CUDA cores after the accumulators are read
+// back with tcgen05.ld (one thread = one row of a 32-channel block, all 32
+// values in registers).
 //
 // Roles in a CTA (one CTA per SM, persistent over tiles of 128 rows x 64
 // channels = 2 blocks = one 128B-swizzled TMA box):
 //   warp 0      TMA producer: the A box + one bulk copy of the tile's two
-//               operand records (1552 B each: the three 16x16 bf16 terms in
-//               the no-swizzle K-major layout and G1) into a STAGES-deep
+//               operand records (6 KB each: the three bf16 terms of K_j in
+//               the no-swizzle K-major layout) into a STAGES-deep
 //               shared-memory ring;
 //   warps 1-2   MMA issuers, one per accumulator buffer (2 x 192 TMEM columns,
 //               allocated by warp 1): warp 1 + m takes the CTA's tiles with
@@ -32,11 +32,11 @@
 //               ring's empty barrier and to the accumulator's full barrier;
 //   warps 3-18  epilogue, two groups of 8 warps taking alternate tiles (and
 //               accumulator buffers): warp w reads TMEM lanes 32 (w % 4)..+31
-//               (rows) of one block, sums the terms, applies G1 and quantizes;
-//               the codes of the tile go to a shared staging buffer (32-byte
-//               swizzle) and leave with one TMA store of 128 rows x 32 bytes
-//               (a thread owns a row, so direct 16-byte stores from a warp
-//               would touch 32 rows and clog the memory pipe).
+//               (rows) of one block, sums the terms and quantizes;
+//               each warp's 32 x 16 bytes of codes go to its own shared
+//               staging buffer and leave with one TMA store (a thread owns a
+//               row, so direct 16-byte stores from a warp would touch 32 rows
+//               and clog the memory pipe).
 // Every wait is bounded in time; a timed-out epilogue writes the E8M0 NaN
 // byte 0xFF as the scale of the blocks it could not finish.
 #include <cuda_bf16.h>
@@ -56,7 +56,7 @@ constexpr int kMmaWarps = 2;                   // one per accumulator buffer
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
 constexpr int kThreadsU = (kFirstEpiWarp + kEpiWarps) * 32;
 constexpr int kBR = 128;                       // rows per tile (= MMA M)
-constexpr int kBlockCols = 96;                 // per block: 2 halves x 3 terms x 16
+constexpr int kBlockCols = 96;                 // per block: 3 terms x 32 outputs
 constexpr int kAccCols = 2 * kBlockCols;       // fp32 columns per accumulator buffer
 constexpr int kTmemCols = 512;                 // 2 buffers (384 columns), power of two
 
@@ -64,14 +64,14 @@ template <int STAGES>
 struct UCfg {
     static constexpr int kABytes = kBR * 128;                 // 128 rows x 64 bf16 = 16 KB
     static constexpr int kBOff = kABytes;                     // operand records
-    static constexpr int kRecBytes = 1552;                    // 3 terms + G1
-    static constexpr int kStageBytes = kABytes + 4096;        // 2 records, padded: 20 KB
+    static constexpr int kRecBytes = static_cast<int>(kUmmaRecordBytes);   // 3 terms of K_j
+    static constexpr int kStageBytes = kABytes + 2 * kRecBytes;          // 28 KB
     // after the ring: barriers + TMEM base (1 KB), 1 KB spare, code staging
-    // for the TMA stores: 2 groups x 2 buffers x 128 rows x 32 B
+    // for the TMA stores: per epilogue warp 2 buffers of 32 rows x 16 B
     static constexpr int kBarOff = STAGES * kStageBytes;
     static constexpr int kStgOff = kBarOff + 2048;
-    static constexpr int kStgBytes = kBR * 32;
-    static constexpr int kSmemBytes = kStgOff + 4 * kStgBytes + 1024;   // + alignment slack
+    static constexpr int kStgBytes = 32 * 16;
+    static constexpr int kSmemBytes = kStgOff + kEpiWarps * 2 * kStgBytes + 1024;   // + slack
     static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
 
@@ -105,8 +105,8 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N = 48 (three 16-column terms), M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((48u >> 3) << 17) |
+// K-major, N = 96 (three 32-column terms), M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((96u >> 3) << 17) |
                             ((128u >> 4) << 24);
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
@@ -246,11 +246,12 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             if (lane == 0) {
                 const uint32_t d0 = tmem_base + a * kAccCols;
                 for (int b = 0; b < nblk; ++b)
-                    for (int h = 0; h < 2; ++h)
-                        umma_bf16(d0 + b * kBlockCols + h * 48,
+                    for (int h = 0; h < 2; ++h)       // input half h: K = 16 step
+                        umma_bf16(d0 + b * kBlockCols,
                                   smem_desc(stage + 64 * b + 32 * h, 16, 1024, 2),
-                                  smem_desc(stage + Cfg::kBOff + b * Cfg::kRecBytes, 128, 256, 0),
-                                  0u);
+                                  smem_desc(stage + Cfg::kBOff + b * Cfg::kRecBytes + h * 3072,
+                                            128, 256, 0),
+                                  static_cast<uint32_t>(h));
                 umma_commit(bar_empty + 8 * s);          // ring stage free once the MMAs read it
                 umma_commit(bar_acc_full + 8 * a);       // accumulators ready
             }
@@ -265,9 +266,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int grp = e >> 3;               // takes tiles (and buffers) with it % 2 == grp
         const int b = (e >> 2) & 1;           // block of the tile
         const int qtr = warp & 3;             // TMEM lane quarter this warp may access
-        const bool leader = (e & 7) == 0 && lane == 0;
         const int r = qtr * 32 + lane;        // row within the tile
-        int64_t it = grp;
+        int it = grp;
         bool ok = true;
         TileWalk tw(blockIdx.x + grp * static_cast<int64_t>(gridDim.x),
                     2 * static_cast<int64_t>(gridDim.x), p.ncol_tiles);
@@ -276,12 +276,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             const int rt = tw.rt, ct = tw.ct;
             const int j = ct * 2 + b;
             const int row = rt * kBR + r;
-            const uint32_t stg = base + Cfg::kStgOff + (grp * 2 + ((it >> 1) & 1)) * Cfg::kStgBytes;
-            // G1 of this block: the fp32 entries at byte 1536 of its operand
-            // record (issued before the accumulator wait, which hides its latency)
-            float4 g1 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (j < p.nb)
-                g1 = ldg_nc_f4(reinterpret_cast<const float *>(records + j * Cfg::kRecBytes + 1536));
+            const uint32_t stg = base + Cfg::kStgOff + (e * 2 + ((it >> 1) & 1)) * Cfg::kStgBytes;
             if (ok) ok = __all_sync(0xffffffffu,
                                     mbar_wait(bar_acc_full + 8 * a, static_cast<uint32_t>((it >> 1) & 1)));
             uint4 codes = make_uint4(0u, 0u, 0u, 0u);
@@ -289,40 +284,26 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                 tc_fence_after();
                 float2 Y[16];
                 if (j < p.nb) {
-                    // columns: half 0 terms 0..2, half 1 terms 0..2 (16 each)
+                    // columns: term hi, mid, lo (32 outputs each); y = (hi + mid) + lo
                     const uint32_t tb = tmem_base + (static_cast<uint32_t>(qtr * 32) << 16) +
                                         a * kAccCols + b * kBlockCols;
-                    uint32_t rr[32];
-                    float z0[16], z1[16];
-                    tmem_ld32(tb, rr);           // Z0^hi, Z0^mid
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tb, r0);
+                    tmem_ld32(tb + 32, r1);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int n = 0; n < 16; ++n)
-                        z0[n] = __uint_as_float(rr[n]) + __uint_as_float(rr[16 + n]);
-                    tmem_ld32(tb + 32, rr);      // Z0^lo, Z1^hi
+                    for (int t = 0; t < 16; ++t)
+                        Y[t] = __fadd2_rn(
+                            make_float2(__uint_as_float(r0[2 * t]), __uint_as_float(r0[2 * t + 1])),
+                            make_float2(__uint_as_float(r1[2 * t]), __uint_as_float(r1[2 * t + 1])));
+                    tmem_ld32(tb + 64, r0);
                     tmem_wait_ld();
-#pragma unroll
-                    for (int n = 0; n < 16; ++n) {
-                        z0[n] += __uint_as_float(rr[n]);
-                        z1[n] = __uint_as_float(rr[16 + n]);
-                    }
-                    tmem_ld32(tb + 64, rr);      // Z1^mid, Z1^lo
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int n = 0; n < 16; ++n)
-                        z1[n] = (z1[n] + __uint_as_float(rr[n])) + __uint_as_float(rr[16 + n]);
                     tc_fence_before();
                     mbar_arrive(bar_acc_empty + 8 * a);
-                    // G1 stage: y_0 = g00 Z_0 + g10 Z_1, y_1 = g01 Z_0 + g11 Z_1
-                    const float2 a00 = make_float2(g1.x, g1.x), a01 = make_float2(g1.y, g1.y);
-                    const float2 a10 = make_float2(g1.z, g1.z), a11 = make_float2(g1.w, g1.w);
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) {
-                        const float2 zz0 = make_float2(z0[2 * t], z0[2 * t + 1]);
-                        const float2 zz1 = make_float2(z1[2 * t], z1[2 * t + 1]);
-                        Y[t] = __ffma2_rn(zz1, a10, __fmul2_rn(zz0, a00));
-                        Y[8 + t] = __ffma2_rn(zz1, a11, __fmul2_rn(zz0, a01));
-                    }
+                    for (int t = 0; t < 16; ++t)
+                        Y[t] = __fadd2_rn(Y[t], make_float2(__uint_as_float(r0[2 * t]),
+                                                            __uint_as_float(r0[2 * t + 1])));
                     if (DEBUG && row < p.m) {
                         float *yd = p.y_debug + static_cast<int64_t>(row) * p.d + j * 32;
 #pragma unroll
@@ -341,21 +322,21 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             } else if (j < p.nb && row < p.m_rows) {
                 store_scale_u(p, row, j, 0xFFu);
             }
-            // Codes -> staging buffer -> one TMA store per tile.  Every thread of
-            // the group passes both barriers on every tile, whatever happened above.
-            if (leader) bulk_wait_group_read<1>();        // this buffer's previous store has read it
-            named_barrier(1 + grp, kEpiThreads / 2);
-            sts128(stg + r * 32 + ((b ^ ((r >> 2) & 1)) << 4), codes);
+            // Codes -> this warp's staging buffer -> one TMA store of 32 rows x
+            // 16 bytes.  Lane 0 issues the stores; the buffer was last read by
+            // the store two tiles ago.
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            sts128(stg + lane * 16, codes);
             fence_proxy_async_smem();
-            named_barrier(1 + grp, kEpiThreads / 2);
-            if (leader) {
-                if (ct * 2 < p.nb)      // padding tiles of the scale layout have no codes
-                    tma_store_2d(&tmQ, static_cast<int32_t>(ct * 32),
-                                 static_cast<int32_t>(rt * kBR), stg);
+            __syncwarp();
+            if (lane == 0) {
+                if (j < p.nb)
+                    tma_store_2d(&tmQ, j * 16, rt * kBR + qtr * 32, stg);
                 bulk_commit_group();
             }
         }
-        if (leader) bulk_wait_group_all();
+        if (lane == 0) bulk_wait_group_all();
     }
 
     tc_fence_before();
@@ -412,12 +393,12 @@ kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expand
     CUtensorMap map, mapq;
     st = make_tensor_map_2d_bf16(&map, A, p.m, p.d, lda, 64, kBR);
     if (st != KQ_OK) return st;
-    st = make_tensor_map_2d_u8(&mapq, p.q, p.m, p.d / 2, p.ldq, 32, kBR,
-                               CU_TENSOR_MAP_SWIZZLE_32B);
+    st = make_tensor_map_2d_u8(&mapq, p.q, p.m, p.d / 2, p.ldq, 16, 32,
+                               CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != KQ_OK) return st;
     const uint8_t *rec = static_cast<const uint8_t *>(K_expanded);
-    if (p.y_debug != nullptr) return launch_umma<8, true>(map, mapq, p, rec, info.sm_count, stream);
-    return launch_umma<8, false>(map, mapq, p, rec, info.sm_count, stream);
+    if (p.y_debug != nullptr) return launch_umma<7, true>(map, mapq, p, rec, info.sm_count, stream);
+    return launch_umma<7, false>(map, mapq, p, rec, info.sm_count, stream);
 }
 
 }  // namespace kq
