@@ -55,7 +55,9 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=40000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--variant", choices=("butterfly", "mma", "umma"), default="butterfly")
+    ap.add_argument("--variant", choices=("butterfly", "mma", "umma"), default="umma",
+                    help="KroQuant kernel: tcgen05 (umma, default), mma.sync, or the CUDA-core "
+                         "butterfly")
     ap.add_argument("--no-baselines", action="store_true",
                     help="skip the diagonal / Hadamard / bare-quantizer side measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -125,10 +127,16 @@ def hbm_peak():
 
 
 def kernel_source_hash() -> str:
+    """Hash of every CUDA / C++ source and header the library is built from."""
+    import glob
     h = hashlib.sha256()
-    for rel in ("w4a4_mxfp4_activation_gb300/csrc/kq_quant.cu",
-                "w4a4_mxfp4_activation_gb300/csrc/kq_device.cuh"):
-        with open(os.path.join(ROOT, rel), "rb") as f:
+    csrc = os.path.join(ROOT, "w4a4_mxfp4_activation_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
+                   + glob.glob(os.path.join(csrc, "*.h")) + glob.glob(os.path.join(csrc, "*.cpp"))
+                   + [os.path.join(ROOT, "include", "kq.h")])
+    for path in files:
+        h.update(os.path.basename(path).encode())
+        with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 

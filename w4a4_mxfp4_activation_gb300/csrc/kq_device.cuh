@@ -250,6 +250,21 @@ __device__ __forceinline__ float inv_scale(uint32_t byte)
     return __uint_as_float((254u - byte) << 23);
 }
 
+// Programmatic dependent launch: returns once the grids this one depends on
+// have completed and their memory is visible (at once when there are none).
+// The persistent quantizers are launched with programmatic stream
+// serialization and call this after their shared-memory / TMEM setup and
+// before their first global-memory access, so the launch of a quantizer
+// overlaps the end of the previous kernel while every read of A and write of
+// q / sf stays ordered after it.  They do not trigger their own dependents
+// early (griddepcontrol.launch_dependents): measured on GB300, a dependent
+// grid pending from the start of a 27 us quantizer slowed it by 1.2 us,
+// while the implicit trigger at grid end keeps the launch-latency overlap.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // max(a, b, c) in one instruction (3-input max.f32; a NaN input is ignored
 // like fmaxf does).
 __device__ __forceinline__ float fmax3(float a, float b, float c)

@@ -50,6 +50,27 @@ kq_status make_tensor_map_2d_u8(CUtensorMap *map, void *base, int64_t rows, int6
                                 CUtensorMapSwizzle swizzle);
 kq_status check_launch();
 
+// Launches a persistent quantizer kernel with programmatic stream
+// serialization: the launch may begin while the previous kernel of the
+// stream is still running; the kernel orders its global-memory accesses
+// after that kernel with griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+kq_status launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem,
+                     cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...) == cudaSuccess ? KQ_OK : KQ_ERR_CUDA;
+}
+
 kq_status launch_quant_tma(Transform t, const uint16_t *A, int64_t lda, const QuantParams &p,
                            cudaStream_t stream);
 kq_status launch_quant_mma(const uint16_t *A, int64_t lda, const void *K_expanded,

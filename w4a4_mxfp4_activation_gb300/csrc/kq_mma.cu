@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_fence_init();
     }
     __syncthreads();
+    grid_dependency_wait();
 
     if (warp == kConsumerWarps) {
         if (lane != 0) return;
@@ -292,8 +293,7 @@ kq_status launch_mma(const CUtensorMap &map, QuantParams p, const uint8_t *recor
     if (p.ntiles == 0) return KQ_OK;
     const int64_t resident = static_cast<int64_t>(slot.occupancy[dev]) * sm_count;
     const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, resident));
-    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(map, p, records);
-    return check_launch();
+    return launch_pdl(kern, grid, kThreads, Cfg::kSmemBytes, stream, map, p, records);
 }
 
 // ---- operand records (kq_expand_blocks, KQ_K_BF16X3) ------------------------------

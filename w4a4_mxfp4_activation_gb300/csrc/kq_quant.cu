@@ -178,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         mbar_fence_init();
     }
     __syncthreads();
+    grid_dependency_wait();
 
     if (warp == kConsumerWarps) {
         // ---------------- producer: one thread issues the TMA loads ----------------
@@ -311,8 +312,7 @@ kq_status launch_one(const CUtensorMap &map, QuantParams p, int sm_count, cudaSt
     if (p.ntiles == 0) return KQ_OK;
     const int64_t resident = static_cast<int64_t>(slot.occupancy[dev]) * sm_count;
     const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, resident));
-    kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(map, p);
-    return check_launch();
+    return launch_pdl(kern, grid, kThreads, Cfg::kSmemBytes, stream, map, p);
 }
 
 template <int T>

@@ -73,6 +73,13 @@ struct UCfg {
     static constexpr int kStgBytes = 32 * 16;
     static constexpr int kSmemBytes = kStgOff + kEpiWarps * 2 * kStgBytes + 1024;   // + slack
     static_assert(kStageBytes % 1024 == 0, "stage alignment");
+    // The two MMA issuers take alternate tiles and wait on the ring's full
+    // barriers by phase parity.  With an even ring every stage is always
+    // consumed by the same issuer, which has itself consumed the stage's
+    // previous phase; with an odd ring an issuer could wait on phase k of a
+    // stage whose phase k - 1 (the other issuer's tile) is still in flight,
+    // and the parity test would pass on phase k - 2.
+    static_assert(STAGES % 2 == 0, "each ring stage must belong to one MMA issuer");
 };
 
 // ---- tcgen05 wrappers ---------------------------------------------------------------
@@ -197,6 +204,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     tc_fence_after();
     uint32_t tmem_base;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(tmem_base) : "r"(tmem_slot) : "memory");
+    grid_dependency_wait();
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -378,8 +386,7 @@ kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, QuantPara
     if (p.ntiles == 0) return KQ_OK;
     // one CTA per SM: each holds 256 of the SM's 512 TMEM columns
     const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, sm_count));
-    kern<<<grid, kThreadsU, Cfg::kSmemBytes, stream>>>(map, mapq, p, records);
-    return check_launch();
+    return launch_pdl(kern, grid, kThreadsU, Cfg::kSmemBytes, stream, map, mapq, p, records);
 }
 
 }  // namespace
@@ -397,8 +404,8 @@ kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expand
                                CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != KQ_OK) return st;
     const uint8_t *rec = static_cast<const uint8_t *>(K_expanded);
-    if (p.y_debug != nullptr) return launch_umma<7, true>(map, mapq, p, rec, info.sm_count, stream);
-    return launch_umma<7, false>(map, mapq, p, rec, info.sm_count, stream);
+    if (p.y_debug != nullptr) return launch_umma<6, true>(map, mapq, p, rec, info.sm_count, stream);
+    return launch_umma<6, false>(map, mapq, p, rec, info.sm_count, stream);
 }
 
 }  // namespace kq
