@@ -38,6 +38,7 @@ METRIC = "KroQuant MXFP4 quantizer GB/s and % HBM peak; speedup vs diag-scale qu
 LAYERS = (("flux_3072", 4608, 3072), ("flux_ffn_down", 4608, 12288))
 DOMINANT = 1                        # the d = 12288 launch dominates the step
 SETS = 4
+ROUND = 8 * SETS                    # steps per replay of a layer's CUDA graph
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -244,11 +245,23 @@ def cpu_cores() -> int:
 
 
 def cpu_baseline(budget_s: float):
+    """The oracle on the host cores: a row sample of the step sized to about
+    budget_s seconds; when the whole step takes less, whole steps repeated."""
     _, t16, _ = cpu_oracle_rate(16)
     rows = max(16, min(LAYERS[0][1], int(16 * budget_s / max(t16, 1e-3))))
-    rate, dt, _ = cpu_oracle_rate(rows)
+    rate, dt, nbytes = cpu_oracle_rate(rows)
+    passes = 1
+    if rows == LAYERS[0][1] and dt < 0.5 * budget_s:
+        extra = max(1, int((budget_s - dt) / max(dt, 1e-3)))
+        for p in range(extra):
+            _, d2, n2 = cpu_oracle_rate(rows, seed=1 + p)
+            dt += d2
+            nbytes += n2
+        passes += extra
+        rate = nbytes / dt / 1e9
+    what = (f"all {rows} rows" if rows == LAYERS[0][1] else f"first {rows} rows")
     return {"value": round(rate, 4), "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"first {rows} rows of each FLUX layer (m=4608, d=3072 and 12288), "
+            "sample": f"{what} of each FLUX layer (m=4608, d=3072 and 12288), {passes} pass(es), "
                       f"{dt:.1f} s of CPU work"}
 
 
@@ -336,53 +349,86 @@ def run_ours(args, dist: Dist):
     DIAG = [torch.from_numpy(synth.smooth_scales(d)).to(dev) for _, _, d in LAYERS]
 
     def graphs_for(kind):
-        """One CUDA graph per (set, layer): a single kernel launch each."""
-        g = [[None] * len(LAYERS) for _ in range(SETS)]
+        """CUDA graphs of the launches: per layer one graph with ROUND
+        launches cycling through the SETS input sets (ROUND steps' worth of
+        that layer, back to back), and one graph per (set, layer) launch for
+        the K % ROUND steps left over."""
+        rounds = [None] * len(LAYERS)
+        single = [[None] * len(LAYERS) for _ in range(SETS)]
         with torch.cuda.stream(stream):
             for s in range(SETS):
                 for li in range(len(LAYERS)):
                     launch(kind, li, s)              # warm the launch path before capture
             stream.synchronize()
-            for s in range(SETS):
-                for li in range(len(LAYERS)):
+            for li in range(len(LAYERS)):
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=stream):
+                    for k in range(ROUND):
+                        launch(kind, li, k % SETS)
+                rounds[li] = gr
+                for s in range(SETS):
                     gr = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(gr, stream=stream):
                         launch(kind, li, s)
-                    g[s][li] = gr
+                    single[s][li] = gr
         stream.synchronize()
-        return g
+        return rounds, single
+
+    order = [DOMINANT] + [li for li in range(len(LAYERS)) if li != DOMINANT]
+
+    def run_steps(g, steps, events):
+        """steps steps (each: every layer once, on its next input set); with
+        events, brackets every replay of the dominant layer's launches and
+        returns the number of dominant launches inside each bracket."""
+        rounds, single = g
+        n_rounds, rem = divmod(steps, ROUND)
+        counts = []
+        for r in range(n_rounds):
+            for li in order:
+                if events is not None and li == DOMINANT:
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    rounds[li].replay()
+                    b.record(stream)
+                    events.append((a, b))
+                    counts.append(ROUND)
+                else:
+                    rounds[li].replay()
+        for k in range(rem):
+            for li in order:
+                if events is not None and li == DOMINANT:
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    single[k % SETS][li].replay()
+                    b.record(stream)
+                    events.append((a, b))
+                    counts.append(1)
+                else:
+                    single[k % SETS][li].replay()
+        return counts
 
     def timed(kind, steps, warmup, per_launch=False, sampler=False):
         g = graphs_for(kind)
-        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(steps)] if per_launch else []
+        events = [] if per_launch else None
         clock = ClockSampler(device_uuid(dev)) if sampler else None
         with torch.cuda.stream(stream):
-            for w in range(warmup):
-                for li in range(len(LAYERS)):
-                    g[w % SETS][li].replay()
+            run_steps(g, warmup, None)
             stream.synchronize()
             dist.barrier()
             torch.cuda.synchronize()
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
             t0.record(stream)
-            for k in range(steps):
-                s = k % SETS
-                for li in range(len(LAYERS)):
-                    if per_launch and li == DOMINANT:
-                        pairs[k][0].record(stream)
-                        g[s][li].replay()
-                        pairs[k][1].record(stream)
-                    else:
-                        g[s][li].replay()
+            counts = run_steps(g, steps, events)
             t1.record(stream)
             stream.synchronize()
             clocks = clock.stop() if clock is not None else None
             dist.barrier()
             torch.cuda.synchronize()
         ms = t0.elapsed_time(t1)
-        launch_ms = [a.elapsed_time(b) for a, b in pairs]
+        # average duration of one dominant launch over the timed region
+        launch_ms = ([sum(a.elapsed_time(b) for a, b in events) / sum(counts)]
+                     if per_launch and events else [])
         return ms, launch_ms, clocks
 
     W, K = args.warmup, args.steps
@@ -414,23 +460,52 @@ def run_ours(args, dist: Dist):
     host_sf = [torch.empty(SF[li][0].shape, dtype=torch.uint8).pin_memory() for li in range(2)]
     h2d = sum(h.numel() * 2 for h in host_A)
     d2h = sum(t.numel() for t in host_q) + sum(t.numel() for t in host_sf)
-    with torch.cuda.stream(stream):
-        def e2e_step(s):
+    # Three streams: host->device copies, the quantizer launches, device->host
+    # copies; step k uses buffer set k % SETS, and events keep a set's input
+    # from being overwritten before its launches ran and its outputs from
+    # being overwritten before they were copied out.  A step's copies thus
+    # overlap the launches and copies of its neighbours.
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(SETS)]
+    ev_done = [torch.cuda.Event() for _ in range(SETS)]
+    ev_out = [torch.cuda.Event() for _ in range(SETS)]
+    used = [False] * SETS
+
+    def e2e_step(s):
+        if used[s]:
+            s_in.wait_event(ev_done[s])             # launches of the set's last use ran
+        with torch.cuda.stream(s_in):
             for li in range(len(LAYERS)):
                 A[li][s].copy_(host_A[li], non_blocking=True)
+            ev_in[s].record(s_in)
+        stream.wait_event(ev_in[s])
+        if used[s]:
+            stream.wait_event(ev_out[s])            # outputs of the set's last use copied out
+        with torch.cuda.stream(stream):
+            for li in range(len(LAYERS)):
                 launch("kroquant", li, s)
+            ev_done[s].record(stream)
+        s_out.wait_event(ev_done[s])
+        with torch.cuda.stream(s_out):
+            for li in range(len(LAYERS)):
                 host_q[li].copy_(Q[li][s], non_blocking=True)
                 host_sf[li].copy_(SF[li][s], non_blocking=True)
-        for w in range(3):
-            e2e_step(w % SETS)
-        stream.synchronize()
-        dist.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for k in range(e2e_steps):
-            e2e_step(k % SETS)
-        e1.record(stream)
-        stream.synchronize()
+            ev_out[s].record(s_out)
+        used[s] = True
+
+    for w in range(3):
+        e2e_step(w % SETS)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    s_in.wait_event(e0)
+    for k in range(e2e_steps):
+        e2e_step(k % SETS)
+    for ev in ev_out:
+        stream.wait_event(ev)
+    e1.record(stream)
+    torch.cuda.synchronize()
     e2e_ms = dist.max(e0.elapsed_time(e1))
     e2e_value = dist.sum(STEP_BYTES * e2e_steps) / (e2e_ms * 1e-3) / 1e9
 
@@ -447,11 +522,15 @@ def run_ours(args, dist: Dist):
                        "output": "mxfp4 (e2m1 codes + e8m0 scales, 128x4 tiled)",
                        "l2": f"{SETS} rotating input/output sets, "
                              f"{SETS * STEP_BYTES / 1e6:.0f} MB footprint > L2",
-                       "launch": "one CUDA graph per layer launch", "parallelism":
+                       "launch": f"per layer one CUDA graph of {ROUND} launches over its "
+                                 f"{SETS} input sets (programmatic dependent launch between "
+                                 "them); events around each dominant-layer graph",
+                       "parallelism":
                            f"replicas x{dist.world} (rows independent, no exchange)"},
             "hbm_frac": round(value / dist.world / peak, 4),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "traffic_unit": "bytes per launch (ncu, cold L2; outputs left in L2)",
                          "kernel": workload, "launch_ms": round(dom_ms, 5),
                          "peak_source": peak_src},
             "vs_diag_scale": round(value / dist.world / baselines["diag"], 4)
