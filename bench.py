@@ -68,6 +68,13 @@ def parse_args():
     ap.add_argument("--m", type=int, default=9216, help="rows of the profiling case")
     ap.add_argument("--d", type=int, default=12288, help="channels of the profiling case")
     ap.add_argument("--launches", type=int, default=3, help="launches of the profiling case")
+    ap.add_argument("--table", action="store_true",
+                    help="per-launch medians of every kernel on every config shape (markdown)")
+    ap.add_argument("--table-reps", type=int, default=50, help="graph replays per kernel")
+    ap.add_argument("--table-warmup", type=int, default=100, help="warm-up launches per kernel")
+    ap.add_argument("--cpu-rate", nargs=3, type=int, metavar=("M", "D", "SECONDS"),
+                    help="print the oracle's GB/s on an M x D KroQuant layer (row sample of "
+                         "about SECONDS of CPU work; OMP_NUM_THREADS sets the cores)")
     return ap.parse_args()
 
 
@@ -576,8 +583,162 @@ def run_profile_case(args):
     print(f"profile case done: {args.profile} m={m} d={d} launches={args.launches}")
 
 
+# ------------------------------------------------------------- config table --
+
+TABLE_CONFIGS = (
+    ("0", (("cfg0_tiny", 256, 1152, "gauss_outlier8"),)),
+    ("1", (("pixart_qkv", 4096, 1152, "pixart"), ("pixart_ffn_down", 4096, 4608, "pixart"))),
+    ("2", (("sana_2240", 4096, 2240, "sana"), ("sana_5600", 4096, 5600, "sana"))),
+    ("3", (("flux_3072", 4608, 3072, "flux"), ("flux_ffn_down", 4608, 12288, "flux"))),
+    ("4", tuple((f"sweep_{m}x{d}", m, d, "flux") for m in (256, 1024, 4096, 16384, 65536)
+                for d in (1152, 3072, 12288))),
+)
+TABLE_KERNELS = ("umma", "butterfly", "mma", "diag", "hadamard", "identity")
+
+
+def oracle_rate_shape(m: int, d: int, seconds: float):
+    """GB/s of the oracle (KroQuant transform + MXFP4, tiled scales) on a row
+    sample of an m x d layer sized to about `seconds` of CPU work."""
+    import numpy as np
+    from oracle import kq_oracle as O
+    from w4a4_mxfp4_activation_gb300 import synth
+
+    def once(rows):
+        A = synth.activations(rows, d, synth.SEED_A + 5, "flux")
+        lu = synth.lu_params(d // 32, synth.SEED_FACTORS + 5)
+        F = O.lu_to_factors(lu.astype(np.float64), +1).astype(np.float32).astype(np.float64)
+        t0 = time.perf_counter()
+        y, bound = O.transform(A, d, "kron", F)
+        O.quantize(y, bound, O.SF_BLOCKED_128x4)
+        return time.perf_counter() - t0
+
+    t = once(min(m, 32))
+    rows = max(1, min(m, int(min(m, 32) * seconds / max(t, 1e-4))))
+    dt = once(rows)
+    return algo_bytes(rows, d) / dt / 1e9, rows
+
+
+def run_table(args):
+    """Per-launch time of each kernel on each config shape, in the bench's
+    steady state: launches back to back from CUDA graphs, rotating over
+    enough input/output sets that their footprint exceeds 3x the L2 (so every
+    launch reads its input from DRAM and evicts earlier outputs), the time
+    per launch being the median over args.table_reps graph replays of the
+    replay's CUDA-event time / its launches."""
+    import numpy as np
+    import torch
+    from w4a4_mxfp4_activation_gb300 import kq, synth
+
+    dev = torch.device("cuda", 0)
+    layout = kq.KQ_SF_BLOCKED_128x4
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    peak, _ = hbm_peak()
+    stream = torch.cuda.Stream(device=dev)
+    print("| config | layer | m x d | sets | " + " | ".join(
+        f"{k} GB/s (% peak)" if k == "umma" else f"{k} GB/s" for k in TABLE_KERNELS) +
+        " | umma / diag |")
+    print("|" + "---|" * (len(TABLE_KERNELS) + 5))
+    for cfg, layers in TABLE_CONFIGS:
+        for name, m, d, model in layers:
+            set_bytes = algo_bytes(m, d)
+            sets = max(4, int(np.ceil(3 * l2 / set_bytes)))
+            # the seeded generator for up to 4096 rows, tiled on the device
+            rows = min(m, 4096)
+            base = torch.from_numpy(synth.activations(rows, d, synth.SEED_A + int(cfg), model)
+                                    .view(np.int16)).to(dev).view(torch.bfloat16)
+            A0 = base.repeat((m + rows - 1) // rows, 1)[:m].contiguous()
+            del base
+            A = [torch.roll(A0, shifts=37 * s, dims=0) for s in range(sets)]
+            del A0
+            F = torch.from_numpy(kq.kq_lu_to_factors(
+                synth.lu_params(d // 32, synth.SEED_FACTORS + int(cfg)), +1)).to(dev)
+            KX = kq.kq_expand_blocks(F, kq.KQ_K_BF16X3)
+            S = torch.from_numpy(synth.smooth_scales(d)).to(dev)
+            Q = [torch.empty((m, d // 2), dtype=torch.uint8, device=dev) for _ in range(sets)]
+            SF = [torch.empty(kq.kq_sf_bytes(m, d, layout), dtype=torch.uint8, device=dev)
+                  for _ in range(sets)]
+            n_launch = max(sets, 32)
+
+            def launch(kind, i):
+                s = i % sets
+                if kind in ("umma", "mma"):
+                    kq.kq_quantize_mxfp4(A[s], d, K_expanded=KX, layout=layout, q=Q[s], sf=SF[s],
+                                         variant=kq.VARIANT_UMMA if kind == "umma"
+                                         else kq.VARIANT_MMA, stream=stream)
+                elif kind == "butterfly":
+                    kq.kq_quantize_mxfp4(A[s], d, factors=F, layout=layout, q=Q[s], sf=SF[s],
+                                         variant=kq.VARIANT_BUTTERFLY, stream=stream)
+                elif kind == "diag":
+                    kq.kq_smooth_quantize_mxfp4(A[s], S, d, layout=layout, q=Q[s], sf=SF[s],
+                                                stream=stream)
+                elif kind == "hadamard":
+                    kq.kq_hadamard_quantize_mxfp4(A[s], d, layout=layout, q=Q[s], sf=SF[s],
+                                                  stream=stream)
+                else:
+                    kq.kq_quantize_mxfp4(A[s], d, layout=layout, q=Q[s], sf=SF[s], stream=stream)
+
+            gbs = {}
+            for kind in TABLE_KERNELS:
+                with torch.cuda.stream(stream):
+                    for i in range(sets):
+                        launch(kind, i)
+                    stream.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        for i in range(n_launch):
+                            launch(kind, i)
+                    reps = max(5, min(args.table_reps, int(2e5 // n_launch)))
+                    for _ in range(max(2, args.table_warmup // n_launch)):
+                        g.replay()
+                    ev = [(torch.cuda.Event(enable_timing=True),
+                           torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+                    for a, b in ev:
+                        a.record(stream)
+                        g.replay()
+                        b.record(stream)
+                    stream.synchronize()
+                med = statistics.median(a.elapsed_time(b) for a, b in ev) / n_launch
+                gbs[kind] = set_bytes / (med * 1e-3) / 1e9
+                del g
+            cells = [f"{gbs['umma']:.0f} ({100 * gbs['umma'] / peak:.0f} %)"] + \
+                [f"{gbs[k]:.0f}" for k in TABLE_KERNELS[1:]]
+            print(f"| {cfg} | {name} | {m}x{d} | {sets} | " + " | ".join(cells) +
+                  f" | {gbs['umma'] / gbs['diag']:.2f} |", flush=True)
+            del A, Q, SF, KX
+            torch.cuda.empty_cache()
+    # the oracle on the host cores: all of them, then one
+    print()
+    print("| config | layer | oracle GB/s, all cores | oracle GB/s, 1 core |")
+    print("|---|---|---|---|")
+    for cfg, layers in TABLE_CONFIGS[:4]:
+        for name, m, d, _ in layers:
+            out = []
+            for env_threads in (None, "1"):
+                env = dict(os.environ)
+                if env_threads:
+                    env["OMP_NUM_THREADS"] = env_threads
+                r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-rate",
+                                    str(m), str(d), "3"], env=env, capture_output=True,
+                                   text=True, check=True)
+                out.append(r.stdout.strip())
+            print(f"| {cfg} | {name} | {out[0]} | {out[1]} |", flush=True)
+    print(f"\nhost: {os.cpu_count()} cores; L2 {l2 >> 20} MiB; per shape max(4, 3 L2 / set) "
+          f"rotating sets, CUDA graphs of max(sets, 32) launches, median over up to "
+          f"{args.table_reps} replays")
+
+
 def main():
     args = parse_args()
+    if args.cpu_rate:
+        m, d, sec = args.cpu_rate
+        rate, rows = oracle_rate_shape(m, d, float(sec))
+        print(f"{rate:.3f} ({rows} rows, {cpu_cores()} cores)")
+        return
+    if args.table:
+        from w4a4_mxfp4_activation_gb300 import build
+        build.build()
+        run_table(args)
+        return
     if args.profile:
         from w4a4_mxfp4_activation_gb300 import build
         build.build()

@@ -323,15 +323,15 @@ __device__ __forceinline__ uint4 quantize_block(const float2 (&Y)[16], uint32_t 
 }
 
 // Row-major walk over (row tile, column tile) pairs: first, first + step,
-// first + 2 step, ... with tile = rt * ncol + ct, without 64-bit division in
-// the loop.  The walk ends when rt reaches the number of row tiles.
+// first + 2 step, ... with tile = rt * ncol + ct, in 32-bit arithmetic (the
+// launchers check that tile counts fit, see tiles_fit_int32) and without any
+// division in the loop.  The walk ends when rt reaches the number of row tiles.
 struct TileWalk {
     int rt, ct;
     int ncol, step_rt, step_ct;
-    __device__ __forceinline__ TileWalk(int64_t first, int64_t step, int64_t ncol_)
-        : rt(static_cast<int>(first / ncol_)), ct(static_cast<int>(first % ncol_)),
-          ncol(static_cast<int>(ncol_)), step_rt(static_cast<int>(step / ncol_)),
-          step_ct(static_cast<int>(step % ncol_))
+    __device__ __forceinline__ TileWalk(int first, int step, int ncol_)
+        : rt(first / ncol_), ct(first % ncol_), ncol(ncol_), step_rt(step / ncol_),
+          step_ct(step % ncol_)
     {
     }
     __device__ __forceinline__ void next()

@@ -50,6 +50,14 @@ kq_status make_tensor_map_2d_u8(CUtensorMap *map, void *base, int64_t rows, int6
                                 CUtensorMapSwizzle swizzle);
 kq_status check_launch();
 
+// The kernels walk tiles in 32-bit arithmetic: row and column tile indices,
+// and the walk's start and stride (at most twice the grid), must fit in int.
+inline bool tiles_fit_int32(const QuantParams &p, int grid)
+{
+    const int64_t lim = (int64_t(1) << 30);
+    return p.nrow_tiles < lim && p.ncol_tiles < lim && p.ntiles < lim && grid < (1 << 20);
+}
+
 // Launches a persistent quantizer kernel with programmatic stream
 // serialization: the launch may begin while the previous kernel of the
 // stream is still running; the kernel orders its global-memory accesses

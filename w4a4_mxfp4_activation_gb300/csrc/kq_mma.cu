@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmA);              // a kernel parameter: no dependency on earlier grids
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kConsumerThreads);
@@ -125,10 +126,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (warp == kConsumerWarps) {
         if (lane != 0) return;
-        tma_prefetch_desc(&tmA);
         const uint64_t pol = l2_policy_evict_first();
         int64_t it = 0;
-        for (TileWalk tw(blockIdx.x, gridDim.x, p.ncol_tiles); tw.rt < p.nrow_tiles; tw.next(), ++it) {
+        for (TileWalk tw(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                             static_cast<int>(p.ncol_tiles));
+             tw.rt < p.nrow_tiles; tw.next(), ++it) {
             const int s = static_cast<int>(it % STAGES);
             const uint32_t ph = static_cast<uint32_t>((it / STAGES) & 1);
             if (it >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1u)) break;
@@ -160,7 +162,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int lm_row = ((lane >> 3) & 1) * 8 + (lane & 7);
     const int lm_kc = lane >> 4;
     int64_t it = 0;
-    for (TileWalk tw(blockIdx.x, gridDim.x, p.ncol_tiles); tw.rt < p.nrow_tiles; tw.next(), ++it) {
+    for (TileWalk tw(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                             static_cast<int>(p.ncol_tiles));
+             tw.rt < p.nrow_tiles; tw.next(), ++it) {
         const int s = static_cast<int>(it % STAGES);
         const uint32_t ph = static_cast<uint32_t>((it / STAGES) & 1);
         const int64_t rt = tw.rt, ct = tw.ct;
@@ -293,6 +297,7 @@ kq_status launch_mma(const CUtensorMap &map, QuantParams p, const uint8_t *recor
     if (p.ntiles == 0) return KQ_OK;
     const int64_t resident = static_cast<int64_t>(slot.occupancy[dev]) * sm_count;
     const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, resident));
+    if (!tiles_fit_int32(p, grid)) return KQ_ERR_SHAPE;
     return launch_pdl(kern, grid, kThreads, Cfg::kSmemBytes, stream, map, p, records);
 }
 

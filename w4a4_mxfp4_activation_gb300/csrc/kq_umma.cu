@@ -188,6 +188,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmA);              // kernel parameters: no dependency on
+        tma_prefetch_desc(&tmQ);              // earlier grids
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
@@ -209,10 +211,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            tma_prefetch_desc(&tmA);
             const uint64_t pol = l2_policy_evict_first();
             int64_t it = 0;
-            for (TileWalk tw(blockIdx.x, gridDim.x, p.ncol_tiles); tw.rt < p.nrow_tiles;
+            for (TileWalk tw(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                             static_cast<int>(p.ncol_tiles));
+                 tw.rt < p.nrow_tiles;
                  tw.next(), ++it) {
                 const int s = static_cast<int>(it % STAGES);
                 const uint32_t ph = static_cast<uint32_t>((it / STAGES) & 1);
@@ -238,8 +241,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int a = warp - 1;               // accumulator buffer; tiles with it % 2 == a
         int64_t it = a;
         bool ok = true;
-        for (TileWalk tw(blockIdx.x + a * static_cast<int64_t>(gridDim.x),
-                         2 * static_cast<int64_t>(gridDim.x), p.ncol_tiles);
+        for (TileWalk tw(static_cast<int>(blockIdx.x + a * gridDim.x),
+                         static_cast<int>(2 * gridDim.x), static_cast<int>(p.ncol_tiles));
              tw.rt < p.nrow_tiles && ok; tw.next(), it += 2) {
             const int s = static_cast<int>(it % STAGES);
             const int64_t ct = tw.ct;
@@ -277,8 +280,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int r = qtr * 32 + lane;        // row within the tile
         int it = grp;
         bool ok = true;
-        TileWalk tw(blockIdx.x + grp * static_cast<int64_t>(gridDim.x),
-                    2 * static_cast<int64_t>(gridDim.x), p.ncol_tiles);
+        TileWalk tw(static_cast<int>(blockIdx.x + grp * gridDim.x),
+                    static_cast<int>(2 * gridDim.x), static_cast<int>(p.ncol_tiles));
         for (; tw.rt < p.nrow_tiles; tw.next(), it += 2) {
             const int a = grp;
             const int rt = tw.rt, ct = tw.ct;
@@ -386,6 +389,7 @@ kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, QuantPara
     if (p.ntiles == 0) return KQ_OK;
     // one CTA per SM: each holds 256 of the SM's 512 TMEM columns
     const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, sm_count));
+    if (!tiles_fit_int32(p, grid)) return KQ_ERR_SHAPE;
     return launch_pdl(kern, grid, kThreadsU, Cfg::kSmemBytes, stream, map, mapq, p, records);
 }
 
