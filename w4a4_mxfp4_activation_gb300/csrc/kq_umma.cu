@@ -10,11 +10,15 @@
 // relative; the activations are exact in bf16).  The three terms sit side by
 // side along N: per block two M = 128, N = 96, K = 16 MMAs (one per
 // 16-channel input half, accumulating) read each A slice from shared memory
-// once, and the epilogue adds the three partial results.  (One MMA per term
-// would re-read A three times; measured on GB300, the tensor core's reads of
-// A then became the bottleneck.  Keeping G1 out of the operands and applying
-// it on the CUDA cores was measured too: the epilogue, not the tensor core,
-// limits this kernel, so the whole transform goes to the tensor core.)
+// once, and the epilogue adds the three partial results.
+// Alternatives measured on GB300 and dropped: one MMA per term re-reads A
+// three times from shared memory; copying A into TMEM once (tcgen05.cp) and
+// accumulating the terms there with 12 N = 32 MMAs per tile frees the
+// epilogue but the longer tcgen05 instruction stream (about 150 cycles per
+// instruction to issue) then limits the tile rate; keeping G1 out of the
+// operands and applying it on the CUDA cores loads the epilogue, which
+// limits this kernel; and a separate, shallower ring for the operand records
+// (more activation tiles in flight) was no faster.
 // The MXFP4 encoding runs on the CUDA cores after the accumulators are read
 // back with tcgen05.ld (one thread = one row of a 32-channel block, all 32
 // values in registers).
@@ -32,11 +36,13 @@
 //               ring's empty barrier and to the accumulator's full barrier;
 //   warps 3-18  epilogue, two groups of 8 warps taking alternate tiles (and
 //               accumulator buffers): warp w reads TMEM lanes 32 (w % 4)..+31
-//               (rows) of one block, sums the terms and quantizes;
-//               each warp's 32 x 16 bytes of codes go to its own shared
-//               staging buffer and leave with one TMA store (a thread owns a
-//               row, so direct 16-byte stores from a warp would touch 32 rows
-//               and clog the memory pipe).
+//               (rows) of one block, sums the terms and quantizes; the two
+//               warps of a 32-row quarter put their 16 bytes of codes per row
+//               side by side in a shared staging buffer, and one TMA store
+//               writes the quarter's 32 rows x 32 bytes (a thread owns a row,
+//               so direct 16-byte stores from a warp would touch 32 rows and
+//               clog the memory pipe; whole 32-byte rows also halve the L2
+//               write transactions of 16-byte ones).
 // Every wait is bounded in time; a timed-out epilogue writes the E8M0 NaN
 // byte 0xFF as the scale of the blocks it could not finish.
 #include <cuda_bf16.h>
@@ -67,11 +73,16 @@ struct UCfg {
     static constexpr int kRecBytes = static_cast<int>(kUmmaRecordBytes);   // 3 terms of K_j
     static constexpr int kStageBytes = kABytes + 2 * kRecBytes;          // 28 KB
     // after the ring: barriers + TMEM base (1 KB), 1 KB spare, code staging
-    // for the TMA stores: per epilogue warp 2 buffers of 32 rows x 16 B
+    // for the TMA stores: per pair of epilogue warps (the two blocks of one
+    // 32-row quarter) 3 buffers of 32 rows x 32 B
     static constexpr int kBarOff = STAGES * kStageBytes;
     static constexpr int kStgOff = kBarOff + 2048;
-    static constexpr int kStgBytes = 32 * 16;
-    static constexpr int kSmemBytes = kStgOff + kEpiWarps * 2 * kStgBytes + 1024;   // + slack
+    static constexpr int kStgBytes = 32 * 32;
+    static constexpr int kStgBufs = 3;
+    // and per pair and buffer the b = 1 warp's 32 scale bytes (tiled layout)
+    static constexpr int kSfStgOff = kStgOff + (kEpiWarps / 2) * kStgBufs * kStgBytes;
+    static constexpr int kSmemBytes =
+        kSfStgOff + (kEpiWarps / 2) * kStgBufs * 32 + 1024;   // + alignment slack
     static_assert(kStageBytes % 1024 == 0, "stage alignment");
     // The two MMA issuers take alternate tiles and wait on the ring's full
     // barriers by phase parity.  With an even ring every stage is always
@@ -278,6 +289,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int b = (e >> 2) & 1;           // block of the tile
         const int qtr = warp & 3;             // TMEM lane quarter this warp may access
         const int r = qtr * 32 + lane;        // row within the tile
+        const int pair = grp * 4 + (e & 3);   // the quarter's two warps (b = 0, 1)
+        int slot = 0;                         // staging buffer of this tile, mod 3
         int it = grp;
         bool ok = true;
         TileWalk tw(static_cast<int>(blockIdx.x + grp * gridDim.x),
@@ -287,7 +300,10 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             const int rt = tw.rt, ct = tw.ct;
             const int j = ct * 2 + b;
             const int row = rt * kBR + r;
-            const uint32_t stg = base + Cfg::kStgOff + (e * 2 + ((it >> 1) & 1)) * Cfg::kStgBytes;
+            const uint32_t stg = base + Cfg::kStgOff + (pair * Cfg::kStgBufs + slot) * Cfg::kStgBytes;
+            const uint32_t sfstg = base + Cfg::kSfStgOff + (pair * Cfg::kStgBufs + slot) * 32;
+            uint32_t sbyte = 0;       // this row's scale byte for block j (0: padding block)
+            bool swrite = false;
             if (ok) ok = __all_sync(0xffffffffu,
                                     mbar_wait(bar_acc_full + 8 * a, static_cast<uint32_t>((it >> 1) & 1)));
             uint4 codes = make_uint4(0u, 0u, 0u, 0u);
@@ -322,32 +338,51 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                             stg_f4(yd + 4 * k, make_float4(Y[2 * k].x, Y[2 * k].y, Y[2 * k + 1].x,
                                                            Y[2 * k + 1].y));
                     }
-                    uint32_t byte;
-                    codes = quantize_block(Y, byte);
-                    store_scale_u(p, row, j, byte);
+                    codes = quantize_block(Y, sbyte);
+                    swrite = true;
                 } else {
                     tc_fence_before();
                     mbar_arrive(bar_acc_empty + 8 * a);
-                    if (p.sf_layout != KQ_SF_ROWMAJOR) store_scale_u(p, row, j, 0u);
+                    swrite = p.sf_layout != KQ_SF_ROWMAJOR;
                 }
             } else if (j < p.nb && row < p.m_rows) {
-                store_scale_u(p, row, j, 0xFFu);
+                sbyte = 0xFFu;        // E8M0 NaN: this block was not computed
+                swrite = true;
             }
-            // Codes -> this warp's staging buffer -> one TMA store of 32 rows x
-            // 16 bytes.  Lane 0 issues the stores; the buffer was last read by
-            // the store two tiles ago.
-            if (lane == 0) bulk_wait_group_read<1>();
-            __syncwarp();
-            sts128(stg + lane * 16, codes);
+            // Scales.  Row-major: one byte per thread.  Tiled: blocks 2 ct and
+            // 2 ct + 1 of a row are adjacent bytes, so the b = 1 warp hands its
+            // byte to the b = 0 warp (through shared memory, across the pair
+            // barrier below) and that warp writes both as one 16-bit store.
+            const bool tiled = p.sf_layout != KQ_SF_ROWMAJOR;
+            if (!tiled) {
+                if (swrite) store_scale_u(p, row, j, sbyte);
+            } else if (b == 1) {
+                asm volatile("st.shared.u8 [%0], %1;" ::"r"(sfstg + lane), "r"(sbyte) : "memory");
+            }
+            // Codes -> the pair's staging buffer (32-byte rows, the 32-byte
+            // swizzle of the tensor map: 16-byte chunk b ^ bit 2 of the row)
+            // -> one TMA store of 32 rows x 32 bytes by the b = 0 warp.  Three
+            // buffers rotate: the store that last read this one was committed
+            // three tiles ago, and the b = 0 warp waited for it to finish
+            // reading (below) before the pair barrier of the previous tile.
+            sts128(stg + lane * 32 + ((b ^ ((lane >> 2) & 1)) << 4), codes);
             fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                if (j < p.nb)
-                    tma_store_2d(&tmQ, j * 16, rt * kBR + qtr * 32, stg);
-                bulk_commit_group();
+            named_barrier(1 + pair, 64);
+            if (tiled && b == 0) {
+                uint32_t partner;
+                asm volatile("ld.shared.u8 %0, [%1];" : "=r"(partner) : "r"(sfstg + lane) : "memory");
+                *reinterpret_cast<uint16_t *>(p.sf + sf_blocked_offset(row, ct * 2, p.ncb)) =
+                    static_cast<uint16_t>(sbyte | (partner << 8));
             }
+            if (b == 0 && lane == 0) {
+                if (ct * 2 < p.nb)      // padding tiles of the scale layout have no codes
+                    tma_store_2d(&tmQ, ct * 32, rt * kBR + qtr * 32, stg);
+                bulk_commit_group();
+                bulk_wait_group_read<1>();
+            }
+            slot = slot == Cfg::kStgBufs - 1 ? 0 : slot + 1;
         }
-        if (lane == 0) bulk_wait_group_all();
+        if (b == 0 && lane == 0) bulk_wait_group_all();
     }
 
     tc_fence_before();
@@ -404,8 +439,8 @@ kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expand
     CUtensorMap map, mapq;
     st = make_tensor_map_2d_bf16(&map, A, p.m, p.d, lda, 64, kBR);
     if (st != KQ_OK) return st;
-    st = make_tensor_map_2d_u8(&mapq, p.q, p.m, p.d / 2, p.ldq, 16, 32,
-                               CU_TENSOR_MAP_SWIZZLE_NONE);
+    st = make_tensor_map_2d_u8(&mapq, p.q, p.m, p.d / 2, p.ldq, 32, 32,
+                               CU_TENSOR_MAP_SWIZZLE_32B);
     if (st != KQ_OK) return st;
     const uint8_t *rec = static_cast<const uint8_t *>(K_expanded);
     if (p.y_debug != nullptr) return launch_umma<6, true>(map, mapq, p, rec, info.sm_count, stream);
