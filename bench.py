@@ -135,13 +135,12 @@ def hbm_peak():
 
 
 def kernel_source_hash() -> str:
-    """Hash of every CUDA / C++ source and header the library is built from."""
-    import glob
+    """Hash of the sources that define the dominant kernel (the tcgen05
+    quantizer: its device code, its launch configuration and tensor maps)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "w4a4_mxfp4_activation_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
-                   + glob.glob(os.path.join(csrc, "*.h")) + glob.glob(os.path.join(csrc, "*.cpp"))
-                   + [os.path.join(ROOT, "include", "kq.h")])
+    files = [os.path.join(csrc, f) for f in ("kq_umma.cu", "kq_device.cuh", "kq_internal.h",
+                                             "kq_records.h")]
     for path in files:
         h.update(os.path.basename(path).encode())
         with open(path, "rb") as f:

@@ -102,13 +102,14 @@ typedef enum kq_kfmt {
  *   m, d, lda  rows, channels (d % 32 == 0), row pitch in elements
  *   factors    device, fp32 [d/32][5][2][2] raw factor entries, or NULL
  *   K_expanded device, output of kq_expand_blocks(..., KQ_K_BF16X3, ...), or
- *              NULL.  With factors != NULL the five 2x2 factors are applied
- *              as an in-register butterfly; with factors == NULL and
- *              K_expanded != NULL the pre-expanded blocks run on the tensor
- *              cores (tcgen05.mma with TMEM accumulators: the dense 16x16
- *              G2..G5 part in bf16 terms, then the G1 stage in fp32);
- *              with both NULL the transform is the identity (the bare
- *              quantizer, "Q4" of [KQ] Tables 3 and 4).
+ *              NULL.  With K_expanded != NULL the transform runs on the
+ *              tensor cores (tcgen05.mma, fp32 accumulation in TMEM) against
+ *              the dense 32x32 K_j as three bf16 terms -- the fastest path;
+ *              otherwise, with factors != NULL, the five 2x2 factors are
+ *              applied as an in-register butterfly on the CUDA cores; with
+ *              both NULL the transform is the identity (the bare quantizer,
+ *              "Q4" of [KQ] Tables 3 and 4).  Both paths compute y to about
+ *              fp32 precision (|error| <= 2^-16 * sum_r |a_r K_rc|).
  *   q, ldq     device, packed codes [m][ldq] (written)
  *   sf         device, scales in sf_layout (written; kq_sf_bytes() bytes)
  *   y_debug    device fp32 [m][d] or NULL: if given, receives y = a . K_j

@@ -264,7 +264,9 @@ kq_status kq_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda
                             uint8_t *sf, kq_sf_layout sf_layout, float *y_debug,
                             cudaStream_t stream)
 {
-    const int variant = factors != nullptr ? 0 : (K_expanded != nullptr ? 3 : 2);
+    // the fastest implementation the arguments allow: tcgen05 on the
+    // expanded blocks, else the butterfly on the raw factors, else identity
+    const int variant = K_expanded != nullptr ? 3 : (factors != nullptr ? 0 : 2);
     return kq_quantize_mxfp4_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout,
                                      y_debug, variant, stream);
 }
