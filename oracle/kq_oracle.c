@@ -18,7 +18,7 @@
  * quantized on its own (Sec. 3.1, MXFP4 per the OCP MX format named in
  * Sec. 4.1 "Data format").
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - shared exponent e = floor(log2 amax) - 2 (2 = emax of E2M1), clamped to
  *     the E8M0 range [-127, 127]; amax == 0 gives e = -127;
  *   - e2m1 rounding is round-to-nearest, ties to the even code, with
@@ -343,4 +343,46 @@ KQO_EXPORT void kqo_encode_e2m1_array(const double *v, int64_t n, uint8_t *codes
 {
     #pragma omp parallel for schedule(static)
     for (int64_t k = 0; k < n; ++k) codes[k] = kqo_encode_e2m1(v[k]);
+}
+
+/* --- 16-bit side output ---------------------------------------------------- */
+
+/* fp64 -> bf16 bit pattern, round to nearest with ties to even.  This is the
+ * cast of the transformed activations to the 16-bit input dtype: [KQ] Sec.
+ * 3.5.1 (K1 stores y "after casting to the input dtype") and App. D
+ * "Quantization" (the activations that feed the low-rank branch of eq. (11)
+ * stay in 16 bits; bf16 for SANA and FLUX).
+ * bf16: 1 sign, 8 exponent, 7 fraction bits.  A finite magnitude is
+ * k * 2^(e - 7) with k in [128, 255] in the binade [2^e, 2^(e+1)),
+ * e in [-126, 127], and k * 2^-133, k in [0, 127], below 2^-126.  The value is
+ * rounded to the nearest multiple of its binade's spacing (ties to an even
+ * multiple, rint in the default rounding mode); a carry to k = 256 moves to
+ * the next binade, and a rounded magnitude of 2^128 is infinity. */
+KQO_EXPORT uint16_t kqo_f64_to_bf16(double x)
+{
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    const double a = fabs(x);
+    if (isnan(x)) return (uint16_t)(sign | 0x7FC0u);
+    if (a == 0.0) return sign;
+    int E;
+    (void)frexp(a, &E);                 /* a in [2^(E-1), 2^E) */
+    int e = E - 1;
+    if (e < -126) e = -126;             /* subnormal range: spacing 2^-133 */
+    const double spacing = ldexp(1.0, e - 7);
+    const double r = rint(a / spacing) * spacing;   /* both steps exact */
+    if (r >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80u);
+    if (r == 0.0) return sign;
+    int E2;
+    (void)frexp(r, &E2);
+    const int e2 = E2 - 1;
+    if (e2 < -126) return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, -133)));
+    const uint16_t field = (uint16_t)(e2 + 127);
+    const uint16_t frac = (uint16_t)(r / ldexp(1.0, e2 - 7) - 128.0);
+    return (uint16_t)(sign | (uint16_t)(field << 7) | frac);
+}
+
+KQO_EXPORT void kqo_f64_to_bf16_array(const double *x, int64_t n, uint16_t *out)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t k = 0; k < n; ++k) out[k] = kqo_f64_to_bf16(x[k]);
 }

@@ -83,6 +83,9 @@ def _bind(path: str) -> ctypes.CDLL:
     L.kqo_dequantize.argtypes = [u8p, i64, u8p, ctypes.c_int, i64, i64, dp]
     L.kqo_encode_f32_range.argtypes = [ctypes.c_uint32, i64, u8p]
     L.kqo_encode_e2m1_array.argtypes = [dp, i64, u8p]
+    L.kqo_f64_to_bf16.argtypes = [ctypes.c_double]
+    L.kqo_f64_to_bf16.restype = ctypes.c_uint16
+    L.kqo_f64_to_bf16_array.argtypes = [dp, i64, u16p]
     return L
 
 
@@ -239,6 +242,18 @@ def encode_e2m1_array(v: np.ndarray) -> np.ndarray:
     out = np.empty(v.size, np.uint8)
     lib().kqo_encode_e2m1_array(_p(v, ctypes.c_double), v.size, _p(out, ctypes.c_uint8))
     return out
+
+
+def round_bf16(x) -> np.ndarray:
+    """fp64 values -> bf16 bit patterns (uint16), round to nearest even: the
+    cast of the transformed activations to the 16-bit input dtype ([KQ] Sec.
+    3.5.1 K1, App. D "Quantization": the low-rank branch of eq. (11) takes A T
+    in 16 bits)."""
+    x = _f64(x)
+    flat = x.ravel()
+    out = np.empty(flat.size, np.uint16)
+    lib().kqo_f64_to_bf16_array(_p(flat, ctypes.c_double), flat.size, _p(out, ctypes.c_uint16))
+    return out.reshape(x.shape)
 
 
 def e2m1_value(code: int) -> float:

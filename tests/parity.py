@@ -13,6 +13,15 @@ For every (row, block) the rules are:
   (iii) same-precision requantization: the oracle's quantizer applied to
         the kernel's own fp32 y reproduces the kernel's scales and codes
         exactly, with no exceptions.
+
+For the 16-bit side output A T (bf16, round to nearest even) of the dual
+quantizer:
+  (iv)  its value lies between the oracle's rounding of y_ref - tol and of
+        y_ref + tol (rounding is monotone, so this is exactly "the bf16 of some
+        value within the rule-(i) tolerance of the exact y"; most elements
+        admit one pattern only, and those that admit two are counted);
+  (v)   with the kernel's own fp32 y at hand, the side output is the oracle's
+        rounding of it, bit for bit.
 """
 from __future__ import annotations
 
@@ -83,4 +92,29 @@ def check(A_bits: np.ndarray, d: int, kind: str, param, layout: int, q_gpu: np.n
         q2, sf2, _ = O.quantize(np.asarray(y_gpu, np.float64)[rows], None, O.SF_ROWMAJOR)
         assert np.array_equal(sf2.reshape(len(rows), nb), sf_g), "requantized scales differ"
         assert np.array_equal(unpack(q2, d), codes_gpu), "requantized codes differ"
+    return out
+
+
+def check_side_output(A_bits: np.ndarray, d: int, kind: str, param, at_gpu: np.ndarray,
+                      y_gpu: np.ndarray | None, rows: np.ndarray | None = None) -> dict:
+    """Rules (iv)-(v) for the bf16 side output on the given rows (all if None)."""
+    m = A_bits.shape[0]
+    rows = np.arange(m) if rows is None else np.asarray(rows, np.int64)
+    y_ref, bound = O.transform(np.ascontiguousarray(A_bits[rows]), d, kind, param)
+    tol = np.ldexp(bound, -16)
+    lo = O.round_bf16(y_ref - tol)
+    hi = O.round_bf16(y_ref + tol)
+    at = np.asarray(at_gpu)[rows][:, :d].astype(np.uint16)
+
+    def val(b):
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+    v, vlo, vhi = val(at), val(lo), val(hi)
+    bad = (v < vlo) | (v > vhi) | np.isnan(v)
+    assert not bad.any(), f"{int(bad.sum())} side-output values outside the rounding window"
+    out = {"side_elements": int(at.size), "side_two_choices": int((lo != hi).sum())}
+    if y_gpu is not None:
+        want = O.round_bf16(np.asarray(y_gpu, np.float64)[rows])
+        assert np.array_equal(want, at), (
+            f"{int((want != at).sum())} side-output patterns differ from the rounding of y")
     return out

@@ -33,6 +33,10 @@ MUTANTS = [
     ("hadamard_sign", "? -s : s;", "? s : -s;", [pins.test_hadamard_closed_form]),
     ("lu_wrong_entry", "G[3] = c * b + u22;", "G[3] = c * a + u22;",
      [pins.test_lu_factor_determinants]),
+    ("bf16_ties_away", "rint(a / spacing) * spacing", "round(a / spacing) * spacing",
+     [pins.test_bf16_rounding_golden, pins.test_bf16_rounding_is_nearest_even]),
+    ("bf16_subnormal_spacing", "if (e < -126) e = -126;", "if (e < -127) e = -127;",
+     [pins.test_bf16_rounding_golden, pins.test_bf16_rounding_is_nearest_even]),
 ]
 
 

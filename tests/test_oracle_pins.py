@@ -309,3 +309,66 @@ def test_layer_error_hadamard_vs_identity_sanity(oracle_lib):
               .astype(np.float32).astype(np.float64)):
         e, ref = oracle_lib.layer_error(A, W, d, F)
         assert 0 < e < 0.5 * ref
+
+
+# --- the 16-bit side output: fp64 -> bf16, round to nearest even ----------------
+
+def _bf16_decode(bits):
+    """bf16 patterns -> fp64 through numpy's fp32 view (independent of the oracle)."""
+    return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def test_bf16_rounding_golden(oracle_lib):
+    """Hand-derived cases: ties in normal and subnormal binades, carries into
+    the next binade, overflow at the top tie, signed zero."""
+    for v, b in read_golden("bf16_rounding.txt"):
+        got = int(oracle_lib.round_bf16(np.array([float.fromhex(v)]))[0])
+        assert got == int(b, 16), (v, hex(got), b)
+
+
+def test_bf16_rounding_is_nearest_even(oracle_lib):
+    """Brute-force property on random doubles over the whole bf16 range
+    (subnormals included) and on exact ties: the result is no farther from x
+    than either adjacent bf16 value, an exact tie goes to the even pattern,
+    the sign is kept, and infinity only appears at or beyond the top tie."""
+    rng = np.random.default_rng(77)
+    n = 200_000
+    x = rng.uniform(1.0, 2.0, n) * np.exp2(rng.integers(-140, 128, n))
+    # exact midpoints between adjacent bf16 values in random binades
+    k = rng.integers(128, 255, n // 4).astype(np.float64)
+    e = rng.integers(-126, 127, n // 4)
+    ties = (k + 0.5) * np.exp2(e - 7)
+    sub = (rng.integers(0, 127, n // 8) + 0.5) * 2.0 ** -133      # subnormal ties
+    x = np.concatenate([x, ties, sub])
+    x *= rng.choice([-1.0, 1.0], x.size)
+    r = oracle_lib.round_bf16(x).astype(np.int64)
+    assert np.array_equal((r >> 15) == 1, np.signbit(x))
+    mag = r & 0x7FFF
+    ax = np.abs(x)
+    top = 2.0 ** 128
+    inf = mag == 0x7F80
+    assert not np.any(mag > 0x7F80)
+    assert np.all(ax[inf] >= (_bf16_decode(0x7F7F) + top) / 2)
+    fin = ~inf
+    m, a = mag[fin], ax[fin]
+    v = _bf16_decode(m)
+    lo = _bf16_decode(np.maximum(m - 1, 0))
+    hi = np.where(m + 1 >= 0x7F80, top, _bf16_decode(np.minimum(m + 1, 0x7F7F)))
+    err = np.abs(a - v)
+    assert np.all(err <= np.abs(a - lo)) and np.all(err <= np.abs(a - hi))
+    tie = ((err == np.abs(a - hi)) & (hi != v)) | ((err == np.abs(a - lo)) & (lo != v))
+    assert tie.sum() > n // 4
+    assert np.all(m[tie] % 2 == 0)
+
+
+def test_bf16_rounding_matches_torch_fp32(oracle_lib):
+    """Special case reducing to a library routine: for fp32-representable x,
+    rounding to bf16 is torch's fp32 -> bf16 conversion (round to nearest even)."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(78)
+    bits = rng.integers(0, 2 ** 32, 400_000, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    want = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle_lib.round_bf16(f.astype(np.float64))
+    assert np.array_equal(got, want)
