@@ -50,6 +50,14 @@ def algo_bytes(m: int, d: int) -> float:
 STEP_BYTES = sum(algo_bytes(m, d) for _, m, d in LAYERS)
 
 
+def algo_bytes_dual(m: int, d: int) -> float:
+    """kq_quantize_mxfp4_dual: the MXFP4 outputs plus the bf16 side output A T."""
+    return algo_bytes(m, d) + m * d * 2
+
+
+STEP_BYTES_DUAL = sum(algo_bytes_dual(m, d) for _, m, d in LAYERS)
+
+
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -63,7 +71,7 @@ def parse_args():
                     help="skip the diagonal / Hadamard / bare-quantizer side measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU time budget of the oracle baseline sample")
-    ap.add_argument("--profile", choices=("kroquant", "diag", "hadamard", "identity"),
+    ap.add_argument("--profile", choices=("kroquant", "dual", "diag", "hadamard", "identity"),
                     help="profiling case for ncu: run one quantizer a few times and exit")
     ap.add_argument("--m", type=int, default=9216, help="rows of the profiling case")
     ap.add_argument("--d", type=int, default=12288, help="channels of the profiling case")
@@ -342,6 +350,9 @@ def run_ours(args, dist: Dist):
         elif kind == "umma":
             kq.kq_quantize_mxfp4(A[li][s], d, K_expanded=KX[li], layout=layout, q=Q[li][s],
                                  sf=SF[li][s], variant=kq.VARIANT_UMMA, stream=stream)
+        elif kind == "dual":
+            kq.kq_quantize_mxfp4_dual(A[li][s], KX[li], d, layout=layout, q=Q[li][s],
+                                      sf=SF[li][s], at=AT[li][s], stream=stream)
         elif kind == "diag":
             kq.kq_smooth_quantize_mxfp4(A[li][s], DIAG[li], d, layout=layout, q=Q[li][s],
                                         sf=SF[li][s], stream=stream)
@@ -353,6 +364,8 @@ def run_ours(args, dist: Dist):
                                  stream=stream)
 
     DIAG = [torch.from_numpy(synth.smooth_scales(d)).to(dev) for _, _, d in LAYERS]
+    # bf16 side outputs of the dual quantizer (allocated when it is measured)
+    AT = [[None] * SETS for _ in LAYERS]
 
     def graphs_for(kind):
         """CUDA graphs of the launches: per layer one graph with ROUND
@@ -450,6 +463,25 @@ def run_ours(args, dist: Dist):
     workload = f"kq_quantize_mxfp4 {args.variant} m={dom_m} d={dom_d}"
     traffic = recorded_traffic(f"flux_ffn_down_{args.variant}")
 
+    # ---- the dual quantizer (MXFP4 + the bf16 side output A T of the
+    #      low-rank branch) on the same step
+    side = None
+    if not args.no_baselines:
+        for li, (_, m, d) in enumerate(LAYERS):
+            AT[li] = [torch.empty((m, d), dtype=torch.bfloat16, device=dev) for _ in range(SETS)]
+        nd = max(ROUND, min(K, 8000))
+        dms, dlaunch, _ = timed("dual", nd, W, per_launch=True)
+        dms = dist.max(dms)
+        side = {"metric": "kq_quantize_mxfp4_dual GB/s (MXFP4 + bf16 A T side output)",
+                "value": round(dist.sum(STEP_BYTES_DUAL * nd) / (dms * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "bytes_per_element": 4.53125, "steps": nd,
+                "ms_per_step": round(dms / nd, 5),
+                "dominant_launch_ms": round(dlaunch[0], 5) if dlaunch else None,
+                "dominant_frac": round(algo_bytes_dual(dom_m, dom_d) / (dlaunch[0] * 1e-3) / 1e9
+                                       / peak, 4) if dlaunch else None}
+        AT = [[None] * SETS for _ in LAYERS]
+        torch.cuda.empty_cache()
+
     # ---- side measurements: the baselines built alongside
     baselines = {}
     if not args.no_baselines:
@@ -542,6 +574,7 @@ def run_ours(args, dist: Dist):
             "vs_diag_scale": round(value / dist.world / baselines["diag"], 4)
             if baselines.get("diag") else None,
             "baselines_gbs": baselines,
+            "side_output": side,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": K * len(LAYERS),
@@ -565,13 +598,17 @@ def run_profile_case(args):
     layout = kq.KQ_SF_BLOCKED_128x4
     q = torch.empty((m, d // 2), dtype=torch.uint8, device="cuda")
     sf = torch.empty(kq.kq_sf_bytes(m, d, layout), dtype=torch.uint8, device="cuda")
-    KX = kq.kq_expand_blocks(F, kq.KQ_K_BF16X3) if args.variant in ("mma", "umma") else None
+    KX = (kq.kq_expand_blocks(F, kq.KQ_K_BF16X3)
+          if args.variant in ("mma", "umma") or args.profile == "dual" else None)
+    at = torch.empty((m, d), dtype=torch.bfloat16, device="cuda") if args.profile == "dual" else None
     variant = {"butterfly": kq.VARIANT_BUTTERFLY, "mma": kq.VARIANT_MMA,
                "umma": kq.VARIANT_UMMA}[args.variant]
     for _ in range(args.launches):
         if args.profile == "kroquant":
             kq.kq_quantize_mxfp4(A, d, factors=F if KX is None else None, K_expanded=KX,
                                  layout=layout, q=q, sf=sf, variant=variant)
+        elif args.profile == "dual":
+            kq.kq_quantize_mxfp4_dual(A, KX, d, layout=layout, q=q, sf=sf, at=at)
         elif args.profile == "diag":
             kq.kq_smooth_quantize_mxfp4(A, s, d, layout=layout, q=q, sf=sf)
         elif args.profile == "hadamard":
@@ -592,7 +629,7 @@ TABLE_CONFIGS = (
     ("4", tuple((f"sweep_{m}x{d}", m, d, "flux") for m in (256, 1024, 4096, 16384, 65536)
                 for d in (1152, 3072, 12288))),
 )
-TABLE_KERNELS = ("umma", "butterfly", "mma", "diag", "hadamard", "identity")
+TABLE_KERNELS = ("umma", "butterfly", "mma", "diag", "hadamard", "identity", "dual")
 
 
 def oracle_rate_shape(m: int, d: int, seconds: float):
@@ -634,7 +671,7 @@ def run_table(args):
     peak, _ = hbm_peak()
     stream = torch.cuda.Stream(device=dev)
     print("| config | layer | m x d | sets | " + " | ".join(
-        f"{k} GB/s (% peak)" if k == "umma" else f"{k} GB/s" for k in TABLE_KERNELS) +
+        f"{k} GB/s (% peak)" if k in ("umma", "dual") else f"{k} GB/s" for k in TABLE_KERNELS) +
         " | umma / diag |")
     print("|" + "---|" * (len(TABLE_KERNELS) + 5))
     for cfg, layers in TABLE_CONFIGS:
@@ -656,6 +693,7 @@ def run_table(args):
             Q = [torch.empty((m, d // 2), dtype=torch.uint8, device=dev) for _ in range(sets)]
             SF = [torch.empty(kq.kq_sf_bytes(m, d, layout), dtype=torch.uint8, device=dev)
                   for _ in range(sets)]
+            AT = [torch.empty((m, d), dtype=torch.bfloat16, device=dev) for _ in range(sets)]
             n_launch = max(sets, 32)
 
             def launch(kind, i):
@@ -667,6 +705,9 @@ def run_table(args):
                 elif kind == "butterfly":
                     kq.kq_quantize_mxfp4(A[s], d, factors=F, layout=layout, q=Q[s], sf=SF[s],
                                          variant=kq.VARIANT_BUTTERFLY, stream=stream)
+                elif kind == "dual":
+                    kq.kq_quantize_mxfp4_dual(A[s], KX, d, layout=layout, q=Q[s], sf=SF[s],
+                                              at=AT[s], stream=stream)
                 elif kind == "diag":
                     kq.kq_smooth_quantize_mxfp4(A[s], S, d, layout=layout, q=Q[s], sf=SF[s],
                                                 stream=stream)
@@ -697,13 +738,14 @@ def run_table(args):
                         b.record(stream)
                     stream.synchronize()
                 med = statistics.median(a.elapsed_time(b) for a, b in ev) / n_launch
-                gbs[kind] = set_bytes / (med * 1e-3) / 1e9
+                nbytes = algo_bytes_dual(m, d) if kind == "dual" else set_bytes
+                gbs[kind] = nbytes / (med * 1e-3) / 1e9
                 del g
-            cells = [f"{gbs['umma']:.0f} ({100 * gbs['umma'] / peak:.0f} %)"] + \
-                [f"{gbs[k]:.0f}" for k in TABLE_KERNELS[1:]]
+            cells = [f"{gbs[k]:.0f} ({100 * gbs[k] / peak:.0f} %)" if k in ("umma", "dual")
+                     else f"{gbs[k]:.0f}" for k in TABLE_KERNELS]
             print(f"| {cfg} | {name} | {m}x{d} | {sets} | " + " | ".join(cells) +
                   f" | {gbs['umma'] / gbs['diag']:.2f} |", flush=True)
-            del A, Q, SF, KX
+            del A, Q, SF, KX, AT
             torch.cuda.empty_cache()
     # the oracle on the host cores: all of them, then one
     print()

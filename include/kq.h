@@ -122,6 +122,26 @@ KQ_API kq_status kq_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int6
                             float *y_debug, cudaStream_t stream);
 
 /*
+ * kq_quantize_mxfp4_dual -- kq_quantize_mxfp4 on the tensor-core path that
+ * also writes the 16-bit side output A T in the same pass: [KQ] eq. (11)
+ * evaluates Q(A T) x Q(W~ - L R) + (A T) L R, the low-rank branch taking
+ * A T in 16 bits (App. D "Quantization"; bf16 for SANA and FLUX), cast from
+ * the transform's fp32 result as K1 does (Sec. 3.5.1).
+ *   K_expanded  device, output of kq_expand_blocks(..., KQ_K_BF16X3, ...)
+ *               (required)
+ *   at, ldat    device, bf16 [m][ldat] (written, columns < d): at[i][c] is y
+ *               rounded to bf16 (nearest, ties to even) -- the same y that is
+ *               quantized into q / sf.  ldat >= d, ldat % 8 == 0, 16-byte
+ *               aligned.  A block that timed out (see Errors above) gets
+ *               bf16 NaNs.
+ *   other arguments as kq_quantize_mxfp4.
+ */
+KQ_API kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                 const void *K_expanded, uint8_t *q, int64_t ldq, uint8_t *sf,
+                                 kq_sf_layout sf_layout, uint16_t *at, int64_t ldat,
+                                 float *y_debug, cudaStream_t stream);
+
+/*
  * kq_smooth_quantize_mxfp4 -- diagonal-scale baseline: T = diag(s),
  * y[i][c] = a[i][c] * s[c], then the same MXFP4 quantizer ([KQ] Sec. 4.4,
  * "Scale", per-channel scaling of SmoothQuant; a SmoothQuant user passes

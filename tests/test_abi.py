@@ -145,3 +145,18 @@ def test_aux_argument_checks(L):
     assert L.kq_test_encode_e2m1(0, 7, FAKE, None) == 2
     assert L.kq_test_encode_e2m1(0xFFFFFFF8, 16, FAKE, None) == 2
     assert L.kq_test_encode_e2m1(0, 0, None, None) == 0
+
+
+def test_dual_argument_checks(L):
+    """kq_quantize_mxfp4_dual validates before launching: the side output and
+    the expanded blocks are required, 16-byte aligned, ldat >= d, ldat % 8 == 0.
+    Every call here fails a check (or has m = 0), so nothing is launched."""
+    vp = ctypes.c_void_p
+    A, K, q, sf, at = vp(4096), vp(8192), vp(12288), vp(16384), vp(20480)
+    f = L.kq_quantize_mxfp4_dual
+    assert f(A, 4, 64, 64, K, q, 32, sf, 0, at, 32, None, None) == 2          # ldat < d
+    assert f(A, 4, 64, 64, None, q, 32, sf, 0, at, 64, None, None) == 1       # no blocks
+    assert f(A, 4, 64, 64, K, q, 32, sf, 0, None, 64, None, None) == 1        # no side output
+    assert f(A, 4, 64, 64, K, q, 32, sf, 0, vp(20488), 64, None, None) == 3   # misaligned
+    assert f(A, 4, 64, 64, K, q, 32, sf, 0, at, 68, None, None) == 3          # ldat % 8
+    assert f(A, 0, 64, 64, None, None, 32, None, 0, None, 64, None, None) == 0  # m = 0

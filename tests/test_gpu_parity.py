@@ -424,3 +424,61 @@ def test_blocked_layout_against_library_gemm():
         (np.abs(got - ref) / (scale + 1e-30)).max())
     assert np.linalg.norm(got - ref) <= (1e-6 if out.dtype == torch.float32 else 1e-2) * \
         np.linalg.norm(ref)
+
+
+# -------------------------------------- 16-bit side output (low-rank branch) --
+
+DUAL_SHAPES = [(256, 1152), (300, 2240), (7, 96), (129, 160), (1, 32)]
+
+
+def run_dual(A_bits, d, layout, factors_gpu, y_debug=True, at=None, q=None, sf=None):
+    records = kq.kq_expand_blocks(dev(factors_gpu), kq.KQ_K_BF16X3)
+    return kq.kq_quantize_mxfp4_dual(to_bf16(A_bits), records, d, layout=layout, q=q, sf=sf,
+                                     at=at, y_debug=y_debug)
+
+
+@pytest.mark.parametrize("m,d", DUAL_SHAPES, ids=[f"{m}x{d}" for m, d in DUAL_SHAPES])
+def test_dual_side_output_parity(m, d):
+    """kq_quantize_mxfp4_dual: codes and scales under rules (i)-(iii) and
+    identical to the single-output call; the bf16 side output under rules
+    (iv)-(v); guard bytes around the side output (ldat > d) untouched."""
+    nb = d // 32
+    A_bits = synth.activations(m, d, 91 + m, "flux")
+    pg, po = lib_factors(nb, 93 + d)
+    ldat = d + 24
+    for layout in (0, 1):
+        at_store = torch.full((m + 2, ldat), -7.0, dtype=torch.bfloat16, device="cuda")
+        at = at_store[1:m + 1, :]
+        q, sf, at_out, y = run_dual(A_bits, d, layout, pg, at=at[:, :ldat])
+        assert at_out.data_ptr() == at.data_ptr()
+        res = parity.check(A_bits, d, "kron", po, layout, np_(q), np_(sf), np_(y))
+        side = parity.check_side_output(A_bits, d, "kron", po,
+                                        np_(at.contiguous().view(torch.int16)).view(np.uint16),
+                                        np_(y))
+        guard = np_(at_store.float())
+        assert (guard[0] == -7.0).all() and (guard[m + 1] == -7.0).all()
+        assert (guard[1:m + 1, d:] == -7.0).all(), "side-output row padding overwritten"
+        nsf = kq.kq_sf_bytes(m, d, layout)       # the buffers may be longer (>= 16 bytes)
+        q1, sf1, _ = run_kind("kron_umma", A_bits, d, layout, pg, y_debug=False)
+        assert torch.equal(q, q1) and torch.equal(sf[:nsf], sf1[:nsf])
+        # the production launch (no debug output) writes the same bytes
+        q2, sf2, at2, _ = run_dual(A_bits, d, layout, pg, y_debug=False)
+        assert torch.equal(q, q2) and torch.equal(sf[:nsf], sf2[:nsf])
+        assert torch.equal(at[:, :d].contiguous().view(torch.int16), at2.view(torch.int16))
+        print(m, d, layout, res, side)
+
+
+def test_dual_side_output_flux_ffn_down():
+    """FLUX FFN-down layer (4608 x 12288) at full size, sampled rows (first
+    and last tiles included)."""
+    m, d = 4608, 12288
+    A_bits = synth.activations(m, d, synth.SEED_A + 3, "flux")
+    pg, po = lib_factors(d // 32, synth.SEED_FACTORS + 3)
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([np.arange(130), np.arange(m - 130, m),
+                                     rng.choice(m, 500, replace=False)]))
+    q, sf, at, y = run_dual(A_bits, d, 1, pg)
+    parity.check(A_bits, d, "kron", po, 1, np_(q), np_(sf), np_(y), rows)
+    side = parity.check_side_output(A_bits, d, "kron", po, np_(at.view(torch.int16)).view(np.uint16),
+                                    np_(y), rows)
+    print(side)

@@ -251,7 +251,7 @@ kq_status kq_quantize_mxfp4_variant(const uint16_t *A, int64_t m, int64_t d, int
     QuantParams p;
     fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
     if (variant == 1) return launch_quant_mma(A, lda, K_expanded, p, stream);
-    if (variant == 3) return launch_quant_umma(A, lda, K_expanded, p, stream);
+    if (variant == 3) return launch_quant_umma(A, lda, K_expanded, p, nullptr, 0, stream);
     if (variant == 0) {
         p.factors = factors;
         return launch_quant_tma(kKron, A, lda, p, stream);
@@ -269,6 +269,22 @@ kq_status kq_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda
     const int variant = K_expanded != nullptr ? 3 : (factors != nullptr ? 0 : 2);
     return kq_quantize_mxfp4_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout,
                                      y_debug, variant, stream);
+}
+
+kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                 const void *K_expanded, uint8_t *q, int64_t ldq, uint8_t *sf,
+                                 kq_sf_layout sf_layout, uint16_t *at, int64_t ldat,
+                                 float *y_debug, cudaStream_t stream)
+{
+    kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
+    if (st != KQ_OK) return st;
+    if (ldat < d || ldat > (1LL << 38)) return KQ_ERR_SHAPE;
+    if (m == 0) return KQ_OK;
+    if (K_expanded == nullptr || at == nullptr) return KQ_ERR_NULL;
+    if (!aligned16(K_expanded) || !aligned16(at) || ldat % 8 != 0) return KQ_ERR_ALIGN;
+    QuantParams p;
+    fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
+    return launch_quant_umma(A, lda, K_expanded, p, at, ldat, stream);
 }
 
 kq_status kq_smooth_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,

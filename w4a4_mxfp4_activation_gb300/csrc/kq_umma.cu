@@ -43,8 +43,17 @@
 //               so direct 16-byte stores from a warp would touch 32 rows and
 //               clog the memory pipe; whole 32-byte rows also halve the L2
 //               write transactions of 16-byte ones).
+// With DUAL, the kernel also writes the 16-bit side output A T that feeds
+// the low-rank branch of eq. (11) ("KroQuant ...", App. D "Quantization":
+// those activations stay in 16 bits; Sec. 3.5.1 K1 casts y to the input
+// dtype): the epilogue rounds y to bf16 and writes it over the tile's
+// activations in its ring stage (the MMAs have read them; same 128 x 64
+// shape and 128B swizzle), and one TMA store per tile sends it to HBM.  The
+// ring stage is then released by the epilogue, once that store has read it,
+// instead of by the MMA commit.
 // Every wait is bounded in time; a timed-out epilogue writes the E8M0 NaN
-// byte 0xFF as the scale of the blocks it could not finish.
+// byte 0xFF as the scale of the blocks it could not finish (and bf16 NaNs
+// into the side output).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -181,10 +190,11 @@ __device__ __forceinline__ void store_scale_u(const QuantParams &p, int64_t row,
     }
 }
 
-template <int STAGES, bool DEBUG>
+template <int STAGES, bool DEBUG, bool DUAL>
 __global__ void __launch_bounds__(kThreadsU, 1)
     quant_umma_kernel(const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmQ, const QuantParams p,
+                      const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmAT, const QuantParams p,
                       const uint8_t *__restrict__ records)
 {
     using Cfg = UCfg<STAGES>;
@@ -201,6 +211,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);              // kernel parameters: no dependency on
         tma_prefetch_desc(&tmQ);              // earlier grids
+        if (DUAL) tma_prefetch_desc(&tmAT);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
@@ -274,7 +285,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                                   smem_desc(stage + Cfg::kBOff + b * Cfg::kRecBytes + h * 3072,
                                             128, 256, 0),
                                   static_cast<uint32_t>(h));
-                umma_commit(bar_empty + 8 * s);          // ring stage free once the MMAs read it
+                if (!DUAL)
+                    umma_commit(bar_empty + 8 * s);      // ring stage free once the MMAs read it
                 umma_commit(bar_acc_full + 8 * a);       // accumulators ready
             }
             __syncwarp();
@@ -291,6 +303,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int r = qtr * 32 + lane;        // row within the tile
         const int pair = grp * 4 + (e & 3);   // the quarter's two warps (b = 0, 1)
         int slot = 0;                         // staging buffer of this tile, mod 3
+        // DUAL: one warp of the group stores the tile's side output and
+        // releases the tile's ring stage as soon as that store has read it
+        // (measured on GB300: deferring the release by a tile, to overlap
+        // the wait, costs more in ring depth than the wait itself)
+        const bool at_leader = DUAL && (e & 7) == 4 && lane == 0;
         int it = grp;
         bool ok = true;
         TileWalk tw(static_cast<int>(blockIdx.x + grp * gridDim.x),
@@ -307,6 +324,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             if (ok) ok = __all_sync(0xffffffffu,
                                     mbar_wait(bar_acc_full + 8 * a, static_cast<uint32_t>((it >> 1) & 1)));
             uint4 codes = make_uint4(0u, 0u, 0u, 0u);
+            uint4 at_w[4];            // DUAL: the row's 32 bf16 of y (bf16 NaN if not computed)
+            if (DUAL) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) at_w[k] = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
+            }
             if (ok) {
                 tc_fence_after();
                 float2 Y[16];
@@ -338,6 +360,18 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                             stg_f4(yd + 4 * k, make_float4(Y[2 * k].x, Y[2 * k].y, Y[2 * k + 1].x,
                                                            Y[2 * k + 1].y));
                     }
+                    if (DUAL) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const __nv_bfloat162 h = __floats2bfloat162_rn(Y[4 * k + t].x, Y[4 * k + t].y);
+                                w[t] = *reinterpret_cast<const uint32_t *>(&h);
+                            }
+                            at_w[k] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
                     codes = quantize_block(Y, sbyte);
                     swrite = true;
                 } else {
@@ -366,6 +400,15 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             // three tiles ago, and the b = 0 warp waited for it to finish
             // reading (below) before the pair barrier of the previous tile.
             sts128(stg + lane * 32 + ((b ^ ((lane >> 2) & 1)) << 4), codes);
+            if (DUAL) {
+                // side output over the tile's activations in its ring stage:
+                // row r, 16-byte chunk 4 b + k at position (4 b + k) ^ (r % 8)
+                // (the 128B swizzle of the activation tensor map)
+                const uint32_t arow = base + static_cast<uint32_t>(it % STAGES) * Cfg::kStageBytes +
+                                      static_cast<uint32_t>(r) * 128;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) sts128(arow + (((4 * b + k) ^ (r & 7)) << 4), at_w[k]);
+            }
             fence_proxy_async_smem();
             named_barrier(1 + pair, 64);
             if (tiled && b == 0) {
@@ -380,9 +423,22 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                 bulk_commit_group();
                 bulk_wait_group_read<1>();
             }
+            if (DUAL) {
+                named_barrier(9 + grp, kEpiThreads / 2);   // the whole tile is in the stage
+                if (at_leader) {
+                    const int s = it % STAGES;
+                    if (ct * 2 < p.nb)
+                        tma_store_2d(&tmAT, ct * 64, rt * kBR,
+                                     base + static_cast<uint32_t>(s) * Cfg::kStageBytes);
+                    bulk_commit_group();
+                    bulk_wait_group_read<0>();
+                    mbar_arrive(bar_empty + 8 * s);
+                }
+            }
             slot = slot == Cfg::kStgBufs - 1 ? 0 : slot + 1;
         }
         if (b == 0 && lane == 0) bulk_wait_group_all();
+        if (at_leader) bulk_wait_group_all();
     }
 
     tc_fence_before();
@@ -399,12 +455,12 @@ struct USlot {
     cudaError_t err[64] = {};
 };
 
-template <int STAGES, bool DEBUG>
-kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, QuantParams p,
-                      const uint8_t *records, int sm_count, cudaStream_t stream)
+template <int STAGES, bool DEBUG, bool DUAL>
+kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, const CUtensorMap &mapat,
+                      QuantParams p, const uint8_t *records, int sm_count, cudaStream_t stream)
 {
     using Cfg = UCfg<STAGES>;
-    auto kern = quant_umma_kernel<STAGES, DEBUG>;
+    auto kern = quant_umma_kernel<STAGES, DEBUG, DUAL>;
     static USlot slot;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
@@ -425,13 +481,14 @@ kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, QuantPara
     // one CTA per SM: each holds 256 of the SM's 512 TMEM columns
     const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, sm_count));
     if (!tiles_fit_int32(p, grid)) return KQ_ERR_SHAPE;
-    return launch_pdl(kern, grid, kThreadsU, Cfg::kSmemBytes, stream, map, mapq, p, records);
+    return launch_pdl(kern, grid, kThreadsU, Cfg::kSmemBytes, stream, map, mapq, mapat, p,
+                      records);
 }
 
 }  // namespace
 
 kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expanded,
-                            const QuantParams &p, cudaStream_t stream)
+                            const QuantParams &p, uint16_t *at, int64_t ldat, cudaStream_t stream)
 {
     DeviceInfo info;
     kq_status st = device_info(info);
@@ -443,8 +500,16 @@ kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expand
                                CU_TENSOR_MAP_SWIZZLE_32B);
     if (st != KQ_OK) return st;
     const uint8_t *rec = static_cast<const uint8_t *>(K_expanded);
-    if (p.y_debug != nullptr) return launch_umma<6, true>(map, mapq, p, rec, info.sm_count, stream);
-    return launch_umma<6, false>(map, mapq, p, rec, info.sm_count, stream);
+    const int sms = info.sm_count;
+    if (at == nullptr) {
+        if (p.y_debug != nullptr) return launch_umma<6, true, false>(map, mapq, map, p, rec, sms, stream);
+        return launch_umma<6, false, false>(map, mapq, map, p, rec, sms, stream);
+    }
+    CUtensorMap mapat;
+    st = make_tensor_map_2d_bf16(&mapat, at, p.m, p.d, ldat, 64, kBR);
+    if (st != KQ_OK) return st;
+    if (p.y_debug != nullptr) return launch_umma<6, true, true>(map, mapq, mapat, p, rec, sms, stream);
+    return launch_umma<6, false, true>(map, mapq, mapat, p, rec, sms, stream);
 }
 
 }  // namespace kq

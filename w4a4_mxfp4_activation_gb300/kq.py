@@ -33,7 +33,7 @@ EXPORTS = (
     "kq_quantize_mxfp4", "kq_smooth_quantize_mxfp4", "kq_hadamard_quantize_mxfp4",
     "kq_expand_blocks", "kq_expanded_bytes", "kq_dequantize", "kq_sf_bytes",
     "kq_status_string", "kq_lu_to_factors", "kq_invert_transpose_factors",
-    "kq_quantize_mxfp4_variant", "kq_test_encode_e2m1",
+    "kq_quantize_mxfp4_variant", "kq_test_encode_e2m1", "kq_quantize_mxfp4_dual",
 )
 
 
@@ -64,6 +64,9 @@ def lib() -> ctypes.CDLL:
             L.kq_quantize_mxfp4_variant.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64, vp, st, vp,
                                                     st, vp]
             L.kq_quantize_mxfp4_variant.restype = st
+            L.kq_quantize_mxfp4_dual.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, st, vp, i64,
+                                                 vp, vp]
+            L.kq_quantize_mxfp4_dual.restype = st
             L.kq_smooth_quantize_mxfp4.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, st, vp, vp]
             L.kq_smooth_quantize_mxfp4.restype = st
             L.kq_hadamard_quantize_mxfp4.argtypes = [vp, i64, i64, i64, vp, i64, vp, st, vp, vp]
@@ -180,6 +183,27 @@ def kq_quantize_mxfp4(A, d: int | None = None, factors=None, K_expanded=None,
         _check(lib().kq_quantize_mxfp4_variant(*args, variant, _stream(stream)),
                "kq_quantize_mxfp4_variant")
     return q, sf, y_debug
+
+
+def kq_quantize_mxfp4_dual(A, K_expanded, d: int | None = None, layout: int = KQ_SF_ROWMAJOR,
+                           q=None, sf=None, at=None, y_debug=None, stream=None):
+    """Quantize A on the tensor-core path and also write the bf16 side output
+    A T.  Returns (q, sf, at, y_debug); ``at`` is allocated as bf16 [m, d]
+    when not given."""
+    import torch
+    A = _bf16_bits(A)
+    m, lda = A.shape
+    d = lda if d is None else d
+    q, sf, y_debug = _outputs(A, m, d, layout, q, sf, y_debug)
+    if at is None:
+        at = torch.empty((m, d), dtype=torch.bfloat16, device=A.device)
+    ldq = q.shape[1] if q.dim() == 2 else d // 2
+    ldat = at.stride(0) if at.dim() == 2 else d
+    _check(lib().kq_quantize_mxfp4_dual(_ptr(A), m, d, A.stride(0), _ptr(K_expanded), _ptr(q), ldq,
+                                        _ptr(sf), layout, _ptr(at), ldat, _ptr(y_debug),
+                                        _stream(stream)),
+           "kq_quantize_mxfp4_dual")
+    return q, sf, at, y_debug
 
 
 def kq_smooth_quantize_mxfp4(A, s, d: int | None = None, layout: int = KQ_SF_ROWMAJOR, q=None,
