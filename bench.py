@@ -478,7 +478,9 @@ def run_ours(args, dist: Dist):
                 "ms_per_step": round(dms / nd, 5),
                 "dominant_launch_ms": round(dlaunch[0], 5) if dlaunch else None,
                 "dominant_frac": round(algo_bytes_dual(dom_m, dom_d) / (dlaunch[0] * 1e-3) / 1e9
-                                       / peak, 4) if dlaunch else None}
+                                       / peak, 4) if dlaunch else None,
+                "traffic": recorded_traffic("flux_ffn_down_dual") if args.variant == "umma"
+                else None}
         AT = [[None] * SETS for _ in LAYERS]
         torch.cuda.empty_cache()
 
