@@ -383,21 +383,68 @@ def test_expand_blocks_fp32():
 
 
 def test_blocked_layout_against_library_gemm():
-    """P8: the packed codes and the 128x4 scale tiles, handed to the
-    library's block-scaled MXFP4 GEMM (torch._scaled_mm), give the fp64
-    product of our own dequantized operands.  Skipped if this torch/cuBLAS
-    build has no MXFP4 GEMM."""
-    if not hasattr(torch, "float4_e2m1fn_x2") or not hasattr(torch, "float8_e8m0fnu"):
-        pytest.skip("torch has no float4_e2m1fn_x2 / float8_e8m0fnu")
+    """P8: the 128x4 scale tiles, handed to a library's block-scaled GEMM,
+    give the fp64 product of our own dequantized operands: the library's
+    reading of the tiled scale layout agrees with ours.  Tried in order:
+    cuBLASLt MXFP4 on the packed codes (also checks the nibble order),
+    cuBLASLt MXFP8 on the codes widened to E4M3 bytes (every E2M1 value is
+    exact in E4M3; the scales and their layout are used as written), and
+    torch._scaled_mm.  Skipped if none offers an MX GEMM here."""
+    import cublaslt_mxfp4 as lt
     m, d, o = 256, 1152, 384
     A_bits = synth.activations(m, d, 41, "pixart")
     W_bits = synth.weights(o, d, seed=42, std=1.0)
     Fg, _ = lib_factors(d // 32, 43)
     qa, sfa, _ = run_kind("kron", A_bits, d, 1, Fg, y_debug=False)
     qw, sfw, _ = run_kind("identity", W_bits, d, 1, None, y_debug=False)
+    out, errors = None, []
+    ws = torch.empty(32 << 20, dtype=torch.uint8, device="cuda")
+    # E2M1 code -> E4M3 byte of the same value (sign bit 3 -> bit 7)
+    e2m1 = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0] * 2) * \
+        torch.tensor([1.0] * 8 + [-1.0] * 8)
+    to_e4m3 = e2m1.to(torch.float8_e4m3fn).view(torch.uint8).cuda()
+
+    def widen(q):
+        q = q.long()
+        return to_e4m3[torch.stack([q & 15, q >> 4], dim=-1).reshape(q.shape[0], -1)]
+
+    wa, ww = widen(qa), widen(qw)
+    for elem, pa, pw, name in ((lt.CUDA_R_4F_E2M1, qa, qw, "MXFP4"),
+                               (lt.CUDA_R_8F_E4M3, wa, ww, "MXFP8")):
+        for dtype, code in ((torch.float32, lt.CUDA_R_32F), (torch.bfloat16, lt.CUDA_R_16BF)):
+            c = torch.zeros((m, o), dtype=dtype, device="cuda")
+            why = lt.mx_gemm(pa.data_ptr(), sfa.data_ptr(), m, pw.data_ptr(), sfw.data_ptr(), o, d,
+                             c.data_ptr(), code, ws.data_ptr(), ws.numel(),
+                             torch.cuda.current_stream().cuda_stream, elem)
+            if why is None:
+                out = c
+                break
+            errors.append(f"cuBLASLt {name} {dtype}: {why}")
+        if out is not None:
+            print("library consumer: cuBLASLt", name, out.dtype)
+            break
+    if out is None and hasattr(torch, "float4_e2m1fn_x2") and hasattr(torch, "float8_e8m0fnu"):
+        out = torch_scaled_mm_mxfp4(qa, sfa, qw, sfw, m, o, d, errors)
+    if out is None:
+        pytest.skip(f"no MXFP4 block-scaled GEMM here: {errors}")
+    print("library MXFP4 GEMM:", out.dtype, "declined:", errors)
+    torch.cuda.synchronize()
+    Aq = np_(kq.kq_dequantize(qa, sfa, m, d, layout=1)).astype(np.float64)
+    Wq = np_(kq.kq_dequantize(qw, sfw, o, d, layout=1)).astype(np.float64)
+    ref = Aq @ Wq.T
+    got = out.float().cpu().numpy().astype(np.float64)
+    scale = np.abs(Aq) @ np.abs(Wq).T
+    tol = 2 ** -13 if out.dtype == torch.float32 else 2 ** -7
+    assert np.all(np.abs(got - ref) <= tol * scale + 1e-30), float(
+        (np.abs(got - ref) / (scale + 1e-30)).max())
+    assert np.linalg.norm(got - ref) <= (1e-5 if out.dtype == torch.float32 else 1e-2) * \
+        np.linalg.norm(ref)
+
+
+def torch_scaled_mm_mxfp4(qa, sfa, qw, sfw, m, o, d, errors):
     nbp = -(-(d // 32) // 4) * 4
     sa, sw = sfa.view(torch.float8_e8m0fnu), sfw.view(torch.float8_e8m0fnu)
-    out, errors = None, []
+    out = None
     for shape_a, shape_w in (((-(-m // 128) * 128, nbp), (-(-o // 128) * 128, nbp)),
                              ((-1,), (-1,))):
         for out_dtype in (torch.bfloat16, torch.float32):
@@ -411,19 +458,7 @@ def test_blocked_layout_against_library_gemm():
                 errors.append(str(e)[-300:])
         if out is not None:
             break
-    if out is None:
-        pytest.skip(f"no MXFP4 block-scaled GEMM here: {errors}")
-    torch.cuda.synchronize()
-    Aq = np_(kq.kq_dequantize(qa, sfa, m, d, layout=1)).astype(np.float64)
-    Wq = np_(kq.kq_dequantize(qw, sfw, o, d, layout=1)).astype(np.float64)
-    ref = Aq @ Wq.T
-    got = out.float().cpu().numpy().astype(np.float64)
-    scale = np.abs(Aq) @ np.abs(Wq).T
-    tol = 1e-5 if out.dtype == torch.float32 else 2 ** -7
-    assert np.all(np.abs(got - ref) <= tol * scale + 1e-30), float(
-        (np.abs(got - ref) / (scale + 1e-30)).max())
-    assert np.linalg.norm(got - ref) <= (1e-6 if out.dtype == torch.float32 else 1e-2) * \
-        np.linalg.norm(ref)
+    return out
 
 
 # -------------------------------------- 16-bit side output (low-rank branch) --
