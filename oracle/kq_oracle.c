@@ -156,6 +156,39 @@ KQO_EXPORT void kqo_transform_hadamard(const uint16_t *A, int64_t m, int64_t d, 
     apply_dense_blocks(A, m, d, lda, Kscratch, y, bound);
 }
 
+/* Full-row Walsh-Hadamard baseline ([KQ] Sec. 4.4, Table 3 "FWHT"; d a
+ * power of two): y = a . H_d / sqrt(d) with the Sylvester-order Hadamard
+ * matrix H_d[r][c] = (-1)^popcount(r & c), computed by the fast transform --
+ * log2(d) passes of butterflies (x, y) -> (x + y, x - y) over pairs h apart,
+ * h = 1, 2, 4, ... (H_2n = [[H_n, H_n], [H_n, -H_n]]; H_d is symmetric, so
+ * a . H_d = H_d . a) -- then one multiply by 1/sqrt(d).
+ * bound = sum_r |a_r| / sqrt(d), the error scale of every output. */
+KQO_EXPORT void kqo_transform_fwht(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                   double *y, double *bound)
+{
+    const double inv = 1.0 / sqrt((double)d);
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < m; ++i) {
+        double *v = y + i * d;
+        double l1 = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            v[c] = bf16_bits_to_f64(A[i * lda + c]);
+            l1 += fabs(v[c]);
+        }
+        for (int64_t h = 1; h < d; h *= 2)
+            for (int64_t base = 0; base < d; base += 2 * h)
+                for (int64_t j = base; j < base + h; ++j) {
+                    const double x = v[j], z = v[j + h];
+                    v[j] = x + z;
+                    v[j + h] = x - z;
+                }
+        for (int64_t c = 0; c < d; ++c) {
+            v[c] *= inv;
+            if (bound) bound[i * d + c] = l1 * inv;
+        }
+    }
+}
+
 /* Diagonal (per-channel scaling, SmoothQuant-style) baseline:
  * T = diag(s), y = a * s[c]  ([KQ] Sec. 4.4, the "Scale" kernel). */
 KQO_EXPORT void kqo_transform_diag(const uint16_t *A, int64_t m, int64_t d, int64_t lda,

@@ -69,6 +69,7 @@ def _bind(path: str) -> ctypes.CDLL:
     L.kqo_transform_hadamard.argtypes = [u16p, i64, i64, i64, dp, dp, dp]
     L.kqo_transform_diag.argtypes = [u16p, i64, i64, i64, dp, dp, dp]
     L.kqo_transform_identity.argtypes = [u16p, i64, i64, i64, dp, dp]
+    L.kqo_transform_fwht.argtypes = [u16p, i64, i64, i64, dp, dp]
     L.kqo_e8m0_exponent.argtypes = [ctypes.c_double]
     L.kqo_e8m0_exponent.restype = ctypes.c_int
     L.kqo_e2m1_value.argtypes = [ctypes.c_uint8]
@@ -196,7 +197,8 @@ def transform(A: np.ndarray, d: int, kind: str, param=None):
     """Return (y, bound), both fp64 [m, d].
 
     kind: 'kron' (param = factors [nb, 5, 2, 2]), 'dense' (param = [nb, 32, 32]),
-    'hadamard', 'diag' (param = s [d]), 'identity'.
+    'hadamard', 'diag' (param = s [d]), 'identity', 'fwht' (full-row
+    Walsh-Hadamard, d a power of two).
     ``bound[i, c] = sum_r |a_r K_rc|`` is the scale the 2^-16 rule uses."""
     A = _bits(A)
     m, lda = A.shape
@@ -222,6 +224,9 @@ def transform(A: np.ndarray, d: int, kind: str, param=None):
         L.kqo_transform_diag(Ap, m, d, lda, _p(s, ctypes.c_double), yp, bp)
     elif kind == "identity":
         L.kqo_transform_identity(Ap, m, d, lda, yp, bp)
+    elif kind == "fwht":
+        assert d & (d - 1) == 0, "the full-row transform needs a power-of-two d"
+        L.kqo_transform_fwht(Ap, m, d, lda, yp, bp)
     else:
         raise ValueError(kind)
     return y, bound

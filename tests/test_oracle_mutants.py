@@ -37,6 +37,8 @@ MUTANTS = [
      [pins.test_bf16_rounding_golden, pins.test_bf16_rounding_is_nearest_even]),
     ("bf16_subnormal_spacing", "if (e < -126) e = -126;", "if (e < -127) e = -127;",
      [pins.test_bf16_rounding_golden, pins.test_bf16_rounding_is_nearest_even]),
+    ("fwht_butterfly_sign", "v[j + h] = x - z;", "v[j + h] = z - x;",
+     [lambda o: pins.test_fwht_matches_library_hadamard(o, 64), pins.test_fwht_closed_forms]),
 ]
 
 

@@ -372,3 +372,42 @@ def test_bf16_rounding_matches_torch_fp32(oracle_lib):
     want = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     got = oracle_lib.round_bf16(f.astype(np.float64))
     assert np.array_equal(got, want)
+
+
+# --- full-row Walsh-Hadamard baseline ------------------------------------------------
+
+@pytest.mark.parametrize("d", [32, 64, 1024, 4096])
+def test_fwht_matches_library_hadamard(oracle_lib, d):
+    """Special case reducing to a library routine: y = a . H_d / sqrt(d) with
+    scipy's Sylvester-order Hadamard matrix."""
+    A = synth.activations(3, d, 120 + d, "flux")
+    y, bound = oracle_lib.transform(A, d, "fwht")
+    a = synth.bf16_bits_to_f32(A).astype(np.float64)
+    H = scipy.linalg.hadamard(d).astype(np.float64)
+    want = a @ H / math.sqrt(d)
+    assert np.allclose(y, want, rtol=0, atol=1e-12 * np.abs(a).sum(axis=1, keepdims=True).max())
+    assert np.allclose(bound, np.abs(a).sum(axis=1, keepdims=True) / math.sqrt(d), rtol=1e-15)
+
+
+def test_fwht_closed_forms(oracle_lib):
+    """One-hot rows give rows of H_d / sqrt(d) ((-1)^popcount(r & c)), the
+    transform keeps the Euclidean norm (H_d / sqrt(d) is orthogonal), and at
+    d = 32 it is the block Hadamard transform."""
+    d = 2048
+    rows = [0, 1, 5, 1000, 2047]
+    A = np.zeros((len(rows), d), np.uint16)
+    for i, r in enumerate(rows):
+        A[i, r] = 0x3F80                                   # 1.0
+    y, _ = oracle_lib.transform(A, d, "fwht")
+    c = np.arange(d)
+    for i, r in enumerate(rows):
+        sign = np.array([1.0 if bin(r & cc).count("1") % 2 == 0 else -1.0 for cc in c])
+        assert np.array_equal(y[i], sign / math.sqrt(d))
+    B = synth.activations(4, 8192, 131, "flux")
+    yb, _ = oracle_lib.transform(B, 8192, "fwht")
+    b = synth.bf16_bits_to_f32(B).astype(np.float64)
+    assert np.allclose(np.linalg.norm(yb, axis=1), np.linalg.norm(b, axis=1), rtol=1e-13)
+    C = synth.activations(5, 32, 132, "flux")
+    y32, _ = oracle_lib.transform(C, 32, "fwht")
+    yh, _ = oracle_lib.transform(C, 32, "hadamard")
+    assert np.allclose(y32, yh, rtol=0, atol=1e-13)
