@@ -656,13 +656,18 @@ def oracle_rate_shape(m: int, d: int, seconds: float):
     return algo_bytes(rows, d) / dt / 1e9, rows
 
 
-def run_table(args):
-    """Per-launch time of each kernel on each config shape, in the bench's
-    steady state: launches back to back from CUDA graphs, rotating over
-    enough input/output sets that their footprint exceeds 3x the L2 (so every
-    launch reads its input from DRAM and evicts earlier outputs), the time
-    per launch being the median over args.table_reps graph replays of the
-    replay's CUDA-event time / its launches."""
+def synth_seed(cfg: str) -> int:
+    from w4a4_mxfp4_activation_gb300 import synth
+    return synth.SEED_A + int(cfg)
+
+
+def measure_shape(args, m, d, model, seed, kinds, peak):
+    """Per-launch median time (us) of each kernel kind on one layer shape, in
+    the bench's steady state: launches back to back from CUDA graphs,
+    rotating over enough input/output sets that their footprint exceeds 3x
+    the L2 (every launch reads its input from DRAM and evicts earlier
+    outputs); the time per launch is the median over graph replays of the
+    replay's CUDA-event time / its launches.  Returns ({kind: us}, sets)."""
     import numpy as np
     import torch
     from w4a4_mxfp4_activation_gb300 import kq, synth
@@ -670,85 +675,112 @@ def run_table(args):
     dev = torch.device("cuda", 0)
     layout = kq.KQ_SF_BLOCKED_128x4
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    peak, _ = hbm_peak()
     stream = torch.cuda.Stream(device=dev)
+    sets = max(4, int(np.ceil(3 * l2 / algo_bytes(m, d))))
+    # the seeded generator for up to 4096 rows, tiled on the device
+    rows = min(m, 4096)
+    base = torch.from_numpy(synth.activations(rows, d, seed, model)
+                            .view(np.int16)).to(dev).view(torch.bfloat16)
+    A0 = base.repeat((m + rows - 1) // rows, 1)[:m].contiguous()
+    del base
+    A = [torch.roll(A0, shifts=37 * s, dims=0) for s in range(sets)]
+    del A0
+    F = torch.from_numpy(kq.kq_lu_to_factors(
+        synth.lu_params(d // 32, synth.SEED_FACTORS + seed), +1)).to(dev)
+    KX = kq.kq_expand_blocks(F, kq.KQ_K_BF16X3)
+    S = torch.from_numpy(synth.smooth_scales(d)).to(dev)
+    Q = [torch.empty((m, d // 2), dtype=torch.uint8, device=dev) for _ in range(sets)]
+    SF = [torch.empty(kq.kq_sf_bytes(m, d, layout), dtype=torch.uint8, device=dev)
+          for _ in range(sets)]
+    AT = ([torch.empty((m, d), dtype=torch.bfloat16, device=dev) for _ in range(sets)]
+          if "dual" in kinds else None)
+    n_launch = max(sets, 32)
+
+    def launch(kind, i):
+        s = i % sets
+        if kind in ("umma", "mma"):
+            kq.kq_quantize_mxfp4(A[s], d, K_expanded=KX, layout=layout, q=Q[s], sf=SF[s],
+                                 variant=kq.VARIANT_UMMA if kind == "umma" else kq.VARIANT_MMA,
+                                 stream=stream)
+        elif kind == "butterfly":
+            kq.kq_quantize_mxfp4(A[s], d, factors=F, layout=layout, q=Q[s], sf=SF[s],
+                                 variant=kq.VARIANT_BUTTERFLY, stream=stream)
+        elif kind == "dual":
+            kq.kq_quantize_mxfp4_dual(A[s], KX, d, layout=layout, q=Q[s], sf=SF[s], at=AT[s],
+                                      stream=stream)
+        elif kind == "diag":
+            kq.kq_smooth_quantize_mxfp4(A[s], S, d, layout=layout, q=Q[s], sf=SF[s],
+                                        stream=stream)
+        elif kind == "hadamard":
+            kq.kq_hadamard_quantize_mxfp4(A[s], d, layout=layout, q=Q[s], sf=SF[s], stream=stream)
+        elif kind == "fwht":
+            kq.kq_fwht_quantize_mxfp4(A[s], d, layout=layout, q=Q[s], sf=SF[s], stream=stream)
+        else:
+            kq.kq_quantize_mxfp4(A[s], d, layout=layout, q=Q[s], sf=SF[s], stream=stream)
+
+    us = {}
+    for kind in kinds:
+        with torch.cuda.stream(stream):
+            for i in range(sets):
+                launch(kind, i)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n_launch):
+                    launch(kind, i)
+            reps = max(5, min(args.table_reps, int(2e5 // n_launch)))
+            for _ in range(max(2, args.table_warmup // n_launch)):
+                g.replay()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(reps)]
+            for a, b in ev:
+                a.record(stream)
+                g.replay()
+                b.record(stream)
+            stream.synchronize()
+        us[kind] = statistics.median(a.elapsed_time(b) for a, b in ev) / n_launch * 1e3
+        del g
+    del A, Q, SF, KX, AT
+    torch.cuda.empty_cache()
+    return us, sets
+
+
+# the pages' Table 3 shapes: power-of-two d, where the full-row FWHT applies
+TABLE3_SHAPES = ((4096, 1024), (4096, 4096), (4096, 16384), (512, 4096), (512, 16384))
+
+
+def run_table(args):
+    """Steady-state GB/s of every kernel on every config shape, the pages'
+    Table 3 comparison on GB300, and the oracle on the host cores."""
+    import torch  # noqa: F401  (initializes CUDA before the measurements)
+    peak, _ = hbm_peak()
     print("| config | layer | m x d | sets | " + " | ".join(
         f"{k} GB/s (% peak)" if k in ("umma", "dual") else f"{k} GB/s" for k in TABLE_KERNELS) +
         " | umma / diag |")
     print("|" + "---|" * (len(TABLE_KERNELS) + 5))
     for cfg, layers in TABLE_CONFIGS:
         for name, m, d, model in layers:
-            set_bytes = algo_bytes(m, d)
-            sets = max(4, int(np.ceil(3 * l2 / set_bytes)))
-            # the seeded generator for up to 4096 rows, tiled on the device
-            rows = min(m, 4096)
-            base = torch.from_numpy(synth.activations(rows, d, synth.SEED_A + int(cfg), model)
-                                    .view(np.int16)).to(dev).view(torch.bfloat16)
-            A0 = base.repeat((m + rows - 1) // rows, 1)[:m].contiguous()
-            del base
-            A = [torch.roll(A0, shifts=37 * s, dims=0) for s in range(sets)]
-            del A0
-            F = torch.from_numpy(kq.kq_lu_to_factors(
-                synth.lu_params(d // 32, synth.SEED_FACTORS + int(cfg)), +1)).to(dev)
-            KX = kq.kq_expand_blocks(F, kq.KQ_K_BF16X3)
-            S = torch.from_numpy(synth.smooth_scales(d)).to(dev)
-            Q = [torch.empty((m, d // 2), dtype=torch.uint8, device=dev) for _ in range(sets)]
-            SF = [torch.empty(kq.kq_sf_bytes(m, d, layout), dtype=torch.uint8, device=dev)
-                  for _ in range(sets)]
-            AT = [torch.empty((m, d), dtype=torch.bfloat16, device=dev) for _ in range(sets)]
-            n_launch = max(sets, 32)
-
-            def launch(kind, i):
-                s = i % sets
-                if kind in ("umma", "mma"):
-                    kq.kq_quantize_mxfp4(A[s], d, K_expanded=KX, layout=layout, q=Q[s], sf=SF[s],
-                                         variant=kq.VARIANT_UMMA if kind == "umma"
-                                         else kq.VARIANT_MMA, stream=stream)
-                elif kind == "butterfly":
-                    kq.kq_quantize_mxfp4(A[s], d, factors=F, layout=layout, q=Q[s], sf=SF[s],
-                                         variant=kq.VARIANT_BUTTERFLY, stream=stream)
-                elif kind == "dual":
-                    kq.kq_quantize_mxfp4_dual(A[s], KX, d, layout=layout, q=Q[s], sf=SF[s],
-                                              at=AT[s], stream=stream)
-                elif kind == "diag":
-                    kq.kq_smooth_quantize_mxfp4(A[s], S, d, layout=layout, q=Q[s], sf=SF[s],
-                                                stream=stream)
-                elif kind == "hadamard":
-                    kq.kq_hadamard_quantize_mxfp4(A[s], d, layout=layout, q=Q[s], sf=SF[s],
-                                                  stream=stream)
-                else:
-                    kq.kq_quantize_mxfp4(A[s], d, layout=layout, q=Q[s], sf=SF[s], stream=stream)
-
-            gbs = {}
-            for kind in TABLE_KERNELS:
-                with torch.cuda.stream(stream):
-                    for i in range(sets):
-                        launch(kind, i)
-                    stream.synchronize()
-                    g = torch.cuda.CUDAGraph()
-                    with torch.cuda.graph(g, stream=stream):
-                        for i in range(n_launch):
-                            launch(kind, i)
-                    reps = max(5, min(args.table_reps, int(2e5 // n_launch)))
-                    for _ in range(max(2, args.table_warmup // n_launch)):
-                        g.replay()
-                    ev = [(torch.cuda.Event(enable_timing=True),
-                           torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-                    for a, b in ev:
-                        a.record(stream)
-                        g.replay()
-                        b.record(stream)
-                    stream.synchronize()
-                med = statistics.median(a.elapsed_time(b) for a, b in ev) / n_launch
-                nbytes = algo_bytes_dual(m, d) if kind == "dual" else set_bytes
-                gbs[kind] = nbytes / (med * 1e-3) / 1e9
-                del g
+            us, sets = measure_shape(args, m, d, model, synth_seed(cfg), TABLE_KERNELS, peak)
+            gbs = {k: (algo_bytes_dual(m, d) if k == "dual" else algo_bytes(m, d)) / us[k] / 1e3
+                   for k in TABLE_KERNELS}
             cells = [f"{gbs[k]:.0f} ({100 * gbs[k] / peak:.0f} %)" if k in ("umma", "dual")
                      else f"{gbs[k]:.0f}" for k in TABLE_KERNELS]
             print(f"| {cfg} | {name} | {m}x{d} | {sets} | " + " | ".join(cells) +
                   f" | {gbs['umma'] / gbs['diag']:.2f} |", flush=True)
-            del A, Q, SF, KX, AT
-            torch.cuda.empty_cache()
+    # [KQ] Table 3 on GB300: latency (us) of the bare quantizer (Q4), the
+    # diagonal scale (Scale), the dense-block tensor-core kernel (tcgen05,
+    # K1's form), the kernel built from the factors (butterfly, K2's input)
+    # and the full-row Walsh-Hadamard transform (FWHT), all with MXFP4 output
+    kinds = ("identity", "diag", "umma", "butterfly", "fwht")
+    print()
+    print("| m | d | Q4 us | Scale us | tcgen05 us | butterfly us | FWHT us | Scale/tcgen05 | "
+          "Scale/butterfly | FWHT/tcgen05 | FWHT/butterfly |")
+    print("|" + "---|" * 11)
+    for m, d in TABLE3_SHAPES:
+        us, _ = measure_shape(args, m, d, "flux", synth_seed("3"), kinds, peak)
+        print(f"| {m} | {d} | " + " | ".join(f"{us[k]:.2f}" for k in kinds) +
+              f" | {us['diag'] / us['umma']:.2f} | {us['diag'] / us['butterfly']:.2f} | "
+              f"{us['fwht'] / us['umma']:.2f} | {us['fwht'] / us['butterfly']:.2f} |", flush=True)
     # the oracle on the host cores: all of them, then one
     print()
     print("| config | layer | oracle GB/s, all cores | oracle GB/s, 1 core |")
@@ -765,9 +797,8 @@ def run_table(args):
                                    text=True, check=True)
                 out.append(r.stdout.strip())
             print(f"| {cfg} | {name} | {out[0]} | {out[1]} |", flush=True)
-    print(f"\nhost: {os.cpu_count()} cores; L2 {l2 >> 20} MiB; per shape max(4, 3 L2 / set) "
-          f"rotating sets, CUDA graphs of max(sets, 32) launches, median over up to "
-          f"{args.table_reps} replays")
+    print(f"\nhost: {os.cpu_count()} cores; per shape max(4, 3 L2 / set) rotating sets, "
+          f"CUDA graphs of max(sets, 32) launches, median over up to {args.table_reps} replays")
 
 
 def main():

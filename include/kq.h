@@ -164,6 +164,19 @@ KQ_API kq_status kq_hadamard_quantize_mxfp4(const uint16_t *A, int64_t m, int64_
                                      kq_sf_layout sf_layout, float *y_debug, cudaStream_t stream);
 
 /*
+ * kq_fwht_quantize_mxfp4 -- full-row Walsh-Hadamard baseline: every row is
+ * transformed by the normalised d-point Walsh-Hadamard matrix,
+ * y = a . H_d / sqrt(d), H_d[r][c] = (-1)^popcount(r & c) (Sylvester order),
+ * then quantized like kq_quantize_mxfp4 ([KQ] Sec. 4.4 and Table 3, "FWHT";
+ * it needs a power-of-two d).  d must be a power of two with
+ * 128 <= d <= 16384 (KQ_ERR_SHAPE otherwise); other arguments as
+ * kq_quantize_mxfp4.
+ */
+KQ_API kq_status kq_fwht_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                 uint8_t *q, int64_t ldq, uint8_t *sf,
+                                 kq_sf_layout sf_layout, float *y_debug, cudaStream_t stream);
+
+/*
  * kq_expand_blocks -- [KQ] Sec. 3.5.1 K1 ("each 32x32 block K_j is
  * materialized"): expand the raw factors into dense blocks by eq. (12),
  * computed in fp64 and then rounded to the requested format.

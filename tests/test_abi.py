@@ -160,3 +160,14 @@ def test_dual_argument_checks(L):
     assert f(A, 4, 64, 64, K, q, 32, sf, 0, vp(20488), 64, None, None) == 3   # misaligned
     assert f(A, 4, 64, 64, K, q, 32, sf, 0, at, 68, None, None) == 3          # ldat % 8
     assert f(A, 0, 64, 64, None, None, 32, None, 0, None, 64, None, None) == 0  # m = 0
+
+
+def test_fwht_argument_checks(L):
+    """The full-row transform needs a power-of-two d in [128, 16384]; nothing
+    is launched when a check fails."""
+    vp = ctypes.c_void_p
+    A, q, sf = vp(4096), vp(8192), vp(12288)
+    f = L.kq_fwht_quantize_mxfp4
+    for d in (96, 64, 3072, 32768):
+        assert f(A, 4, d, d, q, d // 2, sf, 0, None, None) == 2, d
+    assert f(A, 0, 1024, 1024, None, 512, None, 0, None, None) == 0

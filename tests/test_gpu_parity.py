@@ -517,3 +517,41 @@ def test_dual_side_output_flux_ffn_down():
     side = parity.check_side_output(A_bits, d, "kron", po, np_(at.view(torch.int16)).view(np.uint16),
                                     np_(y), rows)
     print(side)
+
+
+# ------------------------------------------- full-row Walsh-Hadamard baseline --
+
+FWHT_SHAPES = [(3, 128), (130, 256), (64, 1024), (129, 2048), (17, 4096), (5, 8192), (9, 16384)]
+
+
+@pytest.mark.parametrize("m,d", FWHT_SHAPES, ids=[f"{m}x{d}" for m, d in FWHT_SHAPES])
+def test_fwht_parity(m, d):
+    """kq_fwht_quantize_mxfp4 against the oracle's fast transform: rules
+    (i)-(iii), both scale layouts, ragged m, lda > d, guard bytes around q."""
+    lda, ldq = d + 64, d // 2 + 32
+    A_bits = synth.activations(m, d, 300 + m, "flux", lda=lda)
+    for layout in (0, 1):
+        sfb = kq.kq_sf_bytes(m, d, layout)
+        q_store = torch.full((m + 2, ldq), 0xA5, dtype=torch.uint8, device="cuda")
+        q = q_store[1:m + 1]
+        sf = torch.full((max(sfb, 16),), 0xA5, dtype=torch.uint8, device="cuda")
+        _, _, y = kq.kq_fwht_quantize_mxfp4(to_bf16(A_bits), d, layout=layout, q=q, sf=sf,
+                                            y_debug=True)
+        qs = np_(q_store)
+        assert (qs[0] == 0xA5).all() and (qs[m + 1] == 0xA5).all()
+        assert (qs[1:m + 1, d // 2:] == 0xA5).all()
+        res = parity.check(np.ascontiguousarray(A_bits[:, :d]), d, "fwht", None, layout,
+                           np_(q)[:, :d // 2], np_(sf)[:sfb], np_(y))
+        q2, sf2, _ = kq.kq_fwht_quantize_mxfp4(to_bf16(A_bits), d, layout=layout)
+        assert torch.equal(q[:, :d // 2], q2) and torch.equal(sf[:sfb], sf2[:sfb])
+        print(m, d, layout, res)
+
+
+def test_fwht_table3_shape_sampled():
+    """The pages' Table 3 shape m = 4096, d = 16384 at full size (sampled rows)."""
+    m, d = 4096, 16384
+    A_bits = synth.activations(m, d, 333, "flux")
+    q, sf, y = kq.kq_fwht_quantize_mxfp4(to_bf16(A_bits), d, layout=1, y_debug=True)
+    rows = np.unique(np.concatenate([np.arange(4), np.arange(m - 4, m),
+                                     np.random.default_rng(5).choice(m, 200, replace=False)]))
+    parity.check(A_bits, d, "fwht", None, 1, np_(q), np_(sf), np_(y), rows)

@@ -287,6 +287,19 @@ kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d, int64_
     return launch_quant_umma(A, lda, K_expanded, p, at, ldat, stream);
 }
 
+kq_status kq_fwht_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                 uint8_t *q, int64_t ldq, uint8_t *sf, kq_sf_layout sf_layout,
+                                 float *y_debug, cudaStream_t stream)
+{
+    kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
+    if (st != KQ_OK) return st;
+    if (d < 128 || d > 16384 || (d & (d - 1)) != 0) return KQ_ERR_SHAPE;
+    if (m == 0) return KQ_OK;
+    QuantParams p;
+    fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
+    return launch_quant_fwht(A, lda, p, stream);
+}
+
 kq_status kq_smooth_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
                                    const float *s, uint8_t *q, int64_t ldq, uint8_t *sf,
                                    kq_sf_layout sf_layout, float *y_debug, cudaStream_t stream)

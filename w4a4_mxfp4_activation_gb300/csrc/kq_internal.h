@@ -84,6 +84,9 @@ kq_status launch_quant_tma(Transform t, const uint16_t *A, int64_t lda, const Qu
 kq_status launch_quant_mma(const uint16_t *A, int64_t lda, const void *K_expanded,
                            const QuantParams &p, cudaStream_t stream);
 kq_status launch_mma_records(const float *factors, int64_t nb, void *out, cudaStream_t stream);
+// Full-row Walsh-Hadamard + MXFP4 (d a power of two, 128 <= d <= 16384).
+kq_status launch_quant_fwht(const uint16_t *A, int64_t lda, const QuantParams &p,
+                            cudaStream_t stream);
 // at != nullptr: also write the bf16 side output A T ([m][ldat], the DUAL kernel)
 kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expanded,
                             const QuantParams &p, uint16_t *at, int64_t ldat, cudaStream_t stream);

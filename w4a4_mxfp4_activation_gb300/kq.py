@@ -34,6 +34,7 @@ EXPORTS = (
     "kq_expand_blocks", "kq_expanded_bytes", "kq_dequantize", "kq_sf_bytes",
     "kq_status_string", "kq_lu_to_factors", "kq_invert_transpose_factors",
     "kq_quantize_mxfp4_variant", "kq_test_encode_e2m1", "kq_quantize_mxfp4_dual",
+    "kq_fwht_quantize_mxfp4",
 )
 
 
@@ -70,6 +71,8 @@ def lib() -> ctypes.CDLL:
             L.kq_smooth_quantize_mxfp4.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, st, vp, vp]
             L.kq_smooth_quantize_mxfp4.restype = st
             L.kq_hadamard_quantize_mxfp4.argtypes = [vp, i64, i64, i64, vp, i64, vp, st, vp, vp]
+            L.kq_fwht_quantize_mxfp4.argtypes = [vp, i64, i64, i64, vp, i64, vp, st, vp, vp]
+            L.kq_fwht_quantize_mxfp4.restype = st
             L.kq_hadamard_quantize_mxfp4.restype = st
             L.kq_expand_blocks.argtypes = [vp, i64, st, vp, vp]
             L.kq_expand_blocks.restype = st
@@ -229,6 +232,20 @@ def kq_hadamard_quantize_mxfp4(A, d: int | None = None, layout: int = KQ_SF_ROWM
     _check(lib().kq_hadamard_quantize_mxfp4(_ptr(A), m, d, A.stride(0), _ptr(q), ldq, _ptr(sf),
                                             layout, _ptr(y_debug), _stream(stream)),
            "kq_hadamard_quantize_mxfp4")
+    return q, sf, y_debug
+
+
+def kq_fwht_quantize_mxfp4(A, d: int | None = None, layout: int = KQ_SF_ROWMAJOR, q=None,
+                           sf=None, y_debug=None, stream=None):
+    """Full-row Walsh-Hadamard baseline (d a power of two, 128..16384)."""
+    A = _bf16_bits(A)
+    m, lda = A.shape
+    d = lda if d is None else d
+    q, sf, y_debug = _outputs(A, m, d, layout, q, sf, y_debug)
+    ldq = q.shape[1] if q.dim() == 2 else d // 2
+    _check(lib().kq_fwht_quantize_mxfp4(_ptr(A), m, d, A.stride(0), _ptr(q), ldq, _ptr(sf),
+                                        layout, _ptr(y_debug), _stream(stream)),
+           "kq_fwht_quantize_mxfp4")
     return q, sf, y_debug
 
 
