@@ -208,6 +208,28 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     const uint32_t tmem_slot = bar_acc_empty + 16;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // The producer (thread 0) walks the CTA's tiles in order; it loads the
+    // activation box and the operand records of tile `it` into ring stage
+    // it % STAGES.
+    TileWalk pw(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                static_cast<int>(p.ncol_tiles));
+    int64_t pit = 0;
+    uint64_t pol = 0;
+    auto issue_tile = [&]() {
+        const int s = static_cast<int>(pit % STAGES);
+        const uint32_t dst = base + s * Cfg::kStageBytes;
+        const int64_t left = p.nb - pw.ct * 2;          // < 1 on padding tiles
+        const uint32_t rbytes =
+            static_cast<uint32_t>((left < 0 ? 0 : (left < 2 ? left : 2)) * Cfg::kRecBytes);
+        mbar_arrive_expect_tx(bar_full + 8 * s, Cfg::kABytes + rbytes);
+        tma_load_2d(dst, &tmA, pw.ct * 64, pw.rt * kBR, bar_full + 8 * s, pol);
+        if (rbytes)
+            bulk_load(dst + Cfg::kBOff, records + static_cast<int64_t>(pw.ct) * 2 * Cfg::kRecBytes,
+                      rbytes, bar_full + 8 * s);
+        pw.next();
+        ++pit;
+    };
+
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);              // kernel parameters: no dependency on
         tma_prefetch_desc(&tmQ);              // earlier grids
@@ -221,6 +243,14 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             mbar_init(bar_acc_empty + 8 * a, kEpiThreads / 2);
         }
         mbar_fence_init();
+        // The first tile's loads go out before the CTA-wide setup barrier
+        // (TMEM allocation), so its DRAM round trip overlaps it; every other
+        // thread touches the ring only after that barrier.  (Measured on
+        // GB300: sending the whole first ring this early made small launches
+        // slower; one tile is faster on every shape tried.)
+        grid_dependency_wait();
+        pol = l2_policy_evict_first();
+        if (pw.rt < p.nrow_tiles) issue_tile();
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
@@ -233,27 +263,13 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            int64_t it = 0;
-            for (TileWalk tw(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
-                             static_cast<int>(p.ncol_tiles));
-                 tw.rt < p.nrow_tiles;
-                 tw.next(), ++it) {
-                const int s = static_cast<int>(it % STAGES);
-                const uint32_t ph = static_cast<uint32_t>((it / STAGES) & 1);
-                if (it >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1u)) break;
-                const int64_t rt = tw.rt, ct = tw.ct;
-                const uint32_t dst = base + s * Cfg::kStageBytes;
-                const int64_t left = p.nb - ct * 2;     // < 1 on padding tiles
-                const uint32_t rbytes = static_cast<uint32_t>(
-                    (left < 0 ? 0 : (left < 2 ? left : 2)) * Cfg::kRecBytes);
-                mbar_arrive_expect_tx(bar_full + 8 * s, Cfg::kABytes + rbytes);
-                tma_load_2d(dst, &tmA, static_cast<int32_t>(ct * 64),
-                            static_cast<int32_t>(rt * kBR), bar_full + 8 * s, pol);
-                if (rbytes)
-                    bulk_load(dst + Cfg::kBOff, records + ct * 2 * Cfg::kRecBytes, rbytes,
-                              bar_full + 8 * s);
+            while (pw.rt < p.nrow_tiles) {
+                const int s = static_cast<int>(pit % STAGES);
+                const uint32_t ph = static_cast<uint32_t>((pit / STAGES) & 1);
+                if (pit >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1u)) break;
+                issue_tile();
             }
+            const int64_t it = pit;
             for (int64_t k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
                 (void)mbar_wait(bar_full + 8 * static_cast<int>(k % STAGES),
                                 static_cast<uint32_t>((k / STAGES) & 1));
