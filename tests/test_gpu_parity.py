@@ -555,3 +555,20 @@ def test_fwht_table3_shape_sampled():
     rows = np.unique(np.concatenate([np.arange(4), np.arange(m - 4, m),
                                      np.random.default_rng(5).choice(m, 200, replace=False)]))
     parity.check(A_bits, d, "fwht", None, 1, np_(q), np_(sf), np_(y), rows)
+
+
+def test_identity_factors_reduce_to_bare_quantizer():
+    """Degenerate case of the method: with every factor the 2x2 identity,
+    K_j = I and y = a exactly (the three-term bf16 split of 0 and 1 is exact,
+    and so are the butterfly's products), so both KroQuant paths must write
+    the bare quantizer's bytes, bit for bit, in both scale layouts."""
+    m, d = 300, 2240
+    A_bits = synth.activations(m, d, 404, "sana")
+    eye = np.tile(np.eye(2, dtype=np.float32), (d // 32, 5, 1, 1))
+    for layout in (0, 1):
+        nsf = kq.kq_sf_bytes(m, d, layout)
+        q0, sf0, _ = run_kind("identity", A_bits, d, layout, y_debug=False)
+        for kind in ("kron", "kron_umma", "kron_mma"):
+            q, sf, y = run_kind(kind, A_bits, d, layout, eye)
+            assert torch.equal(q, q0) and torch.equal(sf[:nsf], sf0[:nsf]), kind
+            assert np.array_equal(np_(y), synth.bf16_bits_to_f32(A_bits)), kind
