@@ -177,6 +177,60 @@ KQ_API kq_status kq_fwht_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d,
                                  kq_sf_layout sf_layout, float *y_debug, cudaStream_t stream);
 
 /*
+ * kq_w4a4_gemm -- the W4A4 product that consumes the quantizer's output,
+ * [KQ] eq. (11) (Q(A T) x Q(W~)) and eq. (2):
+ *     c[i][j] = sum_k deq(qa)[i][k] * deq(qw)[j][k]      (C = A_q W_q^T)
+ * with deq = e2m1(code) * 2^(sf - 127) as in kq_dequantize.  Runs on the
+ * tensor cores (tcgen05.mma, fp32 accumulation in TMEM): every MXFP4 element
+ * times its scale is exact in bf16, so the products are exact and only the
+ * fp32 accumulation rounds.
+ *   qa, ldqa   device, packed codes of the m x k left operand [m][ldqa]
+ *              (as kq_quantize_mxfp4 writes them; ldqa >= k/2, ldqa % 16 == 0)
+ *   sfa        device, its scales in KQ_SF_BLOCKED_128x4 (kq_sf_bytes(m, k))
+ *   qw, ldqw   device, packed codes of the n x k right operand (weights,
+ *              output channel j in row j)
+ *   sfw        device, its scales in KQ_SF_BLOCKED_128x4 (kq_sf_bytes(n, k))
+ *   m, n, k    k % 32 == 0, k > 0; m, n >= 0 (m or n = 0: no-op)
+ *   c, ldc     device fp32 [m][ldc] (written, columns < n), ldc >= n,
+ *              ldc % 4 == 0, 16-byte aligned
+ * Scale bytes of padding blocks (columns past k) are not used; 0xFF (the
+ * E8M0 NaN) in a used block yields NaN.  A kernel that finds its pipeline
+ * stalled for about one second stops; the output tiles it had not written
+ * are then left as they were.
+ */
+KQ_API kq_status kq_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa,
+                              const uint8_t *qw, int64_t ldqw, const uint8_t *sfw,
+                              int64_t m, int64_t n, int64_t k, float *c, int64_t ldc,
+                              cudaStream_t stream);
+
+/*
+ * kq_bf16_gemm -- the unquantized reference product of [KQ] eq. (2),
+ * c = A W^T, on the same tensor-core kernel: bf16 operands, fp32
+ * accumulation.
+ *   a, lda     device, bf16 [m][lda] (lda >= k, lda % 8 == 0)
+ *   w, ldw     device, bf16 [n][ldw] (ldw >= k, ldw % 8 == 0)
+ *   m, n, k    k > 0; m, n >= 0 (m or n = 0: no-op)
+ *   c, ldc     as kq_w4a4_gemm
+ */
+KQ_API kq_status kq_bf16_gemm(const uint16_t *a, int64_t lda, const uint16_t *w, int64_t ldw,
+                              int64_t m, int64_t n, int64_t k, float *c, int64_t ldc,
+                              cudaStream_t stream);
+
+/*
+ * kq_layer_error -- the squared Frobenius norms behind [KQ] eq. (2):
+ *     out[0] = sum_ij (c[i][j] - c_ref[i][j])^2   (||E(T)||_F^2 when c is
+ *              the W4A4 product and c_ref = A W^T)
+ *     out[1] = sum_ij c_ref[i][j]^2
+ * accumulated in fp64 (squares of fp32 differences are exact in fp64; the
+ * order of the additions is not fixed).
+ *   c, ldc, c_ref, ldr  device fp32 [m][ldc], [m][ldr] (ld >= n, % 4 == 0,
+ *                       16-byte aligned)
+ *   out                 device double[2] (overwritten; 8-byte aligned)
+ */
+KQ_API kq_status kq_layer_error(const float *c, int64_t ldc, const float *c_ref, int64_t ldr,
+                                int64_t m, int64_t n, double *out, cudaStream_t stream);
+
+/*
  * kq_expand_blocks -- [KQ] Sec. 3.5.1 K1 ("each 32x32 block K_j is
  * materialized"): expand the raw factors into dense blocks by eq. (12),
  * computed in fp64 and then rounded to the requested format.

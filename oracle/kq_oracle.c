@@ -289,6 +289,17 @@ KQO_EXPORT int64_t kqo_sf_bytes(int64_t m, int64_t nb, int layout)
     return ((m + 127) / 128) * ((nb + 3) / 4) * 512;
 }
 
+/* Scatter row-major scale bytes rm [m][nb] into `out` (kqo_sf_bytes(m, nb,
+ * layout) bytes) at the positions of the given layout; positions that hold
+ * no scale (the padding of the tiled layout) get `fill`. */
+KQO_EXPORT void kqo_sf_place(const uint8_t *rm, int64_t m, int64_t nb, int layout, uint8_t fill,
+                             uint8_t *out)
+{
+    memset(out, fill, (size_t)kqo_sf_bytes(m, nb, layout));
+    for (int64_t i = 0; i < m; ++i)
+        for (int64_t j = 0; j < nb; ++j) out[kqo_sf_offset(i, j, nb, layout)] = rm[i * nb + j];
+}
+
 /* Flags for the comparison rules (bit mask per element):
  *   1: |v| within 1e-3 relative of a rounding midpoint
  *   2: the block's amax within 1e-3 relative of a power of two

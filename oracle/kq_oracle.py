@@ -80,6 +80,7 @@ def _bind(path: str) -> ctypes.CDLL:
     L.kqo_sf_offset.restype = i64
     L.kqo_sf_bytes.argtypes = [i64, i64, ctypes.c_int]
     L.kqo_sf_bytes.restype = i64
+    L.kqo_sf_place.argtypes = [u8p, i64, i64, ctypes.c_int, ctypes.c_uint8, u8p]
     L.kqo_quantize.argtypes = [dp, dp, i64, i64, u8p, i64, u8p, ctypes.c_int, u8p]
     L.kqo_dequantize.argtypes = [u8p, i64, u8p, ctypes.c_int, i64, i64, dp]
     L.kqo_encode_f32_range.argtypes = [ctypes.c_uint32, i64, u8p]
@@ -271,6 +272,16 @@ def sf_offset(i: int, kb: int, nb: int, layout: int) -> int:
 
 def sf_bytes(m: int, nb: int, layout: int) -> int:
     return int(lib().kqo_sf_bytes(m, nb, layout))
+
+
+def sf_place(sf_rowmajor: np.ndarray, layout: int, fill: int = 0) -> np.ndarray:
+    """Scale bytes [m, nb] placed into the given layout; padding positions
+    of the tiled layout get ``fill``."""
+    rm = np.ascontiguousarray(sf_rowmajor, dtype=np.uint8)
+    m, nb = rm.shape
+    out = np.empty(sf_bytes(m, nb, layout), np.uint8)
+    lib().kqo_sf_place(_p(rm, ctypes.c_uint8), m, nb, layout, fill, _p(out, ctypes.c_uint8))
+    return out
 
 
 def quantize(y: np.ndarray, bound: np.ndarray | None, layout: int = SF_ROWMAJOR,

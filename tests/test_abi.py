@@ -171,3 +171,36 @@ def test_fwht_argument_checks(L):
     for d in (96, 64, 3072, 32768):
         assert f(A, 4, d, d, q, d // 2, sf, 0, None, None) == 2, d
     assert f(A, 0, 1024, 1024, None, 512, None, 0, None, None) == 0
+
+
+def test_gemm_argument_checks(L):
+    """The W4A4 / bf16 products and the error sums validate before launching;
+    every call here fails a check (or is empty), so nothing is launched."""
+    vp = ctypes.c_void_p
+    qa, sa, qw, sw, c = vp(4096), vp(8192), vp(12288), vp(16384), vp(20480)
+    g = L.kq_w4a4_gemm
+    assert g(qa, 32, sa, qw, 32, sw, 4, 8, 48, c, 8, None) == 2          # k % 32
+    assert g(qa, 32, sa, qw, 32, sw, 4, 8, 0, c, 8, None) == 2           # k = 0
+    assert g(qa, 16, sa, qw, 32, sw, 4, 8, 64, c, 8, None) == 2          # ldqa < k/2
+    assert g(qa, 32, sa, qw, 32, sw, 4, 8, 64, c, 4, None) == 2          # ldc < n
+    assert g(qa, 32, sa, qw, 32, sw, -1, 8, 64, c, 8, None) == 2
+    assert g(None, 32, sa, qw, 32, sw, 4, 8, 64, c, 8, None) == 1
+    assert g(qa, 32, None, qw, 32, sw, 4, 8, 64, c, 8, None) == 1
+    assert g(qa, 32, sa, qw, 32, sw, 4, 8, 64, None, 8, None) == 1
+    assert g(vp(4104), 32, sa, qw, 32, sw, 4, 8, 64, c, 8, None) == 3    # misaligned
+    assert g(qa, 40, sa, qw, 32, sw, 4, 8, 64, c, 8, None) == 3          # ldqa % 16
+    assert g(qa, 32, sa, qw, 32, sw, 4, 8, 64, c, 10, None) == 3         # ldc % 4
+    assert g(None, 32, None, None, 32, None, 0, 8, 64, None, 8, None) == 0   # m = 0
+    assert g(None, 32, None, None, 32, None, 4, 0, 64, None, 0, None) == 0   # n = 0
+    b = L.kq_bf16_gemm
+    assert b(qa, 64, qw, 64, 4, 8, 0, c, 8, None) == 2
+    assert b(qa, 32, qw, 64, 4, 8, 64, c, 8, None) == 2                  # lda < k
+    assert b(qa, 68, qw, 64, 4, 8, 64, c, 8, None) == 3                  # lda % 8
+    assert b(qa, 64, None, 64, 4, 8, 64, c, 8, None) == 1
+    assert b(None, 64, None, 64, 0, 8, 64, None, 8, None) == 0
+    e = L.kq_layer_error
+    assert e(c, 8, c, 8, 4, 8, None, None) == 1                          # no out
+    assert e(c, 8, c, 8, 4, 8, vp(4100), None) == 3                      # out misaligned
+    assert e(c, 4, c, 8, 4, 8, vp(4096), None) == 2                      # ldc < n
+    assert e(None, 8, c, 8, 4, 8, vp(4096), None) == 1
+    assert e(c, 8, vp(20484), 8, 4, 8, vp(4096), None) == 3

@@ -572,3 +572,165 @@ def test_identity_factors_reduce_to_bare_quantizer():
             q, sf, y = run_kind(kind, A_bits, d, layout, eye)
             assert torch.equal(q, q0) and torch.equal(sf[:nsf], sf0[:nsf]), kind
             assert np.array_equal(np_(y), synth.bf16_bits_to_f32(A_bits)), kind
+
+
+# ------------------------------------------- consumer W4A4 product (eq. 11) --
+
+def mx_operand(rows, k, seed, lo=112, hi=140):
+    """Random packed codes and scales; the scales placed in the 128x4 tiled
+    layout by the oracle, padding bytes 0xFF (E8M0 NaN: a kernel that used
+    one would put NaN into the product).  Returns (q, sf_rowmajor, sf_tiled)."""
+    q = synth.packed_codes(rows, k, seed)
+    sf = synth.scale_bytes(rows, k // 32, seed + 1, lo, hi)
+    return q, sf, O.sf_place(sf, 1, fill=255)
+
+
+def gemm_tolerance(Aq, Wq, k):
+    """fp32 accumulation: every product is exact; each 16-deep tensor-core
+    step and each addition into the accumulator rounds once, relative to
+    at most sum |a_k w_k|."""
+    return (k / 16 + 16) * 2.0 ** -23 * (np.abs(Aq) @ np.abs(Wq).T)
+
+
+def check_product(got, Aq, Wq, k):
+    ref = Aq @ Wq.T
+    tol = gemm_tolerance(Aq, Wq, k)
+    err = np.abs(got.astype(np.float64) - ref)
+    assert np.all(np.isfinite(got))
+    assert np.all(err <= tol), float((err / (tol + 1e-300)).max())
+    return float((err / (tol + 1e-300)).max())
+
+
+GEMM_SHAPES = [(256, 256, 1152), (300, 200, 96), (129, 384, 160), (1, 1, 32), (131, 130, 3072),
+               (128, 128, 64), (5, 700, 2240)]
+
+
+@pytest.mark.parametrize("m,n,k", GEMM_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in GEMM_SHAPES])
+def test_w4a4_gemm_random_codes(m, n, k):
+    """C = deq(qa) deq(qw)^T on random codes and scales against the fp64
+    product of the oracle's dequantization; ragged m, n and k (k = 32 mod 64
+    leaves half of the last K step as padding), C pitch wider than n with
+    canaries in the gap."""
+    qa, _, sfa = mx_operand(m, k, 7 * m + k)
+    qw, _, sfw = mx_operand(n, k, 11 * n + k + 1)
+    ldc = n + 4 + (-(n + 4)) % 4
+    c = torch.full((m, ldc), 12345.0, dtype=torch.float32, device="cuda")
+    kq.kq_w4a4_gemm(dev(qa), dev(sfa), dev(qw), dev(sfw), m, n, k, c=c)
+    got = np_(c)
+    assert np.all(got[:, n:] == 12345.0)
+    Aq = O.dequantize(qa, sfa, 1, m, k)
+    Wq = O.dequantize(qw, sfw, 1, n, k)
+    print("max error / bound:", check_product(got[:, :n], Aq, Wq, k))
+
+
+def test_w4a4_gemm_scale_extremes():
+    """Left scales 2^-127 .. 2^-125 (the dequantized left operand is partly
+    subnormal) against right scales 2^123 .. 2^125: products of order one
+    that only come out right if no operand is flushed to zero."""
+    m, n, k = 130, 140, 256
+    qa, _, sfa = mx_operand(m, k, 91, lo=0, hi=2)
+    qw, _, sfw = mx_operand(n, k, 92, lo=250, hi=252)
+    got = np_(kq.kq_w4a4_gemm(dev(qa), dev(sfa), dev(qw), dev(sfw), m, n, k))
+    Aq = O.dequantize(qa, sfa, 1, m, k)
+    Wq = O.dequantize(qw, sfw, 1, n, k)
+    print("max error / bound:", check_product(got, Aq, Wq, k))
+
+
+def test_w4a4_gemm_flux_ffn_down_sampled():
+    """The FLUX.1 FFN down projection at full size (m = 4608 tokens, k = 12288,
+    n = 3072 output channels); all columns of 192 sampled rows (first, last,
+    random) against the oracle."""
+    m, n, k = 4608, 3072, 12288
+    qa, sfa_rm, sfa = mx_operand(m, k, 501)
+    qw, _, sfw = mx_operand(n, k, 502)
+    got = np_(kq.kq_w4a4_gemm(dev(qa), dev(sfa), dev(qw), dev(sfw), m, n, k))
+    rows = np.unique(np.concatenate([np.arange(64), np.arange(m - 64, m),
+                                     np.random.default_rng(503).choice(m, 64, replace=False)]))
+    Aq = O.dequantize(qa[rows], O.sf_place(sfa_rm[rows], 1), 1, len(rows), k)
+    Wq = O.dequantize(qw, sfw, 1, n, k)
+    print("max error / bound:", check_product(got[rows], Aq, Wq, k))
+
+
+BF16_GEMM_SHAPES = [(256, 384, 1152), (300, 129, 100), (1, 1, 8), (129, 257, 3072)]
+
+
+@pytest.mark.parametrize("m,n,k", BF16_GEMM_SHAPES,
+                         ids=[f"{m}x{n}x{k}" for m, n, k in BF16_GEMM_SHAPES])
+def test_bf16_gemm(m, n, k):
+    """C = A W^T for bf16 operands (row pitch wider than k, zero-padded by the
+    caller's layout only up to the pitch) against the fp64 product."""
+    lda = k + (-k) % 8 + 8
+    A_bits = synth.activations(m, k, 600 + m, "pixart", lda=lda)
+    W_bits = synth.activations(n, k, 700 + n, "gauss_outlier8", lda=lda)
+    A_bits[:, k:] = 0x7FC0                     # NaN beyond k: must not be read
+    W_bits[:, k:] = 0x7FC0
+    got = np_(kq.kq_bf16_gemm(to_bf16(A_bits), to_bf16(W_bits), k=k))
+    a = synth.bf16_bits_to_f32(A_bits[:, :k]).astype(np.float64)
+    w = synth.bf16_bits_to_f32(W_bits[:, :k]).astype(np.float64)
+    print("max error / bound:", check_product(got, a, w, k))
+
+
+def test_gemm_empty_is_noop():
+    c = torch.full((4, 8), 7.0, device="cuda")
+    z = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    kq.kq_w4a4_gemm(z, z, z, z, 0, 8, 64, c=c)
+    kq.kq_w4a4_gemm(z, z, z, z, 4, 0, 64, c=c)
+    assert torch.all(c == 7.0)
+    out = kq.kq_layer_error(c[:0], c[:0])
+    assert np.array_equal(np_(out), [0.0, 0.0])
+
+
+def device_layer_error(A_bits, W_bits, d, Fg, layout_a_kind="kron_umma"):
+    """eq. (2) entirely on the device: quantize A T (tensor-core path) and
+    W T^{-T} (butterfly on the inverse-transposed factors), the W4A4 product,
+    the bf16 reference product, the fp64 error sums."""
+    m, o = A_bits.shape[0], W_bits.shape[0]
+    qa, sfa, _ = run_kind(layout_a_kind, A_bits, d, 1, Fg, y_debug=False)
+    qw, sfw, _ = run_kind("kron", W_bits, d, 1, kq.kq_invert_transpose_factors(Fg),
+                          y_debug=False)
+    cq = kq.kq_w4a4_gemm(qa, sfa, qw, sfw, m, o, d)
+    cr = kq.kq_bf16_gemm(to_bf16(A_bits), to_bf16(W_bits))
+    s = np_(kq.kq_layer_error(cq, cr))
+    return math.sqrt(s[0]), math.sqrt(s[1])
+
+
+def reference_norm_tolerance(A_bits, W_bits, d):
+    """| ||C|| - ||A W^T|| | <= ||C - A W^T||_F, bounded element by element
+    by the fp32 accumulation bound of the product."""
+    a = synth.bf16_bits_to_f32(A_bits).astype(np.float64)
+    w = synth.bf16_bits_to_f32(W_bits).astype(np.float64)
+    return float(np.linalg.norm(gemm_tolerance(a, w, d)))
+
+
+@pytest.mark.parametrize("factor_kind", ["random", "hadamard"])
+def test_layer_error_on_device_config0(factor_kind):
+    """Acceptance (iii) with every step on the GPU: ||E(T)||_F within 1e-3
+    relative of the oracle's; ||A W^T||_F within the fp32 accumulation bound."""
+    m, d, o = 256, 1152, 1152
+    nb = d // 32
+    A_bits = synth.activations(m, d, synth.SEED_A, "gauss_outlier8")
+    W_bits = synth.weights(o, d)
+    if factor_kind == "random":
+        Fg, Fo = lib_factors(nb, synth.SEED_FACTORS)
+    else:
+        Fg = synth.hadamard_factors(nb)
+        Fo = Fg.astype(np.float64)
+    e_gpu, r_gpu = device_layer_error(A_bits, W_bits, d, Fg)
+    e_ref, ref = O.layer_error(A_bits, W_bits, d, Fo, layout=1)
+    assert abs(e_gpu - e_ref) <= 1e-3 * e_ref, (e_gpu, e_ref)
+    assert abs(r_gpu - ref) <= reference_norm_tolerance(A_bits, W_bits, d), (r_gpu, ref)
+
+
+@pytest.mark.parametrize("name,m,d,model,cfg", synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3,
+                         ids=[c[0] for c in synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3])
+def test_layer_error_on_device_configs(name, m, d, model, cfg):
+    """The same on configs 1-3: the first 512 rows of A, a weight of
+    o = min(d, 3072) output channels."""
+    m, o = 512, min(d, 3072)
+    A_bits = synth.activations(m, d, synth.SEED_A + cfg, model)
+    W_bits = synth.weights(o, d, seed=synth.SEED_W + cfg)
+    Fg, Fo = lib_factors(d // 32, synth.SEED_FACTORS + cfg)
+    e_gpu, r_gpu = device_layer_error(A_bits, W_bits, d, Fg)
+    e_ref, ref = O.layer_error(A_bits, W_bits, d, Fo, layout=1)
+    assert abs(e_gpu - e_ref) <= 1e-3 * e_ref, (e_gpu, e_ref)
+    assert abs(r_gpu - ref) <= reference_norm_tolerance(A_bits, W_bits, d), (r_gpu, ref)

@@ -223,6 +223,20 @@ def test_sf_blocked_bijection(oracle_lib, m, nb):
     assert np.array_equal(full[:m, :nb], pos)
 
 
+@pytest.mark.parametrize("m,nb", [(1, 1), (200, 70), (300, 175)])
+def test_sf_place_matches_permutation(oracle_lib, m, nb):
+    """sf_place scatters row-major scales to the positions of the
+    reshape/permute construction and fills every other byte."""
+    rm = np.random.default_rng(m + nb).integers(0, 255, size=(m, nb), dtype=np.uint8)
+    out = oracle_lib.sf_place(rm, 1, fill=255)
+    pos = blocked_sf_positions(m, nb)
+    assert np.array_equal(out[pos], rm)
+    rest = np.ones(out.size, bool)
+    rest[pos.ravel()] = False
+    assert np.all(out[rest] == 255)
+    assert np.array_equal(oracle_lib.sf_place(rm, 0), rm.ravel())
+
+
 # ------------------------------------------------- brute force (P5) --
 
 @pytest.mark.parametrize("m,d", [(1, 32), (2, 64), (3, 128), (4, 1152)])

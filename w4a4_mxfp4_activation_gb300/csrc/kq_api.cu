@@ -300,6 +300,54 @@ kq_status kq_fwht_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_
     return launch_quant_fwht(A, lda, p, stream);
 }
 
+kq_status kq_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, const uint8_t *qw,
+                       int64_t ldqw, const uint8_t *sfw, int64_t m, int64_t n, int64_t k,
+                       float *c, int64_t ldc, cudaStream_t stream)
+{
+    if (m < 0 || n < 0 || k <= 0 || k % 32 != 0 || ldqa < k / 2 || ldqw < k / 2 || ldc < n)
+        return KQ_ERR_SHAPE;
+    // int32 TMA coordinates; row pitches below 2^40 bytes
+    if (m > 0x7fffffffLL || n > 0x7fffffffLL || k > 0x7fffffffLL || ldqa > (1LL << 38) ||
+        ldqw > (1LL << 38) || ldc > (1LL << 38))
+        return KQ_ERR_SHAPE;
+    if (m == 0 || n == 0) return KQ_OK;
+    if (qa == nullptr || sfa == nullptr || qw == nullptr || sfw == nullptr || c == nullptr)
+        return KQ_ERR_NULL;
+    if (!aligned16(qa) || !aligned16(qw) || !aligned16(sfa) || !aligned16(sfw) || !aligned16(c) ||
+        ldqa % 16 != 0 || ldqw % 16 != 0 || ldc % 4 != 0)
+        return KQ_ERR_ALIGN;
+    return launch_w4a4_gemm(qa, ldqa, sfa, qw, ldqw, sfw, m, n, k, c, ldc, stream);
+}
+
+kq_status kq_bf16_gemm(const uint16_t *a, int64_t lda, const uint16_t *w, int64_t ldw, int64_t m,
+                       int64_t n, int64_t k, float *c, int64_t ldc, cudaStream_t stream)
+{
+    if (m < 0 || n < 0 || k <= 0 || lda < k || ldw < k || ldc < n) return KQ_ERR_SHAPE;
+    if (m > 0x7fffffffLL || n > 0x7fffffffLL || k > 0x7fffffffLL || lda > (1LL << 38) ||
+        ldw > (1LL << 38) || ldc > (1LL << 38))
+        return KQ_ERR_SHAPE;
+    if (m == 0 || n == 0) return KQ_OK;
+    if (a == nullptr || w == nullptr || c == nullptr) return KQ_ERR_NULL;
+    if (!aligned16(a) || !aligned16(w) || !aligned16(c) || lda % 8 != 0 || ldw % 8 != 0 ||
+        ldc % 4 != 0)
+        return KQ_ERR_ALIGN;
+    return launch_bf16_gemm(a, lda, w, ldw, m, n, k, c, ldc, stream);
+}
+
+kq_status kq_layer_error(const float *c, int64_t ldc, const float *c_ref, int64_t ldr, int64_t m,
+                         int64_t n, double *out, cudaStream_t stream)
+{
+    if (m < 0 || n < 0 || ldc < n || ldr < n) return KQ_ERR_SHAPE;
+    if (out == nullptr) return KQ_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return KQ_ERR_ALIGN;
+    if (m > 0 && n > 0) {
+        if (c == nullptr || c_ref == nullptr) return KQ_ERR_NULL;
+        if (!aligned16(c) || !aligned16(c_ref) || ldc % 4 != 0 || ldr % 4 != 0)
+            return KQ_ERR_ALIGN;
+    }
+    return launch_layer_error(c, ldc, c_ref, ldr, m, n, out, stream);
+}
+
 kq_status kq_smooth_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
                                    const float *s, uint8_t *q, int64_t ldq, uint8_t *sf,
                                    kq_sf_layout sf_layout, float *y_debug, cudaStream_t stream)

@@ -1,0 +1,518 @@
+// Consumer of the quantizer's output: the W4A4 product of eq. (11) on the
+// 5th-generation tensor cores, sm_103a.
+//
+// "KroQuant: Kronecker-Structured Block Transforms for Efficient Post-
+// Training Quantization of Diffusion Transformers", eq. (11) multiplies the
+// MXFP4-quantized transformed activations by the MXFP4-quantized transformed
+// weights, and eq. (2) measures the layer's error through that product.  This
+// kernel computes
+//     C[i][n] = sum_k deq(A)[i][k] * deq(W)[n][k]
+// from packed E2M1 codes ([rows][d/2] bytes, code 2k in the low nibble) and
+// E8M0 scales in the 128x4 tiled layout of block-scaled MMA -- exactly the
+// bytes kq_quantize_mxfp4 writes -- or, in its bf16 mode, from bf16 A and W
+// (the unquantized reference product of eq. 2).
+//
+// An MXFP4 element times its power-of-two scale has at most two significant
+// bits, so it is exact in bf16 (subnormals included).  Each operand tile is
+// therefore dequantized into bf16 in shared memory and multiplied with
+// tcgen05.mma kind::f16 (fp32 accumulation in TMEM): the same products a
+// block-scaled MXFP4 MMA forms, summed in fp32.
+//
+// Roles in a CTA (persistent over 128 x 128 output tiles; K in steps of 64):
+//   warp 0      producer: per K step the code tiles of A and W (TMA, 128 rows
+//               x 32 bytes each) and their 512-byte scale tiles (bulk copies)
+//               into a 4-deep ring -- or, in the bf16 mode, the two 128 x 64
+//               bf16 operand boxes straight into an operand buffer;
+//   warp 1      MMA issuer: four M = 128, N = 128, K = 16 MMAs per K step
+//               into one of two TMEM accumulators (128 columns each);
+//   warps 2-5   dequantization (MXFP4 mode): thread r turns row r of both
+//               code tiles into bf16 rows of the 128B-swizzled operand
+//               buffers (two of them, double-buffered);
+//   warps 6-9   epilogue: read the accumulator back (tcgen05.ld) and store
+//               the fp32 rows of C.
+// Every wait is bounded in time; a CTA that times out stops and leaves its
+// remaining tiles unwritten, and the call reports nothing (results are then
+// undefined), as for the quantizers.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "kq_device.cuh"
+#include "kq_internal.h"
+
+namespace kq {
+namespace {
+
+constexpr int kGBM = 128, kGBN = 128, kGBK = 64;
+constexpr int kGThreads = 320;
+constexpr int kGStages = 4;                   // code ring
+constexpr int kGCodeBytes = 128 * 32;         // one operand's code tile per K step
+constexpr int kGSfBytes = 512;                // one 128x4 scale tile
+constexpr int kGStageBytes = 2 * kGCodeBytes + 2 * kGSfBytes;   // 9 KB
+constexpr int kGOpBytes = kGBM * 128;         // 128 rows x 64 bf16 (one operand)
+constexpr int kGOpOff = 0;                    // 2 buffers x (A, W): 64 KB, 1 KB aligned
+constexpr int kGRingOff = 4 * kGOpBytes;
+constexpr int kGBarOff = kGRingOff + kGStages * kGStageBytes;
+constexpr int kGSmemBytes = kGBarOff + 1024 + 1024;
+constexpr uint32_t kGTmemCols = 256;
+
+__device__ __forceinline__ void g_tmem_alloc(uint32_t slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void g_tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void g_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void g_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ uint64_t g_desc(uint32_t saddr)
+{
+    // K-major, 128B swizzle: LBO 16 B (unused), SBO 1024 B (8 rows x 128 B)
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(16 >> 4) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// kind::f16: fp32 D, bf16 A and B, both K-major, N = 128, M = 128.
+constexpr uint32_t kGIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
+                             ((128u >> 4) << 24);
+
+__device__ __forceinline__ void g_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(kGIdesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void g_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void g_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// E2M1 code (bits 0-2 magnitude, bit 3 sign) times 2^(byte - 127), as fp32:
+// exact (at most two significant bits; 2^-127 and below are fp32 subnormals).
+__device__ __forceinline__ float e2m1_scaled(uint32_t code, float scale)
+{
+    const uint32_t mag = code & 7u;
+    // magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 as fp32 bit patterns
+    const uint32_t e = mag >> 1, half = mag & 1u;
+    const uint32_t bits = mag < 2 ? (mag == 1 ? 0x3F000000u : 0u)
+                                  : ((126u + e) << 23) | (half << 22);
+    const float v = __uint_as_float(bits | ((code & 8u) << 28));
+    return v * scale;
+}
+
+// 2^(byte - 127) as fp32 (byte 0: the subnormal 2^-127); byte 255 is the
+// E8M0 NaN of the OCP MX format.
+__device__ __forceinline__ float e8m0_value(uint32_t byte)
+{
+    return __uint_as_float(byte == 255u ? 0x7FC00000u : (byte ? byte << 23 : 0x00400000u));
+}
+
+struct GemmArgs {
+    int64_t m, n, k;              // C is m x n, the contraction runs over k
+    int64_t nb;                   // k / 32 scale blocks per row
+    int64_t ncb;                  // ceil(nb / 4): 128x4 scale tiles per row band
+    const uint8_t *sfa, *sfw;     // tiled scales (MXFP4 mode)
+    float *c;
+    int64_t ldc;
+    int64_t mtiles, ntiles, ksteps;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(kGThreads, 1)
+    w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                     const GemmArgs g)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+    const uint32_t bar = base + kGBarOff;
+    const uint32_t code_full = bar, code_empty = bar + 8 * kGStages;
+    const uint32_t op_full = bar + 16 * kGStages, op_free = op_full + 16;
+    const uint32_t acc_full = op_free + 16, acc_empty = acc_full + 16;
+    const uint32_t tmem_slot = acc_empty + 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tiles = g.mtiles * g.ntiles;
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmW);
+        for (int s = 0; s < kGStages; ++s) {
+            mbar_init(code_full + 8 * s, 1);
+            mbar_init(code_empty + 8 * s, 128);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(op_full + 8 * b, BF16 ? 1 : 128);   // TMA (bf16) or the dequant threads
+            mbar_init(op_free + 8 * b, 1);                 // MMA commit
+            mbar_init(acc_full + 8 * b, 1);
+            mbar_init(acc_empty + 8 * b, 128);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 1) g_tmem_alloc(tmem_slot, kGTmemCols);
+    g_fence_before();
+    __syncthreads();
+    g_fence_after();
+    uint32_t tmem_base;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(tmem_base) : "r"(tmem_slot) : "memory");
+    grid_dependency_wait();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int64_t kk = 0;       // global K-step counter of this CTA
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                const int64_t mt = t / g.ntiles, nt = t % g.ntiles;
+                for (int64_t ks = 0; ks < g.ksteps && ok; ++ks, ++kk) {
+                    if (BF16) {
+                        // straight into operand buffer kk % 2 once the MMAs freed it
+                        const int b = static_cast<int>(kk & 1);
+                        if (kk >= 2 && !mbar_wait(op_free + 8 * b, static_cast<uint32_t>(((kk >> 1) - 1) & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t opa = base + kGOpOff + b * 2 * kGOpBytes;
+                        mbar_arrive_expect_tx(op_full + 8 * b, 2 * kGOpBytes);
+                        tma_load_2d(opa, &tmA, static_cast<int32_t>(ks * kGBK),
+                                    static_cast<int32_t>(mt * kGBM), op_full + 8 * b, 0);
+                        tma_load_2d(opa + kGOpBytes, &tmW, static_cast<int32_t>(ks * kGBK),
+                                    static_cast<int32_t>(nt * kGBN), op_full + 8 * b, 0);
+                    } else {
+                        const int s = static_cast<int>(kk % kGStages);
+                        if (kk >= kGStages &&
+                            !mbar_wait(code_empty + 8 * s, static_cast<uint32_t>(((kk / kGStages) - 1) & 1))) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t st = base + kGRingOff + s * kGStageBytes;
+                        mbar_arrive_expect_tx(code_full + 8 * s, kGStageBytes);
+                        tma_load_2d(st, &tmA, static_cast<int32_t>(ks * 32),
+                                    static_cast<int32_t>(mt * kGBM), code_full + 8 * s, 0);
+                        tma_load_2d(st + kGCodeBytes, &tmW, static_cast<int32_t>(ks * 32),
+                                    static_cast<int32_t>(nt * kGBN), code_full + 8 * s, 0);
+                        // the 128x4 scale tile holding this K step's two blocks
+                        bulk_load(st + 2 * kGCodeBytes, g.sfa + (mt * g.ncb + ks / 2) * 512, 512,
+                                  code_full + 8 * s);
+                        bulk_load(st + 2 * kGCodeBytes + kGSfBytes, g.sfw + (nt * g.ncb + ks / 2) * 512,
+                                  512, code_full + 8 * s);
+                    }
+                }
+            }
+            // the last copies issued into each buffer have landed before the
+            // CTA may exit (they have, unless a wait above gave up)
+            const int nbuf = BF16 ? 2 : kGStages;
+            for (int64_t j = kk - 1; j >= 0 && j >= kk - nbuf; --j) {
+                if (BF16)
+                    (void)mbar_wait(op_full + 8 * static_cast<int>(j & 1), static_cast<uint32_t>((j >> 1) & 1));
+                else
+                    (void)mbar_wait(code_full + 8 * static_cast<int>(j % kGStages),
+                                    static_cast<uint32_t>((j / kGStages) & 1));
+            }
+        }
+    } else if (warp == 1) {
+        int64_t kk = 0, tc = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc) {
+            const int a = static_cast<int>(tc & 1);
+            if (tc >= 2)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(acc_empty + 8 * a, static_cast<uint32_t>(((tc >> 1) - 1) & 1)));
+            for (int64_t ks = 0; ks < g.ksteps && ok; ++ks, ++kk) {
+                const int b = static_cast<int>(kk & 1);
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(op_full + 8 * b, static_cast<uint32_t>((kk >> 1) & 1)));
+                if (!ok) break;
+                g_fence_after();
+                if (lane == 0) {
+                    const uint32_t opa = base + kGOpOff + b * 2 * kGOpBytes;
+                    for (int k = 0; k < 4; ++k)
+                        g_mma(tmem_base + a * 128, g_desc(opa + 32 * k), g_desc(opa + kGOpBytes + 32 * k),
+                              (ks > 0 || k > 0) ? 1u : 0u);
+                    g_commit(op_free + 8 * b);
+                    if (ks == g.ksteps - 1) g_commit(acc_full + 8 * a);
+                }
+                __syncwarp();
+            }
+        }
+        if (tc >= 1 && ok)
+            (void)mbar_wait(acc_full + 8 * static_cast<int>((tc - 1) & 1),
+                            static_cast<uint32_t>(((tc - 1) >> 1) & 1));
+    } else if (warp < 6) {
+        if (!BF16) {
+            // dequantization: thread r owns row r of both code tiles
+            const int r = threadIdx.x - 64;
+            int64_t kk = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                for (int64_t ks = 0; ks < g.ksteps; ++ks, ++kk) {
+                    const int s = static_cast<int>(kk % kGStages), b = static_cast<int>(kk & 1);
+                    ok = mbar_wait(code_full + 8 * s, static_cast<uint32_t>((kk / kGStages) & 1));
+                    if (ok && kk >= 2)
+                        ok = mbar_wait(op_free + 8 * b, static_cast<uint32_t>(((kk >> 1) - 1) & 1));
+                    if (!ok) break;
+                    const uint32_t st = base + kGRingOff + s * kGStageBytes;
+                    const uint32_t opa = base + kGOpOff + b * 2 * kGOpBytes;
+                    // scale bytes of row r, blocks 2 ks and 2 ks + 1 (adjacent in the tile)
+                    const int sfo = (r & 31) * 16 + (r >> 5) * 4 + static_cast<int>((ks & 1) * 2);
+#pragma unroll
+                    for (int op = 0; op < 2; ++op) {
+                        const uint32_t codes = st + op * kGCodeBytes + r * 32;
+                        uint32_t sfw2;
+                        asm volatile("ld.shared.u16 %0, [%1];"
+                                     : "=r"(sfw2)
+                                     : "r"(st + 2 * kGCodeBytes + op * kGSfBytes + sfo)
+                                     : "memory");
+                        // blocks past k (the padding columns of the last scale tile)
+                        // hold only zero codes; their scale bytes are not read
+                        const float sc0 = 2 * ks < g.nb ? e8m0_value(sfw2 & 0xFFu) : 0.f;
+                        const float sc1 = 2 * ks + 1 < g.nb ? e8m0_value(sfw2 >> 8) : 0.f;
+                        const uint32_t orow = opa + op * kGOpBytes + r * 128;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {            // 16-byte halves of the 32-byte row
+                            const uint4 w = lds128(codes + 16 * h);
+                            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                            const float sc = h ? sc1 : sc0;      // 32 codes per block
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {        // 8 codes -> 8 bf16 = one 16-byte chunk
+                                uint32_t o[4];
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const uint32_t byte = (wv[q] >> (8 * e)) & 0xFFu;
+                                    const __nv_bfloat162 p = __floats2bfloat162_rn(
+                                        e2m1_scaled(byte & 15u, sc), e2m1_scaled(byte >> 4, sc));
+                                    o[e] = *reinterpret_cast<const uint32_t *>(&p);
+                                }
+                                const int chunk = 4 * h + q;
+                                sts128(orow + ((chunk ^ (r & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+                            }
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    mbar_arrive(code_empty + 8 * s);
+                    mbar_arrive(op_full + 8 * b);
+                }
+            }
+        }
+    } else {
+        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31
+        const int qtr = warp & 3;
+        const int row_in = qtr * 32 + lane;
+        int64_t tc = 0;
+        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
+            const int a = static_cast<int>(tc & 1);
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full + 8 * a,
+                                                              static_cast<uint32_t>((tc >> 1) & 1)));
+            if (!ok) break;
+            g_fence_after();
+            const int64_t mt = t / g.ntiles, nt = t % g.ntiles;
+            const int64_t row = mt * kGBM + row_in;
+            float *crow = g.c + row * g.ldc + nt * kGBN;
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t v[32];
+                g_ld32(tmem_base + (static_cast<uint32_t>(qtr * 32) << 16) + a * 128 + cb * 32, v);
+                if (row < g.m) {
+                    const int64_t col0 = nt * kGBN + cb * 32;
+                    if (col0 + 32 <= g.n) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            stg_f4(crow + cb * 32 + 4 * j,
+                                   make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                               __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+                    } else {
+                        for (int j = 0; j < 32 && col0 + j < g.n; ++j)
+                            crow[cb * 32 + j] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            g_fence_before();
+            mbar_arrive(acc_empty + 8 * a);
+        }
+    }
+
+    g_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        g_fence_after();
+        g_tmem_dealloc(tmem_base, kGTmemCols);
+    }
+}
+
+struct GSlot {
+    std::once_flag once[64];
+    cudaError_t err[64] = {};
+};
+
+template <bool BF16>
+kq_status launch_gemm_t(const CUtensorMap &ma, const CUtensorMap &mw, const GemmArgs &g,
+                        int sm_count, cudaStream_t stream)
+{
+    auto kern = w4a4_gemm_kernel<BF16>;
+    static GSlot slot;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
+    std::call_once(slot.once[dev], [&] {
+        slot.err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kGSmemBytes);
+    });
+    if (slot.err[dev] != cudaSuccess) return KQ_ERR_CUDA;
+    const int64_t tiles = g.mtiles * g.ntiles;
+    if (tiles == 0) return KQ_OK;
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count));
+    return launch_pdl(kern, grid, kGThreads, static_cast<size_t>(kGSmemBytes), stream, ma, mw, g);
+}
+
+// Sums of (c - c_ref)^2 and c_ref^2 in fp64: one partial per thread, a
+// block reduction, one atomic per block and sum.
+__global__ void __launch_bounds__(256) layer_error_kernel(const float *__restrict__ c, int64_t ldc,
+                                                          const float *__restrict__ r, int64_t ldr,
+                                                          int64_t m, int64_t n, double *out)
+{
+    const int64_t n4 = (n + 3) / 4, total = m * n4;
+    double e2 = 0.0, r2 = 0.0;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t i = idx / n4, j = (idx % n4) * 4;
+        const float *cp = c + i * ldc + j, *rp = r + i * ldr + j;
+        if (j + 4 <= n) {
+            const float4 a = ldg_nc_f4(cp), b = ldg_nc_f4(rp);
+            const double d0 = static_cast<double>(a.x) - b.x, d1 = static_cast<double>(a.y) - b.y,
+                         d2 = static_cast<double>(a.z) - b.z, d3 = static_cast<double>(a.w) - b.w;
+            e2 += d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3;
+            r2 += static_cast<double>(b.x) * b.x + static_cast<double>(b.y) * b.y +
+                  static_cast<double>(b.z) * b.z + static_cast<double>(b.w) * b.w;
+        } else {
+            for (int64_t t = 0; j + t < n; ++t) {
+                const double dd = static_cast<double>(cp[t]) - rp[t];
+                e2 += dd * dd;
+                r2 += static_cast<double>(rp[t]) * rp[t];
+            }
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        e2 += __shfl_xor_sync(0xffffffffu, e2, o);
+        r2 += __shfl_xor_sync(0xffffffffu, r2, o);
+    }
+    __shared__ double part[2][8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        part[0][warp] = e2;
+        part[1][warp] = r2;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double se = 0.0, sr = 0.0;
+        for (int w = 0; w < (blockDim.x >> 5); ++w) {
+            se += part[0][w];
+            sr += part[1][w];
+        }
+        atomicAdd(out, se);
+        atomicAdd(out + 1, sr);
+    }
+}
+
+}  // namespace
+
+kq_status launch_layer_error(const float *c, int64_t ldc, const float *r, int64_t ldr, int64_t m,
+                             int64_t n, double *out, cudaStream_t stream)
+{
+    DeviceInfo info;
+    kq_status st = device_info(info);
+    if (st != KQ_OK) return st;
+    if (cudaMemsetAsync(out, 0, 2 * sizeof(double), stream) != cudaSuccess) return KQ_ERR_CUDA;
+    if (m == 0 || n == 0) return KQ_OK;
+    const int64_t work = m * ((n + 3) / 4);
+    const int grid = static_cast<int>(
+        std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(info.sm_count) * 8));
+    layer_error_kernel<<<grid, 256, 0, stream>>>(c, ldc, r, ldr, m, n, out);
+    return check_launch();
+}
+
+kq_status launch_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, const uint8_t *qw,
+                           int64_t ldqw, const uint8_t *sfw, int64_t m, int64_t n, int64_t k,
+                           float *c, int64_t ldc, cudaStream_t stream)
+{
+    DeviceInfo info;
+    kq_status st = device_info(info);
+    if (st != KQ_OK) return st;
+    CUtensorMap ma, mw;
+    st = make_tensor_map_2d_u8(&ma, const_cast<uint8_t *>(qa), m, k / 2, ldqa, 32, kGBM,
+                               CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != KQ_OK) return st;
+    st = make_tensor_map_2d_u8(&mw, const_cast<uint8_t *>(qw), n, k / 2, ldqw, 32, kGBN,
+                               CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != KQ_OK) return st;
+    GemmArgs g;
+    g.m = m;
+    g.n = n;
+    g.k = k;
+    g.nb = k / 32;
+    g.ncb = (k / 32 + 3) / 4;
+    g.sfa = sfa;
+    g.sfw = sfw;
+    g.c = c;
+    g.ldc = ldc;
+    g.mtiles = (m + kGBM - 1) / kGBM;
+    g.ntiles = (n + kGBN - 1) / kGBN;
+    g.ksteps = (k + kGBK - 1) / kGBK;
+    return launch_gemm_t<false>(ma, mw, g, info.sm_count, stream);
+}
+
+kq_status launch_bf16_gemm(const uint16_t *a, int64_t lda, const uint16_t *w, int64_t ldw,
+                           int64_t m, int64_t n, int64_t k, float *c, int64_t ldc,
+                           cudaStream_t stream)
+{
+    DeviceInfo info;
+    kq_status st = device_info(info);
+    if (st != KQ_OK) return st;
+    CUtensorMap ma, mw;
+    st = make_tensor_map_2d_bf16(&ma, a, m, k, lda, kGBK, kGBM);
+    if (st != KQ_OK) return st;
+    st = make_tensor_map_2d_bf16(&mw, w, n, k, ldw, kGBK, kGBN);
+    if (st != KQ_OK) return st;
+    GemmArgs g;
+    g.m = m;
+    g.n = n;
+    g.k = k;
+    g.nb = 0;
+    g.ncb = 0;
+    g.sfa = nullptr;
+    g.sfw = nullptr;
+    g.c = c;
+    g.ldc = ldc;
+    g.mtiles = (m + kGBM - 1) / kGBM;
+    g.ntiles = (n + kGBN - 1) / kGBN;
+    g.ksteps = (k + kGBK - 1) / kGBK;
+    return launch_gemm_t<true>(ma, mw, g, info.sm_count, stream);
+}
+
+}  // namespace kq

@@ -91,6 +91,17 @@ kq_status launch_quant_fwht(const uint16_t *A, int64_t lda, const QuantParams &p
 kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expanded,
                             const QuantParams &p, uint16_t *at, int64_t ldat, cudaStream_t stream);
 
+// C = A_q W_q^T from packed codes + 128x4 tiled scales, and C = A W^T in bf16
+// (tcgen05 GEMM); the fp64 error sums of eq. (2).
+kq_status launch_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, const uint8_t *qw,
+                           int64_t ldqw, const uint8_t *sfw, int64_t m, int64_t n, int64_t k,
+                           float *c, int64_t ldc, cudaStream_t stream);
+kq_status launch_bf16_gemm(const uint16_t *a, int64_t lda, const uint16_t *w, int64_t ldw,
+                           int64_t m, int64_t n, int64_t k, float *c, int64_t ldc,
+                           cudaStream_t stream);
+kq_status launch_layer_error(const float *c, int64_t ldc, const float *r, int64_t ldr, int64_t m,
+                             int64_t n, double *out, cudaStream_t stream);
+
 kq_status validate_quant_args(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
                               const uint8_t *q, int64_t ldq, const uint8_t *sf,
                               kq_sf_layout layout, const float *y_debug);

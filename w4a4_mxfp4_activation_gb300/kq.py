@@ -34,7 +34,7 @@ EXPORTS = (
     "kq_expand_blocks", "kq_expanded_bytes", "kq_dequantize", "kq_sf_bytes",
     "kq_status_string", "kq_lu_to_factors", "kq_invert_transpose_factors",
     "kq_quantize_mxfp4_variant", "kq_test_encode_e2m1", "kq_quantize_mxfp4_dual",
-    "kq_fwht_quantize_mxfp4",
+    "kq_fwht_quantize_mxfp4", "kq_w4a4_gemm", "kq_bf16_gemm", "kq_layer_error",
 )
 
 
@@ -90,6 +90,12 @@ def lib() -> ctypes.CDLL:
             L.kq_invert_transpose_factors.restype = st
             L.kq_test_encode_e2m1.argtypes = [u32, i64, vp, vp]
             L.kq_test_encode_e2m1.restype = st
+            L.kq_w4a4_gemm.argtypes = [vp, i64, vp, vp, i64, vp, i64, i64, i64, vp, i64, vp]
+            L.kq_w4a4_gemm.restype = st
+            L.kq_bf16_gemm.argtypes = [vp, i64, vp, i64, i64, i64, i64, vp, i64, vp]
+            L.kq_bf16_gemm.restype = st
+            L.kq_layer_error.argtypes = [vp, i64, vp, i64, i64, i64, vp, vp]
+            L.kq_layer_error.restype = st
             _lib = L
     return _lib
 
@@ -277,4 +283,53 @@ def kq_test_encode_e2m1(first: int, count: int, out=None, stream=None):
         out = torch.empty(count // 2, dtype=torch.uint8, device="cuda")
     _check(lib().kq_test_encode_e2m1(first, count, _ptr(out), _stream(stream)),
            "kq_test_encode_e2m1")
+    return out
+
+
+# --- the consumer product of eq. (11) and the layer error of eq. (2) ---------------
+
+def _ld(t, default):
+    return t.stride(0) if t.dim() == 2 else default
+
+
+def _gemm_out(m, n, device):
+    """fp32 [m, n] view of a buffer whose row pitch is a multiple of 4."""
+    import torch
+    ldc = n + (-n) % 4
+    return torch.empty((m, ldc), dtype=torch.float32, device=device)[:, :n]
+
+
+def kq_w4a4_gemm(qa, sfa, qw, sfw, m: int, n: int, k: int, c=None, stream=None):
+    """C = deq(qa) deq(qw)^T (fp32 [m, n]) from packed codes and 128x4 tiled
+    scales, on the tensor cores."""
+    if c is None:
+        c = _gemm_out(m, n, qa.device)
+    _check(lib().kq_w4a4_gemm(_ptr(qa), _ld(qa, k // 2), _ptr(sfa), _ptr(qw), _ld(qw, k // 2),
+                              _ptr(sfw), m, n, k, _ptr(c), _ld(c, n), _stream(stream)),
+           "kq_w4a4_gemm")
+    return c
+
+
+def kq_bf16_gemm(a, w, k: int | None = None, c=None, stream=None):
+    """C = A W^T (fp32 [m, n]) for bf16 A [m, k] and W [n, k]."""
+    a, w = _bf16_bits(a), _bf16_bits(w)
+    m, n = a.shape[0], w.shape[0]
+    k = a.shape[1] if k is None else k
+    if c is None:
+        c = _gemm_out(m, n, a.device)
+    _check(lib().kq_bf16_gemm(_ptr(a), a.stride(0), _ptr(w), w.stride(0), m, n, k, _ptr(c),
+                              _ld(c, n), _stream(stream)),
+           "kq_bf16_gemm")
+    return c
+
+
+def kq_layer_error(c, c_ref, out=None, stream=None):
+    """fp64 device [sum (c - c_ref)^2, sum c_ref^2] for fp32 [m, n] c, c_ref."""
+    import torch
+    m, n = c_ref.shape
+    if out is None:
+        out = torch.empty(2, dtype=torch.float64, device=c_ref.device)
+    _check(lib().kq_layer_error(_ptr(c), c.stride(0), _ptr(c_ref), c_ref.stride(0), m, n,
+                                _ptr(out), _stream(stream)),
+           "kq_layer_error")
     return out

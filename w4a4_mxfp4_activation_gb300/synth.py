@@ -109,6 +109,19 @@ def smooth_scales(d: int, seed: int = SEED_S, sigma: float = 0.5) -> np.ndarray:
     return rng.lognormal(0.0, sigma, size=d).astype(np.float32)
 
 
+def packed_codes(rows: int, k: int, seed: int) -> np.ndarray:
+    """Uniform random bytes [rows, k/2]: two 4-bit E2M1 codes each, every
+    code value equally likely (operands of the W4A4 product)."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, 256, size=(rows, k // 2), dtype=np.uint8)
+
+
+def scale_bytes(rows: int, nb: int, seed: int, lo: int, hi: int) -> np.ndarray:
+    """Uniform random E8M0 bytes in [lo, hi], row-major [rows, nb]."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(lo, hi + 1, size=(rows, nb), dtype=np.uint8)
+
+
 # Workloads: (name, m, d, activation model, config id)
 CONFIG0 = [("cfg0_tiny", 256, 1152, "gauss_outlier8", 0)]
 CONFIG1 = [("pixart_qkv", 4096, 1152, "pixart", 1), ("pixart_ffn_down", 4096, 4608, "pixart", 1)]
