@@ -181,9 +181,10 @@ KQ_API kq_status kq_fwht_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d,
  * [KQ] eq. (11) (Q(A T) x Q(W~)) and eq. (2):
  *     c[i][j] = sum_k deq(qa)[i][k] * deq(qw)[j][k]      (C = A_q W_q^T)
  * with deq = e2m1(code) * 2^(sf - 127) as in kq_dequantize.  Runs on the
- * tensor cores (tcgen05.mma, fp32 accumulation in TMEM): every MXFP4 element
- * times its scale is exact in bf16, so the products are exact and only the
- * fp32 accumulation rounds.
+ * FP4 tensor cores (tcgen05.mma kind::mxf4, block-scaled: the instruction
+ * reads the packed codes and applies the E8M0 scales itself), fp32
+ * accumulation in TMEM.  The element products are exact; only the fp32
+ * accumulation rounds.
  *   qa, ldqa   device, packed codes of the m x k left operand [m][ldqa]
  *              (as kq_quantize_mxfp4 writes them; ldqa >= k/2, ldqa % 16 == 0)
  *   sfa        device, its scales in KQ_SF_BLOCKED_128x4 (kq_sf_bytes(m, k))
@@ -202,6 +203,18 @@ KQ_API kq_status kq_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sf
                               const uint8_t *qw, int64_t ldqw, const uint8_t *sfw,
                               int64_t m, int64_t n, int64_t k, float *c, int64_t ldc,
                               cudaStream_t stream);
+
+/*
+ * kq_w4a4_gemm_variant -- kq_w4a4_gemm with the implementation chosen:
+ *   variant 0 = block-scaled FP4 MMA (kind::mxf4, the default), 1 = every
+ *   operand tile dequantized to bf16 in shared memory (exact) and multiplied
+ *   with kind::f16 -- an independent route to the same sums, for checking.
+ *   Other values: KQ_ERR_LAYOUT.
+ */
+KQ_API kq_status kq_w4a4_gemm_variant(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa,
+                                      const uint8_t *qw, int64_t ldqw, const uint8_t *sfw,
+                                      int64_t m, int64_t n, int64_t k, float *c, int64_t ldc,
+                                      int variant, cudaStream_t stream);
 
 /*
  * kq_bf16_gemm -- the unquantized reference product of [KQ] eq. (2),

@@ -602,20 +602,25 @@ def check_product(got, Aq, Wq, k):
 
 
 GEMM_SHAPES = [(256, 256, 1152), (300, 200, 96), (129, 384, 160), (1, 1, 32), (131, 130, 3072),
-               (128, 128, 64), (5, 700, 2240)]
+               (128, 128, 64), (5, 700, 2240), (130, 136, 5600), (64, 64, 224), (257, 260, 1024)]
 
 
+GEMM_VARIANTS = {"mxf4": kq.GEMM_MXF4, "dequant_bf16": kq.GEMM_DEQUANT_BF16}
+
+
+@pytest.mark.parametrize("variant", list(GEMM_VARIANTS))
 @pytest.mark.parametrize("m,n,k", GEMM_SHAPES, ids=[f"{m}x{n}x{k}" for m, n, k in GEMM_SHAPES])
-def test_w4a4_gemm_random_codes(m, n, k):
+def test_w4a4_gemm_random_codes(m, n, k, variant):
     """C = deq(qa) deq(qw)^T on random codes and scales against the fp64
-    product of the oracle's dequantization; ragged m, n and k (k = 32 mod 64
-    leaves half of the last K step as padding), C pitch wider than n with
-    canaries in the gap."""
+    product of the oracle's dequantization; ragged m, n and k (an odd block
+    count puts a padding block, scale byte 0xFF, inside the last K = 64
+    instruction), C pitch wider than n with canaries in the gap."""
     qa, _, sfa = mx_operand(m, k, 7 * m + k)
     qw, _, sfw = mx_operand(n, k, 11 * n + k + 1)
     ldc = n + 4 + (-(n + 4)) % 4
     c = torch.full((m, ldc), 12345.0, dtype=torch.float32, device="cuda")
-    kq.kq_w4a4_gemm(dev(qa), dev(sfa), dev(qw), dev(sfw), m, n, k, c=c)
+    kq.kq_w4a4_gemm(dev(qa), dev(sfa), dev(qw), dev(sfw), m, n, k, c=c,
+                    variant=GEMM_VARIANTS[variant])
     got = np_(c)
     assert np.all(got[:, n:] == 12345.0)
     Aq = O.dequantize(qa, sfa, 1, m, k)
@@ -734,3 +739,21 @@ def test_layer_error_on_device_configs(name, m, d, model, cfg):
     e_ref, ref = O.layer_error(A_bits, W_bits, d, Fo, layout=1)
     assert abs(e_gpu - e_ref) <= 1e-3 * e_ref, (e_gpu, e_ref)
     assert abs(r_gpu - ref) <= reference_norm_tolerance(A_bits, W_bits, d), (r_gpu, ref)
+
+
+def test_w4a4_gemm_variants_agree_on_quantizer_output():
+    """The block-scaled FP4 instruction and the bf16 dequantization route
+    agree on the quantizer's own output to the fp32 accumulation bound
+    (both form exact products)."""
+    m, n, k = 384, 256, 3072
+    A_bits = synth.activations(m, k, 801, "flux")
+    W_bits = synth.weights(n, k, seed=802)
+    Fg, _ = lib_factors(k // 32, 803)
+    qa, sfa, _ = run_kind("kron_umma", A_bits, k, 1, Fg, y_debug=False)
+    qw, sfw, _ = run_kind("kron", W_bits, k, 1, kq.kq_invert_transpose_factors(Fg), y_debug=False)
+    c0 = np_(kq.kq_w4a4_gemm(qa, sfa, qw, sfw, m, n, k, variant=kq.GEMM_MXF4)).astype(np.float64)
+    c1 = np_(kq.kq_w4a4_gemm(qa, sfa, qw, sfw, m, n, k, variant=kq.GEMM_DEQUANT_BF16))
+    Aq = O.dequantize(np_(qa), np_(sfa), 1, m, k)
+    Wq = O.dequantize(np_(qw), np_(sfw), 1, n, k)
+    tol = 2 * gemm_tolerance(Aq, Wq, k)
+    assert np.all(np.abs(c0 - c1) <= tol)

@@ -300,10 +300,12 @@ kq_status kq_fwht_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_
     return launch_quant_fwht(A, lda, p, stream);
 }
 
-kq_status kq_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, const uint8_t *qw,
-                       int64_t ldqw, const uint8_t *sfw, int64_t m, int64_t n, int64_t k,
-                       float *c, int64_t ldc, cudaStream_t stream)
+kq_status kq_w4a4_gemm_variant(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa,
+                               const uint8_t *qw, int64_t ldqw, const uint8_t *sfw, int64_t m,
+                               int64_t n, int64_t k, float *c, int64_t ldc, int variant,
+                               cudaStream_t stream)
 {
+    if (variant < 0 || variant > 1) return KQ_ERR_LAYOUT;
     if (m < 0 || n < 0 || k <= 0 || k % 32 != 0 || ldqa < k / 2 || ldqw < k / 2 || ldc < n)
         return KQ_ERR_SHAPE;
     // int32 TMA coordinates; row pitches below 2^40 bytes
@@ -316,7 +318,14 @@ kq_status kq_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, cons
     if (!aligned16(qa) || !aligned16(qw) || !aligned16(sfa) || !aligned16(sfw) || !aligned16(c) ||
         ldqa % 16 != 0 || ldqw % 16 != 0 || ldc % 4 != 0)
         return KQ_ERR_ALIGN;
-    return launch_w4a4_gemm(qa, ldqa, sfa, qw, ldqw, sfw, m, n, k, c, ldc, stream);
+    return launch_w4a4_gemm(qa, ldqa, sfa, qw, ldqw, sfw, m, n, k, c, ldc, variant, stream);
+}
+
+kq_status kq_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, const uint8_t *qw,
+                       int64_t ldqw, const uint8_t *sfw, int64_t m, int64_t n, int64_t k,
+                       float *c, int64_t ldc, cudaStream_t stream)
+{
+    return kq_w4a4_gemm_variant(qa, ldqa, sfa, qw, ldqw, sfw, m, n, k, c, ldc, 0, stream);
 }
 
 kq_status kq_bf16_gemm(const uint16_t *a, int64_t lda, const uint16_t *w, int64_t ldw, int64_t m,

@@ -367,6 +367,231 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
 }
 
+// ---- block-scaled FP4 kernel (tcgen05.mma kind::mxf4) ---------------------------
+//
+// The tensor cores read the packed E2M1 codes straight from shared memory and
+// apply the E8M0 block scales themselves (one scale per 32 elements along K,
+// two per K = 64 instruction), so nothing is dequantized on the CUDA cores.
+//   stage (K = 256 elements): A codes 128 rows x 128 B and W codes 128 rows x
+//   128 B, both loaded by TMA with the 128-byte swizzle, plus the two 128x4
+//   scale tiles of each operand that cover those 8 blocks (bulk copies of the
+//   tiled layout, unchanged);
+//   TMEM: two 128-column fp32 accumulators, then 16 columns per stage for the
+//   scales (tcgen05.cp 32x128b.warpx4 puts tile row r -- the scales of rows
+//   r, r + 32, r + 64, r + 96 -- into lane r of every lane quarter).
+// Roles: warp 0 producer, warp 1 MMA issuer, warps 2-5 epilogue.
+
+constexpr int kXBK = 256;                          // K elements per stage
+constexpr int kXStages = 6;
+constexpr int kXCodeBytes = 128 * 128;             // one operand's codes per stage
+constexpr int kXSfBytes = 1024;                    // two scale tiles per operand per stage
+constexpr int kXStageBytes = 2 * kXCodeBytes + 2 * kXSfBytes;   // 34 KB, 1 KB aligned
+constexpr int kXBarOff = kXStages * kXStageBytes;
+constexpr int kXSmemBytes = kXBarOff + 256 + 1024;
+constexpr uint32_t kXTmemCols = 512;               // 2 x 128 accumulator + 6 x 16 scales
+constexpr uint32_t kXSfCol = 256;
+
+static_assert(kXSfCol + 16 * kXStages <= kXTmemCols, "scale columns fit in TMEM");
+
+// Shared-memory descriptor of a no-swizzle K-major matrix: core matrices of
+// 8 rows x 16 bytes, SBO = distance between 8-row groups.
+__device__ __forceinline__ uint64_t x_desc_noswz(uint32_t saddr, uint32_t sbo)
+{
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(16 >> 4) << 16) |
+           (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of kind::mxf4: E2M1 A and B (format 1), both K-major,
+// UE8M0 scales (bit 23), N = 128, M = 128, dense K = 64; the scale-data ids
+// (bits 4-5 for B, 29-30 for A) pick the byte of the 32-bit TMEM scale word
+// the instruction starts at.
+__device__ __forceinline__ uint32_t x_idesc(uint32_t sf_id)
+{
+    return (sf_id << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | (1u << 23) |
+           ((128u >> 4) << 24) | (sf_id << 29);
+}
+
+__device__ __forceinline__ void x_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                      uint32_t sfa, uint32_t sfb, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void x_cp_sf(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(192, 1)
+    w4a4_mxf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                     const GemmArgs g)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+    const uint32_t bar = base + kXBarOff;
+    const uint32_t full = bar, empty = bar + 8 * kXStages;
+    const uint32_t acc_full = bar + 16 * kXStages, acc_empty = acc_full + 16;
+    const uint32_t tmem_slot = acc_empty + 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tiles = g.mtiles * g.ntiles;
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmW);
+        for (int s = 0; s < kXStages; ++s) {
+            mbar_init(full + 8 * s, 1);
+            mbar_init(empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + 8 * b, 1);
+            mbar_init(acc_empty + 8 * b, 128);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 1) g_tmem_alloc(tmem_slot, kXTmemCols);
+    g_fence_before();
+    __syncthreads();
+    g_fence_after();
+    uint32_t tmem_base;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(tmem_base) : "r"(tmem_slot) : "memory");
+    grid_dependency_wait();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int64_t kk = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                const int64_t mt = t / g.ntiles, nt = t % g.ntiles;
+                for (int64_t ks = 0; ks < g.ksteps; ++ks, ++kk) {
+                    const int s = static_cast<int>(kk % kXStages);
+                    if (kk >= kXStages &&
+                        !mbar_wait(empty + 8 * s, static_cast<uint32_t>(((kk / kXStages) - 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    // scale tiles holding the blocks this stage's instructions use
+                    const int64_t rem = (g.k - ks * kXBK + 63) / 64;
+                    const int64_t nmma = rem < 4 ? rem : 4;
+                    const uint32_t sf_bytes = static_cast<uint32_t>((nmma + 1) / 2) * 512u;
+                    const uint32_t st = base + s * kXStageBytes;
+                    mbar_arrive_expect_tx(full + 8 * s, 2 * kXCodeBytes + 2 * sf_bytes);
+                    tma_load_2d(st, &tmA, static_cast<int32_t>(ks * 128), static_cast<int32_t>(mt * 128),
+                                full + 8 * s, 0);
+                    tma_load_2d(st + kXCodeBytes, &tmW, static_cast<int32_t>(ks * 128),
+                                static_cast<int32_t>(nt * 128), full + 8 * s, 0);
+                    bulk_load(st + 2 * kXCodeBytes, g.sfa + (mt * g.ncb + 2 * ks) * 512, sf_bytes,
+                              full + 8 * s);
+                    bulk_load(st + 2 * kXCodeBytes + kXSfBytes, g.sfw + (nt * g.ncb + 2 * ks) * 512,
+                              sf_bytes, full + 8 * s);
+                }
+            }
+            // the last copies issued into each stage have landed before exit
+            for (int64_t j = kk - 1; j >= 0 && j >= kk - kXStages; --j)
+                (void)mbar_wait(full + 8 * static_cast<int>(j % kXStages),
+                                static_cast<uint32_t>((j / kXStages) & 1));
+        }
+    } else if (warp == 1) {
+        int64_t kk = 0, tc = 0;
+        bool ok = true;
+        // an odd block count leaves one padding block inside the last
+        // instruction: its scale bytes are set to 2^0 before use
+        const bool pad_fix = (g.nb & 1) != 0;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc) {
+            const int a = static_cast<int>(tc & 1);
+            if (tc >= 2)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(acc_empty + 8 * a, static_cast<uint32_t>(((tc >> 1) - 1) & 1)));
+            for (int64_t ks = 0; ks < g.ksteps && ok; ++ks, ++kk) {
+                const int s = static_cast<int>(kk % kXStages);
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(full + 8 * s, static_cast<uint32_t>((kk / kXStages) & 1)));
+                if (!ok) break;
+                const int64_t rem = (g.k - ks * kXBK + 63) / 64;
+                const int nmma = rem < 4 ? static_cast<int>(rem) : 4;
+                const uint32_t st = base + s * kXStageBytes;
+                const uint32_t sfa_s = st + 2 * kXCodeBytes, sfw_s = sfa_s + kXSfBytes;
+                if (pad_fix && ks == g.ksteps - 1) {
+                    const int kb = static_cast<int>(g.nb - 8 * ks);     // padding block, local index
+                    const uint32_t off = static_cast<uint32_t>((kb >> 2) * 512 + lane * 16 + (kb & 3));
+#pragma unroll
+                    for (int grp = 0; grp < 4; ++grp) {
+                        asm volatile("st.shared.u8 [%0], %1;" ::"r"(sfa_s + off + 4 * grp), "r"(127u) : "memory");
+                        asm volatile("st.shared.u8 [%0], %1;" ::"r"(sfw_s + off + 4 * grp), "r"(127u) : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                g_fence_after();
+                if (lane == 0) {
+                    const uint32_t sft = tmem_base + kXSfCol + 16 * s;
+                    for (int at = 0; at < (nmma + 1) / 2; ++at) {
+                        x_cp_sf(sft + 4 * at, x_desc_noswz(sfa_s + 512 * at, 128));
+                        x_cp_sf(sft + 8 + 4 * at, x_desc_noswz(sfw_s + 512 * at, 128));
+                    }
+                    for (int j = 0; j < nmma; ++j) {
+                        const uint32_t id = 2u * static_cast<uint32_t>(j & 1);
+                        x_mma(tmem_base + a * 128, g_desc(st + 32 * j), g_desc(st + kXCodeBytes + 32 * j),
+                              x_idesc(id), sft + 4 * (j >> 1), sft + 8 + 4 * (j >> 1),
+                              (ks > 0 || j > 0) ? 1u : 0u);
+                    }
+                    g_commit(empty + 8 * s);
+                    if (ks == g.ksteps - 1) g_commit(acc_full + 8 * a);
+                }
+                __syncwarp();
+            }
+        }
+        if (tc >= 1 && ok)
+            (void)mbar_wait(acc_full + 8 * static_cast<int>((tc - 1) & 1),
+                            static_cast<uint32_t>(((tc - 1) >> 1) & 1));
+    } else {
+        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31
+        const int qtr = warp & 3;
+        const int row_in = qtr * 32 + lane;
+        int64_t tc = 0;
+        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
+            const int a = static_cast<int>(tc & 1);
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full + 8 * a,
+                                                              static_cast<uint32_t>((tc >> 1) & 1)));
+            if (!ok) break;
+            g_fence_after();
+            const int64_t mt = t / g.ntiles, nt = t % g.ntiles;
+            const int64_t row = mt * 128 + row_in;
+            float *crow = g.c + row * g.ldc + nt * 128;
+            for (int cb = 0; cb < 4; ++cb) {
+                uint32_t v[32];
+                g_ld32(tmem_base + (static_cast<uint32_t>(qtr * 32) << 16) + a * 128 + cb * 32, v);
+                if (row < g.m) {
+                    const int64_t col0 = nt * 128 + cb * 32;
+                    if (col0 + 32 <= g.n) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            stg_f4(crow + cb * 32 + 4 * j,
+                                   make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                               __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+                    } else {
+                        for (int j = 0; j < 32 && col0 + j < g.n; ++j)
+                            crow[cb * 32 + j] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+            g_fence_before();
+            mbar_arrive(acc_empty + 8 * a);
+        }
+    }
+
+    g_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        g_fence_after();
+        g_tmem_dealloc(tmem_base, kXTmemCols);
+    }
+}
+
 struct GSlot {
     std::once_flag once[64];
     cudaError_t err[64] = {};
@@ -440,6 +665,46 @@ __global__ void __launch_bounds__(256) layer_error_kernel(const float *__restric
     }
 }
 
+kq_status launch_w4a4_mxf4(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, const uint8_t *qw,
+                           int64_t ldqw, const uint8_t *sfw, int64_t m, int64_t n, int64_t k,
+                           float *c, int64_t ldc, cudaStream_t stream)
+{
+    DeviceInfo info;
+    kq_status st = device_info(info);
+    if (st != KQ_OK) return st;
+    CUtensorMap ma, mw;
+    st = make_tensor_map_2d_u8(&ma, const_cast<uint8_t *>(qa), m, k / 2, ldqa, 128, 128,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != KQ_OK) return st;
+    st = make_tensor_map_2d_u8(&mw, const_cast<uint8_t *>(qw), n, k / 2, ldqw, 128, 128,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != KQ_OK) return st;
+    GemmArgs g;
+    g.m = m;
+    g.n = n;
+    g.k = k;
+    g.nb = k / 32;
+    g.ncb = (k / 32 + 3) / 4;
+    g.sfa = sfa;
+    g.sfw = sfw;
+    g.c = c;
+    g.ldc = ldc;
+    g.mtiles = (m + 127) / 128;
+    g.ntiles = (n + 127) / 128;
+    g.ksteps = (k + kXBK - 1) / kXBK;
+    static GSlot slot;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
+    std::call_once(slot.once[dev], [&] {
+        slot.err[dev] = cudaFuncSetAttribute(w4a4_mxf4_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmemBytes);
+    });
+    if (slot.err[dev] != cudaSuccess) return KQ_ERR_CUDA;
+    const int64_t tiles = g.mtiles * g.ntiles;
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, info.sm_count));
+    return launch_pdl(w4a4_mxf4_kernel, grid, 192, static_cast<size_t>(kXSmemBytes), stream, ma, mw, g);
+}
+
 }  // namespace
 
 kq_status launch_layer_error(const float *c, int64_t ldc, const float *r, int64_t ldr, int64_t m,
@@ -459,8 +724,9 @@ kq_status launch_layer_error(const float *c, int64_t ldc, const float *r, int64_
 
 kq_status launch_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, const uint8_t *qw,
                            int64_t ldqw, const uint8_t *sfw, int64_t m, int64_t n, int64_t k,
-                           float *c, int64_t ldc, cudaStream_t stream)
+                           float *c, int64_t ldc, int variant, cudaStream_t stream)
 {
+    if (variant == 0) return launch_w4a4_mxf4(qa, ldqa, sfa, qw, ldqw, sfw, m, n, k, c, ldc, stream);
     DeviceInfo info;
     kq_status st = device_info(info);
     if (st != KQ_OK) return st;

@@ -91,11 +91,12 @@ kq_status launch_quant_fwht(const uint16_t *A, int64_t lda, const QuantParams &p
 kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expanded,
                             const QuantParams &p, uint16_t *at, int64_t ldat, cudaStream_t stream);
 
-// C = A_q W_q^T from packed codes + 128x4 tiled scales, and C = A W^T in bf16
-// (tcgen05 GEMM); the fp64 error sums of eq. (2).
+// C = A_q W_q^T from packed codes + 128x4 tiled scales (variant 0: block-scaled
+// kind::mxf4 MMA; 1: dequantized to bf16 in shared memory, kind::f16), and
+// C = A W^T in bf16 (tcgen05 GEMM); the fp64 error sums of eq. (2).
 kq_status launch_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, const uint8_t *qw,
                            int64_t ldqw, const uint8_t *sfw, int64_t m, int64_t n, int64_t k,
-                           float *c, int64_t ldc, cudaStream_t stream);
+                           float *c, int64_t ldc, int variant, cudaStream_t stream);
 kq_status launch_bf16_gemm(const uint16_t *a, int64_t lda, const uint16_t *w, int64_t ldw,
                            int64_t m, int64_t n, int64_t k, float *c, int64_t ldc,
                            cudaStream_t stream);

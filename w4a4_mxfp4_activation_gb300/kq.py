@@ -34,7 +34,8 @@ EXPORTS = (
     "kq_expand_blocks", "kq_expanded_bytes", "kq_dequantize", "kq_sf_bytes",
     "kq_status_string", "kq_lu_to_factors", "kq_invert_transpose_factors",
     "kq_quantize_mxfp4_variant", "kq_test_encode_e2m1", "kq_quantize_mxfp4_dual",
-    "kq_fwht_quantize_mxfp4", "kq_w4a4_gemm", "kq_bf16_gemm", "kq_layer_error",
+    "kq_fwht_quantize_mxfp4", "kq_w4a4_gemm", "kq_w4a4_gemm_variant", "kq_bf16_gemm",
+    "kq_layer_error",
 )
 
 
@@ -92,6 +93,9 @@ def lib() -> ctypes.CDLL:
             L.kq_test_encode_e2m1.restype = st
             L.kq_w4a4_gemm.argtypes = [vp, i64, vp, vp, i64, vp, i64, i64, i64, vp, i64, vp]
             L.kq_w4a4_gemm.restype = st
+            L.kq_w4a4_gemm_variant.argtypes = [vp, i64, vp, vp, i64, vp, i64, i64, i64, vp, i64, st,
+                                               vp]
+            L.kq_w4a4_gemm_variant.restype = st
             L.kq_bf16_gemm.argtypes = [vp, i64, vp, i64, i64, i64, i64, vp, i64, vp]
             L.kq_bf16_gemm.restype = st
             L.kq_layer_error.argtypes = [vp, i64, vp, i64, i64, i64, vp, vp]
@@ -299,14 +303,23 @@ def _gemm_out(m, n, device):
     return torch.empty((m, ldc), dtype=torch.float32, device=device)[:, :n]
 
 
-def kq_w4a4_gemm(qa, sfa, qw, sfw, m: int, n: int, k: int, c=None, stream=None):
+GEMM_MXF4 = 0
+GEMM_DEQUANT_BF16 = 1
+
+
+def kq_w4a4_gemm(qa, sfa, qw, sfw, m: int, n: int, k: int, c=None, variant: int | None = None,
+                 stream=None):
     """C = deq(qa) deq(qw)^T (fp32 [m, n]) from packed codes and 128x4 tiled
-    scales, on the tensor cores."""
+    scales, on the tensor cores (``variant``: GEMM_MXF4 or GEMM_DEQUANT_BF16;
+    None = the library's default)."""
     if c is None:
         c = _gemm_out(m, n, qa.device)
-    _check(lib().kq_w4a4_gemm(_ptr(qa), _ld(qa, k // 2), _ptr(sfa), _ptr(qw), _ld(qw, k // 2),
-                              _ptr(sfw), m, n, k, _ptr(c), _ld(c, n), _stream(stream)),
-           "kq_w4a4_gemm")
+    args = (_ptr(qa), _ld(qa, k // 2), _ptr(sfa), _ptr(qw), _ld(qw, k // 2), _ptr(sfw), m, n, k,
+            _ptr(c), _ld(c, n))
+    if variant is None:
+        _check(lib().kq_w4a4_gemm(*args, _stream(stream)), "kq_w4a4_gemm")
+    else:
+        _check(lib().kq_w4a4_gemm_variant(*args, variant, _stream(stream)), "kq_w4a4_gemm_variant")
     return c
 
 
