@@ -382,13 +382,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
 // Roles: warp 0 producer, warp 1 MMA issuer, warps 2-5 epilogue.
 
 constexpr int kXBK = 256;                          // K elements per stage
-constexpr int kXStages = 6;
+constexpr int kXStages = 4;
 constexpr int kXCodeBytes = 128 * 128;             // one operand's codes per stage
 constexpr int kXSfBytes = 1024;                    // two scale tiles per operand per stage
 constexpr int kXStageBytes = 2 * kXCodeBytes + 2 * kXSfBytes;   // 34 KB, 1 KB aligned
 constexpr int kXBarOff = kXStages * kXStageBytes;
 constexpr int kXSmemBytes = kXBarOff + 256 + 1024;
-constexpr uint32_t kXTmemCols = 512;               // 2 x 128 accumulator + 6 x 16 scales
+constexpr uint32_t kXTmemCols = 512;               // 2 x 128 accumulator + 16 per stage for scales
 constexpr uint32_t kXSfCol = 256;
 
 static_assert(kXSfCol + 16 * kXStages <= kXTmemCols, "scale columns fit in TMEM");
@@ -405,7 +405,7 @@ __device__ __forceinline__ uint64_t x_desc_noswz(uint32_t saddr, uint32_t sbo)
 // UE8M0 scales (bit 23), N = 128, M = 128, dense K = 64; the scale-data ids
 // (bits 4-5 for B, 29-30 for A) pick the byte of the 32-bit TMEM scale word
 // the instruction starts at.
-__device__ __forceinline__ uint32_t x_idesc(uint32_t sf_id)
+__host__ __device__ constexpr uint32_t x_idesc(uint32_t sf_id)
 {
     return (sf_id << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | (1u << 23) |
            ((128u >> 4) << 24) | (sf_id << 29);
@@ -528,16 +528,29 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 g_fence_after();
                 if (lane == 0) {
-                    const uint32_t sft = tmem_base + kXSfCol + 16 * s;
-                    for (int at = 0; at < (nmma + 1) / 2; ++at) {
-                        x_cp_sf(sft + 4 * at, x_desc_noswz(sfa_s + 512 * at, 128));
-                        x_cp_sf(sft + 8 + 4 * at, x_desc_noswz(sfw_s + 512 * at, 128));
-                    }
-                    for (int j = 0; j < nmma; ++j) {
-                        const uint32_t id = 2u * static_cast<uint32_t>(j & 1);
-                        x_mma(tmem_base + a * 128, g_desc(st + 32 * j), g_desc(st + kXCodeBytes + 32 * j),
-                              x_idesc(id), sft + 4 * (j >> 1), sft + 8 + 4 * (j >> 1),
-                              (ks > 0 || j > 0) ? 1u : 0u);
+                    // descriptors advance in 16-byte units: +2 = the next 32 bytes
+                    // of codes (K = 64), +32 = the next 512-byte scale tile
+                    const uint32_t sft = tmem_base + kXSfCol + 16 * s, acc = tmem_base + a * 128;
+                    const uint64_t da = g_desc(st), db = g_desc(st + kXCodeBytes);
+                    const uint64_t dsa = x_desc_noswz(sfa_s, 128), dsw = x_desc_noswz(sfw_s, 128);
+                    constexpr uint32_t id0 = x_idesc(0), id2 = x_idesc(2);
+                    if (nmma == 4) {
+                        x_cp_sf(sft, dsa);
+                        x_cp_sf(sft + 8, dsw);
+                        x_mma(acc, da, db, id0, sft, sft + 8, ks > 0 ? 1u : 0u);
+                        x_mma(acc, da + 2, db + 2, id2, sft, sft + 8, 1u);
+                        x_cp_sf(sft + 4, dsa + 32);
+                        x_cp_sf(sft + 12, dsw + 32);
+                        x_mma(acc, da + 4, db + 4, id0, sft + 4, sft + 12, 1u);
+                        x_mma(acc, da + 6, db + 6, id2, sft + 4, sft + 12, 1u);
+                    } else {
+                        for (int at = 0; at < (nmma + 1) / 2; ++at) {
+                            x_cp_sf(sft + 4 * at, dsa + 32 * at);
+                            x_cp_sf(sft + 8 + 4 * at, dsw + 32 * at);
+                        }
+                        for (int j = 0; j < nmma; ++j)
+                            x_mma(acc, da + 2 * j, db + 2 * j, (j & 1) ? id2 : id0, sft + 4 * (j >> 1),
+                                  sft + 8 + 4 * (j >> 1), (ks > 0 || j > 0) ? 1u : 0u);
                     }
                     g_commit(empty + 8 * s);
                     if (ks == g.ksteps - 1) g_commit(acc_full + 8 * a);
