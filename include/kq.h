@@ -208,7 +208,9 @@ KQ_API kq_status kq_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sf
  * kq_w4a4_gemm_variant -- kq_w4a4_gemm with the implementation chosen:
  *   variant 0 = block-scaled FP4 MMA (kind::mxf4, the default), 1 = every
  *   operand tile dequantized to bf16 in shared memory (exact) and multiplied
- *   with kind::f16 -- an independent route to the same sums, for checking.
+ *   with kind::f16 -- an independent route to the same sums, for checking;
+ *   2 / 3 = the FP4 kernel with its tile width fixed at 128 / 256 columns of
+ *   C (variant 0 picks 256 when K >= 2048 and the wide tiles fill the GPU).
  *   Other values: KQ_ERR_LAYOUT.
  */
 KQ_API kq_status kq_w4a4_gemm_variant(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa,

@@ -190,6 +190,7 @@ def test_gemm_argument_checks(L):
     assert g(vp(4104), 32, sa, qw, 32, sw, 4, 8, 64, c, 8, None) == 3    # misaligned
     assert g(qa, 40, sa, qw, 32, sw, 4, 8, 64, c, 8, None) == 3          # ldqa % 16
     assert g(qa, 32, sa, qw, 32, sw, 4, 8, 64, c, 10, None) == 3         # ldc % 4
+    assert L.kq_w4a4_gemm_variant(qa, 32, sa, qw, 32, sw, 4, 8, 64, c, 8, 4, None) == 4
     assert g(None, 32, None, None, 32, None, 0, 8, 64, None, 8, None) == 0   # m = 0
     assert g(None, 32, None, None, 32, None, 4, 0, 64, None, 0, None) == 0   # n = 0
     b = L.kq_bf16_gemm

@@ -605,7 +605,8 @@ GEMM_SHAPES = [(256, 256, 1152), (300, 200, 96), (129, 384, 160), (1, 1, 32), (1
                (128, 128, 64), (5, 700, 2240), (130, 136, 5600), (64, 64, 224), (257, 260, 1024)]
 
 
-GEMM_VARIANTS = {"mxf4": kq.GEMM_MXF4, "dequant_bf16": kq.GEMM_DEQUANT_BF16}
+GEMM_VARIANTS = {"mxf4": kq.GEMM_MXF4, "mxf4_narrow": kq.GEMM_MXF4_NARROW,
+                 "mxf4_wide": kq.GEMM_MXF4_WIDE, "dequant_bf16": kq.GEMM_DEQUANT_BF16}
 
 
 @pytest.mark.parametrize("variant", list(GEMM_VARIANTS))

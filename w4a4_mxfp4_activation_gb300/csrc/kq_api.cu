@@ -305,7 +305,7 @@ kq_status kq_w4a4_gemm_variant(const uint8_t *qa, int64_t ldqa, const uint8_t *s
                                int64_t n, int64_t k, float *c, int64_t ldc, int variant,
                                cudaStream_t stream)
 {
-    if (variant < 0 || variant > 1) return KQ_ERR_LAYOUT;
+    if (variant < 0 || variant > 3) return KQ_ERR_LAYOUT;
     if (m < 0 || n < 0 || k <= 0 || k % 32 != 0 || ldqa < k / 2 || ldqw < k / 2 || ldc < n)
         return KQ_ERR_SHAPE;
     // int32 TMA coordinates; row pitches below 2^40 bytes

@@ -372,26 +372,47 @@ __global__ void __launch_bounds__(kGThreads, 1)
 // The tensor cores read the packed E2M1 codes straight from shared memory and
 // apply the E8M0 block scales themselves (one scale per 32 elements along K,
 // two per K = 64 instruction), so nothing is dequantized on the CUDA cores.
-//   stage (K = 256 elements): A codes 128 rows x 128 B and W codes 128 rows x
-//   128 B, both loaded by TMA with the 128-byte swizzle, plus the two 128x4
-//   scale tiles of each operand that cover those 8 blocks (bulk copies of the
-//   tiled layout, unchanged);
-//   TMEM: two 128-column fp32 accumulators, then 16 columns per stage for the
+// A CTA computes 128 x (128 NH) tiles of C (persistent over tiles, K in
+// stages of 256 elements), NH = 1 or 2 halves of 128 W rows:
+//   stage: A codes 128 rows x 128 B and W codes 128 NH rows x 128 B (TMA,
+//   128-byte swizzle), the two 128x4 scale tiles of A and the 2 NH of W that
+//   cover the stage's 8 blocks (bulk copies of the tiled layout, unchanged);
+//   TMEM: 256 accumulator columns -- two 128-column buffers for NH = 1, one
+//   256-column buffer for NH = 2 (W rows 128 h .. + 127 -> columns 128 h ..,
+//   one N = 128 instruction each) -- then 8 + 8 NH columns per stage for the
 //   scales (tcgen05.cp 32x128b.warpx4 puts tile row r -- the scales of rows
 //   r, r + 32, r + 64, r + 96 -- into lane r of every lane quarter).
-// Roles: warp 0 producer, warp 1 MMA issuer, warps 2-5 epilogue.
+// Issuing costs more than executing at this size (a commit is worth several
+// instructions), so the wide tile halves the scale copies and commits per
+// flop; its single accumulator cannot overlap the epilogue with the next
+// tile, which pays only when K is long.
+// Roles: warp 0 producer, warp 1 MMA issuer, 4 NH epilogue warps: NH per TMEM
+// lane quarter, 128 columns each, read their part of the accumulator into
+// registers and release it before they store, so the next tile's MMAs start
+// while the stores drain.
 
 constexpr int kXBK = 256;                          // K elements per stage
-constexpr int kXStages = 4;
-constexpr int kXCodeBytes = 128 * 128;             // one operand's codes per stage
-constexpr int kXSfBytes = 1024;                    // two scale tiles per operand per stage
-constexpr int kXStageBytes = 2 * kXCodeBytes + 2 * kXSfBytes;   // 34 KB, 1 KB aligned
-constexpr int kXBarOff = kXStages * kXStageBytes;
-constexpr int kXSmemBytes = kXBarOff + 256 + 1024;
-constexpr uint32_t kXTmemCols = 512;               // 2 x 128 accumulator + 16 per stage for scales
-constexpr uint32_t kXSfCol = 256;
+constexpr int kXACodeBytes = 128 * 128;            // A codes per stage
+constexpr uint32_t kXTmemCols = 512;
+constexpr uint32_t kXSfCol = 256;                  // scale columns follow the accumulators
 
-static_assert(kXSfCol + 16 * kXStages <= kXTmemCols, "scale columns fit in TMEM");
+template <int NH>
+struct XCfg {
+    static constexpr int kBN = 128 * NH;                  // tile width (C columns, W rows)
+    static constexpr int kStages = 4;
+    static constexpr int kThreads = 64 + 128 * NH;
+    static constexpr int kAccBufs = NH == 1 ? 2 : 1;
+    static constexpr int kWCodeBytes = kBN * 128;
+    static constexpr int kSfaOff = kXACodeBytes + kWCodeBytes;
+    static constexpr int kSfwOff = kSfaOff + 1024;        // A: two scale tiles; W: NH halves x 2
+    static constexpr int kStageBytes = kSfwOff + 1024 * NH;
+    static constexpr int kBarOff = kStages * kStageBytes;
+    static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+    static constexpr uint32_t kSfStride = 8 + 8 * NH;     // TMEM scale columns per stage
+    static_assert(kStageBytes % 1024 == 0, "stages keep the 1 KB alignment of the swizzle");
+    static_assert(kXSfCol + kSfStride * kStages <= kXTmemCols, "scale columns fit in TMEM");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
+};
 
 // Shared-memory descriptor of a no-swizzle K-major matrix: core matrices of
 // 8 rows x 16 bytes, SBO = distance between 8-row groups.
@@ -427,18 +448,24 @@ __device__ __forceinline__ void x_cp_sf(uint32_t taddr, uint64_t sdesc)
                  : "memory");
 }
 
-__global__ void __launch_bounds__(192, 1)
+template <int NH>
+__global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
     w4a4_mxf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const GemmArgs g)
 {
+    using C = XCfg<NH>;
+    constexpr int kXStages = C::kStages, kXBN = C::kBN, kXWCodeBytes = C::kWCodeBytes;
+    constexpr int kXSfaOff = C::kSfaOff, kXSfwOff = C::kSfwOff, kXStageBytes = C::kStageBytes;
+    constexpr uint32_t kXSfStride = C::kSfStride;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
-    const uint32_t bar = base + kXBarOff;
+    const uint32_t bar = base + C::kBarOff;
     const uint32_t full = bar, empty = bar + 8 * kXStages;
     const uint32_t acc_full = bar + 16 * kXStages, acc_empty = acc_full + 16;
     const uint32_t tmem_slot = acc_empty + 16;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles = g.mtiles * g.ntiles;
+    const int64_t wrt = (g.n + 127) / 128;            // 128-row scale tiles of W
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
@@ -447,9 +474,9 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(full + 8 * s, 1);
             mbar_init(empty + 8 * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < C::kAccBufs; ++b) {
             mbar_init(acc_full + 8 * b, 1);
-            mbar_init(acc_empty + 8 * b, 128);
+            mbar_init(acc_empty + 8 * b, 128 * NH);
         }
         mbar_fence_init();
     }
@@ -474,20 +501,25 @@ __global__ void __launch_bounds__(192, 1)
                         ok = false;
                         break;
                     }
-                    // scale tiles holding the blocks this stage's instructions use
+                    // scale tiles holding the blocks this stage's instructions
+                    // use (none for a half of W past the edge of C)
                     const int64_t rem = (g.k - ks * kXBK + 63) / 64;
                     const int64_t nmma = rem < 4 ? rem : 4;
                     const uint32_t sf_bytes = static_cast<uint32_t>((nmma + 1) / 2) * 512u;
+                    const bool w1 = NH == 2 && 2 * nt + 1 < wrt;
                     const uint32_t st = base + s * kXStageBytes;
-                    mbar_arrive_expect_tx(full + 8 * s, 2 * kXCodeBytes + 2 * sf_bytes);
-                    tma_load_2d(st, &tmA, static_cast<int32_t>(ks * 128), static_cast<int32_t>(mt * 128),
+                    mbar_arrive_expect_tx(full + 8 * s, kXACodeBytes + kXWCodeBytes +
+                                                            (w1 ? 3u : 2u) * sf_bytes);
+                    const int32_t x = static_cast<int32_t>(ks * 128);
+                    tma_load_2d(st, &tmA, x, static_cast<int32_t>(mt * 128), full + 8 * s, 0);
+                    tma_load_2d(st + kXACodeBytes, &tmW, x, static_cast<int32_t>(nt * kXBN),
                                 full + 8 * s, 0);
-                    tma_load_2d(st + kXCodeBytes, &tmW, static_cast<int32_t>(ks * 128),
-                                static_cast<int32_t>(nt * 128), full + 8 * s, 0);
-                    bulk_load(st + 2 * kXCodeBytes, g.sfa + (mt * g.ncb + 2 * ks) * 512, sf_bytes,
+                    bulk_load(st + kXSfaOff, g.sfa + (mt * g.ncb + 2 * ks) * 512, sf_bytes, full + 8 * s);
+                    bulk_load(st + kXSfwOff, g.sfw + (NH * nt * g.ncb + 2 * ks) * 512, sf_bytes,
                               full + 8 * s);
-                    bulk_load(st + 2 * kXCodeBytes + kXSfBytes, g.sfw + (nt * g.ncb + 2 * ks) * 512,
-                              sf_bytes, full + 8 * s);
+                    if (w1)
+                        bulk_load(st + kXSfwOff + 1024, g.sfw + ((2 * nt + 1) * g.ncb + 2 * ks) * 512,
+                                  sf_bytes, full + 8 * s);
                 }
             }
             // the last copies issued into each stage have landed before exit
@@ -502,10 +534,13 @@ __global__ void __launch_bounds__(192, 1)
         // instruction: its scale bytes are set to 2^0 before use
         const bool pad_fix = (g.nb & 1) != 0;
         for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc) {
-            const int a = static_cast<int>(tc & 1);
-            if (tc >= 2)
+            // accumulator buffer b of tile tc is free once the epilogue has
+            // read tile tc - kAccBufs from it
+            const int b = static_cast<int>(tc % C::kAccBufs);
+            const int64_t use = tc / C::kAccBufs;
+            if (use >= 1)
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(acc_empty + 8 * a, static_cast<uint32_t>(((tc >> 1) - 1) & 1)));
+                                mbar_wait(acc_empty + 8 * b, static_cast<uint32_t>((use - 1) & 1)));
             for (int64_t ks = 0; ks < g.ksteps && ok; ++ks, ++kk) {
                 const int s = static_cast<int>(kk % kXStages);
                 ok = __all_sync(0xffffffffu,
@@ -514,7 +549,7 @@ __global__ void __launch_bounds__(192, 1)
                 const int64_t rem = (g.k - ks * kXBK + 63) / 64;
                 const int nmma = rem < 4 ? static_cast<int>(rem) : 4;
                 const uint32_t st = base + s * kXStageBytes;
-                const uint32_t sfa_s = st + 2 * kXCodeBytes, sfw_s = sfa_s + kXSfBytes;
+                const uint32_t sfa_s = st + kXSfaOff, sfw_s = st + kXSfwOff;
                 if (pad_fix && ks == g.ksteps - 1) {
                     const int kb = static_cast<int>(g.nb - 8 * ks);     // padding block, local index
                     const uint32_t off = static_cast<uint32_t>((kb >> 2) * 512 + lane * 16 + (kb & 3));
@@ -522,78 +557,123 @@ __global__ void __launch_bounds__(192, 1)
                     for (int grp = 0; grp < 4; ++grp) {
                         asm volatile("st.shared.u8 [%0], %1;" ::"r"(sfa_s + off + 4 * grp), "r"(127u) : "memory");
                         asm volatile("st.shared.u8 [%0], %1;" ::"r"(sfw_s + off + 4 * grp), "r"(127u) : "memory");
+                        if (NH == 2)
+                            asm volatile("st.shared.u8 [%0], %1;" ::"r"(sfw_s + 1024 + off + 4 * grp),
+                                         "r"(127u)
+                                         : "memory");
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
                 g_fence_after();
                 if (lane == 0) {
-                    // descriptors advance in 16-byte units: +2 = the next 32 bytes
-                    // of codes (K = 64), +32 = the next 512-byte scale tile
-                    const uint32_t sft = tmem_base + kXSfCol + 16 * s, acc = tmem_base + a * 128;
-                    const uint64_t da = g_desc(st), db = g_desc(st + kXCodeBytes);
+                    // TMEM scale columns of stage s: A tile at at 4 at, W half h
+                    // tile at at 8 + 4 (NH at + h).  Descriptors advance in
+                    // 16-byte units: +2 = the next 32 bytes of codes (K = 64),
+                    // +32 = the next 512-byte scale tile, +1024 = the next 128
+                    // rows of W.
+                    const uint32_t sft = tmem_base + kXSfCol + kXSfStride * s;
+                    const uint32_t acc = tmem_base + 128 * b;
+                    const uint64_t da = g_desc(st), db = g_desc(st + kXACodeBytes);
                     const uint64_t dsa = x_desc_noswz(sfa_s, 128), dsw = x_desc_noswz(sfw_s, 128);
                     constexpr uint32_t id0 = x_idesc(0), id2 = x_idesc(2);
-                    if (nmma == 4) {
-                        x_cp_sf(sft, dsa);
-                        x_cp_sf(sft + 8, dsw);
-                        x_mma(acc, da, db, id0, sft, sft + 8, ks > 0 ? 1u : 0u);
-                        x_mma(acc, da + 2, db + 2, id2, sft, sft + 8, 1u);
-                        x_cp_sf(sft + 4, dsa + 32);
-                        x_cp_sf(sft + 12, dsw + 32);
-                        x_mma(acc, da + 4, db + 4, id0, sft + 4, sft + 12, 1u);
-                        x_mma(acc, da + 6, db + 6, id2, sft + 4, sft + 12, 1u);
-                    } else {
-                        for (int at = 0; at < (nmma + 1) / 2; ++at) {
-                            x_cp_sf(sft + 4 * at, dsa + 32 * at);
-                            x_cp_sf(sft + 8 + 4 * at, dsw + 32 * at);
+                    for (int at = 0; at < (nmma + 1) / 2; ++at) {
+                        x_cp_sf(sft + 4 * at, dsa + 32 * at);
+#pragma unroll
+                        for (int hh = 0; hh < NH; ++hh)
+                            x_cp_sf(sft + 8 + 4 * (NH * at + hh), dsw + 64 * hh + 32 * at);
+                        for (int j = 2 * at; j < 2 * at + 2 && j < nmma; ++j) {
+                            const uint32_t id = (j & 1) ? id2 : id0;
+                            const uint32_t accum = (ks > 0 || j > 0) ? 1u : 0u;
+#pragma unroll
+                            for (int hh = 0; hh < NH; ++hh)
+                                x_mma(acc + 128 * hh, da + 2 * j, db + 1024 * hh + 2 * j, id, sft + 4 * at,
+                                      sft + 8 + 4 * (NH * at + hh), accum);
                         }
-                        for (int j = 0; j < nmma; ++j)
-                            x_mma(acc, da + 2 * j, db + 2 * j, (j & 1) ? id2 : id0, sft + 4 * (j >> 1),
-                                  sft + 8 + 4 * (j >> 1), (ks > 0 || j > 0) ? 1u : 0u);
                     }
                     g_commit(empty + 8 * s);
-                    if (ks == g.ksteps - 1) g_commit(acc_full + 8 * a);
+                    if (ks == g.ksteps - 1) g_commit(acc_full + 8 * b);
                 }
                 __syncwarp();
             }
         }
-        if (tc >= 1 && ok)
-            (void)mbar_wait(acc_full + 8 * static_cast<int>((tc - 1) & 1),
-                            static_cast<uint32_t>(((tc - 1) >> 1) & 1));
+        if (tc >= 1 && ok) {
+            const int64_t last = tc - 1;
+            (void)mbar_wait(acc_full + 8 * static_cast<int>(last % C::kAccBufs),
+                            static_cast<uint32_t>((last / C::kAccBufs) & 1));
+        }
     } else {
-        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31
-        const int qtr = warp & 3;
+        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 and the 128
+        // columns of half h = (w - 2) / 4 of the tile
+        const int qtr = warp & 3, h = (warp - 2) >> 2;
         const int row_in = qtr * 32 + lane;
         int64_t tc = 0;
         for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
-            const int a = static_cast<int>(tc & 1);
-            const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full + 8 * a,
-                                                              static_cast<uint32_t>((tc >> 1) & 1)));
+            const int b = static_cast<int>(tc % C::kAccBufs);
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full + 8 * b,
+                                                              static_cast<uint32_t>((tc / C::kAccBufs) & 1)));
             if (!ok) break;
             g_fence_after();
+            uint32_t v[128];
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(qtr * 32) << 16) + 128 * (b + h);
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+                "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+                "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+                "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+                "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                  "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+                  "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+                  "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+                  "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+                  "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35]), "=r"(v[36]),
+                  "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]), "=r"(v[42]),
+                  "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]),
+                  "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]),
+                  "=r"(v[55]), "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]),
+                  "=r"(v[61]), "=r"(v[62]), "=r"(v[63])
+                : "r"(taddr)
+                : "memory");
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+                "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+                "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+                "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+                "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+                : "=r"(v[64]), "=r"(v[65]), "=r"(v[66]), "=r"(v[67]), "=r"(v[68]), "=r"(v[69]),
+                  "=r"(v[70]), "=r"(v[71]), "=r"(v[72]), "=r"(v[73]), "=r"(v[74]), "=r"(v[75]),
+                  "=r"(v[76]), "=r"(v[77]), "=r"(v[78]), "=r"(v[79]), "=r"(v[80]), "=r"(v[81]),
+                  "=r"(v[82]), "=r"(v[83]), "=r"(v[84]), "=r"(v[85]), "=r"(v[86]), "=r"(v[87]),
+                  "=r"(v[88]), "=r"(v[89]), "=r"(v[90]), "=r"(v[91]), "=r"(v[92]), "=r"(v[93]),
+                  "=r"(v[94]), "=r"(v[95]), "=r"(v[96]), "=r"(v[97]), "=r"(v[98]), "=r"(v[99]),
+                  "=r"(v[100]), "=r"(v[101]), "=r"(v[102]), "=r"(v[103]), "=r"(v[104]), "=r"(v[105]),
+                  "=r"(v[106]), "=r"(v[107]), "=r"(v[108]), "=r"(v[109]), "=r"(v[110]), "=r"(v[111]),
+                  "=r"(v[112]), "=r"(v[113]), "=r"(v[114]), "=r"(v[115]), "=r"(v[116]), "=r"(v[117]),
+                  "=r"(v[118]), "=r"(v[119]), "=r"(v[120]), "=r"(v[121]), "=r"(v[122]), "=r"(v[123]),
+                  "=r"(v[124]), "=r"(v[125]), "=r"(v[126]), "=r"(v[127])
+                : "r"(taddr + 64)
+                : "memory");
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            g_fence_before();
+            mbar_arrive(acc_empty + 8 * b);      // the accumulator may be overwritten now
             const int64_t mt = t / g.ntiles, nt = t % g.ntiles;
             const int64_t row = mt * 128 + row_in;
-            float *crow = g.c + row * g.ldc + nt * 128;
-            for (int cb = 0; cb < 4; ++cb) {
-                uint32_t v[32];
-                g_ld32(tmem_base + (static_cast<uint32_t>(qtr * 32) << 16) + a * 128 + cb * 32, v);
-                if (row < g.m) {
-                    const int64_t col0 = nt * 128 + cb * 32;
-                    if (col0 + 32 <= g.n) {
+            const int64_t col0 = nt * kXBN + 128 * h;
+            if (row < g.m && col0 < g.n) {
+                float *crow = g.c + row * g.ldc + col0;
+                if (col0 + 128 <= g.n) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            stg_f4(crow + cb * 32 + 4 * j,
-                                   make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                               __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
-                    } else {
-                        for (int j = 0; j < 32 && col0 + j < g.n; ++j)
-                            crow[cb * 32 + j] = __uint_as_float(v[j]);
-                    }
+                    for (int j = 0; j < 32; ++j)
+                        stg_f4(crow + 4 * j, make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                         __uint_as_float(v[4 * j + 2]),
+                                                         __uint_as_float(v[4 * j + 3])));
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 128; ++j)
+                        if (col0 + j < g.n) crow[j] = __uint_as_float(v[j]);
                 }
             }
-            g_fence_before();
-            mbar_arrive(acc_empty + 8 * a);
         }
     }
 
@@ -678,9 +758,28 @@ __global__ void __launch_bounds__(256) layer_error_kernel(const float *__restric
     }
 }
 
+template <int NH>
+kq_status launch_mxf4_t(const CUtensorMap &ma, const CUtensorMap &mw, const GemmArgs &g,
+                        int sm_count, cudaStream_t stream)
+{
+    using C = XCfg<NH>;
+    auto kern = w4a4_mxf4_kernel<NH>;
+    static GSlot slot;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
+    std::call_once(slot.once[dev], [&] {
+        slot.err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+    });
+    if (slot.err[dev] != cudaSuccess) return KQ_ERR_CUDA;
+    const int64_t tiles = g.mtiles * g.ntiles;
+    const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count));
+    return launch_pdl(kern, grid, C::kThreads, static_cast<size_t>(C::kSmemBytes), stream, ma, mw, g);
+}
+
 kq_status launch_w4a4_mxf4(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, const uint8_t *qw,
                            int64_t ldqw, const uint8_t *sfw, int64_t m, int64_t n, int64_t k,
-                           float *c, int64_t ldc, cudaStream_t stream)
+                           float *c, int64_t ldc, int wide_sel, cudaStream_t stream)
 {
     DeviceInfo info;
     kq_status st = device_info(info);
@@ -689,8 +788,14 @@ kq_status launch_w4a4_mxf4(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, 
     st = make_tensor_map_2d_u8(&ma, const_cast<uint8_t *>(qa), m, k / 2, ldqa, 128, 128,
                                CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != KQ_OK) return st;
-    st = make_tensor_map_2d_u8(&mw, const_cast<uint8_t *>(qw), n, k / 2, ldqw, 128, 128,
-                               CU_TENSOR_MAP_SWIZZLE_128B);
+    // the wide tile pays when a tile runs long enough (K >= 2048) to hide its
+    // epilogue and there are tiles enough to fill the GPU
+    const int64_t mtiles = (m + 127) / 128;
+    const bool wide = wide_sel >= 0 ? wide_sel == 1
+                                    : (k >= 2048 && mtiles * ((n + 255) / 256) >= info.sm_count);
+    const int bn = wide ? 256 : 128;
+    st = make_tensor_map_2d_u8(&mw, const_cast<uint8_t *>(qw), n, k / 2, ldqw, 128,
+                               static_cast<uint32_t>(bn), CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != KQ_OK) return st;
     GemmArgs g;
     g.m = m;
@@ -703,19 +808,10 @@ kq_status launch_w4a4_mxf4(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, 
     g.c = c;
     g.ldc = ldc;
     g.mtiles = (m + 127) / 128;
-    g.ntiles = (n + 127) / 128;
+    g.ntiles = (n + bn - 1) / bn;
     g.ksteps = (k + kXBK - 1) / kXBK;
-    static GSlot slot;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
-    std::call_once(slot.once[dev], [&] {
-        slot.err[dev] = cudaFuncSetAttribute(w4a4_mxf4_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kXSmemBytes);
-    });
-    if (slot.err[dev] != cudaSuccess) return KQ_ERR_CUDA;
-    const int64_t tiles = g.mtiles * g.ntiles;
-    const int grid = static_cast<int>(std::min<int64_t>(tiles, info.sm_count));
-    return launch_pdl(w4a4_mxf4_kernel, grid, 192, static_cast<size_t>(kXSmemBytes), stream, ma, mw, g);
+    return wide ? launch_mxf4_t<2>(ma, mw, g, info.sm_count, stream)
+                : launch_mxf4_t<1>(ma, mw, g, info.sm_count, stream);
 }
 
 }  // namespace
@@ -739,7 +835,9 @@ kq_status launch_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, 
                            int64_t ldqw, const uint8_t *sfw, int64_t m, int64_t n, int64_t k,
                            float *c, int64_t ldc, int variant, cudaStream_t stream)
 {
-    if (variant == 0) return launch_w4a4_mxf4(qa, ldqa, sfa, qw, ldqw, sfw, m, n, k, c, ldc, stream);
+    if (variant == 0) return launch_w4a4_mxf4(qa, ldqa, sfa, qw, ldqw, sfw, m, n, k, c, ldc, -1, stream);
+    if (variant == 2 || variant == 3)
+        return launch_w4a4_mxf4(qa, ldqa, sfa, qw, ldqw, sfw, m, n, k, c, ldc, variant - 2, stream);
     DeviceInfo info;
     kq_status st = device_info(info);
     if (st != KQ_OK) return st;

@@ -305,13 +305,15 @@ def _gemm_out(m, n, device):
 
 GEMM_MXF4 = 0
 GEMM_DEQUANT_BF16 = 1
+GEMM_MXF4_NARROW = 2
+GEMM_MXF4_WIDE = 3
 
 
 def kq_w4a4_gemm(qa, sfa, qw, sfw, m: int, n: int, k: int, c=None, variant: int | None = None,
                  stream=None):
     """C = deq(qa) deq(qw)^T (fp32 [m, n]) from packed codes and 128x4 tiled
-    scales, on the tensor cores (``variant``: GEMM_MXF4 or GEMM_DEQUANT_BF16;
-    None = the library's default)."""
+    scales, on the tensor cores (``variant``: GEMM_MXF4, GEMM_DEQUANT_BF16,
+    GEMM_MXF4_NARROW or GEMM_MXF4_WIDE; None = the library's default)."""
     if c is None:
         c = _gemm_out(m, n, qa.device)
     args = (_ptr(qa), _ld(qa, k // 2), _ptr(sfa), _ptr(qw), _ld(qw, k // 2), _ptr(sfw), m, n, k,
