@@ -378,16 +378,20 @@ __global__ void __launch_bounds__(kGThreads, 1)
 //   128-byte swizzle), the two 128x4 scale tiles of A and the 2 NH of W that
 //   cover the stage's 8 blocks (bulk copies of the tiled layout, unchanged);
 //   TMEM: 256 accumulator columns -- two 128-column buffers for NH = 1, one
-//   256-column buffer for NH = 2 (W rows 128 h .. + 127 -> columns 128 h ..,
-//   one N = 128 instruction each) -- then 8 + 8 NH columns per stage for the
-//   scales (tcgen05.cp 32x128b.warpx4 puts tile row r -- the scales of rows
-//   r, r + 32, r + 64, r + 96 -- into lane r of every lane quarter).
-// Issuing costs more than executing at this size (a commit is worth several
-// instructions), so the wide tile halves the scale copies and commits per
-// flop; its single accumulator cannot overlap the epilogue with the next
-// tile, which pays only when K is long.
-// Roles: warp 0 producer, warp 1 MMA issuer, 4 NH epilogue warps: NH per TMEM
-// lane quarter, 128 columns each, read their part of the accumulator into
+//   256-column buffer for NH = 2 (one N = 256 instruction per K = 64, W row j
+//   -> column j) -- then 8 + 8 NH columns per stage for the scales: A tile at
+//   at column 4 at; W half h tile at at 8 + 4 (NH at + h) (tcgen05.cp
+//   32x128b.warpx4 puts tile row r -- the scales of rows r, r + 32, r + 64,
+//   r + 96 -- into lane r of every lane quarter; an N = 256 instruction reads
+//   W rows 128-255 from the 4 columns after rows 0-127).
+// Every tcgen05 instruction costs its issuing thread tens of nanoseconds, and
+// different threads issue in parallel, so the design keeps the instructions
+// per flop low (N = 256 instructions, stages released in pairs by one commit)
+// and spreads them over threads.
+// Roles: warp 0 producer, warp 1 MMA issuer, warps 2-3 scale copiers (the
+// tcgen05.cp of a stage, dealt alternately to two threads, ahead of the MMAs,
+// reported on sf_ready[s] by a commit from each), 4 NH epilogue warps: NH per
+// TMEM lane quarter, 128 columns each, read their part of the accumulator into
 // registers and release it before they store, so the next tile's MMAs start
 // while the stores drain.
 
@@ -400,7 +404,7 @@ template <int NH>
 struct XCfg {
     static constexpr int kBN = 128 * NH;                  // tile width (C columns, W rows)
     static constexpr int kStages = 4;
-    static constexpr int kThreads = 64 + 128 * NH;
+    static constexpr int kThreads = 128 + 128 * NH;       // producer, MMA, 2 copiers, epilogue
     static constexpr int kAccBufs = NH == 1 ? 2 : 1;
     static constexpr int kWCodeBytes = kBN * 128;
     static constexpr int kSfaOff = kXACodeBytes + kWCodeBytes;
@@ -410,12 +414,14 @@ struct XCfg {
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;
     static constexpr uint32_t kSfStride = 8 + 8 * NH;     // TMEM scale columns per stage
     static_assert(kStageBytes % 1024 == 0, "stages keep the 1 KB alignment of the swizzle");
+    static_assert(kStages % 2 == 0, "stages are released in pairs");
     static_assert(kXSfCol + kSfStride * kStages <= kXTmemCols, "scale columns fit in TMEM");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 };
 
 // Shared-memory descriptor of a no-swizzle K-major matrix: core matrices of
-// 8 rows x 16 bytes, SBO = distance between 8-row groups.
+// 8 rows x 16 bytes, SBO = distance between 8-row groups (one 16-byte chunk
+// per row here, so the chunk stride is unused).
 __device__ __forceinline__ uint64_t x_desc_noswz(uint32_t saddr, uint32_t sbo)
 {
     return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(16 >> 4) << 16) |
@@ -460,8 +466,8 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     const uint32_t bar = base + C::kBarOff;
-    const uint32_t full = bar, empty = bar + 8 * kXStages;
-    const uint32_t acc_full = bar + 16 * kXStages, acc_empty = acc_full + 16;
+    const uint32_t full = bar, empty = bar + 8 * kXStages, sf_ready = bar + 16 * kXStages;
+    const uint32_t acc_full = bar + 24 * kXStages, acc_empty = acc_full + 16;
     const uint32_t tmem_slot = acc_empty + 16;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles = g.mtiles * g.ntiles;
@@ -473,6 +479,7 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
         for (int s = 0; s < kXStages; ++s) {
             mbar_init(full + 8 * s, 1);
             mbar_init(empty + 8 * s, 1);
+            mbar_init(sf_ready + 8 * s, 2);           // one commit per scale copier
         }
         for (int b = 0; b < C::kAccBufs; ++b) {
             mbar_init(acc_full + 8 * b, 1);
@@ -496,8 +503,10 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
                 const int64_t mt = t / g.ntiles, nt = t % g.ntiles;
                 for (int64_t ks = 0; ks < g.ksteps; ++ks, ++kk) {
                     const int s = static_cast<int>(kk % kXStages);
+                    // stages are released in pairs (s, s + 1 for even s): one
+                    // commit per pair, on the pair's barrier
                     if (kk >= kXStages &&
-                        !mbar_wait(empty + 8 * s, static_cast<uint32_t>(((kk / kXStages) - 1) & 1))) {
+                        !mbar_wait(empty + 8 * (s >> 1), static_cast<uint32_t>(((kk / kXStages) - 1) & 1))) {
                         ok = false;
                         break;
                     }
@@ -528,84 +537,96 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
                                 static_cast<uint32_t>((j / kXStages) & 1));
         }
     } else if (warp == 1) {
-        int64_t kk = 0, tc = 0;
-        bool ok = true;
-        // an odd block count leaves one padding block inside the last
-        // instruction: its scale bytes are set to 2^0 before use
-        const bool pad_fix = (g.nb & 1) != 0;
-        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc) {
-            // accumulator buffer b of tile tc is free once the epilogue has
-            // read tile tc - kAccBufs from it
-            const int b = static_cast<int>(tc % C::kAccBufs);
-            const int64_t use = tc / C::kAccBufs;
-            if (use >= 1)
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(acc_empty + 8 * b, static_cast<uint32_t>((use - 1) & 1)));
-            for (int64_t ks = 0; ks < g.ksteps && ok; ++ks, ++kk) {
-                const int s = static_cast<int>(kk % kXStages);
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(full + 8 * s, static_cast<uint32_t>((kk / kXStages) & 1)));
-                if (!ok) break;
-                const int64_t rem = (g.k - ks * kXBK + 63) / 64;
-                const int nmma = rem < 4 ? static_cast<int>(rem) : 4;
-                const uint32_t st = base + s * kXStageBytes;
-                const uint32_t sfa_s = st + kXSfaOff, sfw_s = st + kXSfwOff;
-                if (pad_fix && ks == g.ksteps - 1) {
-                    const int kb = static_cast<int>(g.nb - 8 * ks);     // padding block, local index
-                    const uint32_t off = static_cast<uint32_t>((kb >> 2) * 512 + lane * 16 + (kb & 3));
-#pragma unroll
-                    for (int grp = 0; grp < 4; ++grp) {
-                        asm volatile("st.shared.u8 [%0], %1;" ::"r"(sfa_s + off + 4 * grp), "r"(127u) : "memory");
-                        asm volatile("st.shared.u8 [%0], %1;" ::"r"(sfw_s + off + 4 * grp), "r"(127u) : "memory");
-                        if (NH == 2)
-                            asm volatile("st.shared.u8 [%0], %1;" ::"r"(sfw_s + 1024 + off + 4 * grp),
-                                         "r"(127u)
-                                         : "memory");
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
-                g_fence_after();
-                if (lane == 0) {
-                    // TMEM scale columns of stage s: A tile at at 4 at, W half h
-                    // tile at at 8 + 4 (NH at + h).  Descriptors advance in
-                    // 16-byte units: +2 = the next 32 bytes of codes (K = 64),
-                    // +32 = the next 512-byte scale tile, +1024 = the next 128
-                    // rows of W.
+        // MMA issuer: one thread, no warp-wide votes or syncs per stage
+        if (lane == 0) {
+            int64_t kk = 0, tc = 0;
+            bool ok = true;
+            constexpr uint32_t id0 = x_idesc(0), id2 = x_idesc(2);
+            constexpr uint32_t kIdN = static_cast<uint32_t>((NH - 1) * (128 >> 3)) << 17;  // N += 128
+            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc) {
+                // accumulator buffer b of tile tc is free once the epilogue has
+                // read tile tc - kAccBufs from it
+                const int b = static_cast<int>(tc % C::kAccBufs);
+                const int64_t use = tc / C::kAccBufs;
+                if (use >= 1) ok = mbar_wait(acc_empty + 8 * b, static_cast<uint32_t>((use - 1) & 1));
+                const uint32_t acc = tmem_base + 128 * b;
+                for (int64_t ks = 0; ks < g.ksteps && ok; ++ks, ++kk) {
+                    const int s = static_cast<int>(kk % kXStages);
+                    const uint32_t par = static_cast<uint32_t>((kk / kXStages) & 1);
+                    ok = mbar_wait(sf_ready + 8 * s, par) && mbar_wait(full + 8 * s, par);
+                    if (!ok) break;
+                    g_fence_after();
+                    const int64_t rem = (g.k - ks * kXBK + 63) / 64;
+                    const int nmma = rem < 4 ? static_cast<int>(rem) : 4;
+                    const uint32_t st = base + s * kXStageBytes;
+                    // descriptors advance in 16-byte units: +2 = the next 32
+                    // bytes of codes (K = 64)
                     const uint32_t sft = tmem_base + kXSfCol + kXSfStride * s;
-                    const uint32_t acc = tmem_base + 128 * b;
                     const uint64_t da = g_desc(st), db = g_desc(st + kXACodeBytes);
-                    const uint64_t dsa = x_desc_noswz(sfa_s, 128), dsw = x_desc_noswz(sfw_s, 128);
-                    constexpr uint32_t id0 = x_idesc(0), id2 = x_idesc(2);
-                    for (int at = 0; at < (nmma + 1) / 2; ++at) {
-                        x_cp_sf(sft + 4 * at, dsa + 32 * at);
-#pragma unroll
-                        for (int hh = 0; hh < NH; ++hh)
-                            x_cp_sf(sft + 8 + 4 * (NH * at + hh), dsw + 64 * hh + 32 * at);
-                        for (int j = 2 * at; j < 2 * at + 2 && j < nmma; ++j) {
-                            const uint32_t id = (j & 1) ? id2 : id0;
-                            const uint32_t accum = (ks > 0 || j > 0) ? 1u : 0u;
-#pragma unroll
-                            for (int hh = 0; hh < NH; ++hh)
-                                x_mma(acc + 128 * hh, da + 2 * j, db + 1024 * hh + 2 * j, id, sft + 4 * at,
-                                      sft + 8 + 4 * (NH * at + hh), accum);
-                        }
-                    }
-                    g_commit(empty + 8 * s);
+                    for (int j = 0; j < nmma; ++j)
+                        x_mma(acc, da + 2 * j, db + 2 * j, ((j & 1) ? id2 : id0) + kIdN, sft + 4 * (j >> 1),
+                              sft + 8 + 4 * (NH * (j >> 1)), (ks > 0 || j > 0) ? 1u : 0u);
+                    if (kk & 1) g_commit(empty + 8 * (s >> 1));
                     if (ks == g.ksteps - 1) g_commit(acc_full + 8 * b);
                 }
-                __syncwarp();
+            }
+            if (tc >= 1 && ok) {
+                const int64_t last = tc - 1;
+                (void)mbar_wait(acc_full + 8 * static_cast<int>(last % C::kAccBufs),
+                                static_cast<uint32_t>((last / C::kAccBufs) & 1));
             }
         }
-        if (tc >= 1 && ok) {
-            const int64_t last = tc - 1;
-            (void)mbar_wait(acc_full + 8 * static_cast<int>(last % C::kAccBufs),
-                            static_cast<uint32_t>((last / C::kAccBufs) & 1));
+        __syncwarp();
+    } else if (warp < 4) {
+        // scale copiers: the copies of a stage (per scale tile at: A, then W's
+        // halves) are dealt alternately to the two threads, which issue them
+        // in parallel with the MMAs and report on sf_ready[s] with a commit.
+        // An odd block count leaves one padding block inside the last
+        // instruction: a copier sets its scale bytes to 2^0 before the copy.
+        if (lane == 0) {
+            const int cid = warp - 2;
+            const bool pad_fix = (g.nb & 1) != 0;
+            int64_t kk = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                for (int64_t ks = 0; ks < g.ksteps; ++ks, ++kk) {
+                    const int s = static_cast<int>(kk % kXStages);
+                    ok = mbar_wait(full + 8 * s, static_cast<uint32_t>((kk / kXStages) & 1));
+                    if (!ok) break;
+                    g_fence_after();
+                    const int64_t rem = (g.k - ks * kXBK + 63) / 64;
+                    const int nmma = rem < 4 ? static_cast<int>(rem) : 4;
+                    const uint32_t st = base + s * kXStageBytes;
+                    const uint32_t sft = tmem_base + kXSfCol + kXSfStride * s;
+                    const int pad_kb = (pad_fix && ks == g.ksteps - 1) ? static_cast<int>(g.nb - 8 * ks) : -1;
+                    int e = 0;
+                    for (int at = 0; at < (nmma + 1) / 2; ++at)
+                        for (int r = 0; r <= NH; ++r, ++e) {
+                            if ((e & 1) != cid) continue;
+                            // region r: 0 = A, 1 + h = half h of W
+                            const uint32_t src = (r == 0 ? st + kXSfaOff : st + kXSfwOff + 1024 * (r - 1)) + 512 * at;
+                            const uint32_t dst = r == 0 ? sft + 4 * at : sft + 8 + 4 * (NH * at + r - 1);
+                            if (pad_kb >= 0 && (pad_kb >> 2) == at) {
+                                // byte (kb % 4) of word grp of each 16-byte row
+                                for (int row = 0; row < 32; ++row)
+#pragma unroll
+                                    for (int grp = 0; grp < 4; ++grp)
+                                        asm volatile("st.shared.u8 [%0], %1;"
+                                                     ::"r"(src + 16 * row + 4 * grp + (pad_kb & 3)), "r"(127u)
+                                                     : "memory");
+                                fence_proxy_async_smem();
+                            }
+                            x_cp_sf(dst, x_desc_noswz(src, 128));
+                        }
+                    g_commit(sf_ready + 8 * s);
+                }
+            }
         }
+        __syncwarp();
     } else {
         // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 and the 128
-        // columns of half h = (w - 2) / 4 of the tile
-        const int qtr = warp & 3, h = (warp - 2) >> 2;
+        // columns of half h = (w - 4) / 4 of the tile
+        const int qtr = warp & 3, h = (warp - 4) >> 2;
         const int row_in = qtr * 32 + lane;
         int64_t tc = 0;
         for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
