@@ -71,10 +71,14 @@ def parse_args():
                     help="skip the diagonal / Hadamard / bare-quantizer side measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU time budget of the oracle baseline sample")
-    ap.add_argument("--profile", choices=("kroquant", "dual", "diag", "hadamard", "identity"),
+    ap.add_argument("--gemm", action="store_true",
+                    help="table of the W4A4 consumer product (kind::mxf4) on the layer shapes")
+    ap.add_argument("--profile", choices=("kroquant", "dual", "diag", "hadamard", "identity",
+                                          "gemm"),
                     help="profiling case for ncu: run one quantizer a few times and exit")
     ap.add_argument("--m", type=int, default=9216, help="rows of the profiling case")
     ap.add_argument("--d", type=int, default=12288, help="channels of the profiling case")
+    ap.add_argument("--n", type=int, default=3072, help="output channels of the gemm profiling case")
     ap.add_argument("--launches", type=int, default=3, help="launches of the profiling case")
     ap.add_argument("--table", action="store_true",
                     help="per-launch medians of every kernel on every config shape (markdown)")
@@ -140,6 +144,61 @@ def hbm_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def fp4_peak():
+    """Dense FP4 tensor peak: the measured bf16 GEMM rate times the nominal
+    FP4 / bf16 ratio of the part (13.5 / 2.25 PFLOP/s)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]) * 6.0, "measured bf16 x 6"
+    except (OSError, KeyError, ValueError):
+        return 1900.0 * 6.0, "fallback bf16 x 6"
+
+
+def gemm_case(m: int, n: int, k: int, seed: int, dev):
+    """Operands of an m x n x k W4A4 product: random packed codes and E8M0
+    bytes in [118, 136] (tiled layout), plus bf16 A and W of the same shapes
+    for the reference product."""
+    import numpy as np
+    import torch
+    from w4a4_mxfp4_activation_gb300 import kq, synth
+    qa = torch.from_numpy(synth.packed_codes(m, k, seed)).to(dev)
+    qw = torch.from_numpy(synth.packed_codes(n, k, seed + 1)).to(dev)
+    sfa = torch.from_numpy(synth.scale_bytes(kq.kq_sf_bytes(m, k, 1), 1, seed + 2, 118, 136)
+                           .reshape(-1)).to(dev)
+    sfw = torch.from_numpy(synth.scale_bytes(kq.kq_sf_bytes(n, k, 1), 1, seed + 3, 118, 136)
+                           .reshape(-1)).to(dev)
+    a = torch.from_numpy(synth.activations(m, k, seed + 4, "flux").view(np.int16)).to(dev) \
+        .view(torch.bfloat16)
+    w = torch.from_numpy(synth.weights(n, k, seed + 5).view(np.int16)).to(dev).view(torch.bfloat16)
+    return qa, sfa, qw, sfw, a, w
+
+
+def time_launches(fn, stream, reps: int = 20, rounds: int = 5) -> float:
+    """Median over `rounds` CUDA-event brackets of `reps` back-to-back calls
+    (a CUDA graph of them) on `stream`: microseconds per call."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                fn()
+        g.replay()
+        stream.synchronize()
+        out = []
+        for _ in range(rounds):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            stream.synchronize()
+            out.append(a.elapsed_time(b) * 1e3 / reps)
+    return statistics.median(out)
 
 
 def kernel_source_hash() -> str:
@@ -494,6 +553,33 @@ def run_ours(args, dist: Dist):
             name = f"kroquant_{kind}" if kind in ("mma", "butterfly", "umma") else kind
             baselines[name] = round(STEP_BYTES * nb_steps / (dist.max(bms) * 1e-3) / 1e9, 2)
 
+    # ---- the consumer of the quantizer's output: the W4A4 product of the
+    #      FFN-down layer (A_q: this step's quantized activations, 4608 x
+    #      12288; W_q: 3072 x 12288 random codes and scales) on the FP4 tensor
+    #      cores, with the bf16-dequantization route and the bf16 reference
+    #      product A W^T for context
+    consumer = None
+    if not args.no_baselines:
+        gm, gn, gk = dom_m, 3072, dom_d
+        _, _, qw, sfw, ga, gw = gemm_case(gm, gn, gk, 9000 + dist.rank, dev)
+        cq = torch.empty((gm, gn), dtype=torch.float32, device=dev)
+        qa, sfa = Q[DOMINANT][0], SF[DOMINANT][0]
+        us_fp4 = time_launches(lambda: kq.kq_w4a4_gemm(qa, sfa, qw, sfw, gm, gn, gk, c=cq,
+                                                       stream=stream), stream)
+        us_deq = time_launches(lambda: kq.kq_w4a4_gemm(qa, sfa, qw, sfw, gm, gn, gk, c=cq,
+                                                       variant=kq.GEMM_DEQUANT_BF16,
+                                                       stream=stream), stream, reps=4, rounds=3)
+        us_ref = time_launches(lambda: kq.kq_bf16_gemm(ga, gw, c=cq, stream=stream), stream)
+        flops = 2.0 * gm * gn * gk
+        fpeak, fsrc = fp4_peak()
+        consumer = {"metric": "kq_w4a4_gemm TFLOP/s (kind::mxf4, C = A_q W_q^T, fp32 out)",
+                    "shape": f"{gm}x{gn}x{gk}", "us": round(us_fp4, 2),
+                    "tflops": round(flops / us_fp4 / 1e6, 1), "peak_tflops": round(fpeak, 1),
+                    "frac": round(flops / us_fp4 / 1e6 / fpeak, 4), "peak_source": fsrc,
+                    "dequant_bf16_us": round(us_deq, 2), "bf16_reference_us": round(us_ref, 2)}
+        del cq, qw, sfw, ga, gw
+        torch.cuda.empty_cache()
+
     # ---- end to end through the public call with host buffers
     e2e_steps = max(3, min(K, 100))
     host_q = [torch.empty(Q[li][0].shape, dtype=torch.uint8).pin_memory() for li in range(2)]
@@ -577,6 +663,7 @@ def run_ours(args, dist: Dist):
             if baselines.get("diag") else None,
             "baselines_gbs": baselines,
             "side_output": side,
+            "consumer_gemm": consumer,
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": K * len(LAYERS),
@@ -605,6 +692,15 @@ def run_profile_case(args):
     at = torch.empty((m, d), dtype=torch.bfloat16, device="cuda") if args.profile == "dual" else None
     variant = {"butterfly": kq.VARIANT_BUTTERFLY, "mma": kq.VARIANT_MMA,
                "umma": kq.VARIANT_UMMA}[args.variant]
+    if args.profile == "gemm":
+        n = args.n
+        qa, sfa, qw, sfw, _, _ = gemm_case(m, n, d, 9000, "cuda")
+        c = torch.empty((m, n), dtype=torch.float32, device="cuda")
+        for _ in range(args.launches):
+            kq.kq_w4a4_gemm(qa, sfa, qw, sfw, m, n, d, c=c)
+        torch.cuda.synchronize()
+        print(f"profile case done: gemm m={m} n={n} k={d} launches={args.launches}")
+        return
     for _ in range(args.launches):
         if args.profile == "kroquant":
             kq.kq_quantize_mxfp4(A, d, factors=F if KX is None else None, K_expanded=KX,
@@ -801,8 +897,57 @@ def run_table(args):
           f"CUDA graphs of max(sets, 32) launches, median over up to {args.table_reps} replays")
 
 
+GEMM_TABLE = (
+    ("cfg0 projection", 256, 1152, 1152),
+    ("PixArt-Sigma FFN up", 4096, 4608, 1152),
+    ("PixArt-Sigma FFN down", 4096, 1152, 4608),
+    ("SANA FFN up", 4096, 5600, 2240),
+    ("SANA FFN down", 4096, 2240, 5600),
+    ("FLUX projection", 4608, 3072, 3072),
+    ("FLUX FFN up", 4608, 12288, 3072),
+    ("FLUX FFN down", 4608, 3072, 12288),
+)
+
+
+def run_gemm_table(args):
+    """The W4A4 product C = A_q W_q^T on the layer shapes (m tokens, n output
+    channels, k input channels): the FP4 tensor-core kernel, the bf16
+    dequantization route, the bf16 reference product A W^T of this library and
+    of cuBLAS (torch.matmul)."""
+    import torch
+    from w4a4_mxfp4_activation_gb300 import kq
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    fpeak, fsrc = fp4_peak()
+    print(f"| layer | m x n x k | kind::mxf4 us | TFLOP/s | % of FP4 peak ({fpeak:.0f}, {fsrc}) | "
+          "dequant-bf16 us | bf16 reference us | cuBLAS bf16 us | mxf4 / cuBLAS bf16 |")
+    print("|" + "---|" * 9)
+    for name, m, n, k in GEMM_TABLE:
+        qa, sfa, qw, sfw, a, w = gemm_case(m, n, k, 9100, dev)
+        c = torch.empty((m, n + (-n) % 4), dtype=torch.float32, device=dev)[:, :n]
+        t4 = time_launches(lambda: kq.kq_w4a4_gemm(qa, sfa, qw, sfw, m, n, k, c=c, stream=stream),
+                           stream)
+        td = time_launches(lambda: kq.kq_w4a4_gemm(qa, sfa, qw, sfw, m, n, k, c=c,
+                                                   variant=kq.GEMM_DEQUANT_BF16, stream=stream),
+                           stream, reps=4, rounds=3)
+        tb = time_launches(lambda: kq.kq_bf16_gemm(a, w, c=c, stream=stream), stream)
+        tc = time_launches(lambda: torch.matmul(a, w.t()), stream)
+        tf = 2.0 * m * n * k / t4 / 1e6
+        print(f"| {name} | {m}x{n}x{k} | {t4:.2f} | {tf:.0f} | {100 * tf / fpeak:.1f} | {td:.1f} | "
+              f"{tb:.2f} | {tc:.2f} | {tc / t4:.2f} |", flush=True)
+        del qa, sfa, qw, sfw, a, w, c
+        torch.cuda.empty_cache()
+    print("\nmedian of 5 replays of a CUDA graph of 20 launches (4 for dequant-bf16), same stream; "
+          "operands resident, random codes and scales")
+
+
 def main():
     args = parse_args()
+    if args.gemm:
+        from w4a4_mxfp4_activation_gb300 import build
+        build.build()
+        run_gemm_table(args)
+        return
     if args.cpu_rate:
         m, d, sec = args.cpu_rate
         rate, rows = oracle_rate_shape(m, d, float(sec))
