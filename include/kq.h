@@ -142,6 +142,26 @@ KQ_API kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d,
                                  float *y_debug, cudaStream_t stream);
 
 /*
+ * kq_quantize_mxfp4_shared -- kq_quantize_mxfp4 with one factor set shared
+ * by every 32-channel block, K_j = K for all j ([KQ] Sec. 3.5.1 on K2: "many
+ * column blocks share the same Kronecker factors", the case where storing
+ * the transform per block is wasted).
+ *   factors     device fp32 [5][2][2]: the shared G1..G5, or NULL
+ *   K_expanded  device, kq_expand_blocks(factors, 1, KQ_K_BF16X3, ...)
+ *               (kq_expanded_bytes(1, KQ_K_BF16X3) bytes), or NULL; with it
+ *               the transform runs on the tensor cores, otherwise the
+ *               butterfly applies `factors`.  One of the two is required
+ *               (KQ_ERR_NULL).
+ *   other arguments as kq_quantize_mxfp4; the result equals
+ *   kq_quantize_mxfp4 given the set repeated d/32 times.
+ */
+KQ_API kq_status kq_quantize_mxfp4_shared(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                          const float *factors, const void *K_expanded,
+                                          uint8_t *q, int64_t ldq, uint8_t *sf,
+                                          kq_sf_layout sf_layout, float *y_debug,
+                                          cudaStream_t stream);
+
+/*
  * kq_smooth_quantize_mxfp4 -- diagonal-scale baseline: T = diag(s),
  * y[i][c] = a[i][c] * s[c], then the same MXFP4 quantizer ([KQ] Sec. 4.4,
  * "Scale", per-channel scaling of SmoothQuant; a SmoothQuant user passes

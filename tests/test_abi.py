@@ -205,3 +205,16 @@ def test_gemm_argument_checks(L):
     assert e(c, 4, c, 8, 4, 8, vp(4096), None) == 2                      # ldc < n
     assert e(None, 8, c, 8, 4, 8, vp(4096), None) == 1
     assert e(c, 8, vp(20484), 8, 4, 8, vp(4096), None) == 3
+
+
+def test_shared_argument_checks(L):
+    """kq_quantize_mxfp4_shared needs the shared factors or their record;
+    nothing is launched when a check fails."""
+    vp = ctypes.c_void_p
+    A, q, sf, F = vp(4096), vp(8192), vp(12288), vp(16384)
+    f = L.kq_quantize_mxfp4_shared
+    assert f(A, 4, 64, 64, None, None, q, 32, sf, 0, None, None) == 1
+    assert f(A, 4, 64, 64, vp(16388), None, q, 32, sf, 0, None, None) == 3
+    assert f(A, 4, 64, 64, None, vp(16392), q, 32, sf, 0, None, None) == 3
+    assert f(A, 4, 48, 64, F, None, q, 32, sf, 0, None, None) == 2
+    assert f(A, 0, 64, 64, None, None, q, 32, sf, 0, None, None) == 0

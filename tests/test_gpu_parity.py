@@ -758,3 +758,38 @@ def test_w4a4_gemm_variants_agree_on_quantizer_output():
     Wq = O.dequantize(np_(qw), np_(sfw), 1, n, k)
     tol = 2 * gemm_tolerance(Aq, Wq, k)
     assert np.all(np.abs(c0 - c1) <= tol)
+
+
+# ------------------------------------------------------- shared factors --
+
+SHARED_SHAPES = [(256, 1152), (300, 2240), (7, 96), (129, 5600)]
+
+
+@pytest.mark.parametrize("path", ["umma", "butterfly"])
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("m,d", SHARED_SHAPES, ids=[f"{m}x{d}" for m, d in SHARED_SHAPES])
+def test_shared_factors(m, d, layout, path):
+    """One factor set for every block: parity with the oracle given the set
+    repeated d/32 times (rules i-iii), and the same bytes as the per-block
+    entry point given that repeated set."""
+    nb = d // 32
+    A_bits = synth.activations(m, d, 1700 + m, "sana")
+    lu = synth.lu_params(1, 1701)
+    F1 = kq.kq_lu_to_factors(lu, +1)                          # [1, 5, 2, 2]
+    Fo = np.broadcast_to(O.lu_to_factors(lu.astype(np.float64), +1).astype(np.float32)
+                         .astype(np.float64), (nb, 5, 2, 2))
+    A = to_bf16(A_bits)
+    if path == "umma":
+        rec = kq.kq_expand_blocks(dev(F1), kq.KQ_K_BF16X3)
+        q, sf, y = kq.kq_quantize_mxfp4_shared(A, d, K_expanded=rec, layout=layout, y_debug=True)
+        Frep = np.ascontiguousarray(np.broadcast_to(F1, (nb, 5, 2, 2)))
+        q2, sf2, _ = kq.kq_quantize_mxfp4(A, d, K_expanded=kq.kq_expand_blocks(dev(Frep), kq.KQ_K_BF16X3),
+                                          layout=layout, variant=kq.VARIANT_UMMA)
+    else:
+        q, sf, y = kq.kq_quantize_mxfp4_shared(A, d, factors=dev(F1[0]), layout=layout, y_debug=True)
+        Frep = np.ascontiguousarray(np.broadcast_to(F1, (nb, 5, 2, 2)))
+        q2, sf2, _ = kq.kq_quantize_mxfp4(A, d, factors=dev(Frep), layout=layout,
+                                          variant=kq.VARIANT_BUTTERFLY)
+    nbytes = kq.kq_sf_bytes(m, d, layout)
+    assert np.array_equal(np_(q), np_(q2)) and np.array_equal(np_(sf)[:nbytes], np_(sf2)[:nbytes])
+    parity.check(A_bits, d, "kron", np.ascontiguousarray(Fo), layout, np_(q), np_(sf), np_(y))

@@ -128,6 +128,7 @@ void fill_quant_params(QuantParams &p, int64_t m, int64_t d, int64_t rows_per_ti
     p.sf_layout = static_cast<int>(layout);
     p.ncb = (p.nb + 3) / 4;
     p.y_debug = y_debug;
+    p.shared_params = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -355,6 +356,27 @@ kq_status kq_layer_error(const float *c, int64_t ldc, const float *c_ref, int64_
             return KQ_ERR_ALIGN;
     }
     return launch_layer_error(c, ldc, c_ref, ldr, m, n, out, stream);
+}
+
+kq_status kq_quantize_mxfp4_shared(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                   const float *factors, const void *K_expanded, uint8_t *q,
+                                   int64_t ldq, uint8_t *sf, kq_sf_layout sf_layout,
+                                   float *y_debug, cudaStream_t stream)
+{
+    kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
+    if (st != KQ_OK) return st;
+    if (m == 0) return KQ_OK;
+    if (factors == nullptr && K_expanded == nullptr) return KQ_ERR_NULL;
+    if ((factors != nullptr && !aligned16(factors)) || (K_expanded != nullptr && !aligned16(K_expanded)))
+        return KQ_ERR_ALIGN;
+    DeviceInfo info;
+    if ((st = device_info(info)) != KQ_OK) return st;
+    QuantParams p;
+    fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
+    p.shared_params = 1;
+    if (K_expanded != nullptr) return launch_quant_umma(A, lda, K_expanded, p, nullptr, 0, stream);
+    p.factors = factors;
+    return launch_quant_tma(kKron, A, lda, p, stream);
 }
 
 kq_status kq_smooth_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,

@@ -34,6 +34,7 @@ struct QuantParams {
     int sf_layout;
     int64_t ncb;        // ceil(nb / 4), for the blocked layout
     float *y_debug;     // [m][d] or null
+    int shared_params;  // 1: every block takes block 0's factors / operand records
 };
 
 // Per-device facts the launchers need.

@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if constexpr (param_bytes_per_block<T>() > 0) {
                 const int64_t left = p.nb - ct * 4;
                 pbytes = static_cast<uint32_t>((left < 4 ? left : 4) * param_bytes_per_block<T>());
-                psrc = (T == kKron) ? static_cast<const void *>(p.factors + ct * 4 * 20)
+                psrc = (T == kKron) ? static_cast<const void *>(p.factors + (p.shared_params ? 0 : ct * 4 * 20))
                                     : static_cast<const void *>(p.s + ct * 4 * 32);
             }
             mbar_arrive_expect_tx(bar_full + 8 * s, Cfg::kABytes + pbytes);
@@ -208,7 +208,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             tma_load_2d(dst + Cfg::kBoxBytes, &tmA, static_cast<int32_t>(ct * 128 + 64),
                         static_cast<int32_t>(rt * BR), bar_full + 8 * s, pol);
             if constexpr (param_stride<T>() == param_bytes_per_block<T>()) {
-                if (pbytes) bulk_load(dst + Cfg::kABytes, psrc, pbytes, bar_full + 8 * s);
+                if (T == kKron && p.shared_params) {
+                    // one factor set for every block: a copy of it per block slot
+                    const uint32_t per = param_bytes_per_block<T>();
+                    for (uint32_t off = 0; off < pbytes; off += per)
+                        bulk_load(dst + Cfg::kABytes + off, psrc, per, bar_full + 8 * s);
+                } else if (pbytes) {
+                    bulk_load(dst + Cfg::kABytes, psrc, pbytes, bar_full + 8 * s);
+                }
             } else {
                 // one copy per block into its padded slot
                 const uint32_t per = param_bytes_per_block<T>();

@@ -223,9 +223,14 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             static_cast<uint32_t>((left < 0 ? 0 : (left < 2 ? left : 2)) * Cfg::kRecBytes);
         mbar_arrive_expect_tx(bar_full + 8 * s, Cfg::kABytes + rbytes);
         tma_load_2d(dst, &tmA, pw.ct * 64, pw.rt * kBR, bar_full + 8 * s, pol);
-        if (rbytes)
+        if (p.shared_params) {
+            // one operand record for every block: a copy of it per block slot
+            for (uint32_t off = 0; off < rbytes; off += Cfg::kRecBytes)
+                bulk_load(dst + Cfg::kBOff + off, records, Cfg::kRecBytes, bar_full + 8 * s);
+        } else if (rbytes) {
             bulk_load(dst + Cfg::kBOff, records + static_cast<int64_t>(pw.ct) * 2 * Cfg::kRecBytes,
                       rbytes, bar_full + 8 * s);
+        }
         pw.next();
         ++pit;
     };

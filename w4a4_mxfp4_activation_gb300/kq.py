@@ -35,7 +35,7 @@ EXPORTS = (
     "kq_status_string", "kq_lu_to_factors", "kq_invert_transpose_factors",
     "kq_quantize_mxfp4_variant", "kq_test_encode_e2m1", "kq_quantize_mxfp4_dual",
     "kq_fwht_quantize_mxfp4", "kq_w4a4_gemm", "kq_w4a4_gemm_variant", "kq_bf16_gemm",
-    "kq_layer_error",
+    "kq_layer_error", "kq_quantize_mxfp4_shared",
 )
 
 
@@ -69,6 +69,9 @@ def lib() -> ctypes.CDLL:
             L.kq_quantize_mxfp4_dual.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, st, vp, i64,
                                                  vp, vp]
             L.kq_quantize_mxfp4_dual.restype = st
+            L.kq_quantize_mxfp4_shared.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64, vp, st, vp,
+                                                   vp]
+            L.kq_quantize_mxfp4_shared.restype = st
             L.kq_smooth_quantize_mxfp4.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, st, vp, vp]
             L.kq_smooth_quantize_mxfp4.restype = st
             L.kq_hadamard_quantize_mxfp4.argtypes = [vp, i64, i64, i64, vp, i64, vp, st, vp, vp]
@@ -217,6 +220,24 @@ def kq_quantize_mxfp4_dual(A, K_expanded, d: int | None = None, layout: int = KQ
                                         _stream(stream)),
            "kq_quantize_mxfp4_dual")
     return q, sf, at, y_debug
+
+
+def kq_quantize_mxfp4_shared(A, d: int | None = None, factors=None, K_expanded=None,
+                             layout: int = KQ_SF_ROWMAJOR, q=None, sf=None, y_debug=None,
+                             stream=None):
+    """Quantize A with one factor set ([5, 2, 2] fp32 CUDA tensor, or its
+    expanded record from kq_expand_blocks(factors[None], KQ_K_BF16X3)) shared
+    by every block.  Returns (q, sf, y_debug)."""
+    A = _bf16_bits(A)
+    m, lda = A.shape
+    d = lda if d is None else d
+    q, sf, y_debug = _outputs(A, m, d, layout, q, sf, y_debug)
+    ldq = q.shape[1] if q.dim() == 2 else d // 2
+    _check(lib().kq_quantize_mxfp4_shared(_ptr(A), m, d, A.stride(0), _ptr(factors),
+                                          _ptr(K_expanded), _ptr(q), ldq, _ptr(sf), layout,
+                                          _ptr(y_debug), _stream(stream)),
+           "kq_quantize_mxfp4_shared")
+    return q, sf, y_debug
 
 
 def kq_smooth_quantize_mxfp4(A, s, d: int | None = None, layout: int = KQ_SF_ROWMAJOR, q=None,
