@@ -90,6 +90,21 @@ typedef enum kq_kfmt {
                            plus G1 in fp32) */
 } kq_kfmt;
 
+/* Input formats of kq_quantize_mxfp4_ex: A holds bf16 or fp16 bit patterns. */
+typedef enum {
+    KQ_IN_BF16 = 0,
+    KQ_IN_F16 = 1
+} kq_in_format;
+
+/* Transforms of kq_quantize_mxfp4_ex (the CUDA-core kernels). */
+typedef enum {
+    KQ_TRANSFORM_KRON = 0,      /* eq. (12) from the raw factors (butterfly) */
+    KQ_TRANSFORM_DIAG = 1,      /* y = a * s[c] */
+    KQ_TRANSFORM_HADAMARD = 2,  /* H32 / sqrt(32) per block */
+    KQ_TRANSFORM_IDENTITY = 3,  /* the bare quantizer */
+    KQ_TRANSFORM_FWHT = 4       /* H_d / sqrt(d) over the row */
+} kq_transform;
+
 /* Alignment rules shared by the quantizer entry points:
  *   A, q, sf, y_debug, factors, s, K_expanded: 16-byte aligned;
  *   lda % 8 == 0 (16-byte row pitch), ldq % 16 == 0. */
@@ -160,6 +175,25 @@ KQ_API kq_status kq_quantize_mxfp4_shared(const uint16_t *A, int64_t m, int64_t 
                                           uint8_t *q, int64_t ldq, uint8_t *sf,
                                           kq_sf_layout sf_layout, float *y_debug,
                                           cudaStream_t stream);
+
+/*
+ * kq_quantize_mxfp4_ex -- the CUDA-core quantizers with the input format
+ * chosen: bf16, or fp16 as PixArt-Sigma runs and as [KQ] times its kernels
+ * (Sec. 4.1 "Data format", Sec. 4.4: FP16 activations).  fp16 values enter
+ * the transform exactly (every fp16 is an fp32).
+ *   A          device, [m][lda] 16-bit patterns in in_format
+ *   transform  KQ_TRANSFORM_*; param = factors [d/32][5][2][2] (KRON) or
+ *              s [d] (DIAG), device fp32, 16-byte aligned; NULL otherwise
+ *              (ignored).  FWHT needs a power-of-two d in [128, 16384].
+ *   other arguments as kq_quantize_mxfp4.  An unknown format or transform
+ *   gives KQ_ERR_LAYOUT.  The tensor-core path (kq_quantize_mxfp4 with
+ *   K_expanded) reads bf16 only: its MMA takes both operands in one type.
+ */
+KQ_API kq_status kq_quantize_mxfp4_ex(const uint16_t *A, kq_in_format in_format, int64_t m,
+                                      int64_t d, int64_t lda, kq_transform transform,
+                                      const float *param, uint8_t *q, int64_t ldq, uint8_t *sf,
+                                      kq_sf_layout sf_layout, float *y_debug,
+                                      cudaStream_t stream);
 
 /*
  * kq_smooth_quantize_mxfp4 -- diagonal-scale baseline: T = diag(s),

@@ -47,6 +47,31 @@ static double bf16_bits_to_f64(uint16_t h)
 
 KQO_EXPORT double kqo_bf16_to_f64(uint16_t h) { return bf16_bits_to_f64(h); }
 
+/* IEEE 754 binary16: sign, 5-bit exponent with bias 15, 10-bit fraction;
+ * exponent 0 holds zero and the subnormals f * 2^-24, exponent 31 Inf/NaN. */
+static double f16_bits_to_f64(uint16_t h)
+{
+    int sign = h >> 15, e = (h >> 10) & 31, f = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);   /* (1 + f / 2^10) * 2^(e - 15) */
+    return sign ? -v : v;
+}
+
+KQO_EXPORT double kqo_f16_to_f64(uint16_t h) { return f16_bits_to_f64(h); }
+
+/* Format of the 16-bit activations the transforms read: 0 = bf16, 1 = fp16.
+ * Process-wide; the Python wrapper sets it around each call. */
+static int g_input_f16 = 0;
+
+KQO_EXPORT void kqo_set_input_format(int f16) { g_input_f16 = f16 != 0; }
+
+static double in_to_f64(uint16_t h) { return g_input_f16 ? f16_bits_to_f64(h) : bf16_bits_to_f64(h); }
+
 /* --- [KQ] Sec. 3.2, eq. (6): unit-|det| LU factor ----------------------------
  * lu = {a, b, c}; G = [[1,0],[c,1]] . [[a,b],[0,u22]] with
  *   u22 = -1/a  (det_sign = -1, the paper's form, eq. 6)
@@ -109,7 +134,7 @@ static void apply_dense_blocks(const uint16_t *A, int64_t m, int64_t d, int64_t 
         for (int64_t j = 0; j < nb; ++j) {
             const double *K = Kall + j * 1024;
             for (int r = 0; r < 32; ++r)
-                a[r] = bf16_bits_to_f64(A[i * lda + j * 32 + r]);
+                a[r] = in_to_f64(A[i * lda + j * 32 + r]);
             for (int c = 0; c < 32; ++c) {
                 double acc = 0.0, mag = 0.0;
                 for (int r = 0; r < 32; ++r) {
@@ -172,7 +197,7 @@ KQO_EXPORT void kqo_transform_fwht(const uint16_t *A, int64_t m, int64_t d, int6
         double *v = y + i * d;
         double l1 = 0.0;
         for (int64_t c = 0; c < d; ++c) {
-            v[c] = bf16_bits_to_f64(A[i * lda + c]);
+            v[c] = in_to_f64(A[i * lda + c]);
             l1 += fabs(v[c]);
         }
         for (int64_t h = 1; h < d; h *= 2)
@@ -197,7 +222,7 @@ KQO_EXPORT void kqo_transform_diag(const uint16_t *A, int64_t m, int64_t d, int6
     #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < m; ++i)
         for (int64_t c = 0; c < d; ++c) {
-            double t = bf16_bits_to_f64(A[i * lda + c]) * s[c];
+            double t = in_to_f64(A[i * lda + c]) * s[c];
             y[i * d + c] = t;
             if (bound) bound[i * d + c] = fabs(t);
         }
@@ -210,7 +235,7 @@ KQO_EXPORT void kqo_transform_identity(const uint16_t *A, int64_t m, int64_t d, 
     #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < m; ++i)
         for (int64_t c = 0; c < d; ++c) {
-            double t = bf16_bits_to_f64(A[i * lda + c]);
+            double t = in_to_f64(A[i * lda + c]);
             y[i * d + c] = t;
             if (bound) bound[i * d + c] = fabs(t);
         }

@@ -61,6 +61,9 @@ def _bind(path: str) -> ctypes.CDLL:
                           ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_uint16))
     L.kqo_bf16_to_f64.argtypes = [ctypes.c_uint16]
     L.kqo_bf16_to_f64.restype = ctypes.c_double
+    L.kqo_f16_to_f64.argtypes = [ctypes.c_uint16]
+    L.kqo_f16_to_f64.restype = ctypes.c_double
+    L.kqo_set_input_format.argtypes = [ctypes.c_int]
     L.kqo_lu_to_factor.argtypes = [dp, ctypes.c_int, dp]
     L.kqo_expand_block.argtypes = [dp, dp]
     L.kqo_hadamard_block.argtypes = [dp]
@@ -194,13 +197,33 @@ def hadamard_block() -> np.ndarray:
 
 # --- transforms: y = a . K_j per 32-block (eq. 4) ------------------------------
 
-def transform(A: np.ndarray, d: int, kind: str, param=None):
+_format_lock = threading.Lock()
+
+
+def f16_to_f64(h: int) -> float:
+    """fp16 bit pattern -> its value (IEEE 754 binary16)."""
+    return float(lib().kqo_f16_to_f64(int(h)))
+
+
+def transform(A: np.ndarray, d: int, kind: str, param=None, in_format: str = "bf16"):
     """Return (y, bound), both fp64 [m, d].
 
     kind: 'kron' (param = factors [nb, 5, 2, 2]), 'dense' (param = [nb, 32, 32]),
     'hadamard', 'diag' (param = s [d]), 'identity', 'fwht' (full-row
-    Walsh-Hadamard, d a power of two).
+    Walsh-Hadamard, d a power of two).  in_format: 'bf16' or 'f16', the
+    format of A's 16-bit patterns.
     ``bound[i, c] = sum_r |a_r K_rc|`` is the scale the 2^-16 rule uses."""
+    if in_format not in ("bf16", "f16"):
+        raise ValueError(in_format)
+    with _format_lock:
+        lib().kqo_set_input_format(1 if in_format == "f16" else 0)
+        try:
+            return _transform(A, d, kind, param)
+        finally:
+            lib().kqo_set_input_format(0)
+
+
+def _transform(A: np.ndarray, d: int, kind: str, param=None):
     A = _bits(A)
     m, lda = A.shape
     assert d % 32 == 0 and d <= lda

@@ -48,13 +48,15 @@ def gather_scales(sf: np.ndarray, rows: np.ndarray, nb: int, layout: int) -> np.
 
 
 def check(A_bits: np.ndarray, d: int, kind: str, param, layout: int, q_gpu: np.ndarray,
-          sf_gpu: np.ndarray, y_gpu: np.ndarray | None, rows: np.ndarray | None = None) -> dict:
+          sf_gpu: np.ndarray, y_gpu: np.ndarray | None, rows: np.ndarray | None = None,
+          in_format: str = "bf16") -> dict:
     """Apply rules (i)-(iii) on the given rows (all rows if None).  Raises
     AssertionError on a violation; returns the flagged counts."""
     m = A_bits.shape[0]
     rows = np.arange(m) if rows is None else np.asarray(rows, np.int64)
     nb = d // 32
-    y_ref, bound = O.transform(np.ascontiguousarray(A_bits[rows]), d, kind, param)
+    y_ref, bound = O.transform(np.ascontiguousarray(A_bits[rows]), d, kind, param,
+                               in_format=in_format)
     q_ref, sf_ref, flags = O.quantize(y_ref, bound, O.SF_ROWMAJOR)
     codes_ref = unpack(q_ref, d)
     codes_gpu = unpack(np.asarray(q_gpu)[rows], d)
@@ -100,7 +102,8 @@ def check_side_output(A_bits: np.ndarray, d: int, kind: str, param, at_gpu: np.n
     """Rules (iv)-(v) for the bf16 side output on the given rows (all if None)."""
     m = A_bits.shape[0]
     rows = np.arange(m) if rows is None else np.asarray(rows, np.int64)
-    y_ref, bound = O.transform(np.ascontiguousarray(A_bits[rows]), d, kind, param)
+    y_ref, bound = O.transform(np.ascontiguousarray(A_bits[rows]), d, kind, param,
+                               in_format=in_format)
     tol = np.ldexp(bound, -16)
     lo = O.round_bf16(y_ref - tol)
     hi = O.round_bf16(y_ref + tol)

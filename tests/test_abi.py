@@ -218,3 +218,19 @@ def test_shared_argument_checks(L):
     assert f(A, 4, 64, 64, None, vp(16392), q, 32, sf, 0, None, None) == 3
     assert f(A, 4, 48, 64, F, None, q, 32, sf, 0, None, None) == 2
     assert f(A, 0, 64, 64, None, None, q, 32, sf, 0, None, None) == 0
+
+
+def test_ex_argument_checks(L):
+    """kq_quantize_mxfp4_ex: format, transform and parameter checks, before
+    any launch."""
+    vp = ctypes.c_void_p
+    A, q, sf, P = vp(4096), vp(8192), vp(12288), vp(16384)
+    f = L.kq_quantize_mxfp4_ex
+    assert f(A, 2, 4, 64, 64, 0, P, q, 32, sf, 0, None, None) == 4          # format
+    assert f(A, 1, 4, 64, 64, 5, P, q, 32, sf, 0, None, None) == 4          # transform
+    assert f(A, 1, 4, 64, 64, 0, None, q, 32, sf, 0, None, None) == 1       # kron needs factors
+    assert f(A, 1, 4, 64, 64, 1, None, q, 32, sf, 0, None, None) == 1       # diag needs s
+    assert f(A, 1, 4, 64, 64, 0, vp(16388), q, 32, sf, 0, None, None) == 3
+    assert f(A, 1, 4, 64, 64, 4, None, q, 32, sf, 0, None, None) == 2       # fwht: d < 128
+    assert f(A, 1, 4, 96, 96, 2, None, q, 56, sf, 0, None, None) == 3       # ldq % 16
+    assert f(A, 1, 0, 64, 64, 0, None, q, 32, sf, 0, None, None) == 0       # m = 0

@@ -793,3 +793,53 @@ def test_shared_factors(m, d, layout, path):
     nbytes = kq.kq_sf_bytes(m, d, layout)
     assert np.array_equal(np_(q), np_(q2)) and np.array_equal(np_(sf)[:nbytes], np_(sf2)[:nbytes])
     parity.check(A_bits, d, "kron", np.ascontiguousarray(Fo), layout, np_(q), np_(sf), np_(y))
+
+
+# ------------------------------------------------------------ fp16 input --
+
+F16_SHAPES = [(256, 1152), (300, 2240), (7, 96), (4096, 4096)]
+
+
+@pytest.mark.parametrize("kind", ["kron", "diag", "hadamard", "identity", "fwht"])
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("m,d", F16_SHAPES, ids=[f"{m}x{d}" for m, d in F16_SHAPES])
+def test_f16_input_parity(m, d, layout, kind):
+    """fp16 activations (PixArt-Sigma's format, and the pages' timing
+    precision) through the CUDA-core quantizers, against the oracle reading
+    the same fp16 patterns: rules (i)-(iii)."""
+    if kind == "fwht" and (d & (d - 1) or d < 128):
+        pytest.skip("the full-row transform needs a power-of-two d >= 128")
+    A_bits = synth.activations(m, d, 1900 + m, "pixart", fmt="f16")
+    A = dev(A_bits.view(np.int16)).view(torch.float16)
+    gp, op = None, None
+    if kind == "kron":
+        gp, op = lib_factors(d // 32, 1901)
+    elif kind == "diag":
+        s = synth.smooth_scales(d)
+        gp, op = s, s.astype(np.float64)
+    q, sf, y = kq.kq_quantize_mxfp4_ex(A, kind, None if gp is None else dev(gp), d,
+                                       in_format=kq.KQ_IN_F16, layout=layout, y_debug=True)
+    rows = None if m * d <= 2_000_000 else np.arange(0, m, 7)
+    parity.check(A_bits, d, kind, op, layout, np_(q), np_(sf), np_(y), rows, in_format="f16")
+
+
+def test_ex_bf16_matches_entry_points():
+    """kq_quantize_mxfp4_ex with bf16 input writes the bytes of the
+    dedicated entry points (butterfly, diagonal, Hadamard, identity)."""
+    m, d = 300, 2240
+    A_bits = synth.activations(m, d, 1950, "sana")
+    A = to_bf16(A_bits)
+    F, _ = lib_factors(d // 32, 1951)
+    s = synth.smooth_scales(d)
+    pairs = [
+        (kq.kq_quantize_mxfp4_ex(A, "kron", dev(F), d, layout=1),
+         kq.kq_quantize_mxfp4(A, d, factors=dev(F), layout=1, variant=kq.VARIANT_BUTTERFLY)),
+        (kq.kq_quantize_mxfp4_ex(A, "diag", dev(s), d, layout=1),
+         kq.kq_smooth_quantize_mxfp4(A, dev(s), d, layout=1)),
+        (kq.kq_quantize_mxfp4_ex(A, "hadamard", None, d, layout=1),
+         kq.kq_hadamard_quantize_mxfp4(A, d, layout=1)),
+        (kq.kq_quantize_mxfp4_ex(A, "identity", None, d, layout=1),
+         kq.kq_quantize_mxfp4(A, d, layout=1)),
+    ]
+    for (q1, s1, _), (q2, s2, _) in pairs:
+        assert torch.equal(q1, q2) and torch.equal(s1, s2)

@@ -39,6 +39,11 @@ MUTANTS = [
      [pins.test_bf16_rounding_golden, pins.test_bf16_rounding_is_nearest_even]),
     ("fwht_butterfly_sign", "v[j + h] = x - z;", "v[j + h] = z - x;",
      [lambda o: pins.test_fwht_matches_library_hadamard(o, 64), pins.test_fwht_closed_forms]),
+    ("f16_exponent_bias", "v = ldexp((double)(1024 + f), e - 25);",
+     "v = ldexp((double)(1024 + f), e - 24);",
+     [pins.test_f16_conversion_all_patterns, pins.test_f16_closed_forms]),
+    ("f16_subnormal_scale", "v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);",
+     [pins.test_f16_conversion_all_patterns, pins.test_f16_closed_forms]),
 ]
 
 

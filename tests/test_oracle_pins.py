@@ -425,3 +425,53 @@ def test_fwht_closed_forms(oracle_lib):
     y32, _ = oracle_lib.transform(C, 32, "fwht")
     yh, _ = oracle_lib.transform(C, 32, "hadamard")
     assert np.allclose(y32, yh, rtol=0, atol=1e-13)
+
+
+# ------------------------------------------------ fp16 input (Sec. 4.1) --
+
+def test_f16_conversion_all_patterns(oracle_lib):
+    """The oracle's binary16 decoding against numpy's float16 on all 65536
+    bit patterns (a library routine: NaNs compared as NaN)."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle_lib.f16_to_f64(int(h)) for h in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_f16_closed_forms(oracle_lib):
+    """Values of binary16 fixed by its definition (bias 15, 10-bit fraction,
+    subnormals f * 2^-24)."""
+    cases = {0x3C00: 1.0, 0x7BFF: 65504.0, 0x0001: 2.0 ** -24, 0x03FF: 1023 * 2.0 ** -24,
+             0x0400: 2.0 ** -14, 0xC000: -2.0, 0x3555: 1365 / 4096, 0x8000: -0.0,
+             0x7C00: float("inf"), 0xFC00: float("-inf")}
+    for h, v in cases.items():
+        got = oracle_lib.f16_to_f64(h)
+        assert got == v and np.signbit(got) == np.signbit(v), (hex(h), got, v)
+
+
+@pytest.mark.parametrize("kind", ["kron", "diag", "identity", "hadamard", "fwht"])
+def test_f16_input_equals_bf16_input_on_shared_values(oracle_lib, kind):
+    """Activations exactly representable in both formats (8 significant bits,
+    exponents inside fp16's range) give the same y and bound whether they
+    arrive as fp16 or as bf16 patterns."""
+    rng = np.random.default_rng(11)
+    m, d = 3, 256
+    vals = np.ldexp(rng.integers(-255, 256, size=(m, d)).astype(np.float64),
+                    rng.integers(-12, 4, size=(m, d)))
+    f16 = vals.astype(np.float16).view(np.uint16)
+    assert np.array_equal(f16.view(np.float16).astype(np.float64), vals)
+    bf16 = (vals.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((bf16.astype(np.uint32) << 16).view(np.float32).astype(np.float64), vals)
+    param = None
+    if kind == "kron":
+        param = rng.standard_normal((d // 32, 5, 2, 2))
+    elif kind == "diag":
+        param = rng.lognormal(0.0, 0.5, size=d)
+    y16, b16 = oracle_lib.transform(f16, d, kind, param, in_format="f16")
+    yb, bb = oracle_lib.transform(bf16, d, kind, param)
+    assert np.array_equal(y16, yb) and np.array_equal(b16, bb)
+    # and the format switch does not leak into the next call
+    y2, _ = oracle_lib.transform(bf16, d, kind, param)
+    assert np.array_equal(y2, yb)

@@ -129,6 +129,7 @@ void fill_quant_params(QuantParams &p, int64_t m, int64_t d, int64_t rows_per_ti
     p.ncb = (p.nb + 3) / 4;
     p.y_debug = y_debug;
     p.shared_params = 0;
+    p.in_f16 = 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -377,6 +378,35 @@ kq_status kq_quantize_mxfp4_shared(const uint16_t *A, int64_t m, int64_t d, int6
     if (K_expanded != nullptr) return launch_quant_umma(A, lda, K_expanded, p, nullptr, 0, stream);
     p.factors = factors;
     return launch_quant_tma(kKron, A, lda, p, stream);
+}
+
+kq_status kq_quantize_mxfp4_ex(const uint16_t *A, kq_in_format in_format, int64_t m, int64_t d,
+                               int64_t lda, kq_transform transform, const float *param,
+                               uint8_t *q, int64_t ldq, uint8_t *sf, kq_sf_layout sf_layout,
+                               float *y_debug, cudaStream_t stream)
+{
+    if (in_format != KQ_IN_BF16 && in_format != KQ_IN_F16) return KQ_ERR_LAYOUT;
+    if (transform < KQ_TRANSFORM_KRON || transform > KQ_TRANSFORM_FWHT) return KQ_ERR_LAYOUT;
+    kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
+    if (st != KQ_OK) return st;
+    if (transform == KQ_TRANSFORM_FWHT && (d < 128 || d > 16384 || (d & (d - 1)) != 0))
+        return KQ_ERR_SHAPE;
+    if (m == 0) return KQ_OK;
+    const bool needs_param = transform == KQ_TRANSFORM_KRON || transform == KQ_TRANSFORM_DIAG;
+    if (needs_param && param == nullptr) return KQ_ERR_NULL;
+    if (needs_param && !aligned16(param)) return KQ_ERR_ALIGN;
+    DeviceInfo info;
+    if ((st = device_info(info)) != KQ_OK) return st;
+    QuantParams p;
+    fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
+    p.in_f16 = in_format == KQ_IN_F16 ? 1 : 0;
+    switch (transform) {
+    case KQ_TRANSFORM_KRON: p.factors = param; return launch_quant_tma(kKron, A, lda, p, stream);
+    case KQ_TRANSFORM_DIAG: p.s = param; return launch_quant_tma(kDiag, A, lda, p, stream);
+    case KQ_TRANSFORM_HADAMARD: return launch_quant_tma(kHadamard, A, lda, p, stream);
+    case KQ_TRANSFORM_IDENTITY: return launch_quant_tma(kIdentity, A, lda, p, stream);
+    default: return launch_quant_fwht(A, lda, p, stream);
+    }
 }
 
 kq_status kq_smooth_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,

@@ -13,6 +13,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 namespace kq {
 
@@ -230,6 +231,16 @@ __device__ __forceinline__ void stg_f4(float *p, float4 v)
 // A 32-bit word holds two bf16 values, element 2t in the low half.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// The same for two fp16 values (exact: every fp16 is an fp32).
+__device__ __forceinline__ float f16_lo(uint32_t w)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xffffu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t w)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
 
 // ---- MXFP4 epilogue -----------------------------------------------------------------
 

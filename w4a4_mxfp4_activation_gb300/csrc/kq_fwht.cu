@@ -130,8 +130,8 @@ __global__ void __launch_bounds__(kFThreads, 2) fwht_quant_kernel(const uint16_t
                 const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    v[8 * k + 2 * e] = bf16_lo(u[e]);
-                    v[8 * k + 2 * e + 1] = bf16_hi(u[e]);
+                    v[8 * k + 2 * e] = p.in_f16 ? f16_lo(u[e]) : bf16_lo(u[e]);
+                    v[8 * k + 2 * e + 1] = p.in_f16 ? f16_hi(u[e]) : bf16_hi(u[e]);
                 }
             }
         } else {

@@ -35,6 +35,7 @@ struct QuantParams {
     int64_t ncb;        // ceil(nb / 4), for the blocked layout
     float *y_debug;     // [m][d] or null
     int shared_params;  // 1: every block takes block 0's factors / operand records
+    int in_f16;         // 1: A holds fp16 bit patterns (CUDA-core kernels), 0: bf16
 };
 
 // Per-device facts the launchers need.

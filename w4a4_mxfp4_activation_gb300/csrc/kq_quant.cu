@@ -267,12 +267,22 @@ __global__ void __launch_bounds__(kThreads, 2)
                 continue;
             }
             float2 Y[16];
+            if (p.in_f16) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                Y[4 * k + 0] = make_float2(bf16_lo(w[k].x), bf16_hi(w[k].x));
-                Y[4 * k + 1] = make_float2(bf16_lo(w[k].y), bf16_hi(w[k].y));
-                Y[4 * k + 2] = make_float2(bf16_lo(w[k].z), bf16_hi(w[k].z));
-                Y[4 * k + 3] = make_float2(bf16_lo(w[k].w), bf16_hi(w[k].w));
+                for (int k = 0; k < 4; ++k) {
+                    Y[4 * k + 0] = make_float2(f16_lo(w[k].x), f16_hi(w[k].x));
+                    Y[4 * k + 1] = make_float2(f16_lo(w[k].y), f16_hi(w[k].y));
+                    Y[4 * k + 2] = make_float2(f16_lo(w[k].z), f16_hi(w[k].z));
+                    Y[4 * k + 3] = make_float2(f16_lo(w[k].w), f16_hi(w[k].w));
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    Y[4 * k + 0] = make_float2(bf16_lo(w[k].x), bf16_hi(w[k].x));
+                    Y[4 * k + 1] = make_float2(bf16_lo(w[k].y), bf16_hi(w[k].y));
+                    Y[4 * k + 2] = make_float2(bf16_lo(w[k].z), bf16_hi(w[k].z));
+                    Y[4 * k + 3] = make_float2(bf16_lo(w[k].w), bf16_hi(w[k].w));
+                }
             }
             apply_transform<T>(Y, prm);
             if (p.y_debug != nullptr && row < p.m) {

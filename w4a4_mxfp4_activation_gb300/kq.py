@@ -24,6 +24,9 @@ KQ_SF_ROWMAJOR = 0
 KQ_SF_BLOCKED_128x4 = 1
 KQ_K_FP32 = 0
 KQ_K_BF16X3 = 1
+KQ_IN_BF16 = 0
+KQ_IN_F16 = 1
+KQ_TRANSFORM = {"kron": 0, "diag": 1, "hadamard": 2, "identity": 3, "fwht": 4}
 VARIANT_BUTTERFLY = 0
 VARIANT_MMA = 1
 VARIANT_IDENTITY = 2
@@ -35,7 +38,7 @@ EXPORTS = (
     "kq_status_string", "kq_lu_to_factors", "kq_invert_transpose_factors",
     "kq_quantize_mxfp4_variant", "kq_test_encode_e2m1", "kq_quantize_mxfp4_dual",
     "kq_fwht_quantize_mxfp4", "kq_w4a4_gemm", "kq_w4a4_gemm_variant", "kq_bf16_gemm",
-    "kq_layer_error", "kq_quantize_mxfp4_shared",
+    "kq_layer_error", "kq_quantize_mxfp4_shared", "kq_quantize_mxfp4_ex",
 )
 
 
@@ -72,6 +75,9 @@ def lib() -> ctypes.CDLL:
             L.kq_quantize_mxfp4_shared.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64, vp, st, vp,
                                                    vp]
             L.kq_quantize_mxfp4_shared.restype = st
+            L.kq_quantize_mxfp4_ex.argtypes = [vp, st, i64, i64, i64, st, vp, vp, i64, vp, st, vp,
+                                               vp]
+            L.kq_quantize_mxfp4_ex.restype = st
             L.kq_smooth_quantize_mxfp4.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, st, vp, vp]
             L.kq_smooth_quantize_mxfp4.restype = st
             L.kq_hadamard_quantize_mxfp4.argtypes = [vp, i64, i64, i64, vp, i64, vp, st, vp, vp]
@@ -237,6 +243,26 @@ def kq_quantize_mxfp4_shared(A, d: int | None = None, factors=None, K_expanded=N
                                           _ptr(K_expanded), _ptr(q), ldq, _ptr(sf), layout,
                                           _ptr(y_debug), _stream(stream)),
            "kq_quantize_mxfp4_shared")
+    return q, sf, y_debug
+
+
+def kq_quantize_mxfp4_ex(A, transform: str, param=None, d: int | None = None,
+                         in_format: int = KQ_IN_BF16, layout: int = KQ_SF_ROWMAJOR, q=None,
+                         sf=None, y_debug=None, stream=None):
+    """CUDA-core quantizer with the input format chosen: A holds bf16 or
+    fp16 16-bit patterns ([m, lda] CUDA tensor of dtype bfloat16, float16,
+    int16 or uint16); transform in KQ_TRANSFORM.  Returns (q, sf, y_debug)."""
+    import torch
+    if A.dtype not in (torch.bfloat16, torch.float16, torch.int16, torch.uint16):
+        raise TypeError("A must hold 16-bit patterns")
+    m, lda = A.shape
+    d = lda if d is None else d
+    q, sf, y_debug = _outputs(A, m, d, layout, q, sf, y_debug)
+    ldq = q.shape[1] if q.dim() == 2 else d // 2
+    _check(lib().kq_quantize_mxfp4_ex(_ptr(A), in_format, m, d, A.stride(0),
+                                      KQ_TRANSFORM[transform], _ptr(param), _ptr(q), ldq,
+                                      _ptr(sf), layout, _ptr(y_debug), _stream(stream)),
+           "kq_quantize_mxfp4_ex")
     return q, sf, y_debug
 
 

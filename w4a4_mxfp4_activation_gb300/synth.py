@@ -39,12 +39,19 @@ def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return rounded.astype(np.uint16)
 
 
+def f64_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """fp64 -> fp16 (round to nearest even, numpy) as uint16 bit patterns."""
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64).astype(np.float16)).view(np.uint16)
+
+
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
     return (np.asarray(h, dtype=np.uint32) << 16).view(np.float32)
 
 
-def activations(m: int, d: int, seed: int, model: str, lda: int | None = None) -> np.ndarray:
-    """bf16 bit patterns [m, lda] (columns d..lda-1 are zero padding)."""
+def activations(m: int, d: int, seed: int, model: str, lda: int | None = None,
+                fmt: str = "bf16") -> np.ndarray:
+    """bf16 (or, fmt='f16', fp16) bit patterns [m, lda] (columns d..lda-1
+    are zero padding)."""
     rng = np.random.default_rng(seed)
     x = rng.standard_normal((m, d))
     if model == "gauss_outlier8":
@@ -64,7 +71,7 @@ def activations(m: int, d: int, seed: int, model: str, lda: int | None = None) -
             x[:, ch] *= rng.uniform(30.0, 300.0, size=n_out)
     else:
         raise ValueError(f"unknown activation model {model!r}")
-    bits = f64_to_bf16_bits(x)
+    bits = f64_to_f16_bits(x) if fmt == "f16" else f64_to_bf16_bits(x)
     if lda is not None and lda != d:
         out = np.zeros((m, lda), np.uint16)
         out[:, :d] = bits
