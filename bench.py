@@ -82,6 +82,8 @@ def parse_args():
     ap.add_argument("--launches", type=int, default=3, help="launches of the profiling case")
     ap.add_argument("--table", action="store_true",
                     help="per-launch medians of every kernel on every config shape (markdown)")
+    ap.add_argument("--table3-only", action="store_true",
+                    help="with --table: only the pages' Table 3 comparison (bf16 and fp16 input)")
     ap.add_argument("--table-reps", type=int, default=50, help="graph replays per kernel")
     ap.add_argument("--table-warmup", type=int, default=100, help="warm-up launches per kernel")
     ap.add_argument("--cpu-rate", nargs=3, type=int, metavar=("M", "D", "SECONDS"),
@@ -781,6 +783,15 @@ def measure_shape(args, m, d, model, seed, kinds, peak):
     del base
     A = [torch.roll(A0, shifts=37 * s, dims=0) for s in range(sets)]
     del A0
+    A16 = None
+    if any(k.endswith("_f16") for k in kinds):
+        # the same model drawn in fp16 (PixArt-Sigma's format)
+        base16 = torch.from_numpy(synth.activations(rows, d, seed, model, fmt="f16")
+                                  .view(np.int16)).to(dev).view(torch.float16)
+        B16 = base16.repeat((m + rows - 1) // rows, 1)[:m].contiguous()
+        del base16
+        A16 = [torch.roll(B16, shifts=37 * s, dims=0) for s in range(sets)]
+        del B16
     F = torch.from_numpy(kq.kq_lu_to_factors(
         synth.lu_params(d // 32, synth.SEED_FACTORS + seed), +1)).to(dev)
     KX = kq.kq_expand_blocks(F, kq.KQ_K_BF16X3)
@@ -811,6 +822,12 @@ def measure_shape(args, m, d, model, seed, kinds, peak):
             kq.kq_hadamard_quantize_mxfp4(A[s], d, layout=layout, q=Q[s], sf=SF[s], stream=stream)
         elif kind == "fwht":
             kq.kq_fwht_quantize_mxfp4(A[s], d, layout=layout, q=Q[s], sf=SF[s], stream=stream)
+        elif kind.endswith("_f16"):
+            t = {"identity_f16": "identity", "diag_f16": "diag", "butterfly_f16": "kron",
+                 "fwht_f16": "fwht"}[kind]
+            prm = F if t == "kron" else (S if t == "diag" else None)
+            kq.kq_quantize_mxfp4_ex(A16[s], t, prm, d, in_format=kq.KQ_IN_F16, layout=layout,
+                                    q=Q[s], sf=SF[s], stream=stream)
         else:
             kq.kq_quantize_mxfp4(A[s], d, layout=layout, q=Q[s], sf=SF[s], stream=stream)
 
@@ -836,7 +853,7 @@ def measure_shape(args, m, d, model, seed, kinds, peak):
             stream.synchronize()
         us[kind] = statistics.median(a.elapsed_time(b) for a, b in ev) / n_launch * 1e3
         del g
-    del A, Q, SF, KX, AT
+    del A, A16, Q, SF, KX, AT
     torch.cuda.empty_cache()
     return us, sets
 
@@ -850,6 +867,9 @@ def run_table(args):
     Table 3 comparison on GB300, and the oracle on the host cores."""
     import torch  # noqa: F401  (initializes CUDA before the measurements)
     peak, _ = hbm_peak()
+    if args.table3_only:
+        run_table3(args, peak)
+        return
     print("| config | layer | m x d | sets | " + " | ".join(
         f"{k} GB/s (% peak)" if k in ("umma", "dual") else f"{k} GB/s" for k in TABLE_KERNELS) +
         " | umma / diag |")
@@ -863,20 +883,7 @@ def run_table(args):
                      else f"{gbs[k]:.0f}" for k in TABLE_KERNELS]
             print(f"| {cfg} | {name} | {m}x{d} | {sets} | " + " | ".join(cells) +
                   f" | {gbs['umma'] / gbs['diag']:.2f} |", flush=True)
-    # [KQ] Table 3 on GB300: latency (us) of the bare quantizer (Q4), the
-    # diagonal scale (Scale), the dense-block tensor-core kernel (tcgen05,
-    # K1's form), the kernel built from the factors (butterfly, K2's input)
-    # and the full-row Walsh-Hadamard transform (FWHT), all with MXFP4 output
-    kinds = ("identity", "diag", "umma", "butterfly", "fwht")
-    print()
-    print("| m | d | Q4 us | Scale us | tcgen05 us | butterfly us | FWHT us | Scale/tcgen05 | "
-          "Scale/butterfly | FWHT/tcgen05 | FWHT/butterfly |")
-    print("|" + "---|" * 11)
-    for m, d in TABLE3_SHAPES:
-        us, _ = measure_shape(args, m, d, "flux", synth_seed("3"), kinds, peak)
-        print(f"| {m} | {d} | " + " | ".join(f"{us[k]:.2f}" for k in kinds) +
-              f" | {us['diag'] / us['umma']:.2f} | {us['diag'] / us['butterfly']:.2f} | "
-              f"{us['fwht'] / us['umma']:.2f} | {us['fwht'] / us['butterfly']:.2f} |", flush=True)
+    run_table3(args, peak)
     # the oracle on the host cores: all of them, then one
     print()
     print("| config | layer | oracle GB/s, all cores | oracle GB/s, 1 core |")
@@ -895,6 +902,37 @@ def run_table(args):
             print(f"| {cfg} | {name} | {out[0]} | {out[1]} |", flush=True)
     print(f"\nhost: {os.cpu_count()} cores; per shape max(4, 3 L2 / set) rotating sets, "
           f"CUDA graphs of max(sets, 32) launches, median over up to {args.table_reps} replays")
+
+
+def run_table3(args, peak):
+    """[KQ] Table 3 on GB300 (bf16 and fp16 activations)."""
+    # [KQ] Table 3 on GB300: latency (us) of the bare quantizer (Q4), the
+    # diagonal scale (Scale), the dense-block tensor-core kernel (tcgen05,
+    # K1's form), the kernel built from the factors (butterfly, K2's input)
+    # and the full-row Walsh-Hadamard transform (FWHT), all with MXFP4 output
+    kinds = ("identity", "diag", "umma", "butterfly", "fwht")
+    print()
+    print("| m | d | Q4 us | Scale us | tcgen05 us | butterfly us | FWHT us | Scale/tcgen05 | "
+          "Scale/butterfly | FWHT/tcgen05 | FWHT/butterfly |")
+    print("|" + "---|" * 11)
+    for m, d in TABLE3_SHAPES:
+        us, _ = measure_shape(args, m, d, "flux", synth_seed("3"), kinds, peak)
+        print(f"| {m} | {d} | " + " | ".join(f"{us[k]:.2f}" for k in kinds) +
+              f" | {us['diag'] / us['umma']:.2f} | {us['diag'] / us['butterfly']:.2f} | "
+              f"{us['fwht'] / us['umma']:.2f} | {us['fwht'] / us['butterfly']:.2f} |", flush=True)
+    # the same with fp16 activations, the precision the pages time in: the
+    # CUDA-core kernels (the tensor-core path reads bf16)
+    kinds16 = ("identity_f16", "diag_f16", "butterfly_f16", "fwht_f16")
+    print()
+    print("fp16 activations (the pages' timing precision):")
+    print()
+    print("| m | d | Q4 us | Scale us | butterfly us | FWHT us | Scale/butterfly | FWHT/butterfly |")
+    print("|" + "---|" * 8)
+    for m, d in TABLE3_SHAPES:
+        us, _ = measure_shape(args, m, d, "flux", synth_seed("3"), kinds16, peak)
+        print(f"| {m} | {d} | " + " | ".join(f"{us[k]:.2f}" for k in kinds16) +
+              f" | {us['diag_f16'] / us['butterfly_f16']:.2f} | "
+              f"{us['fwht_f16'] / us['butterfly_f16']:.2f} |", flush=True)
 
 
 GEMM_TABLE = (
