@@ -384,16 +384,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
 //   32x128b.warpx4 puts tile row r -- the scales of rows r, r + 32, r + 64,
 //   r + 96 -- into lane r of every lane quarter; an N = 256 instruction reads
 //   W rows 128-255 from the 4 columns after rows 0-127).
-// Every tcgen05 instruction costs its issuing thread tens of nanoseconds, and
-// different threads issue in parallel, so the design keeps the instructions
-// per flop low (N = 256 instructions, stages released in pairs by one commit)
-// and spreads them over threads.
-// Roles: warp 0 producer, warp 1 MMA issuer, warps 2-3 scale copiers (the
-// tcgen05.cp of a stage, dealt alternately to two threads, ahead of the MMAs,
-// reported on sf_ready[s] by a commit from each), 4 NH epilogue warps: NH per
-// TMEM lane quarter, 128 columns each, read their part of the accumulator into
-// registers and release it before they store, so the next tile's MMAs start
-// while the stores drain.
+// The SM issues tcgen05 instructions at a bounded rate (tens of nanoseconds
+// each, a commit several times that), so the design keeps them per flop low:
+// N = 256 instructions, stages released in pairs by one commit, the scale
+// copies issued by the MMA thread itself (in-order, no commit between them
+// and the MMAs), and the issuing warp kept converged with its operands
+// warp-uniform, one elected lane issuing (an issue loop inside a one-lane
+// branch ran the copies at half the rate).
+// Roles: warp 0 producer, warp 1 scale copies + MMAs, 4 NH epilogue warps:
+// NH per TMEM lane quarter, 128 columns each, read their part of the
+// accumulator into registers and release it before they store, so the next
+// tile's MMAs start while the stores drain.
 
 constexpr int kXBK = 256;                          // K elements per stage
 constexpr int kXACodeBytes = 128 * 128;            // A codes per stage
@@ -404,7 +405,7 @@ template <int NH>
 struct XCfg {
     static constexpr int kBN = 128 * NH;                  // tile width (C columns, W rows)
     static constexpr int kStages = 4;
-    static constexpr int kThreads = 128 + 128 * NH;       // producer, MMA, 2 copiers, epilogue
+    static constexpr int kThreads = 64 + 128 * NH;        // producer, MMA, epilogue
     static constexpr int kAccBufs = NH == 1 ? 2 : 1;
     static constexpr int kWCodeBytes = kBN * 128;
     static constexpr int kSfaOff = kXACodeBytes + kWCodeBytes;
@@ -448,6 +449,15 @@ __device__ __forceinline__ void x_mma(uint32_t d, uint64_t a, uint64_t b, uint32
         : "memory");
 }
 
+// One lane of the (converged) warp, the same for every caller.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(pred));
+    return pred != 0;
+}
+
 __device__ __forceinline__ void x_cp_sf(uint32_t taddr, uint64_t sdesc)
 {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
@@ -466,8 +476,8 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     const uint32_t bar = base + C::kBarOff;
-    const uint32_t full = bar, empty = bar + 8 * kXStages, sf_ready = bar + 16 * kXStages;
-    const uint32_t acc_full = bar + 24 * kXStages, acc_empty = acc_full + 16;
+    const uint32_t full = bar, empty = bar + 8 * kXStages;
+    const uint32_t acc_full = bar + 16 * kXStages, acc_empty = acc_full + 16;
     const uint32_t tmem_slot = acc_empty + 16;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles = g.mtiles * g.ntiles;
@@ -479,7 +489,6 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
         for (int s = 0; s < kXStages; ++s) {
             mbar_init(full + 8 * s, 1);
             mbar_init(empty + 8 * s, 1);
-            mbar_init(sf_ready + 8 * s, 2);           // one commit per scale copier
         }
         for (int b = 0; b < C::kAccBufs; ++b) {
             mbar_init(acc_full + 8 * b, 1);
@@ -537,96 +546,87 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
                                 static_cast<uint32_t>((j / kXStages) & 1));
         }
     } else if (warp == 1) {
-        // MMA issuer: one thread, no warp-wide votes or syncs per stage
-        if (lane == 0) {
-            int64_t kk = 0, tc = 0;
-            bool ok = true;
-            constexpr uint32_t id0 = x_idesc(0), id2 = x_idesc(2);
-            constexpr uint32_t kIdN = static_cast<uint32_t>((NH - 1) * (128 >> 3)) << 17;  // N += 128
-            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc) {
-                // accumulator buffer b of tile tc is free once the epilogue has
-                // read tile tc - kAccBufs from it
-                const int b = static_cast<int>(tc % C::kAccBufs);
-                const int64_t use = tc / C::kAccBufs;
-                if (use >= 1) ok = mbar_wait(acc_empty + 8 * b, static_cast<uint32_t>((use - 1) & 1));
-                const uint32_t acc = tmem_base + 128 * b;
-                for (int64_t ks = 0; ks < g.ksteps && ok; ++ks, ++kk) {
-                    const int s = static_cast<int>(kk % kXStages);
-                    const uint32_t par = static_cast<uint32_t>((kk / kXStages) & 1);
-                    ok = mbar_wait(sf_ready + 8 * s, par) && mbar_wait(full + 8 * s, par);
-                    if (!ok) break;
-                    g_fence_after();
-                    const int64_t rem = (g.k - ks * kXBK + 63) / 64;
-                    const int nmma = rem < 4 ? static_cast<int>(rem) : 4;
-                    const uint32_t st = base + s * kXStageBytes;
-                    // descriptors advance in 16-byte units: +2 = the next 32
-                    // bytes of codes (K = 64)
-                    const uint32_t sft = tmem_base + kXSfCol + kXSfStride * s;
-                    const uint64_t da = g_desc(st), db = g_desc(st + kXACodeBytes);
-                    for (int j = 0; j < nmma; ++j)
-                        x_mma(acc, da + 2 * j, db + 2 * j, ((j & 1) ? id2 : id0) + kIdN, sft + 4 * (j >> 1),
-                              sft + 8 + 4 * (NH * (j >> 1)), (ks > 0 || j > 0) ? 1u : 0u);
+        // MMA issuer: the whole warp runs the loop, so that descriptors and
+        // addresses are warp-uniform values; one elected lane issues a
+        // stage's scale copies (A tile, then W's halves, per scale tile at)
+        // and its MMAs -- in order from one thread, the copies need no
+        // commit before the MMAs that read them.  An odd block count leaves
+        // one padding block inside the last instruction: the warp first sets
+        // its scale bytes to 2^0 (lane r: row r of each tile).
+        int64_t kk = 0, tc = 0;
+        bool ok = true;
+        const bool pad_fix = (g.nb & 1) != 0;
+        constexpr uint32_t id0 = x_idesc(0), id2 = x_idesc(2);
+        constexpr uint32_t kIdN = static_cast<uint32_t>((NH - 1) * (128 >> 3)) << 17;  // N += 128
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc) {
+            // accumulator buffer b of tile tc is free once the epilogue has
+            // read tile tc - kAccBufs from it
+            const int b = static_cast<int>(tc % C::kAccBufs);
+            const int64_t use = tc / C::kAccBufs;
+            if (use >= 1)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(acc_empty + 8 * b, static_cast<uint32_t>((use - 1) & 1)));
+            const uint32_t acc = tmem_base + 128 * b;
+            for (int64_t ks = 0; ks < g.ksteps && ok; ++ks, ++kk) {
+                const int s = static_cast<int>(kk % kXStages);
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(full + 8 * s, static_cast<uint32_t>((kk / kXStages) & 1)));
+                if (!ok) break;
+                const int64_t rem = (g.k - ks * kXBK + 63) / 64;
+                const int nmma = rem < 4 ? static_cast<int>(rem) : 4;
+                const uint32_t st = base + s * kXStageBytes;
+                const uint32_t sfa_s = st + kXSfaOff, sfw_s = st + kXSfwOff;
+                if (pad_fix && ks == g.ksteps - 1) {
+                    const int kb = static_cast<int>(g.nb - 8 * ks);     // padding block, local index
+                    const uint32_t off = static_cast<uint32_t>((kb >> 2) * 512 + 16 * lane + (kb & 3));
+#pragma unroll
+                    for (int grp = 0; grp < 4; ++grp) {
+                        asm volatile("st.shared.u8 [%0], %1;" ::"r"(sfa_s + off + 4 * grp), "r"(127u) : "memory");
+#pragma unroll
+                        for (int hh = 0; hh < NH; ++hh)
+                            asm volatile("st.shared.u8 [%0], %1;" ::"r"(sfw_s + 1024 * hh + off + 4 * grp),
+                                         "r"(127u)
+                                         : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                g_fence_after();
+                // TMEM scale columns of stage s: A tile at at 4 at, W half h
+                // tile at at 8 + 4 (NH at + h); one N = 128 NH instruction
+                // reads the tiles of W's halves from consecutive 4-column
+                // groups.  Descriptors advance in 16-byte units: +2 = the next
+                // 32 bytes of codes (K = 64), +32 = the next 512-byte scale
+                // tile, +64 = the next half's scale tiles of W.
+                const uint32_t sft = tmem_base + kXSfCol + kXSfStride * s;
+                const uint64_t da = g_desc(st), db = g_desc(st + kXACodeBytes);
+                const uint64_t dsa = x_desc_noswz(sfa_s, 128), dsw = x_desc_noswz(sfw_s, 128);
+                if (elect_one()) {
+                    for (int at = 0; at < (nmma + 1) / 2; ++at) {
+                        x_cp_sf(sft + 4 * at, dsa + 32 * at);
+#pragma unroll
+                        for (int hh = 0; hh < NH; ++hh)
+                            x_cp_sf(sft + 8 + 4 * (NH * at + hh), dsw + 64 * hh + 32 * at);
+                        for (int j = 2 * at; j < 2 * at + 2 && j < nmma; ++j)
+                            x_mma(acc, da + 2 * j, db + 2 * j, ((j & 1) ? id2 : id0) + kIdN, sft + 4 * at,
+                                  sft + 8 + 4 * (NH * at), (ks > 0 || j > 0) ? 1u : 0u);
+                    }
                     if (kk & 1) g_commit(empty + 8 * (s >> 1));
                     if (ks == g.ksteps - 1) g_commit(acc_full + 8 * b);
                 }
-            }
-            if (tc >= 1 && ok) {
-                const int64_t last = tc - 1;
-                (void)mbar_wait(acc_full + 8 * static_cast<int>(last % C::kAccBufs),
-                                static_cast<uint32_t>((last / C::kAccBufs) & 1));
+                __syncwarp();
             }
         }
-        __syncwarp();
-    } else if (warp < 4) {
-        // scale copiers: the copies of a stage (per scale tile at: A, then W's
-        // halves) are dealt alternately to the two threads, which issue them
-        // in parallel with the MMAs and report on sf_ready[s] with a commit.
-        // An odd block count leaves one padding block inside the last
-        // instruction: a copier sets its scale bytes to 2^0 before the copy.
-        if (lane == 0) {
-            const int cid = warp - 2;
-            const bool pad_fix = (g.nb & 1) != 0;
-            int64_t kk = 0;
-            bool ok = true;
-            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-                for (int64_t ks = 0; ks < g.ksteps; ++ks, ++kk) {
-                    const int s = static_cast<int>(kk % kXStages);
-                    ok = mbar_wait(full + 8 * s, static_cast<uint32_t>((kk / kXStages) & 1));
-                    if (!ok) break;
-                    g_fence_after();
-                    const int64_t rem = (g.k - ks * kXBK + 63) / 64;
-                    const int nmma = rem < 4 ? static_cast<int>(rem) : 4;
-                    const uint32_t st = base + s * kXStageBytes;
-                    const uint32_t sft = tmem_base + kXSfCol + kXSfStride * s;
-                    const int pad_kb = (pad_fix && ks == g.ksteps - 1) ? static_cast<int>(g.nb - 8 * ks) : -1;
-                    int e = 0;
-                    for (int at = 0; at < (nmma + 1) / 2; ++at)
-                        for (int r = 0; r <= NH; ++r, ++e) {
-                            if ((e & 1) != cid) continue;
-                            // region r: 0 = A, 1 + h = half h of W
-                            const uint32_t src = (r == 0 ? st + kXSfaOff : st + kXSfwOff + 1024 * (r - 1)) + 512 * at;
-                            const uint32_t dst = r == 0 ? sft + 4 * at : sft + 8 + 4 * (NH * at + r - 1);
-                            if (pad_kb >= 0 && (pad_kb >> 2) == at) {
-                                // byte (kb % 4) of word grp of each 16-byte row
-                                for (int row = 0; row < 32; ++row)
-#pragma unroll
-                                    for (int grp = 0; grp < 4; ++grp)
-                                        asm volatile("st.shared.u8 [%0], %1;"
-                                                     ::"r"(src + 16 * row + 4 * grp + (pad_kb & 3)), "r"(127u)
-                                                     : "memory");
-                                fence_proxy_async_smem();
-                            }
-                            x_cp_sf(dst, x_desc_noswz(src, 128));
-                        }
-                    g_commit(sf_ready + 8 * s);
-                }
-            }
+        if (tc >= 1 && ok) {
+            const int64_t last = tc - 1;
+            (void)mbar_wait(acc_full + 8 * static_cast<int>(last % C::kAccBufs),
+                            static_cast<uint32_t>((last / C::kAccBufs) & 1));
         }
         __syncwarp();
     } else {
         // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 and the 128
-        // columns of half h = (w - 4) / 4 of the tile
-        const int qtr = warp & 3, h = (warp - 4) >> 2;
+        // columns of half h = (w - 2) / 4 of the tile
+        const int qtr = warp & 3, h = (warp - 2) >> 2;
         const int row_in = qtr * 32 + lane;
         int64_t tc = 0;
         for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
