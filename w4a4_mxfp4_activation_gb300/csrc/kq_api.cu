@@ -91,6 +91,22 @@ kq_status make_tensor_map_2d_u8(CUtensorMap *map, void *base, int64_t rows, int6
     return r == CUDA_SUCCESS ? KQ_OK : KQ_ERR_CUDA;
 }
 
+kq_status make_tensor_map_2d_f32(CUtensorMap *map, void *base, int64_t rows, int64_t cols,
+                                 int64_t ld_elems, uint32_t box_cols, uint32_t box_rows,
+                                 CUtensorMapSwizzle swizzle)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr) return KQ_ERR_CUDA;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_elems) * 4};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KQ_OK : KQ_ERR_CUDA;
+}
+
 // ---------------------------------------------------------------------------
 // argument checks (host only; nothing is enqueued when they fail)
 

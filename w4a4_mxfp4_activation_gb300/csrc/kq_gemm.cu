@@ -405,17 +405,25 @@ template <int NH>
 struct XCfg {
     static constexpr int kBN = 128 * NH;                  // tile width (C columns, W rows)
     static constexpr int kStages = 4;
-    static constexpr int kThreads = 64 + 128 * NH;        // producer, MMA, epilogue
+    static constexpr bool kPairs = kStages % 2 == 0;       // stages released in pairs
+    static constexpr int kEpiWarps = 4 * NH;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
     static constexpr int kAccBufs = NH == 1 ? 2 : 1;
     static constexpr int kWCodeBytes = kBN * 128;
     static constexpr int kSfaOff = kXACodeBytes + kWCodeBytes;
     static constexpr int kSfwOff = kSfaOff + 1024;        // A: two scale tiles; W: NH halves x 2
     static constexpr int kStageBytes = kSfwOff + 1024 * NH;
-    static constexpr int kBarOff = kStages * kStageBytes;
+    // per epilogue warp kBoxBufs staging boxes of 32 rows x kBoxCols fp32 for
+    // the TMA stores of C (128-byte swizzle for 32 columns, 64-byte for 16);
+    // the wide tile keeps 4 stages by storing narrower boxes, one at a time
+    static constexpr int kBoxCols = NH == 1 ? 32 : 16;
+    static constexpr int kBoxBufs = NH == 1 ? 2 : 1;
+    static constexpr int kBoxBytes = 32 * kBoxCols * 4;
+    static constexpr int kStagingOff = kStages * kStageBytes;
+    static constexpr int kBarOff = kStagingOff + kEpiWarps * kBoxBufs * kBoxBytes;
     static constexpr int kSmemBytes = kBarOff + 256 + 1024;
     static constexpr uint32_t kSfStride = 8 + 8 * NH;     // TMEM scale columns per stage
     static_assert(kStageBytes % 1024 == 0, "stages keep the 1 KB alignment of the swizzle");
-    static_assert(kStages % 2 == 0, "stages are released in pairs");
     static_assert(kXSfCol + kSfStride * kStages <= kXTmemCols, "scale columns fit in TMEM");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 };
@@ -467,7 +475,7 @@ __device__ __forceinline__ void x_cp_sf(uint32_t taddr, uint64_t sdesc)
 template <int NH>
 __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
     w4a4_mxf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                     const GemmArgs g)
+                     const __grid_constant__ CUtensorMap tmC, const GemmArgs g)
 {
     using C = XCfg<NH>;
     constexpr int kXStages = C::kStages, kXBN = C::kBN, kXWCodeBytes = C::kWCodeBytes;
@@ -486,6 +494,7 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmC);
         for (int s = 0; s < kXStages; ++s) {
             mbar_init(full + 8 * s, 1);
             mbar_init(empty + 8 * s, 1);
@@ -515,7 +524,8 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
                     // stages are released in pairs (s, s + 1 for even s): one
                     // commit per pair, on the pair's barrier
                     if (kk >= kXStages &&
-                        !mbar_wait(empty + 8 * (s >> 1), static_cast<uint32_t>(((kk / kXStages) - 1) & 1))) {
+                        !mbar_wait(empty + 8 * (C::kPairs ? s >> 1 : s),
+                                   static_cast<uint32_t>(((kk / kXStages) - 1) & 1))) {
                         ok = false;
                         break;
                     }
@@ -611,7 +621,10 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
                             x_mma(acc, da + 2 * j, db + 2 * j, ((j & 1) ? id2 : id0) + kIdN, sft + 4 * at,
                                   sft + 8 + 4 * (NH * at), (ks > 0 || j > 0) ? 1u : 0u);
                     }
-                    if (kk & 1) g_commit(empty + 8 * (s >> 1));
+                    if (!C::kPairs)
+                        g_commit(empty + 8 * s);
+                    else if (kk & 1)
+                        g_commit(empty + 8 * (s >> 1));
                     if (ks == g.ksteps - 1) g_commit(acc_full + 8 * b);
                 }
                 __syncwarp();
@@ -627,8 +640,9 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
         // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 and the 128
         // columns of half h = (w - 2) / 4 of the tile
         const int qtr = warp & 3, h = (warp - 2) >> 2;
-        const int row_in = qtr * 32 + lane;
-        int64_t tc = 0;
+        const uint32_t stg = base + C::kStagingOff +
+                             static_cast<uint32_t>(C::kBoxBufs * C::kBoxBytes * (warp - 2));
+        int64_t tc = 0, nbox = 0;
         for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
             const int b = static_cast<int>(tc % C::kAccBufs);
             const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full + 8 * b,
@@ -678,24 +692,59 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             g_fence_before();
             mbar_arrive(acc_empty + 8 * b);      // the accumulator may be overwritten now
+            // C through shared memory: 128 / kBoxCols boxes per warp, each
+            // written row = lane in the swizzle of the TMA map, then one TMA
+            // store (clipped at the last row of C) while the next box is filled
+            // (the TMA store writes whole 16-byte units of a row, so its map
+            // covers the first n4 = 4 floor(n / 4) columns; the last n % 4
+            // columns are stored directly)
             const int64_t mt = t / g.ntiles, nt = t % g.ntiles;
-            const int64_t row = mt * 128 + row_in;
-            const int64_t col0 = nt * kXBN + 128 * h;
-            if (row < g.m && col0 < g.n) {
-                float *crow = g.c + row * g.ldc + col0;
-                if (col0 + 128 <= g.n) {
+            const int64_t y0 = mt * 128 + 32 * qtr, x0 = nt * kXBN + 128 * h;
+            const int64_t n4 = g.n & ~int64_t(3);
+            constexpr int kBC = C::kBoxCols, kChunks = kBC / 4;
+            if (y0 < g.m && x0 < n4) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        stg_f4(crow + 4 * j, make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                         __uint_as_float(v[4 * j + 2]),
-                                                         __uint_as_float(v[4 * j + 3])));
-                } else {
+                for (int c = 0; c < 128 / kBC; ++c, ++nbox) {
+                    if (x0 + kBC * c >= n4) break;           // boxes past column n4 of C
+                    const uint32_t buf =
+                        stg + static_cast<uint32_t>(C::kBoxBytes) * static_cast<uint32_t>(nbox % C::kBoxBufs);
+                    if (nbox >= C::kBoxBufs) {
+                        // the box's last store has read it
+                        if (lane == 0) {
+                            if constexpr (C::kBoxBufs == 2)
+                                bulk_wait_group_read<1>();
+                            else
+                                bulk_wait_group_read<0>();
+                        }
+                        __syncwarp();
+                    }
+                    // 16-byte chunk q of row r sits at q ^ (r & 7) (128-byte
+                    // swizzle) or q ^ ((r >> 1) & 3) (64-byte swizzle)
+                    const uint32_t sw = kBC == 32 ? static_cast<uint32_t>(lane & 7)
+                                                  : static_cast<uint32_t>((lane >> 1) & 3);
 #pragma unroll
-                    for (int j = 0; j < 128; ++j)
-                        if (col0 + j < g.n) crow[j] = __uint_as_float(v[j]);
+                    for (int q = 0; q < kChunks; ++q)
+                        sts128(buf + static_cast<uint32_t>(kBC * 4 * lane) + ((q ^ sw) << 4),
+                               make_uint4(v[kBC * c + 4 * q], v[kBC * c + 4 * q + 1], v[kBC * c + 4 * q + 2],
+                                          v[kBC * c + 4 * q + 3]));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, static_cast<int32_t>(x0 + kBC * c), static_cast<int32_t>(y0), buf);
+                        bulk_commit_group();
+                    }
+                    __syncwarp();
                 }
             }
+            if (n4 < g.n && x0 <= n4 && n4 < x0 + 128 && y0 + lane < g.m) {
+                float *crow = g.c + (y0 + lane) * g.ldc + x0;
+#pragma unroll
+                for (int j = 0; j < 128; ++j)
+                    if (x0 + j >= n4 && x0 + j < g.n) crow[j] = __uint_as_float(v[j]);
+            }
         }
+        if (lane == 0) bulk_wait_group_all();   // the stores have read shared memory and landed
+        __syncwarp();
     }
 
     g_fence_before();
@@ -780,8 +829,8 @@ __global__ void __launch_bounds__(256) layer_error_kernel(const float *__restric
 }
 
 template <int NH>
-kq_status launch_mxf4_t(const CUtensorMap &ma, const CUtensorMap &mw, const GemmArgs &g,
-                        int sm_count, cudaStream_t stream)
+kq_status launch_mxf4_t(const CUtensorMap &ma, const CUtensorMap &mw, const CUtensorMap &mc,
+                        const GemmArgs &g, int sm_count, cudaStream_t stream)
 {
     using C = XCfg<NH>;
     auto kern = w4a4_mxf4_kernel<NH>;
@@ -795,7 +844,8 @@ kq_status launch_mxf4_t(const CUtensorMap &ma, const CUtensorMap &mw, const Gemm
     if (slot.err[dev] != cudaSuccess) return KQ_ERR_CUDA;
     const int64_t tiles = g.mtiles * g.ntiles;
     const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count));
-    return launch_pdl(kern, grid, C::kThreads, static_cast<size_t>(C::kSmemBytes), stream, ma, mw, g);
+    return launch_pdl(kern, grid, C::kThreads, static_cast<size_t>(C::kSmemBytes), stream, ma, mw, mc,
+                      g);
 }
 
 kq_status launch_w4a4_mxf4(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, const uint8_t *qw,
@@ -831,8 +881,14 @@ kq_status launch_w4a4_mxf4(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, 
     g.mtiles = (m + 127) / 128;
     g.ntiles = (n + bn - 1) / bn;
     g.ksteps = (k + kXBK - 1) / kXBK;
-    return wide ? launch_mxf4_t<2>(ma, mw, g, info.sm_count, stream)
-                : launch_mxf4_t<1>(ma, mw, g, info.sm_count, stream);
+    CUtensorMap mc;   // the first 4 floor(n / 4) columns (at least 4: never stored past n)
+    const int64_t n4 = std::max<int64_t>(n & ~int64_t(3), 4);
+    const uint32_t box_cols = static_cast<uint32_t>(wide ? XCfg<2>::kBoxCols : XCfg<1>::kBoxCols);
+    st = make_tensor_map_2d_f32(&mc, c, m, n4, ldc, box_cols, 32,
+                                box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (st != KQ_OK) return st;
+    return wide ? launch_mxf4_t<2>(ma, mw, mc, g, info.sm_count, stream)
+                : launch_mxf4_t<1>(ma, mw, mc, g, info.sm_count, stream);
 }
 
 }  // namespace

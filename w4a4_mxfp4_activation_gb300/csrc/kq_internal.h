@@ -50,6 +50,9 @@ kq_status make_tensor_map_2d_bf16(CUtensorMap *map, const void *base, int64_t ro
 kq_status make_tensor_map_2d_u8(CUtensorMap *map, void *base, int64_t rows, int64_t cols,
                                 int64_t ld_bytes, uint32_t box_cols, uint32_t box_rows,
                                 CUtensorMapSwizzle swizzle);
+kq_status make_tensor_map_2d_f32(CUtensorMap *map, void *base, int64_t rows, int64_t cols,
+                                 int64_t ld_elems, uint32_t box_cols, uint32_t box_rows,
+                                 CUtensorMapSwizzle swizzle);
 kq_status check_launch();
 
 // The kernels walk tiles in 32-bit arithmetic: row and column tile indices,
