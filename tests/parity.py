@@ -102,8 +102,7 @@ def check_side_output(A_bits: np.ndarray, d: int, kind: str, param, at_gpu: np.n
     """Rules (iv)-(v) for the bf16 side output on the given rows (all if None)."""
     m = A_bits.shape[0]
     rows = np.arange(m) if rows is None else np.asarray(rows, np.int64)
-    y_ref, bound = O.transform(np.ascontiguousarray(A_bits[rows]), d, kind, param,
-                               in_format=in_format)
+    y_ref, bound = O.transform(np.ascontiguousarray(A_bits[rows]), d, kind, param)
     tol = np.ldexp(bound, -16)
     lo = O.round_bf16(y_ref - tol)
     hi = O.round_bf16(y_ref + tol)

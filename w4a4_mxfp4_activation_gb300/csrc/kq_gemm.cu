@@ -457,7 +457,7 @@ __device__ __forceinline__ void x_mma(uint32_t d, uint64_t a, uint64_t b, uint32
         : "memory");
 }
 
-// One lane of the (converged) warp, the same for every caller.
+// elect.sync: one lane of the converged warp.
 __device__ __forceinline__ bool elect_one()
 {
     uint32_t pred;
@@ -566,6 +566,9 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
         int64_t kk = 0, tc = 0;
         bool ok = true;
         const bool pad_fix = (g.nb & 1) != 0;
+        // the issuing lane, elected once: a commit tracks only the tcgen05
+        // operations of its own thread, so one lane issues everything
+        const bool leader = elect_one();
         constexpr uint32_t id0 = x_idesc(0), id2 = x_idesc(2);
         constexpr uint32_t kIdN = static_cast<uint32_t>((NH - 1) * (128 >> 3)) << 17;  // N += 128
         for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc) {
@@ -611,7 +614,7 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
                 const uint32_t sft = tmem_base + kXSfCol + kXSfStride * s;
                 const uint64_t da = g_desc(st), db = g_desc(st + kXACodeBytes);
                 const uint64_t dsa = x_desc_noswz(sfa_s, 128), dsw = x_desc_noswz(sfw_s, 128);
-                if (elect_one()) {
+                if (leader) {
                     for (int at = 0; at < (nmma + 1) / 2; ++at) {
                         x_cp_sf(sft + 4 * at, dsa + 32 * at);
 #pragma unroll

@@ -118,6 +118,15 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
                  : "memory");
 }
 
+// elect.sync: one lane of the converged warp.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(pred));
+    return pred != 0;
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -284,6 +293,9 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int a = warp - 1;               // accumulator buffer; tiles with it % 2 == a
         int64_t it = a;
         bool ok = true;
+        // the issuing lane, elected once (a commit tracks only the tcgen05
+        // operations of its own thread)
+        const bool leader = elect_one();
         for (TileWalk tw(static_cast<int>(blockIdx.x + a * gridDim.x),
                          static_cast<int>(2 * gridDim.x), static_cast<int>(p.ncol_tiles));
              tw.rt < p.nrow_tiles && ok; tw.next(), it += 2) {
@@ -297,7 +309,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             const uint32_t stage = base + s * Cfg::kStageBytes;
             tc_fence_after();
-            if (lane == 0) {
+            if (leader) {
                 const uint32_t d0 = tmem_base + a * kAccCols;
                 for (int b = 0; b < nblk; ++b)
                     for (int h = 0; h < 2; ++h)       // input half h: K = 16 step
