@@ -264,7 +264,7 @@ KQ_API kq_status kq_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sf
  *   operand tile dequantized to bf16 in shared memory (exact) and multiplied
  *   with kind::f16 -- an independent route to the same sums, for checking;
  *   2 / 3 = the FP4 kernel with its tile width fixed at 128 / 256 columns of
- *   C (variant 0 picks 256 when K >= 2048 and the wide tiles fill the GPU).
+ *   C (variant 0 picks the width from the number of tiles per SM and K).
  *   Other values: KQ_ERR_LAYOUT.
  */
 KQ_API kq_status kq_w4a4_gemm_variant(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa,

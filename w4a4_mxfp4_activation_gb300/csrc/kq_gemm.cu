@@ -862,11 +862,18 @@ kq_status launch_w4a4_mxf4(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, 
     st = make_tensor_map_2d_u8(&ma, const_cast<uint8_t *>(qa), m, k / 2, ldqa, 128, 128,
                                CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != KQ_OK) return st;
-    // the wide tile pays when a tile runs long enough (K >= 2048) to hide its
-    // epilogue and there are tiles enough to fill the GPU
-    const int64_t mtiles = (m + 127) / 128;
-    const bool wide = wide_sel >= 0 ? wide_sel == 1
-                                    : (k >= 2048 && mtiles * ((n + 255) / 256) >= info.sm_count);
+    // Tile width by a wave model fitted on GB300: a CTA's time is its tile
+    // count times (K stages x the stage time + the tile's exposed epilogue),
+    // in narrow-stage units -- a wide stage (twice the work) costs 1.35, the
+    // narrow tile's epilogue is mostly hidden behind its second accumulator
+    // (0.5), the wide tile's single accumulator exposes about 2.
+    const int64_t mtiles = (m + 127) / 128, ksteps = (k + kXBK - 1) / kXBK;
+    auto cost = [&](int64_t bn, double per_stage, double per_tile) {
+        const int64_t tiles = mtiles * ((n + bn - 1) / bn);
+        const int64_t waves = (tiles + info.sm_count - 1) / info.sm_count;
+        return static_cast<double>(waves) * (static_cast<double>(ksteps) * per_stage + per_tile);
+    };
+    const bool wide = wide_sel >= 0 ? wide_sel == 1 : cost(256, 1.35, 2.0) < cost(128, 1.0, 0.5);
     const int bn = wide ? 256 : 128;
     st = make_tensor_map_2d_u8(&mw, const_cast<uint8_t *>(qw), n, k / 2, ldqw, 128,
                                static_cast<uint32_t>(bn), CU_TENSOR_MAP_SWIZZLE_128B);
