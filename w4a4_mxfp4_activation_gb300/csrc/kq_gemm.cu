@@ -91,6 +91,15 @@ __device__ __forceinline__ void g_mma(uint32_t d, uint64_t a, uint64_t b, uint32
         "l"(a), "l"(b), "r"(kGIdesc), "r"(acc)
         : "memory");
 }
+__device__ __forceinline__ void g_mma_id(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 __device__ __forceinline__ void g_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -396,14 +405,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
 // accumulator into registers and release it before they store, so the next
 // tile's MMAs start while the stores drain.
 
-constexpr int kXBK = 256;                          // K elements per stage
 constexpr int kXACodeBytes = 128 * 128;            // A codes per stage
 constexpr uint32_t kXTmemCols = 512;
 constexpr uint32_t kXSfCol = 256;                  // scale columns follow the accumulators
 
-template <int NH>
+// MX = true: the FP4 product (codes + scale tiles, kind::mxf4, K = 256 per
+// stage); MX = false: the bf16 product A W^T on the same structure (kind::f16,
+// K = 64 per stage -- again 128 bytes of every operand row -- no scales).
+template <int NH, bool MX>
 struct XCfg {
     static constexpr int kBN = 128 * NH;                  // tile width (C columns, W rows)
+    static constexpr int kBK = MX ? 256 : 64;             // K elements per stage
     static constexpr int kStages = 4;
     static constexpr bool kPairs = kStages % 2 == 0;       // stages released in pairs
     static constexpr int kEpiWarps = 4 * NH;
@@ -412,7 +424,7 @@ struct XCfg {
     static constexpr int kWCodeBytes = kBN * 128;
     static constexpr int kSfaOff = kXACodeBytes + kWCodeBytes;
     static constexpr int kSfwOff = kSfaOff + 1024;        // A: two scale tiles; W: NH halves x 2
-    static constexpr int kStageBytes = kSfwOff + 1024 * NH;
+    static constexpr int kStageBytes = MX ? kSfwOff + 1024 * NH : kSfaOff;
     // per epilogue warp kBoxBufs staging boxes of 32 rows x kBoxCols fp32 for
     // the TMA stores of C (128-byte swizzle for 32 columns, 64-byte for 16);
     // the wide tile keeps 4 stages by storing narrower boxes, one at a time
@@ -472,13 +484,14 @@ __device__ __forceinline__ void x_cp_sf(uint32_t taddr, uint64_t sdesc)
                  : "memory");
 }
 
-template <int NH>
-__global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
+template <int NH, bool MX>
+__global__ void __launch_bounds__(XCfg<NH, MX>::kThreads, 1)
     w4a4_mxf4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmC, const GemmArgs g)
 {
-    using C = XCfg<NH>;
+    using C = XCfg<NH, MX>;
     constexpr int kXStages = C::kStages, kXBN = C::kBN, kXWCodeBytes = C::kWCodeBytes;
+    constexpr int kXBK = C::kBK;
     constexpr int kXSfaOff = C::kSfaOff, kXSfwOff = C::kSfwOff, kXStageBytes = C::kStageBytes;
     constexpr uint32_t kXSfStride = C::kSfStride;
     extern __shared__ uint8_t smem_raw[];
@@ -533,21 +546,26 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
                     // use (none for a half of W past the edge of C)
                     const int64_t rem = (g.k - ks * kXBK + 63) / 64;
                     const int64_t nmma = rem < 4 ? rem : 4;
-                    const uint32_t sf_bytes = static_cast<uint32_t>((nmma + 1) / 2) * 512u;
+                    const uint32_t sf_bytes = MX ? static_cast<uint32_t>((nmma + 1) / 2) * 512u : 0u;
                     const bool w1 = NH == 2 && 2 * nt + 1 < wrt;
                     const uint32_t st = base + s * kXStageBytes;
                     mbar_arrive_expect_tx(full + 8 * s, kXACodeBytes + kXWCodeBytes +
                                                             (w1 ? 3u : 2u) * sf_bytes);
-                    const int32_t x = static_cast<int32_t>(ks * 128);
+                    // 128 bytes of every row: 128 packed-code bytes or 64 bf16
+                    const int32_t x = static_cast<int32_t>(ks * (MX ? 128 : 64));
                     tma_load_2d(st, &tmA, x, static_cast<int32_t>(mt * 128), full + 8 * s, 0);
                     tma_load_2d(st + kXACodeBytes, &tmW, x, static_cast<int32_t>(nt * kXBN),
                                 full + 8 * s, 0);
-                    bulk_load(st + kXSfaOff, g.sfa + (mt * g.ncb + 2 * ks) * 512, sf_bytes, full + 8 * s);
-                    bulk_load(st + kXSfwOff, g.sfw + (NH * nt * g.ncb + 2 * ks) * 512, sf_bytes,
-                              full + 8 * s);
-                    if (w1)
-                        bulk_load(st + kXSfwOff + 1024, g.sfw + ((2 * nt + 1) * g.ncb + 2 * ks) * 512,
-                                  sf_bytes, full + 8 * s);
+                    if constexpr (MX) {
+                        bulk_load(st + kXSfaOff, g.sfa + (mt * g.ncb + 2 * ks) * 512, sf_bytes,
+                                  full + 8 * s);
+                        bulk_load(st + kXSfwOff, g.sfw + (NH * nt * g.ncb + 2 * ks) * 512, sf_bytes,
+                                  full + 8 * s);
+                        if (w1)
+                            bulk_load(st + kXSfwOff + 1024,
+                                      g.sfw + ((2 * nt + 1) * g.ncb + 2 * ks) * 512, sf_bytes,
+                                      full + 8 * s);
+                    }
                 }
             }
             // the last copies issued into each stage have landed before exit
@@ -565,7 +583,7 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
         // its scale bytes to 2^0 (lane r: row r of each tile).
         int64_t kk = 0, tc = 0;
         bool ok = true;
-        const bool pad_fix = (g.nb & 1) != 0;
+        const bool pad_fix = MX && (g.nb & 1) != 0;
         // the issuing lane, elected once: a commit tracks only the tcgen05
         // operations of its own thread, so one lane issues everything
         const bool leader = elect_one();
@@ -614,7 +632,20 @@ __global__ void __launch_bounds__(XCfg<NH>::kThreads, 1)
                 const uint32_t sft = tmem_base + kXSfCol + kXSfStride * s;
                 const uint64_t da = g_desc(st), db = g_desc(st + kXACodeBytes);
                 const uint64_t dsa = x_desc_noswz(sfa_s, 128), dsw = x_desc_noswz(sfw_s, 128);
-                if (leader) {
+                if (leader && !MX) {
+                    // kind::f16: four K = 16 steps of 32 bytes; zero fill past k
+                    constexpr uint32_t kIdF16 = (1u << 4) | (1u << 7) | (1u << 10) |
+                                                ((static_cast<uint32_t>(kXBN) >> 3) << 17) |
+                                                ((128u >> 4) << 24);
+                    for (int j = 0; j < 4; ++j)
+                        g_mma_id(acc, da + 2 * j, db + 2 * j, kIdF16, (ks > 0 || j > 0) ? 1u : 0u);
+                    if (!C::kPairs)
+                        g_commit(empty + 8 * s);
+                    else if (kk & 1)
+                        g_commit(empty + 8 * (s >> 1));
+                    if (ks == g.ksteps - 1) g_commit(acc_full + 8 * b);
+                }
+                if (leader && MX) {
                     for (int at = 0; at < (nmma + 1) / 2; ++at) {
                         x_cp_sf(sft + 4 * at, dsa + 32 * at);
 #pragma unroll
@@ -831,12 +862,12 @@ __global__ void __launch_bounds__(256) layer_error_kernel(const float *__restric
     }
 }
 
-template <int NH>
+template <int NH, bool MX>
 kq_status launch_mxf4_t(const CUtensorMap &ma, const CUtensorMap &mw, const CUtensorMap &mc,
                         const GemmArgs &g, int sm_count, cudaStream_t stream)
 {
-    using C = XCfg<NH>;
-    auto kern = w4a4_mxf4_kernel<NH>;
+    using C = XCfg<NH, MX>;
+    auto kern = w4a4_mxf4_kernel<NH, MX>;
     static GSlot slot;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
@@ -867,7 +898,7 @@ kq_status launch_w4a4_mxf4(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, 
     // in narrow-stage units -- a wide stage (twice the work) costs 1.35, the
     // narrow tile's epilogue is mostly hidden behind its second accumulator
     // (0.5), the wide tile's single accumulator exposes about 2.
-    const int64_t mtiles = (m + 127) / 128, ksteps = (k + kXBK - 1) / kXBK;
+    const int64_t mtiles = (m + 127) / 128, ksteps = (k + 255) / 256;
     auto cost = [&](int64_t bn, double per_stage, double per_tile) {
         const int64_t tiles = mtiles * ((n + bn - 1) / bn);
         const int64_t waves = (tiles + info.sm_count - 1) / info.sm_count;
@@ -890,15 +921,15 @@ kq_status launch_w4a4_mxf4(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, 
     g.ldc = ldc;
     g.mtiles = (m + 127) / 128;
     g.ntiles = (n + bn - 1) / bn;
-    g.ksteps = (k + kXBK - 1) / kXBK;
+    g.ksteps = (k + 255) / 256;
     CUtensorMap mc;   // the first 4 floor(n / 4) columns (at least 4: never stored past n)
     const int64_t n4 = std::max<int64_t>(n & ~int64_t(3), 4);
-    const uint32_t box_cols = static_cast<uint32_t>(wide ? XCfg<2>::kBoxCols : XCfg<1>::kBoxCols);
+    const uint32_t box_cols = static_cast<uint32_t>(wide ? XCfg<2, true>::kBoxCols : XCfg<1, true>::kBoxCols);
     st = make_tensor_map_2d_f32(&mc, c, m, n4, ldc, box_cols, 32,
                                 box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (st != KQ_OK) return st;
-    return wide ? launch_mxf4_t<2>(ma, mw, mc, g, info.sm_count, stream)
-                : launch_mxf4_t<1>(ma, mw, mc, g, info.sm_count, stream);
+    return wide ? launch_mxf4_t<2, true>(ma, mw, mc, g, info.sm_count, stream)
+                : launch_mxf4_t<1, true>(ma, mw, mc, g, info.sm_count, stream);
 }
 
 }  // namespace
@@ -958,10 +989,24 @@ kq_status launch_bf16_gemm(const uint16_t *a, int64_t lda, const uint16_t *w, in
     DeviceInfo info;
     kq_status st = device_info(info);
     if (st != KQ_OK) return st;
-    CUtensorMap ma, mw;
-    st = make_tensor_map_2d_bf16(&ma, a, m, k, lda, kGBK, kGBM);
+    // tile width by the same wave model as the FP4 product (K stages of 64)
+    const int64_t mtiles = (m + 127) / 128, ksteps = (k + 63) / 64;
+    auto cost = [&](int64_t bn, double per_stage, double per_tile) {
+        const int64_t tiles = mtiles * ((n + bn - 1) / bn);
+        const int64_t waves = (tiles + info.sm_count - 1) / info.sm_count;
+        return static_cast<double>(waves) * (static_cast<double>(ksteps) * per_stage + per_tile);
+    };
+    const bool wide = cost(256, 1.35, 2.0) < cost(128, 1.0, 0.5);
+    const int bn = wide ? 256 : 128;
+    CUtensorMap ma, mw, mc;
+    st = make_tensor_map_2d_bf16(&ma, a, m, k, lda, 64, 128);
     if (st != KQ_OK) return st;
-    st = make_tensor_map_2d_bf16(&mw, w, n, k, ldw, kGBK, kGBN);
+    st = make_tensor_map_2d_bf16(&mw, w, n, k, ldw, 64, static_cast<uint32_t>(bn));
+    if (st != KQ_OK) return st;
+    const int64_t n4 = std::max<int64_t>(n & ~int64_t(3), 4);
+    const uint32_t box_cols = static_cast<uint32_t>(wide ? XCfg<2, false>::kBoxCols : XCfg<1, false>::kBoxCols);
+    st = make_tensor_map_2d_f32(&mc, c, m, n4, ldc, box_cols, 32,
+                                box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     if (st != KQ_OK) return st;
     GemmArgs g;
     g.m = m;
@@ -973,10 +1018,11 @@ kq_status launch_bf16_gemm(const uint16_t *a, int64_t lda, const uint16_t *w, in
     g.sfw = nullptr;
     g.c = c;
     g.ldc = ldc;
-    g.mtiles = (m + kGBM - 1) / kGBM;
-    g.ntiles = (n + kGBN - 1) / kGBN;
-    g.ksteps = (k + kGBK - 1) / kGBK;
-    return launch_gemm_t<true>(ma, mw, g, info.sm_count, stream);
+    g.mtiles = mtiles;
+    g.ntiles = (n + bn - 1) / bn;
+    g.ksteps = ksteps;
+    return wide ? launch_mxf4_t<2, false>(ma, mw, mc, g, info.sm_count, stream)
+                : launch_mxf4_t<1, false>(ma, mw, mc, g, info.sm_count, stream);
 }
 
 }  // namespace kq
