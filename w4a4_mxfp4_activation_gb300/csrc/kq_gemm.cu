@@ -1,38 +1,36 @@
 // Consumer of the quantizer's output: the W4A4 product of eq. (11) on the
-// 5th-generation tensor cores, sm_103a.
+// 5th-generation tensor cores, sm_103a, and the pieces of the layer error of
+// eq. (2).
 //
 // "KroQuant: Kronecker-Structured Block Transforms for Efficient Post-
 // Training Quantization of Diffusion Transformers", eq. (11) multiplies the
 // MXFP4-quantized transformed activations by the MXFP4-quantized transformed
-// weights, and eq. (2) measures the layer's error through that product.  This
-// kernel computes
+// weights, and eq. (2) measures the layer's error through that product:
 //     C[i][n] = sum_k deq(A)[i][k] * deq(W)[n][k]
 // from packed E2M1 codes ([rows][d/2] bytes, code 2k in the low nibble) and
 // E8M0 scales in the 128x4 tiled layout of block-scaled MMA -- exactly the
-// bytes kq_quantize_mxfp4 writes -- or, in its bf16 mode, from bf16 A and W
-// (the unquantized reference product of eq. 2).
+// bytes kq_quantize_mxfp4 writes.  Three kernels:
+//   w4a4_mxf4_kernel<NH, true>   the product on the FP4 tensor cores
+//                                (tcgen05.mma kind::mxf4, block-scaled): the
+//                                library's W4A4 GEMM;
+//   w4a4_mxf4_kernel<NH, false>  the same structure on bf16 A and W (kind::f16):
+//                                the unquantized reference product A W^T;
+//   w4a4_gemm_kernel             a checking route for the W4A4 product: every
+//                                operand tile dequantized to bf16 in shared
+//                                memory (exact: an MXFP4 element times its
+//                                power-of-two scale has at most two significant
+//                                bits) and multiplied with kind::f16;
+// and the fp64 error sums.  Every wait is bounded in time; a CTA that times
+// out stops and leaves its remaining tiles unwritten, and the call reports
+// nothing (results are then undefined), as for the quantizers.
 //
-// An MXFP4 element times its power-of-two scale has at most two significant
-// bits, so it is exact in bf16 (subnormals included).  Each operand tile is
-// therefore dequantized into bf16 in shared memory and multiplied with
-// tcgen05.mma kind::f16 (fp32 accumulation in TMEM): the same products a
-// block-scaled MXFP4 MMA forms, summed in fp32.
-//
-// Roles in a CTA (persistent over 128 x 128 output tiles; K in steps of 64):
-//   warp 0      producer: per K step the code tiles of A and W (TMA, 128 rows
-//               x 32 bytes each) and their 512-byte scale tiles (bulk copies)
-//               into a 4-deep ring -- or, in the bf16 mode, the two 128 x 64
-//               bf16 operand boxes straight into an operand buffer;
-//   warp 1      MMA issuer: four M = 128, N = 128, K = 16 MMAs per K step
-//               into one of two TMEM accumulators (128 columns each);
-//   warps 2-5   dequantization (MXFP4 mode): thread r turns row r of both
-//               code tiles into bf16 rows of the 128B-swizzled operand
-//               buffers (two of them, double-buffered);
-//   warps 6-9   epilogue: read the accumulator back (tcgen05.ld) and store
-//               the fp32 rows of C.
-// Every wait is bounded in time; a CTA that times out stops and leaves its
-// remaining tiles unwritten, and the call reports nothing (results are then
-// undefined), as for the quantizers.
+// The checking kernel (persistent over 128 x 128 output tiles; K in steps of
+// 64): warp 0 loads per K step the code tiles of A and W (TMA, 128 rows x 32
+// bytes each) and their 512-byte scale tiles (bulk copies) into a 4-deep
+// ring; warp 1 issues four M = 128, N = 128, K = 16 MMAs per K step into one
+// of two TMEM accumulators; warps 2-5 dequantize (thread r turns row r of
+// both code tiles into bf16 rows of the 128B-swizzled, double-buffered
+// operand buffers); warps 6-9 read the accumulator back and store fp32 rows.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -158,7 +156,6 @@ struct GemmArgs {
     int64_t mtiles, ntiles, ksteps;
 };
 
-template <bool BF16>
 __global__ void __launch_bounds__(kGThreads, 1)
     w4a4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                      const GemmArgs g)
@@ -181,7 +178,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             mbar_init(code_empty + 8 * s, 128);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(op_full + 8 * b, BF16 ? 1 : 128);   // TMA (bf16) or the dequant threads
+            mbar_init(op_full + 8 * b, 128);               // the dequantization threads
             mbar_init(op_free + 8 * b, 1);                 // MMA commit
             mbar_init(acc_full + 8 * b, 1);
             mbar_init(acc_empty + 8 * b, 128);
@@ -203,50 +200,30 @@ __global__ void __launch_bounds__(kGThreads, 1)
             for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
                 const int64_t mt = t / g.ntiles, nt = t % g.ntiles;
                 for (int64_t ks = 0; ks < g.ksteps && ok; ++ks, ++kk) {
-                    if (BF16) {
-                        // straight into operand buffer kk % 2 once the MMAs freed it
-                        const int b = static_cast<int>(kk & 1);
-                        if (kk >= 2 && !mbar_wait(op_free + 8 * b, static_cast<uint32_t>(((kk >> 1) - 1) & 1))) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t opa = base + kGOpOff + b * 2 * kGOpBytes;
-                        mbar_arrive_expect_tx(op_full + 8 * b, 2 * kGOpBytes);
-                        tma_load_2d(opa, &tmA, static_cast<int32_t>(ks * kGBK),
-                                    static_cast<int32_t>(mt * kGBM), op_full + 8 * b, 0);
-                        tma_load_2d(opa + kGOpBytes, &tmW, static_cast<int32_t>(ks * kGBK),
-                                    static_cast<int32_t>(nt * kGBN), op_full + 8 * b, 0);
-                    } else {
-                        const int s = static_cast<int>(kk % kGStages);
-                        if (kk >= kGStages &&
-                            !mbar_wait(code_empty + 8 * s, static_cast<uint32_t>(((kk / kGStages) - 1) & 1))) {
-                            ok = false;
-                            break;
-                        }
-                        const uint32_t st = base + kGRingOff + s * kGStageBytes;
-                        mbar_arrive_expect_tx(code_full + 8 * s, kGStageBytes);
-                        tma_load_2d(st, &tmA, static_cast<int32_t>(ks * 32),
-                                    static_cast<int32_t>(mt * kGBM), code_full + 8 * s, 0);
-                        tma_load_2d(st + kGCodeBytes, &tmW, static_cast<int32_t>(ks * 32),
-                                    static_cast<int32_t>(nt * kGBN), code_full + 8 * s, 0);
-                        // the 128x4 scale tile holding this K step's two blocks
-                        bulk_load(st + 2 * kGCodeBytes, g.sfa + (mt * g.ncb + ks / 2) * 512, 512,
-                                  code_full + 8 * s);
-                        bulk_load(st + 2 * kGCodeBytes + kGSfBytes, g.sfw + (nt * g.ncb + ks / 2) * 512,
-                                  512, code_full + 8 * s);
+                    const int s = static_cast<int>(kk % kGStages);
+                    if (kk >= kGStages &&
+                        !mbar_wait(code_empty + 8 * s, static_cast<uint32_t>(((kk / kGStages) - 1) & 1))) {
+                        ok = false;
+                        break;
                     }
+                    const uint32_t st = base + kGRingOff + s * kGStageBytes;
+                    mbar_arrive_expect_tx(code_full + 8 * s, kGStageBytes);
+                    tma_load_2d(st, &tmA, static_cast<int32_t>(ks * 32),
+                                static_cast<int32_t>(mt * kGBM), code_full + 8 * s, 0);
+                    tma_load_2d(st + kGCodeBytes, &tmW, static_cast<int32_t>(ks * 32),
+                                static_cast<int32_t>(nt * kGBN), code_full + 8 * s, 0);
+                    // the 128x4 scale tile holding this K step's two blocks
+                    bulk_load(st + 2 * kGCodeBytes, g.sfa + (mt * g.ncb + ks / 2) * 512, 512,
+                              code_full + 8 * s);
+                    bulk_load(st + 2 * kGCodeBytes + kGSfBytes, g.sfw + (nt * g.ncb + ks / 2) * 512,
+                              512, code_full + 8 * s);
                 }
             }
             // the last copies issued into each buffer have landed before the
             // CTA may exit (they have, unless a wait above gave up)
-            const int nbuf = BF16 ? 2 : kGStages;
-            for (int64_t j = kk - 1; j >= 0 && j >= kk - nbuf; --j) {
-                if (BF16)
-                    (void)mbar_wait(op_full + 8 * static_cast<int>(j & 1), static_cast<uint32_t>((j >> 1) & 1));
-                else
-                    (void)mbar_wait(code_full + 8 * static_cast<int>(j % kGStages),
-                                    static_cast<uint32_t>((j / kGStages) & 1));
-            }
+            for (int64_t j = kk - 1; j >= 0 && j >= kk - kGStages; --j)
+                (void)mbar_wait(code_full + 8 * static_cast<int>(j % kGStages),
+                                static_cast<uint32_t>((j / kGStages) & 1));
         }
     } else if (warp == 1) {
         int64_t kk = 0, tc = 0;
@@ -277,7 +254,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             (void)mbar_wait(acc_full + 8 * static_cast<int>((tc - 1) & 1),
                             static_cast<uint32_t>(((tc - 1) >> 1) & 1));
     } else if (warp < 6) {
-        if (!BF16) {
+        {
             // dequantization: thread r owns row r of both code tiles
             const int r = threadIdx.x - 64;
             int64_t kk = 0;
@@ -794,11 +771,10 @@ struct GSlot {
     cudaError_t err[64] = {};
 };
 
-template <bool BF16>
-kq_status launch_gemm_t(const CUtensorMap &ma, const CUtensorMap &mw, const GemmArgs &g,
-                        int sm_count, cudaStream_t stream)
+kq_status launch_dequant(const CUtensorMap &ma, const CUtensorMap &mw, const GemmArgs &g,
+                         int sm_count, cudaStream_t stream)
 {
-    auto kern = w4a4_gemm_kernel<BF16>;
+    auto kern = w4a4_gemm_kernel;
     static GSlot slot;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
@@ -979,7 +955,7 @@ kq_status launch_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa, 
     g.mtiles = (m + kGBM - 1) / kGBM;
     g.ntiles = (n + kGBN - 1) / kGBN;
     g.ksteps = (k + kGBK - 1) / kGBK;
-    return launch_gemm_t<false>(ma, mw, g, info.sm_count, stream);
+    return launch_dequant(ma, mw, g, info.sm_count, stream);
 }
 
 kq_status launch_bf16_gemm(const uint16_t *a, int64_t lda, const uint16_t *w, int64_t ldw,
