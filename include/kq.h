@@ -119,7 +119,9 @@ typedef enum {
  *   K_expanded device, output of kq_expand_blocks(..., KQ_K_BF16X3, ...), or
  *              NULL.  With K_expanded != NULL the transform runs on the
  *              tensor cores (tcgen05.mma, fp32 accumulation in TMEM) against
- *              the dense 32x32 K_j as three bf16 terms -- the fastest path;
+ *              the dense 32x32 K_j as three bf16 terms -- the fastest path
+ *              (when factors are given as well, layers of fewer than 2^21
+ *              elements take the butterfly below, faster there);
  *              otherwise, with factors != NULL, the five 2x2 factors are
  *              applied as an in-register butterfly on the CUDA cores; with
  *              both NULL the transform is the identity (the bare quantizer,

@@ -843,3 +843,20 @@ def test_ex_bf16_matches_entry_points():
     ]
     for (q1, s1, _), (q2, s2, _) in pairs:
         assert torch.equal(q1, q2) and torch.equal(s1, s2)
+
+
+@pytest.mark.parametrize("m,d,expect", [(256, 1152, "butterfly"), (1024, 1152, "butterfly"),
+                                        (1024, 3072, "umma")])
+def test_default_dispatch_with_both_factor_forms(m, d, expect):
+    """kq_quantize_mxfp4 given the raw factors and the expanded blocks runs
+    the butterfly below 2^21 elements and the tensor cores above: its bytes
+    equal those of that variant called explicitly."""
+    A_bits = synth.activations(m, d, 2100 + m, "flux")
+    A = to_bf16(A_bits)
+    F, _ = lib_factors(d // 32, 2101)
+    Fd = dev(F)
+    KX = kq.kq_expand_blocks(Fd, kq.KQ_K_BF16X3)
+    q, sf, _ = kq.kq_quantize_mxfp4(A, d, factors=Fd, K_expanded=KX, layout=1)
+    v = kq.VARIANT_BUTTERFLY if expect == "butterfly" else kq.VARIANT_UMMA
+    q2, sf2, _ = kq.kq_quantize_mxfp4(A, d, factors=Fd, K_expanded=KX, layout=1, variant=v)
+    assert torch.equal(q, q2) and torch.equal(sf, sf2)

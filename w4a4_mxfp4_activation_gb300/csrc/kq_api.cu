@@ -283,8 +283,13 @@ kq_status kq_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda
                             cudaStream_t stream)
 {
     // the fastest implementation the arguments allow: tcgen05 on the
-    // expanded blocks, else the butterfly on the raw factors, else identity
-    const int variant = K_expanded != nullptr ? 3 : (factors != nullptr ? 0 : 2);
+    // expanded blocks, else the butterfly on the raw factors, else identity.
+    // With both given, layers below 2^21 elements take the butterfly: there
+    // every kernel is latency-bound and the tensor-core pipeline's longer
+    // first tile costs more than its arithmetic saves (measured on GB300:
+    // butterfly faster up to 1024 x 1152, tcgen05 from 1024 x 3072 on).
+    int variant = K_expanded != nullptr ? 3 : (factors != nullptr ? 0 : 2);
+    if (variant == 3 && factors != nullptr && m * d < (int64_t(1) << 21)) variant = 0;
     return kq_quantize_mxfp4_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout,
                                      y_debug, variant, stream);
 }
