@@ -10,21 +10,21 @@
 // on chip before any output block is known.
 //
 // Layout of the work: a persistent CTA of 512 threads transforms 16384
-// elements per iteration (16384 / d rows).  Thread t owns one 32-channel
-// block of one row:
-//   1. it takes the block from a shared staging area, where four 16-byte
-//      cp.async copies brought it during the previous iteration's passes,
-//      issues the copies for its block of the next iteration, runs the first
-//      five butterfly stages (pairs 1..16 apart) in registers and writes the
-//      32 values to a shared fp32 buffer padded to 36 floats per 32 (so that
-//      a thread's own block moves in 16-byte vectors and both those and 32
-//      lanes' strided scalar accesses are free of bank conflicts);
-//   2. the stages with pairs 32..512 apart, then 1024..8192 apart, each run as
-//      one pass: a thread gathers r values at the stage's stride into
-//      registers, applies log2(r) stages, writes them back (r = 32, or less
-//      in the last pass);
-//   3. it reads its block back, multiplies by 1/sqrt(d), quantizes and
-//      stores 16 bytes of codes and one scale byte.
+// elements per iteration (16384 / d rows).  The butterfly stages of H_d act on
+// one bit of the channel index each and commute, so they run in the order
+// that keeps shared-memory traffic lowest:
+//   1. the iteration's rows arrive by 16-byte cp.async copies into a bf16
+//      staging tile in natural order (consecutive threads, consecutive
+//      chunks), issued during the previous iteration;
+//   2. the stages with pairs 32 apart and more run as passes: a thread
+//      gathers r values at the pass's stride (lanes at consecutive channels,
+//      so every access is conflict-free), applies log2(r) stages in registers
+//      and writes them to a shared fp32 buffer padded to 36 floats per 32 --
+//      the first pass reads the bf16 staging tile, a second one (d > 1024)
+//      the fp32 buffer;
+//   3. each thread then reads one 32-channel block of a row, applies the five
+//      stages with pairs 1..16 apart in registers, multiplies by 1/sqrt(d),
+//      quantizes and stores 16 bytes of codes and one scale byte.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -39,8 +39,8 @@ namespace {
 constexpr int kFThreads = 512;
 constexpr int kFElems = 16384;                       // elements per iteration
 constexpr int kFSmemFloats = kFElems + kFElems / 8;  // padded: 36 floats per 32
-// staging for the next iteration's bf16 input: chunk k (16 bytes) of thread t
-// at k * 8 KB + 16 t, so that a warp's accesses are contiguous
+// bf16 staging of the next iteration's rows, natural order: element e of the
+// iteration (row_local * d + channel) at byte 2 e
 constexpr int kFStageOff = kFSmemFloats * 4;
 constexpr int kFSmemBytes = kFStageOff + kFElems * 2;
 
@@ -71,22 +71,38 @@ __device__ __forceinline__ void wht_regs(float (&v)[32])
 
 // One pass over the stages with pairs S, 2S, ..., (R/2)S apart: groups of R
 // values at stride S; group g of a row = (lo, hi) with lo = g % S (the lanes
-// of a warp take consecutive lo) and base lo + hi * S * R.
-template <int D, int S, int R>
-__device__ __forceinline__ void wht_pass(float *buf, int row_local, int tr)
+// of a warp take consecutive lo, i.e. consecutive channels) and base
+// lo + hi * S * R.  FROM_STAGING: the values come from the 16-bit staging
+// tile (bf16, or fp16 when f16); they always go to the padded fp32 buffer.
+template <int D, int S, int R, bool FROM_STAGING>
+__device__ __forceinline__ void wht_pass(float *buf, const uint16_t *stg, int row_local, int tr,
+                                         bool f16)
 {
     static_assert(S % 32 == 0, "pass strides are multiples of 32");
     constexpr int kThreadsPerRow = D / 32;
-    constexpr int kGroupsPerThread = 32 / R;
+    constexpr int kGroupsPerThread = (D / R) / kThreadsPerRow;
+    static_assert(kGroupsPerThread >= 1, "every thread takes at least one group");
 #pragma unroll 1
     for (int q = 0; q < kGroupsPerThread; ++q) {
         const int g = tr + q * kThreadsPerRow;
-        // S is a multiple of 32, so the padded index of base + k S is
-        // pad(base) + k (S + S / 8): one register and immediate offsets
-        float *pb = buf + pad(row_local * D + (g % S) + (g / S) * S * R);
+        const int e0 = row_local * D + (g % S) + (g / S) * S * R;
+        // S is a multiple of 32, so the padded index of e0 + k S is
+        // pad(e0) + k (S + S / 8)
+        float *pb = buf + pad(e0);
         float v[32];
+        if constexpr (FROM_STAGING) {
+            const uint16_t *sb = stg + e0;
+            if (f16) {
 #pragma unroll
-        for (int k = 0; k < R; ++k) v[k] = pb[k * (S + S / 8)];
+                for (int k = 0; k < R; ++k) v[k] = __half2float(__ushort_as_half(sb[k * S]));
+            } else {
+#pragma unroll
+                for (int k = 0; k < R; ++k) v[k] = __uint_as_float(static_cast<uint32_t>(sb[k * S]) << 16);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < R; ++k) v[k] = pb[k * (S + S / 8)];
+        }
         wht_regs<R>(v);
 #pragma unroll
         for (int k = 0; k < R; ++k) pb[k * (S + S / 8)] = v[k];
@@ -94,74 +110,74 @@ __device__ __forceinline__ void wht_pass(float *buf, int row_local, int tr)
 }
 
 template <int LOGD, bool DEBUG>
-__global__ void __launch_bounds__(kFThreads, 2) fwht_quant_kernel(const uint16_t *__restrict__ A,
-                                                                  int64_t lda, const QuantParams p)
+__global__ void __launch_bounds__(kFThreads, 2) fwht_quant_kernel(const uint16_t *A, int64_t lda,
+                                                                  const QuantParams p)
 {
     constexpr int D = 1 << LOGD;
     constexpr int kRows = kFElems / D;               // rows per iteration
     constexpr int kThreadsPerRow = D / 32;
+    constexpr int kChunksPerRow = D / 8;             // 16-byte chunks of a bf16 row
     extern __shared__ float fbuf[];
+    uint16_t *stg = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(fbuf) + kFStageOff);
     grid_dependency_wait();
     const int t = threadIdx.x;
     const int row_local = t / kThreadsPerRow, tr = t % kThreadsPerRow;
-    const int b = tr;                                // the thread's 32-channel block
+    const int b = tr;                                // the thread's 32-channel block in step 3
+    const bool f16 = p.in_f16 != 0;
     const float inv = 1.0f / sqrtf(static_cast<float>(D));   // exact when d = 4^k
     const int64_t groups = (p.m_rows + kRows - 1) / kRows;
-    const uint32_t stage = smem_addr(fbuf) + kFStageOff + 16 * t;
-    // copies of this thread's block of rows group g into its staging chunks
+    const uint32_t stg_s = smem_addr(stg);
+    // copies of the rows of iteration g: chunk c = t + 512 i of the staging
+    // tile (row c / kChunksPerRow, channels 8 (c % kChunksPerRow) ..); rows
+    // past m are zero
     auto issue = [&](int64_t g) {
-        const int64_t r = g * kRows + row_local;
-        if (g < groups && r < p.m) {
-            const uint16_t *src = A + r * lda + b * 32;
+        if (g < groups) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) cp_async16(stage + k * 8192, src + 8 * k);
+            for (int i = 0; i < 4; ++i) {
+                const int c = t + kFThreads * i;
+                const int64_t r = g * kRows + c / kChunksPerRow;
+                const uint32_t dst = stg_s + 16 * c;
+                if (r < p.m)
+                    cp_async16(dst, A + r * lda + 8 * (c % kChunksPerRow));
+                else
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
+            }
         }
         cp_async_commit();
     };
     issue(blockIdx.x);
     for (int64_t grp = blockIdx.x; grp < groups; grp += gridDim.x) {
         const int64_t row = grp * kRows + row_local;
-        float v[32];
         cp_async_wait_all();
-        if (row < p.m) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint4 w = lds128(stage + k * 8192);
-                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    v[8 * k + 2 * e] = p.in_f16 ? f16_lo(u[e]) : bf16_lo(u[e]);
-                    v[8 * k + 2 * e + 1] = p.in_f16 ? f16_hi(u[e]) : bf16_hi(u[e]);
-                }
-            }
+        __syncthreads();                             // every chunk of the tile has landed
+        // stages with pairs 32 apart and more: the first pass reads the staging tile
+        if constexpr (LOGD > 10) {
+            wht_pass<D, 1024, (1 << (LOGD - 10)), true>(fbuf, stg, row_local, tr, f16);   // 1024..8192
+            __syncthreads();
+            issue(grp + gridDim.x);                  // staging consumed: next tile in flight
+            wht_pass<D, 32, 32, false>(fbuf, stg, row_local, tr, f16);                    // 32..512
         } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = 0.f;
+            wht_pass<D, 32, (1 << (LOGD - 5)), true>(fbuf, stg, row_local, tr, f16);
+            __syncthreads();
+            issue(grp + gridDim.x);
         }
-        issue(grp + gridDim.x);                      // in flight during the passes below
-        wht_regs<32>(v);                             // pairs 1..16 apart
-        const int own = pad(row_local * D + b * 32);   // a multiple of 36: 16-byte aligned
-        float4 *own4 = reinterpret_cast<float4 *>(fbuf + own);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            own4[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         __syncthreads();
-        if constexpr (LOGD > 5) {                    // pairs 32..512 apart
-            constexpr int R1 = (LOGD - 5 >= 5) ? 32 : (1 << (LOGD - 5));
-            wht_pass<D, 32, R1>(fbuf, row_local, tr);
-            __syncthreads();
-        }
-        if constexpr (LOGD > 10) {                   // pairs 1024..8192 apart
-            wht_pass<D, 1024, (1 << (LOGD - 10))>(fbuf, row_local, tr);
-            __syncthreads();
-        }
-        float2 Y[16];
+        // the thread's own block: stages with pairs 1..16 apart, then quantize
+        const int own = pad(row_local * D + b * 32);   // a multiple of 36: 16-byte aligned
+        const float4 *own4 = reinterpret_cast<const float4 *>(fbuf + own);
+        float v[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const float4 w = own4[k];
-            Y[2 * k] = make_float2(w.x * inv, w.y * inv);
-            Y[2 * k + 1] = make_float2(w.z * inv, w.w * inv);
+            v[4 * k] = w.x;
+            v[4 * k + 1] = w.y;
+            v[4 * k + 2] = w.z;
+            v[4 * k + 3] = w.w;
         }
+        wht_regs<32>(v);
+        float2 Y[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) Y[k] = make_float2(v[2 * k] * inv, v[2 * k + 1] * inv);
         if (row < p.m_rows) {
             if (DEBUG && row < p.m) {
                 float *yd = p.y_debug + row * p.d + b * 32;
