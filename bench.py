@@ -74,7 +74,7 @@ def parse_args():
     ap.add_argument("--gemm", action="store_true",
                     help="table of the W4A4 consumer product (kind::mxf4) on the layer shapes")
     ap.add_argument("--profile", choices=("kroquant", "dual", "diag", "hadamard", "identity",
-                                          "gemm"),
+                                          "fwht", "gemm"),
                     help="profiling case for ncu: run one quantizer a few times and exit")
     ap.add_argument("--m", type=int, default=9216, help="rows of the profiling case")
     ap.add_argument("--d", type=int, default=12288, help="channels of the profiling case")
@@ -713,6 +713,8 @@ def run_profile_case(args):
             kq.kq_smooth_quantize_mxfp4(A, s, d, layout=layout, q=q, sf=sf)
         elif args.profile == "hadamard":
             kq.kq_hadamard_quantize_mxfp4(A, d, layout=layout, q=q, sf=sf)
+        elif args.profile == "fwht":
+            kq.kq_fwht_quantize_mxfp4(A, d, layout=layout, q=q, sf=sf)
         else:
             kq.kq_quantize_mxfp4(A, d, layout=layout, q=q, sf=sf)
     torch.cuda.synchronize()
