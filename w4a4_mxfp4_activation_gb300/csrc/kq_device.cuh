@@ -267,13 +267,20 @@ __device__ __forceinline__ float inv_scale(uint32_t byte)
 // serialization and call this after their shared-memory / TMEM setup and
 // before their first global-memory access, so the launch of a quantizer
 // overlaps the end of the previous kernel while every read of A and write of
-// q / sf stays ordered after it.  They do not trigger their own dependents
-// early (griddepcontrol.launch_dependents): measured on GB300, a dependent
-// grid pending from the start of a 27 us quantizer slowed it by 1.2 us,
-// while the implicit trigger at grid end keeps the launch-latency overlap.
+// q / sf stays ordered after it.
 __device__ __forceinline__ void grid_dependency_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the grids that depend on this one be scheduled once every CTA has
+// called it (or exited); their grid_dependency_wait still waits for this
+// grid to complete.  Measured on GB300: called from the start of a 27 us
+// quantizer it slowed it by 1.2 us; the tcgen05 quantizer calls it when its
+// producer has issued its last tile.
+__device__ __forceinline__ void grid_dependents_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // max(a, b, c) in one instruction (3-input max.f32; a NaN input is ignored
