@@ -285,12 +285,12 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             }
             // The next grid may be scheduled once every CTA is this far: its
             // CTAs then take the SMs as this grid's CTAs exit, instead of
-            // being launched after the last exit (measured on GB300: 4096 x
-            // 1152 5.15 -> 4.62 us, 4608 x 3072 8.57 -> 8.38 us, larger layers
-            // unchanged; the dual kernel gained on small layers as well but
-            // lost 2-3 % from about 8 tiles per CTA on, so it triggers below
-            // that only).
-            if (!DUAL || p.ntiles < 8 * static_cast<int64_t>(gridDim.x)) grid_dependents_launch();
+            // being launched after the last exit.  Measured on GB300 by
+            // tiles per CTA: 4096 x 1152 (4) 5.15 -> 4.62 us, 4608 x 3072
+            // (11) 8.57 -> 8.38 us, 4608 x 12288 (45) unchanged, but 16384 x
+            // 12288 (162) +0.8 % and 65536 x 12288 (647) +3.2 %; the dual
+            // kernel gained at 4 and lost 2-3 % from 45 on.
+            if (p.ntiles < (DUAL ? 8 : 48) * static_cast<int64_t>(gridDim.x)) grid_dependents_launch();
             const int64_t it = pit;
             for (int64_t k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
                 (void)mbar_wait(bar_full + 8 * static_cast<int>(k % STAGES),
