@@ -50,6 +50,17 @@ def algo_bytes(m: int, d: int) -> float:
 STEP_BYTES = sum(algo_bytes(m, d) for _, m, d in LAYERS)
 
 
+def round_lengths(steps: int) -> list:
+    """The timed region's structure: rounds of min(steps left, ROUND) steps;
+    each round replays every layer's CUDA graph of that many launches, so the
+    launches run back to back in the same way whatever the step count."""
+    out, left = [], steps
+    while left > 0:
+        out.append(min(left, ROUND))
+        left -= out[-1]
+    return out
+
+
 def algo_bytes_dual(m: int, d: int) -> float:
     """kq_quantize_mxfp4_dual: the MXFP4 outputs plus the bf16 side output A T."""
     return algo_bytes(m, d) + m * d * 2
@@ -64,9 +75,13 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=40000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--variant", choices=("butterfly", "mma", "umma"), default="umma",
-                    help="KroQuant kernel: tcgen05 (umma, default), mma.sync, or the CUDA-core "
-                         "butterfly")
+    ap.add_argument("--variant", choices=("butterfly", "umma"), default="umma",
+                    help="KroQuant kernel: tcgen05 (umma, default) or the CUDA-core butterfly")
+    ap.add_argument("--schedule", choices=("counter", "fixed"), default="counter",
+                    help="tile schedule of the tcgen05 kernel: taken from a workspace counter "
+                         "(kq_quantize_mxfp4_ws, default) or a fixed walk (kq_quantize_mxfp4)")
+    ap.add_argument("--isolated", type=int, default=20,
+                    help="single-launch measurements of the dominant layer (isolated_launch)")
     ap.add_argument("--no-baselines", action="store_true",
                     help="skip the diagonal / Hadamard / bare-quantizer side measurements")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -205,11 +220,15 @@ def time_launches(fn, stream, reps: int = 20, rounds: int = 5) -> float:
 
 def kernel_source_hash() -> str:
     """Hash of the sources that define the dominant kernel (the tcgen05
-    quantizer: its device code, its launch configuration and tensor maps)."""
+    quantizer): its device code, its launch configuration, the entry points
+    that build its tensor maps and choose the path, and the build script
+    that holds the compile command."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "w4a4_mxfp4_activation_gb300", "csrc")
+    pkg = os.path.join(ROOT, "w4a4_mxfp4_activation_gb300")
+    csrc = os.path.join(pkg, "csrc")
     files = [os.path.join(csrc, f) for f in ("kq_umma.cu", "kq_device.cuh", "kq_internal.h",
-                                             "kq_records.h")]
+                                             "kq_records.h", "kq_api.cu")]
+    files.append(os.path.join(pkg, "build.py"))
     for path in files:
         h.update(os.path.basename(path).encode())
         with open(path, "rb") as f:
@@ -233,51 +252,115 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 100 ms) of the benchmarked GPU while alive."""
+    """SM clock and clock-event reasons of the benchmarked GPU, sampled in a
+    background thread while alive: read-only NVML queries in this process
+    (libnvidia-ml from the driver), else nvidia-smi writing to a file.
+    Samples carry host timestamps so that those inside a window (the timed
+    region) can be told from the rest."""
 
-    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    # nvmlClocksEventReasons bits
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, uuid: str | None):
+    def __init__(self, uuid: str | None, out_dir: str | None = None):
+        import threading
         self.uuid = uuid
+        self.samples = []            # (host time, sm MHz, max MHz, reason bits)
         self.proc = None
+        self.path = None
+        self.stop_ev = threading.Event()
+        self.thread = None
+        self.source = None
+        nv = self._nvml()
+        if nv is not None:
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._poll, args=nv, daemon=True)
+            self.thread.start()
+            return
         try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv", dir=out_dir)
+            os.close(fd)
+            self.t0 = time.time()
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20", "-f", self.path], stdout=subprocess.DEVNULL,
+                stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi"
         except OSError:
             self.proc = None
 
-    def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
+    def _nvml(self):
+        import ctypes
         try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        mhz, mx, reasons = [], [], set()
-        for line in out.splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            if self.uuid and self.uuid not in f[0] and f[0] not in self.uuid:
-                continue
+            L = ctypes.CDLL("libnvidia-ml.so.1")
+            if L.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            if self.uuid is None or L.nvmlDeviceGetHandleByUUID(self.uuid.encode(),
+                                                                ctypes.byref(h)) != 0:
+                return None
+            reasons = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                L.nvmlDeviceGetCurrentClocksThrottleReasons
+            return L, h, reasons
+        except (OSError, AttributeError):
+            return None
+
+    def _poll(self, L, h, reasons):
+        import ctypes
+        mhz, mx, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_ev.is_set():
+            t = time.perf_counter()
+            if (L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and
+                    L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                    reasons(h, ctypes.byref(bits)) == 0):
+                self.samples.append((t, float(mhz.value), float(mx.value), int(bits.value)))
+            self.stop_ev.wait(0.0002)
+
+    def stop(self):
+        if self.thread is not None:
+            self.stop_ev.set()
+            self.thread.join(timeout=5)
+        if self.proc is not None:
+            self.proc.terminate()
             try:
-                mhz.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for name, val in zip(self.REASONS, f[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not mhz:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(mhz)}
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            try:
+                with open(self.path) as f:
+                    lines = f.read().splitlines()
+                os.unlink(self.path)
+            except OSError:
+                lines = []
+            for k, line in enumerate(lines):
+                fl = [x.strip() for x in line.split(",")]
+                if len(fl) < 7 or (self.uuid and self.uuid not in fl[0] and fl[0] not in self.uuid):
+                    continue
+                try:
+                    bits = sum(b for (name, b), v in zip(self.REASON_BITS.items(),
+                                                         (fl[6], fl[3], fl[5], fl[4]))
+                               if v.lower().startswith("active"))
+                    self.samples.append((None, float(fl[1]), float(fl[2]), bits))
+                except ValueError:
+                    continue
+
+    def summary(self, window=None):
+        """Median SM clock, max clock and the throttle reasons seen, over the
+        samples inside window = (t0, t1) (perf_counter seconds), or all."""
+        pts = [x for x in self.samples
+               if window is None or x[0] is None or window[0] <= x[0] <= window[1]]
+        if not pts:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": self.source}
+        reasons = sorted(name for name, b in self.REASON_BITS.items()
+                         if any(p[3] & b for p in pts))
+        return {"sm_mhz": statistics.median(p[1] for p in pts),
+                "sm_max_mhz": max(p[2] for p in pts), "reasons": reasons, "samples": len(pts),
+                "source": self.source}
 
 
 def device_uuid(dev) -> str | None:
@@ -398,22 +481,27 @@ def run_ours(args, dist: Dist):
         KX.append(kq.kq_expand_blocks(F[-1], kq.KQ_K_BF16X3))
     torch.cuda.synchronize()
 
+    # the tcgen05 kernel's tile counters (one stream: its launches never overlap)
+    WS = kq.sched_workspace(dev)
+
     def launch(kind, li, s):
         _, m, d = LAYERS[li]
         if kind == "kroquant":
-            kind = args.variant
+            kind = args.variant if args.variant != "umma" else (
+                "umma_ws" if args.schedule == "counter" else "umma")
         if kind == "butterfly":
             kq.kq_quantize_mxfp4(A[li][s], d, factors=F[li], layout=layout, q=Q[li][s],
                                  sf=SF[li][s], variant=kq.VARIANT_BUTTERFLY, stream=stream)
-        elif kind == "mma":
-            kq.kq_quantize_mxfp4(A[li][s], d, K_expanded=KX[li], layout=layout, q=Q[li][s],
-                                 sf=SF[li][s], variant=kq.VARIANT_MMA, stream=stream)
         elif kind == "umma":
             kq.kq_quantize_mxfp4(A[li][s], d, K_expanded=KX[li], layout=layout, q=Q[li][s],
-                                 sf=SF[li][s], variant=kq.VARIANT_UMMA, stream=stream)
+                                 sf=SF[li][s], stream=stream)
+        elif kind == "umma_ws":
+            kq.kq_quantize_mxfp4_ws(A[li][s], WS, d, K_expanded=KX[li], layout=layout,
+                                    q=Q[li][s], sf=SF[li][s], stream=stream)
         elif kind == "dual":
             kq.kq_quantize_mxfp4_dual(A[li][s], KX[li], d, layout=layout, q=Q[li][s],
-                                      sf=SF[li][s], at=AT[li][s], stream=stream)
+                                      sf=SF[li][s], at=AT[li][s], stream=stream,
+                                      workspace=WS if args.schedule == "counter" else None)
         elif kind == "diag":
             kq.kq_smooth_quantize_mxfp4(A[li][s], DIAG[li], d, layout=layout, q=Q[li][s],
                                         sf=SF[li][s], stream=stream)
@@ -428,69 +516,59 @@ def run_ours(args, dist: Dist):
     # bf16 side outputs of the dual quantizer (allocated when it is measured)
     AT = [[None] * SETS for _ in LAYERS]
 
-    def graphs_for(kind):
-        """CUDA graphs of the launches: per layer one graph with ROUND
-        launches cycling through the SETS input sets (ROUND steps' worth of
-        that layer, back to back), and one graph per (set, layer) launch for
-        the K % ROUND steps left over."""
-        rounds = [None] * len(LAYERS)
+    def graphs_for(kind, lengths):
+        """Per layer and per length L in `lengths`, a CUDA graph of L
+        launches of that layer back to back, cycling through its SETS input
+        sets, with programmatic dependent launch between them; and per
+        (set, layer) a one-launch graph for the isolated measurement."""
+        per_len = {}
         single = [[None] * len(LAYERS) for _ in range(SETS)]
         with torch.cuda.stream(stream):
             for s in range(SETS):
                 for li in range(len(LAYERS)):
                     launch(kind, li, s)              # warm the launch path before capture
             stream.synchronize()
-            for li in range(len(LAYERS)):
-                gr = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gr, stream=stream):
-                    for k in range(ROUND):
-                        launch(kind, li, k % SETS)
-                rounds[li] = gr
-                for s in range(SETS):
+            for n in sorted(set(x for x in lengths if x > 0)):
+                per_len[n] = []
+                for li in range(len(LAYERS)):
+                    gr = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gr, stream=stream):
+                        for k in range(n):
+                            launch(kind, li, k % SETS)
+                    per_len[n].append(gr)
+            for s in range(SETS):
+                for li in range(len(LAYERS)):
                     gr = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(gr, stream=stream):
                         launch(kind, li, s)
                     single[s][li] = gr
         stream.synchronize()
-        return rounds, single
+        return per_len, single
 
     order = [DOMINANT] + [li for li in range(len(LAYERS)) if li != DOMINANT]
 
     def run_steps(g, steps, events):
-        """steps steps (each: every layer once, on its next input set); with
-        events, brackets every replay of the dominant layer's launches and
-        returns the number of dominant launches inside each bracket."""
-        rounds, single = g
-        n_rounds, rem = divmod(steps, ROUND)
+        """`steps` steps (each: every layer once); with events, brackets
+        every replay of the dominant layer's graph and returns the number of
+        dominant launches inside each bracket."""
+        per_len, _ = g
         counts = []
-        for r in range(n_rounds):
+        for n in round_lengths(steps):
             for li in order:
                 if events is not None and li == DOMINANT:
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record(stream)
-                    rounds[li].replay()
+                    per_len[n][li].replay()
                     b.record(stream)
                     events.append((a, b))
-                    counts.append(ROUND)
+                    counts.append(n)
                 else:
-                    rounds[li].replay()
-        for k in range(rem):
-            for li in order:
-                if events is not None and li == DOMINANT:
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record(stream)
-                    single[k % SETS][li].replay()
-                    b.record(stream)
-                    events.append((a, b))
-                    counts.append(1)
-                else:
-                    single[k % SETS][li].replay()
+                    per_len[n][li].replay()
         return counts
 
-    def timed(kind, steps, warmup, per_launch=False, sampler=False):
-        g = graphs_for(kind)
+    def timed(kind, steps, warmup, per_launch=False, clocks=None):
+        g = graphs_for(kind, round_lengths(steps) + round_lengths(warmup))
         events = [] if per_launch else None
-        clock = ClockSampler(device_uuid(dev)) if sampler else None
         with torch.cuda.stream(stream):
             run_steps(g, warmup, None)
             stream.synchronize()
@@ -498,31 +576,54 @@ def run_ours(args, dist: Dist):
             torch.cuda.synchronize()
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
+            h0 = time.perf_counter()
             t0.record(stream)
             counts = run_steps(g, steps, events)
             t1.record(stream)
             stream.synchronize()
-            clocks = clock.stop() if clock is not None else None
+            h1 = time.perf_counter()
             dist.barrier()
             torch.cuda.synchronize()
         ms = t0.elapsed_time(t1)
         # average duration of one dominant launch over the timed region
         launch_ms = ([sum(a.elapsed_time(b) for a, b in events) / sum(counts)]
                      if per_launch and events else [])
-        return ms, launch_ms, clocks
+        return ms, launch_ms, (h0, h1), g
+
+    def isolated(kind, g, n):
+        """Median CUDA-event time (ms) of one dominant-layer launch replayed
+        alone (a one-launch graph between two events: no programmatic overlap
+        with a neighbour, start-up and drain exposed), over n launches
+        rotating through the input sets."""
+        _, single = g
+        out = []
+        with torch.cuda.stream(stream):
+            for k in range(n + 2):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                single[k % SETS][DOMINANT].replay()
+                b.record(stream)
+                b.synchronize()
+                if k >= 2:
+                    out.append(a.elapsed_time(b))
+        return statistics.median(out)
 
     W, K = args.warmup, args.steps
-    ms, launch_ms, clocks = timed("kroquant", K, W, per_launch=True, sampler=True)
+    clock = ClockSampler(device_uuid(dev), os.environ.get("TMPDIR"))
+    ms, launch_ms, window, g_main = timed("kroquant", K, W, per_launch=True)
+    iso_ms = isolated("kroquant", g_main, max(3, args.isolated))
+    del g_main
     ms_max = dist.max(ms)
     total_bytes = dist.sum(STEP_BYTES * K)
     value = total_bytes / (ms_max * 1e-3) / 1e9
     peak, peak_src = hbm_peak()
-
     dom_m, dom_d = LAYERS[DOMINANT][1], LAYERS[DOMINANT][2]
     dom_ms = statistics.mean(launch_ms) if launch_ms else float("nan")
     achieved = algo_bytes(dom_m, dom_d) / (dom_ms * 1e-3) / 1e9
-    workload = f"kq_quantize_mxfp4 {args.variant} m={dom_m} d={dom_d}"
-    traffic = recorded_traffic(f"flux_ffn_down_{args.variant}")
+    kname = "umma_ws" if args.variant == "umma" and args.schedule == "counter" else args.variant
+    workload = f"kq_quantize_mxfp4{'_ws' if kname == 'umma_ws' else ''} {args.variant} " \
+               f"m={dom_m} d={dom_d}"
+    traffic = recorded_traffic(f"flux_ffn_down_{kname}")
 
     # ---- the dual quantizer (MXFP4 + the bf16 side output A T of the
     #      low-rank branch) on the same step
@@ -531,7 +632,7 @@ def run_ours(args, dist: Dist):
         for li, (_, m, d) in enumerate(LAYERS):
             AT[li] = [torch.empty((m, d), dtype=torch.bfloat16, device=dev) for _ in range(SETS)]
         nd = max(ROUND, min(K, 8000))
-        dms, dlaunch, _ = timed("dual", nd, W, per_launch=True)
+        dms, dlaunch, _, _ = timed("dual", nd, W, per_launch=True)
         dms = dist.max(dms)
         side = {"metric": "kq_quantize_mxfp4_dual GB/s (MXFP4 + bf16 A T side output)",
                 "value": round(dist.sum(STEP_BYTES_DUAL * nd) / (dms * 1e-3) / 1e9, 2),
@@ -546,14 +647,23 @@ def run_ours(args, dist: Dist):
         torch.cuda.empty_cache()
 
     # ---- side measurements: the baselines built alongside
+    # (same launch structure, steps and warm-up as the headline step; the
+    #  diagonal kernel also in the isolated form)
     baselines = {}
+    iso_diag_ms = None
     if not args.no_baselines:
         nb_steps = max(3, min(K, 4000))
-        others = [v for v in ("butterfly", "mma", "umma") if v != args.variant]
+        others = [v for v in ("butterfly", "umma", "umma_ws") if v != kname]
         for kind in (*others, "diag", "hadamard", "identity"):
-            bms, _, _ = timed(kind, nb_steps, 3)
-            name = f"kroquant_{kind}" if kind in ("mma", "butterfly", "umma") else kind
+            bms, _, _, g = timed(kind, nb_steps, W)
+            if kind == "diag":
+                iso_diag_ms = isolated("diag", g, max(3, args.isolated))
+            del g
+            name = f"kroquant_{kind}" if kind in ("butterfly", "umma", "umma_ws") else kind
             baselines[name] = round(STEP_BYTES * nb_steps / (dist.max(bms) * 1e-3) / 1e9, 2)
+    clock.stop()
+    clocks = clock.summary(window)
+    run_clocks = clock.summary()
 
     # ---- the consumer of the quantizer's output: the W4A4 product of the
     #      FFN-down layer (A_q: this step's quantized activations, 4608 x
@@ -647,11 +757,14 @@ def run_ours(args, dist: Dist):
             "data": "synthetic",
             "config": {"workload": "flux_layer_pair", "m": 4608, "d": [3072, 12288],
                        "transform": f"kroquant_{args.variant}", "input": "bf16",
+                       "schedule": ("tiles from a workspace counter (kq_quantize_mxfp4_ws)"
+                                    if kname == "umma_ws" else "fixed tile walk"),
                        "output": "mxfp4 (e2m1 codes + e8m0 scales, 128x4 tiled)",
                        "l2": f"{SETS} rotating input/output sets, "
                              f"{SETS * STEP_BYTES / 1e6:.0f} MB footprint > L2",
-                       "launch": f"per layer one CUDA graph of {ROUND} launches over its "
-                                 f"{SETS} input sets (programmatic dependent launch between "
+                       "launch": f"rounds of min(steps left, {ROUND}) steps: per round and "
+                                 "layer one CUDA graph of that many launches of the layer over "
+                                 f"its {SETS} input sets (programmatic dependent launch between "
                                  "them); events around each dominant-layer graph",
                        "parallelism":
                            f"replicas x{dist.world} (rows independent, no exchange)"},
@@ -660,7 +773,18 @@ def run_ours(args, dist: Dist):
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "traffic_unit": "bytes per launch (ncu, cold L2; outputs left in L2)",
                          "kernel": workload, "launch_ms": round(dom_ms, 5),
+                         "mode": "launches back to back inside the timed region's layer graphs",
+                         "launch_us_x_sm_mhz": round(dom_ms * 1e3 * clocks["sm_mhz"], 1)
+                         if clocks.get("sm_mhz") else None,
                          "peak_source": peak_src},
+            "isolated_launch": {
+                "us": round(iso_ms * 1e3, 3),
+                "gbs": round(algo_bytes(dom_m, dom_d) / (iso_ms * 1e-3) / 1e9, 2),
+                "frac": round(algo_bytes(dom_m, dom_d) / (iso_ms * 1e-3) / 1e9 / peak, 4),
+                "diag_us": round(iso_diag_ms * 1e3, 3) if iso_diag_ms else None,
+                "vs_diag_scale": round(iso_diag_ms / iso_ms, 4) if iso_diag_ms else None,
+                "how": "median over launches of one dominant-layer launch replayed alone as a "
+                       "one-launch CUDA graph between two events (no overlap with a neighbour)"},
             "vs_diag_scale": round(value / dist.world / baselines["diag"], 4)
             if baselines.get("diag") else None,
             "baselines_gbs": baselines,
@@ -670,6 +794,7 @@ def run_ours(args, dist: Dist):
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": K * len(LAYERS),
             "clocks": clocks,
+            "clocks_whole_run": run_clocks,
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu
@@ -690,10 +815,10 @@ def run_profile_case(args):
     q = torch.empty((m, d // 2), dtype=torch.uint8, device="cuda")
     sf = torch.empty(kq.kq_sf_bytes(m, d, layout), dtype=torch.uint8, device="cuda")
     KX = (kq.kq_expand_blocks(F, kq.KQ_K_BF16X3)
-          if args.variant in ("mma", "umma") or args.profile == "dual" else None)
+          if args.variant == "umma" or args.profile == "dual" else None)
     at = torch.empty((m, d), dtype=torch.bfloat16, device="cuda") if args.profile == "dual" else None
-    variant = {"butterfly": kq.VARIANT_BUTTERFLY, "mma": kq.VARIANT_MMA,
-               "umma": kq.VARIANT_UMMA}[args.variant]
+    variant = {"butterfly": kq.VARIANT_BUTTERFLY, "umma": kq.VARIANT_UMMA}[args.variant]
+    ws = kq.sched_workspace("cuda") if args.schedule == "counter" else None
     if args.profile == "gemm":
         n = args.n
         qa, sfa, qw, sfw, _, _ = gemm_case(m, n, d, 9000, "cuda")
@@ -704,11 +829,13 @@ def run_profile_case(args):
         print(f"profile case done: gemm m={m} n={n} k={d} launches={args.launches}")
         return
     for _ in range(args.launches):
-        if args.profile == "kroquant":
+        if args.profile == "kroquant" and variant == kq.VARIANT_UMMA and ws is not None:
+            kq.kq_quantize_mxfp4_ws(A, ws, d, K_expanded=KX, layout=layout, q=q, sf=sf)
+        elif args.profile == "kroquant":
             kq.kq_quantize_mxfp4(A, d, factors=F if KX is None else None, K_expanded=KX,
                                  layout=layout, q=q, sf=sf, variant=variant)
         elif args.profile == "dual":
-            kq.kq_quantize_mxfp4_dual(A, KX, d, layout=layout, q=q, sf=sf, at=at)
+            kq.kq_quantize_mxfp4_dual(A, KX, d, layout=layout, q=q, sf=sf, at=at, workspace=ws)
         elif args.profile == "diag":
             kq.kq_smooth_quantize_mxfp4(A, s, d, layout=layout, q=q, sf=sf)
         elif args.profile == "hadamard":
@@ -731,7 +858,7 @@ TABLE_CONFIGS = (
     ("4", tuple((f"sweep_{m}x{d}", m, d, "flux") for m in (256, 1024, 4096, 16384, 65536)
                 for d in (1152, 3072, 12288))),
 )
-TABLE_KERNELS = ("umma", "butterfly", "mma", "diag", "hadamard", "identity", "dual")
+TABLE_KERNELS = ("umma_ws", "umma", "butterfly", "diag", "hadamard", "identity", "dual")
 
 
 def oracle_rate_shape(m: int, d: int, seconds: float):
@@ -803,20 +930,23 @@ def measure_shape(args, m, d, model, seed, kinds, peak):
           for _ in range(sets)]
     AT = ([torch.empty((m, d), dtype=torch.bfloat16, device=dev) for _ in range(sets)]
           if "dual" in kinds else None)
+    WS = kq.sched_workspace(dev)
     n_launch = max(sets, 32)
 
     def launch(kind, i):
         s = i % sets
-        if kind in ("umma", "mma"):
+        if kind == "umma":
             kq.kq_quantize_mxfp4(A[s], d, K_expanded=KX, layout=layout, q=Q[s], sf=SF[s],
-                                 variant=kq.VARIANT_UMMA if kind == "umma" else kq.VARIANT_MMA,
-                                 stream=stream)
+                                 variant=kq.VARIANT_UMMA, stream=stream)
+        elif kind == "umma_ws":
+            kq.kq_quantize_mxfp4_ws(A[s], WS, d, K_expanded=KX, layout=layout, q=Q[s], sf=SF[s],
+                                    stream=stream)
         elif kind == "butterfly":
             kq.kq_quantize_mxfp4(A[s], d, factors=F, layout=layout, q=Q[s], sf=SF[s],
                                  variant=kq.VARIANT_BUTTERFLY, stream=stream)
         elif kind == "dual":
             kq.kq_quantize_mxfp4_dual(A[s], KX, d, layout=layout, q=Q[s], sf=SF[s], at=AT[s],
-                                      stream=stream)
+                                      stream=stream, workspace=WS)
         elif kind == "diag":
             kq.kq_smooth_quantize_mxfp4(A[s], S, d, layout=layout, q=Q[s], sf=SF[s],
                                         stream=stream)
@@ -873,18 +1003,18 @@ def run_table(args):
         run_table3(args, peak)
         return
     print("| config | layer | m x d | sets | " + " | ".join(
-        f"{k} GB/s (% peak)" if k in ("umma", "dual") else f"{k} GB/s" for k in TABLE_KERNELS) +
-        " | umma / diag |")
+        f"{k} GB/s (% peak)" if k in ("umma_ws", "umma", "dual") else f"{k} GB/s"
+        for k in TABLE_KERNELS) + " | umma_ws / diag |")
     print("|" + "---|" * (len(TABLE_KERNELS) + 5))
     for cfg, layers in TABLE_CONFIGS:
         for name, m, d, model in layers:
             us, sets = measure_shape(args, m, d, model, synth_seed(cfg), TABLE_KERNELS, peak)
             gbs = {k: (algo_bytes_dual(m, d) if k == "dual" else algo_bytes(m, d)) / us[k] / 1e3
                    for k in TABLE_KERNELS}
-            cells = [f"{gbs[k]:.0f} ({100 * gbs[k] / peak:.0f} %)" if k in ("umma", "dual")
+            cells = [f"{gbs[k]:.0f} ({100 * gbs[k] / peak:.0f} %)" if k in ("umma_ws", "umma", "dual")
                      else f"{gbs[k]:.0f}" for k in TABLE_KERNELS]
             print(f"| {cfg} | {name} | {m}x{d} | {sets} | " + " | ".join(cells) +
-                  f" | {gbs['umma'] / gbs['diag']:.2f} |", flush=True)
+                  f" | {gbs['umma_ws'] / gbs['diag']:.2f} |", flush=True)
     run_table3(args, peak)
     # the oracle on the host cores: all of them, then one
     print()

@@ -81,13 +81,10 @@ typedef enum kq_sf_layout {
 
 typedef enum kq_kfmt {
     KQ_K_FP32 = 0,      /* dense K_j, fp32 row-major [nb][32][32] */
-    KQ_K_BF16X3 = 1     /* operand records of the tensor-core variants (opaque,
-                           6144 + 1552 bytes per block), each a three-term bf16
-                           split hi + mid + lo: first nb tcgen05 records (the
-                           dense 32x32 K_j in the shared-memory operand
-                           layout), then nb mma.sync records (K'_j = G2 (x) G3
-                           (x) G4 (x) G5 as a 16x16 block in fragment order,
-                           plus G1 in fp32) */
+    KQ_K_BF16X3 = 1     /* operand records of the tensor-core kernel (opaque,
+                           6144 bytes per block): the dense 32x32 K_j as a
+                           three-term bf16 split hi + mid + lo, in the
+                           shared-memory operand layout of its MMAs */
 } kq_kfmt;
 
 /* Input formats of kq_quantize_mxfp4_ex: A holds bf16 or fp16 bit patterns. */
@@ -157,6 +154,39 @@ KQ_API kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d,
                                  const void *K_expanded, uint8_t *q, int64_t ldq, uint8_t *sf,
                                  kq_sf_layout sf_layout, uint16_t *at, int64_t ldat,
                                  float *y_debug, cudaStream_t stream);
+
+/*
+ * kq_quantize_mxfp4_ws / kq_quantize_mxfp4_dual_ws -- kq_quantize_mxfp4 and
+ * kq_quantize_mxfp4_dual with a scheduling workspace: on the tensor-core
+ * path the persistent CTAs take their 128-row x 64-channel tiles one at a
+ * time from a counter in `workspace` instead of a fixed share, so that CTAs
+ * that start late or stream slower take fewer tiles and the launch ends
+ * sooner.  Every tile is computed the same way by whichever CTA takes it, so
+ * the results equal those of the calls without workspace, byte for byte.
+ * The other kernels the arguments may select ignore the workspace.
+ *   workspace  device, KQ_SCHED_WORKSPACE_BYTES bytes, 4-byte aligned
+ *              (KQ_ERR_NULL / KQ_ERR_ALIGN otherwise), owned by the caller.
+ *              Words 0 and 1 must be zero before the first call (e.g. one
+ *              cudaMemset); every call leaves them zero again when its kernel
+ *              ends.  Word 2 counts the CTAs that found their pipeline
+ *              stalled (see Errors above; the library never clears it): on
+ *              this path the blocks of a tile taken by such a CTA keep their
+ *              old bytes unless the CTA knew the tile when it stopped, in
+ *              which case they get the scale byte 0xFF.  Calls that may run
+ *              at the same time (different streams) need different
+ *              workspaces.
+ *   other arguments as kq_quantize_mxfp4 / kq_quantize_mxfp4_dual.
+ */
+#define KQ_SCHED_WORKSPACE_BYTES 16
+KQ_API kq_status kq_quantize_mxfp4_ws(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                      const float *factors, const void *K_expanded, uint8_t *q,
+                                      int64_t ldq, uint8_t *sf, kq_sf_layout sf_layout,
+                                      float *y_debug, uint32_t *workspace, cudaStream_t stream);
+KQ_API kq_status kq_quantize_mxfp4_dual_ws(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                           const void *K_expanded, uint8_t *q, int64_t ldq,
+                                           uint8_t *sf, kq_sf_layout sf_layout, uint16_t *at,
+                                           int64_t ldat, float *y_debug, uint32_t *workspace,
+                                           cudaStream_t stream);
 
 /*
  * kq_quantize_mxfp4_shared -- kq_quantize_mxfp4 with one factor set shared
@@ -261,20 +291,6 @@ KQ_API kq_status kq_w4a4_gemm(const uint8_t *qa, int64_t ldqa, const uint8_t *sf
                               cudaStream_t stream);
 
 /*
- * kq_w4a4_gemm_variant -- kq_w4a4_gemm with the implementation chosen:
- *   variant 0 = block-scaled FP4 MMA (kind::mxf4, the default), 1 = every
- *   operand tile dequantized to bf16 in shared memory (exact) and multiplied
- *   with kind::f16 -- an independent route to the same sums, for checking;
- *   2 / 3 = the FP4 kernel with its tile width fixed at 128 / 256 columns of
- *   C (variant 0 picks the width from the number of tiles per SM and K).
- *   Other values: KQ_ERR_LAYOUT.
- */
-KQ_API kq_status kq_w4a4_gemm_variant(const uint8_t *qa, int64_t ldqa, const uint8_t *sfa,
-                                      const uint8_t *qw, int64_t ldqw, const uint8_t *sfw,
-                                      int64_t m, int64_t n, int64_t k, float *c, int64_t ldc,
-                                      int variant, cudaStream_t stream);
-
-/*
  * kq_bf16_gemm -- the unquantized reference product of [KQ] eq. (2),
  * c = A W^T, on the same tensor-core kernel: bf16 operands, fp32
  * accumulation.
@@ -356,31 +372,6 @@ KQ_API kq_status kq_lu_to_factors(const float *lu, int64_t nb, int det_sign, flo
  *   kq_quantize_mxfp4 to quantize the rows of W T^{-T}.
  */
 KQ_API kq_status kq_invert_transpose_factors(const float *factors, int64_t nb, float *out);
-
-/*
- * Verification and benchmarking hooks.
- *
- * kq_quantize_mxfp4_variant -- kq_quantize_mxfp4 with the block-transform
- *   implementation chosen explicitly: variant 0 = in-register butterfly
- *   from the raw factors (needs factors), 1 = warp-level mma.sync on the
- *   pre-expanded operand records (needs K_expanded), 2 = identity,
- *   3 = tcgen05 tensor cores with TMEM accumulators on the pre-expanded
- *   operand records (needs K_expanded).
- */
-KQ_API kq_status kq_quantize_mxfp4_variant(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
-                                    const float *factors, const void *K_expanded,
-                                    uint8_t *q, int64_t ldq, uint8_t *sf,
-                                    kq_sf_layout sf_layout, float *y_debug, int variant,
-                                    cudaStream_t stream);
-
-/*
- * kq_test_encode_e2m1 -- runs the quantizers' E2M1 encoder on the fp32 bit
- *   patterns first, first+1, ..., first+count-1 with the scale fixed at 2^0
- *   (v = y), writing count/2 packed bytes (code of the even pattern in bits
- *   0-3).  count must be a multiple of 8; out is device memory, 16-byte
- *   aligned.  Used for the exhaustive rounding check.
- */
-KQ_API kq_status kq_test_encode_e2m1(uint32_t first, int64_t count, uint8_t *out, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -25,6 +25,9 @@ quantizer:
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 from oracle import kq_oracle as O
@@ -47,17 +50,54 @@ def gather_scales(sf: np.ndarray, rows: np.ndarray, nb: int, layout: int) -> np.
     return sf[off]
 
 
-def check(A_bits: np.ndarray, d: int, kind: str, param, layout: int, q_gpu: np.ndarray,
-          sf_gpu: np.ndarray, y_gpu: np.ndarray | None, rows: np.ndarray | None = None,
-          in_format: str = "bf16") -> dict:
-    """Apply rules (i)-(iii) on the given rows (all rows if None).  Raises
-    AssertionError on a violation; returns the flagged counts."""
+CHUNK = 4096
+
+
+def reference(A_bits: np.ndarray, d: int, kind: str, param, rows: np.ndarray | None = None,
+              in_format: str = "bf16") -> dict:
+    """The oracle's result on the given rows (all if None), for check(ref=...)
+    when one input is compared with several outputs."""
     m = A_bits.shape[0]
     rows = np.arange(m) if rows is None else np.asarray(rows, np.int64)
-    nb = d // 32
-    y_ref, bound = O.transform(np.ascontiguousarray(A_bits[rows]), d, kind, param,
-                               in_format=in_format)
+    src = A_bits if len(rows) == m else np.ascontiguousarray(A_bits[rows])
+    y_ref, bound = O.transform(np.ascontiguousarray(src), d, kind, param, in_format=in_format)
     q_ref, sf_ref, flags = O.quantize(y_ref, bound, O.SF_ROWMAJOR)
+    return dict(rows=rows, y=y_ref, bound=bound, q=q_ref, sf=sf_ref, flags=flags)
+
+
+def record(config: str, layer: str, m: int, d: int, kind: str, layout: int, res: dict):
+    """Append one parity result as a JSON line to $KQ_PARITY_REPORT (if set):
+    the per-config flag counts reported next to the benchmark."""
+    path = os.environ.get("KQ_PARITY_REPORT")
+    if not path:
+        return
+    with open(path, "a") as f:
+        f.write(json.dumps({"config": config, "layer": layer, "m": m, "d": d, "kind": kind,
+                            "layout": layout, **res}) + "\n")
+
+
+def check(A_bits: np.ndarray, d: int, kind: str, param, layout: int, q_gpu: np.ndarray,
+          sf_gpu: np.ndarray, y_gpu: np.ndarray | None, rows: np.ndarray | None = None,
+          in_format: str = "bf16", ref: dict | None = None) -> dict:
+    """Apply rules (i)-(iii) on the given rows (all rows if None).  Raises
+    AssertionError on a violation; returns the flagged counts.  Without a
+    precomputed ``ref``, large row sets are checked in chunks of CHUNK rows
+    (the counts summed) to bound the host memory."""
+    nb = d // 32
+    if ref is None:
+        all_rows = np.arange(A_bits.shape[0]) if rows is None else np.asarray(rows, np.int64)
+        if len(all_rows) > CHUNK:
+            out = {}
+            for k in range(0, len(all_rows), CHUNK):
+                part = check(A_bits, d, kind, param, layout, q_gpu, sf_gpu, y_gpu,
+                             all_rows[k:k + CHUNK], in_format)
+                for key, v in part.items():
+                    out[key] = max(out.get(key, 0.0), v) if key == "y_max_err_over_tol" \
+                        else out.get(key, 0) + v
+            return out
+        ref = reference(A_bits, d, kind, param, rows, in_format)
+    rows = ref["rows"]
+    y_ref, bound, q_ref, sf_ref, flags = ref["y"], ref["bound"], ref["q"], ref["sf"], ref["flags"]
     codes_ref = unpack(q_ref, d)
     codes_gpu = unpack(np.asarray(q_gpu)[rows], d)
     sf_g = gather_scales(sf_gpu, rows, nb, layout)

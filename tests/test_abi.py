@@ -12,6 +12,7 @@ from conftest import ROOT
 from w4a4_mxfp4_activation_gb300 import kq, synth
 
 HEADER = os.path.join(ROOT, "include", "kq.h")
+TESTING_HEADER = os.path.join(ROOT, "include", "kq_testing.h")
 
 
 @pytest.fixture(scope="module")
@@ -21,8 +22,8 @@ def L():
     return kq.lib()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"KQ_API\s+[\w\s\*]+?\b(kq_\w+)\s*\(", text)))
 
@@ -33,12 +34,25 @@ def test_header_declares_the_api():
                      "kq_hadamard_quantize_mxfp4", "kq_dequantize"):
         assert required in names
     assert set(names) == set(kq.EXPORTS)
+    # the verification hooks stay out of the public header
+    hooks = declared_functions(TESTING_HEADER)
+    assert set(hooks) == set(kq.TESTING_EXPORTS)
+    assert not set(hooks) & set(names)
 
 
 def test_library_exports_every_declared_symbol(L):
-    for name in declared_functions():
+    for name in declared_functions() + declared_functions(TESTING_HEADER):
         assert hasattr(L, name), name
         assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_mma_sync_variant_is_not_built(L):
+    """The warp-level mma.sync transform lost to both other implementations
+    and is no longer in the library: its variant number is rejected before
+    anything runs."""
+    vp = ctypes.c_void_p
+    assert L.kq_quantize_mxfp4_variant(vp(4096), 4, 64, 64, vp(8192), vp(8192), vp(12288), 32,
+                                       vp(16384), 0, None, 1, None) == 4
 
 
 def test_status_strings(L):
@@ -58,7 +72,7 @@ def test_sf_bytes_matches_oracle(L, oracle_lib):
 
 def test_expanded_bytes(L):
     assert kq.kq_expanded_bytes(36, kq.KQ_K_FP32) == 36 * 4096
-    assert kq.kq_expanded_bytes(36, kq.KQ_K_BF16X3) == 36 * (6144 + 1552)
+    assert kq.kq_expanded_bytes(36, kq.KQ_K_BF16X3) == 36 * 6144
     assert kq.kq_expanded_bytes(0, kq.KQ_K_FP32) == 0
 
 
@@ -122,7 +136,7 @@ def test_quantize_argument_checks(L):
     assert _q(L, m=0, A=None, q=None, sf=None) == 0
     assert _q(L, variant=4) == 4
     assert _q(L, variant=3, K=None) == 1
-    assert _q(L, variant=1, K=None) == 1
+    assert _q(L, variant=1, K=FAKE) == 4         # the mma.sync variant is not built
     assert _q(L, variant=0, f=None) == 1
 
 
@@ -234,3 +248,36 @@ def test_ex_argument_checks(L):
     assert f(A, 1, 4, 64, 64, 4, None, q, 32, sf, 0, None, None) == 2       # fwht: d < 128
     assert f(A, 1, 4, 96, 96, 2, None, q, 56, sf, 0, None, None) == 3       # ldq % 16
     assert f(A, 1, 0, 64, 64, 0, None, q, 32, sf, 0, None, None) == 0       # m = 0
+
+
+def test_workspace_argument_checks(L):
+    """kq_quantize_mxfp4_ws / kq_quantize_mxfp4_dual_ws: the workspace is
+    required and 4-byte aligned; the other checks are those of the plain
+    entry points.  Every call fails a check (or has m = 0): nothing launches."""
+    vp = ctypes.c_void_p
+    A, K, q, sf, at, ws = vp(4096), vp(8192), vp(12288), vp(16384), vp(20480), vp(24576)
+    f = L.kq_quantize_mxfp4_ws
+    assert f(A, 4, 64, 64, None, K, q, 32, sf, 0, None, None, None) == 1       # no workspace
+    assert f(A, 4, 64, 64, None, K, q, 32, sf, 0, None, vp(24578), None) == 3  # misaligned
+    assert f(A, 4, 60, 64, None, K, q, 32, sf, 0, None, ws, None) == 2         # d % 32
+    assert f(A, 4, 64, 64, None, vp(8200), q, 32, sf, 0, None, ws, None) == 3  # blocks alignment
+    assert f(A, 0, 64, 64, None, K, q, 32, sf, 0, None, ws, None) == 0         # m = 0
+    g = L.kq_quantize_mxfp4_dual_ws
+    assert g(A, 4, 64, 64, K, q, 32, sf, 0, at, 64, None, None, None) == 1     # no workspace
+    assert g(A, 4, 64, 64, K, q, 32, sf, 0, at, 64, None, vp(24577), None) == 3
+    assert g(A, 4, 64, 64, K, q, 32, sf, 0, at, 32, None, ws, None) == 2       # ldat < d
+    assert g(A, 4, 64, 64, None, q, 32, sf, 0, at, 64, None, ws, None) == 1    # no blocks
+    assert g(A, 0, 64, 64, K, q, 32, sf, 0, at, 64, None, ws, None) == 0       # m = 0
+
+
+def test_stall_hook_argument_checks(L):
+    """kq_test_quantize_stall takes a wait limit between 1 ms and 1 s and the
+    checks of the tensor-core path; nothing launches when one fails."""
+    vp = ctypes.c_void_p
+    A, K, q, sf, ws = vp(4096), vp(8192), vp(12288), vp(16384), vp(24576)
+    h = L.kq_test_quantize_stall
+    assert h(A, 4, 64, 64, K, q, 32, sf, 0, None, 0, 999_999, None) == 2          # limit < 1 ms
+    assert h(A, 4, 64, 64, K, q, 32, sf, 0, None, 0, 2_000_000_000, None) == 2    # limit > 1 s
+    assert h(A, 4, 64, 64, None, q, 32, sf, 0, None, 0, 10_000_000, None) == 1    # no blocks
+    assert h(A, 4, 64, 64, K, q, 32, sf, 0, vp(24578), 0, 10_000_000, None) == 3  # workspace
+    assert h(A, 0, 64, 64, K, q, 32, sf, 0, ws, 0, 10_000_000, None) == 0         # m = 0

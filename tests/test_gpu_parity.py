@@ -52,13 +52,36 @@ def lib_factors(nb, seed, sign=+1):
         .astype(np.float32).astype(np.float64)
 
 
+_WS = {}
+
+
+def workspace():
+    """One scheduling workspace for the whole module (calls run one at a
+    time on the current stream); its words 0-1 must read zero after every
+    call and word 2 (CTAs that stopped waiting) must stay zero."""
+    if "ws" not in _WS:
+        _WS["ws"] = kq.sched_workspace("cuda")
+    return _WS["ws"]
+
+
+def check_workspace_clean():
+    torch.cuda.synchronize()
+    assert np_(workspace()).tolist() == [0, 0, 0, 0]
+
+
 def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None, q=None, sf=None):
     A = to_bf16(A_bits)
-    if kind in ("kron_umma", "kron_mma"):
+    if kind == "kron_umma":
         records = kq.kq_expand_blocks(dev(param_gpu), kq.KQ_K_BF16X3)
-        variant = kq.VARIANT_UMMA if kind == "kron_umma" else kq.VARIANT_MMA
         return kq.kq_quantize_mxfp4(A, d, K_expanded=records, layout=layout, y_debug=y_debug,
-                                    variant=variant, q=q, sf=sf)
+                                    variant=kq.VARIANT_UMMA, q=q, sf=sf)
+    if kind == "kron_ws":
+        # the tensor-core kernel taking its tiles from the workspace counter
+        records = kq.kq_expand_blocks(dev(param_gpu), kq.KQ_K_BF16X3)
+        out = kq.kq_quantize_mxfp4_ws(A, workspace(), d, K_expanded=records, layout=layout,
+                                      y_debug=y_debug, q=q, sf=sf)
+        check_workspace_clean()
+        return out
     if kind == "kron":
         return kq.kq_quantize_mxfp4(A, d, factors=dev(param_gpu), layout=layout, y_debug=y_debug,
                                     variant=variant, q=q, sf=sf)
@@ -73,12 +96,12 @@ def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None
 
 
 def oracle_kind(kind):
-    return "kron" if kind in ("kron_mma", "kron_umma") else kind
+    return "kron" if kind in ("kron_ws", "kron_umma") else kind
 
 
 def params_for(kind, nb, d, seed):
     """(gpu param, oracle param) for a transform kind."""
-    if kind in ("kron", "kron_mma", "kron_umma"):
+    if kind in ("kron", "kron_ws", "kron_umma"):
         return lib_factors(nb, seed)
     if kind == "diag":
         s = synth.smooth_scales(d)
@@ -134,28 +157,26 @@ CASES = synth.CONFIG0 + synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3
 
 
 @pytest.mark.parametrize("name,m,d,model,cfg", CASES, ids=[c[0] for c in CASES])
-@pytest.mark.parametrize("kind", ["kron", "kron_mma", "kron_umma", "diag", "hadamard", "identity"])
+@pytest.mark.parametrize("kind", ["kron", "kron_ws", "kron_umma", "diag", "hadamard", "identity"])
 def test_config_parity(name, m, d, model, cfg, kind):
-    """Configs 0-3 at full size, both scale layouts (flux shapes compare a
-    seeded sample of rows, always including the first and last tiles)."""
+    """Configs 0-3 at full size, every row and block, both scale layouts
+    (the oracle's result computed once and compared with both)."""
     nb = d // 32
     A_bits = synth.activations(m, d, synth.SEED_A + cfg, model)
     pg, po = params_for(kind, nb, d, synth.SEED_FACTORS + cfg)
-    rows = None
-    if m * d > 30_000_000:
-        rng = np.random.default_rng(cfg)
-        rows = np.unique(np.concatenate([np.arange(130), np.arange(m - 130, m),
-                                         rng.choice(m, 700, replace=False)]))
+    ref = parity.reference(A_bits, d, oracle_kind(kind), po)
     for layout in (0, 1):
         q, sf, y = run_kind(kind, A_bits, d, layout, pg)
-        res = parity.check(A_bits, d, oracle_kind(kind), po, layout, np_(q), np_(sf), np_(y), rows)
+        res = parity.check(A_bits, d, oracle_kind(kind), po, layout, np_(q), np_(sf), np_(y),
+                           ref=ref)
         # the production launch (no debug output) writes the same bytes
         q2, sf2, _ = run_kind(kind, A_bits, d, layout, pg, y_debug=False)
         assert torch.equal(q, q2) and torch.equal(sf, sf2)
+        parity.record(f"config {cfg}", name, m, d, kind, layout, res)
         print(name, kind, layout, res)
 
 
-def test_mma_matches_butterfly_outside_flags():
+def test_umma_matches_butterfly_outside_flags():
     """The tensor-core and the butterfly implementations of the same
     transform agree on every unflagged code (both are checked against the
     oracle elsewhere)."""
@@ -163,7 +184,7 @@ def test_mma_matches_butterfly_outside_flags():
     A_bits = synth.activations(m, d, synth.SEED_A + 1, "pixart")
     Fg, Fo = lib_factors(d // 32, synth.SEED_FACTORS + 1)
     qb, sfb, _ = run_kind("kron", A_bits, d, 1, Fg, y_debug=False)
-    qm, sfm, _ = run_kind("kron_mma", A_bits, d, 1, Fg, y_debug=False)
+    qm, sfm, _ = run_kind("kron_umma", A_bits, d, 1, Fg, y_debug=False)
     rows = np.arange(0, m, 7)
     _, _, flags = O.quantize(*O.transform(np.ascontiguousarray(A_bits[rows]), d, "kron", Fo),
                              O.SF_ROWMAJOR)
@@ -220,9 +241,9 @@ def test_layer_error_config0(factor_kind):
 @pytest.mark.parametrize("name,m,d,model,cfg", synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3,
                          ids=[c[0] for c in synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3])
 def test_layer_error_configs(name, m, d, model, cfg):
-    """E(T) on configs 1-3: first 512 rows of A, a weight of o = min(d, 3072)
-    output channels."""
-    m, o = 512, min(d, 3072)
+    """E(T) on configs 1-3: first 512 rows of A, a square weight of o = d
+    output channels (an FFN-down-like d x d projection)."""
+    m, o = 512, d
     nb = d // 32
     A_bits = synth.activations(m, d, synth.SEED_A + cfg, model)
     W_bits = synth.weights(o, d, seed=synth.SEED_W + cfg)
@@ -245,25 +266,31 @@ SWEEP = [(m, d) for m in synth.SWEEP_M for d in synth.SWEEP_D]
 
 @pytest.mark.parametrize("m,d", SWEEP, ids=[f"{m}x{d}" for m, d in SWEEP])
 def test_sweep_parity(m, d):
-    """Config 4: 4 layers' factor sets per point; KroQuant, diagonal and
-    Hadamard quantizers; large points compare a seeded row sample."""
+    """Config 4: 4 layers' factor sets per point; KroQuant (butterfly, both
+    tensor-core schedules), diagonal and Hadamard quantizers.  Every row up
+    to m = 16384; at m = 65536 a seeded sample of 4096 rows (the first and
+    last tiles always included)."""
     nb = d // 32
     A_bits = synth.activations(m, d, synth.SEED_A + 4, "flux")
     rng = np.random.default_rng(m + d)
     rows = None
-    if m * d > 20_000_000:
+    if m > 16384:
         rows = np.unique(np.concatenate([np.arange(128), np.arange(m - 128, m),
-                                         rng.choice(m, 400, replace=False)]))
+                                         rng.choice(m, 4096, replace=False)]))
     for layer in range(4):
         Fg, Fo = lib_factors(nb, synth.SEED_FACTORS + 4 + layer)
-        kind = ("kron", "kron_umma", "kron_mma", "kron_umma")[layer]
+        kind = ("kron", "kron_umma", "kron_ws", "kron_umma")[layer]
         q, sf, y = run_kind(kind, A_bits, d, layer % 2, Fg)
-        parity.check(A_bits, d, "kron", Fo, layer % 2, np_(q), np_(sf), np_(y), rows)
+        res = parity.check(A_bits, d, "kron", Fo, layer % 2, np_(q), np_(sf), np_(y), rows)
+        parity.record("config 4", f"sweep layer {layer}", m, d, kind, layer % 2, res)
+        del q, sf, y
     s = synth.smooth_scales(d)
     q, sf, y = run_kind("diag", A_bits, d, 1, s)
-    parity.check(A_bits, d, "diag", s.astype(np.float64), 1, np_(q), np_(sf), np_(y), rows)
+    res = parity.check(A_bits, d, "diag", s.astype(np.float64), 1, np_(q), np_(sf), np_(y), rows)
+    parity.record("config 4", "sweep", m, d, "diag", 1, res)
     q, sf, y = run_kind("hadamard", A_bits, d, 0)
-    parity.check(A_bits, d, "hadamard", None, 0, np_(q), np_(sf), np_(y), rows)
+    res = parity.check(A_bits, d, "hadamard", None, 0, np_(q), np_(sf), np_(y), rows)
+    parity.record("config 4", "sweep", m, d, "hadamard", 0, res)
 
 
 # ------------------------------------------------------------ edge cases --
@@ -272,7 +299,7 @@ EDGE_SHAPES = [(1, 32), (7, 96), (127, 160), (129, 64), (200, 5600), (3, 2240), 
 
 
 @pytest.mark.parametrize("m,d", EDGE_SHAPES, ids=[f"{m}x{d}" for m, d in EDGE_SHAPES])
-@pytest.mark.parametrize("kind", ["kron", "kron_mma", "kron_umma", "diag", "hadamard", "identity"])
+@pytest.mark.parametrize("kind", ["kron", "kron_ws", "kron_umma", "diag", "hadamard", "identity"])
 def test_ragged_shapes_with_pitches_and_canaries(m, d, kind):
     """Ragged m and d (partial tiles and block-columns), lda > d, ldq > d/2,
     and guard bytes around every output that must stay untouched."""
@@ -329,7 +356,7 @@ def test_special_values():
     y_k[4] /= 2.0 ** 8
     bits_k = synth.f64_to_bf16_bits(y_k)
     Fg, Fo = lib_factors(1, 3)
-    for kind in ("kron", "kron_mma", "kron_umma"):
+    for kind in ("kron", "kron_ws", "kron_umma"):
         q, sf, yd = run_kind(kind, bits_k, 32, 0, Fg)
         parity.check(bits_k, 32, "kron", Fo, 0, np_(q), np_(sf), np_(yd))
 
@@ -341,7 +368,7 @@ def test_raw_factor_interface():
     nb = d // 32
     A_bits = synth.activations(m, d, 9, "sana")
     F = synth.random_factors(nb, 12, scale=0.8)
-    for kind in ("kron", "kron_mma", "kron_umma"):
+    for kind in ("kron", "kron_ws", "kron_umma"):
         q, sf, y = run_kind(kind, A_bits, d, 1, F)
         parity.check(A_bits, d, "kron", F.astype(np.float64), 1, np_(q), np_(sf), np_(y))
     Fg, Fo = lib_factors(nb, 13, sign=-1)
@@ -568,7 +595,7 @@ def test_identity_factors_reduce_to_bare_quantizer():
     for layout in (0, 1):
         nsf = kq.kq_sf_bytes(m, d, layout)
         q0, sf0, _ = run_kind("identity", A_bits, d, layout, y_debug=False)
-        for kind in ("kron", "kron_umma", "kron_mma"):
+        for kind in ("kron", "kron_umma", "kron_ws"):
             q, sf, y = run_kind(kind, A_bits, d, layout, eye)
             assert torch.equal(q, q0) and torch.equal(sf[:nsf], sf0[:nsf]), kind
             assert np.array_equal(np_(y), synth.bf16_bits_to_f32(A_bits)), kind
@@ -730,9 +757,9 @@ def test_layer_error_on_device_config0(factor_kind):
 @pytest.mark.parametrize("name,m,d,model,cfg", synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3,
                          ids=[c[0] for c in synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3])
 def test_layer_error_on_device_configs(name, m, d, model, cfg):
-    """The same on configs 1-3: the first 512 rows of A, a weight of
-    o = min(d, 3072) output channels."""
-    m, o = 512, min(d, 3072)
+    """The same on configs 1-3: the first 512 rows of A, a square weight of
+    o = d output channels."""
+    m, o = 512, d
     A_bits = synth.activations(m, d, synth.SEED_A + cfg, model)
     W_bits = synth.weights(o, d, seed=synth.SEED_W + cfg)
     Fg, Fo = lib_factors(d // 32, synth.SEED_FACTORS + cfg)
@@ -860,3 +887,178 @@ def test_default_dispatch_with_both_factor_forms(m, d, expect):
     v = kq.VARIANT_BUTTERFLY if expect == "butterfly" else kq.VARIANT_UMMA
     q2, sf2, _ = kq.kq_quantize_mxfp4(A, d, factors=Fd, K_expanded=KX, layout=1, variant=v)
     assert torch.equal(q, q2) and torch.equal(sf, sf2)
+
+
+# ------------------------------------------------ scheduling workspace --
+
+# (256, 5120): 160 tiles on 152 CTAs, so a CTA that starts late may take none
+WS_SHAPES = [(1, 64), (129, 96), (300, 1152), (256, 5120), (4096, 1152), (4608, 3072)]
+
+
+@pytest.mark.parametrize("m,d", WS_SHAPES, ids=[f"{m}x{d}" for m, d in WS_SHAPES])
+def test_workspace_schedule_matches_fixed_walk(m, d):
+    """kq_quantize_mxfp4_ws: the CTAs take tiles from the workspace counter;
+    every byte equals the fixed walk's (both scale layouts, with and without
+    the debug output), the counters are zero again after every call, and one
+    workspace serves calls back to back."""
+    A_bits = synth.activations(m, d, 2200 + m, "flux")
+    A = to_bf16(A_bits)
+    F, Fo = lib_factors(d // 32, 2201 + d)
+    KX = kq.kq_expand_blocks(dev(F), kq.KQ_K_BF16X3)
+    ws = workspace()
+    for layout in (0, 1):
+        nsf = kq.kq_sf_bytes(m, d, layout)       # the buffers may be longer (>= 16 bytes)
+        q0, s0, y0 = kq.kq_quantize_mxfp4(A, d, K_expanded=KX, layout=layout, y_debug=True)
+        for rep in range(3):
+            q1, s1, y1 = kq.kq_quantize_mxfp4_ws(A, ws, d, K_expanded=KX, layout=layout,
+                                                 y_debug=(rep == 0))
+            check_workspace_clean()
+            assert torch.equal(q0, q1) and torch.equal(s0[:nsf], s1[:nsf])
+            if rep == 0:
+                assert torch.equal(y0.view(torch.int32), y1.view(torch.int32))
+        if m * d <= 2_000_000:
+            parity.check(A_bits, d, "kron", Fo, layout, np_(q0), np_(s0), np_(y0))
+
+
+def test_dual_workspace_matches_fixed_walk():
+    """kq_quantize_mxfp4_dual_ws writes the same codes, scales and bf16 side
+    output as kq_quantize_mxfp4_dual, and leaves its workspace zero."""
+    m, d = 4608, 3072
+    A = to_bf16(synth.activations(m, d, 2300, "flux"))
+    F, _ = lib_factors(d // 32, 2301)
+    KX = kq.kq_expand_blocks(dev(F), kq.KQ_K_BF16X3)
+    nsf = kq.kq_sf_bytes(m, d, 1)
+    q0, s0, at0, _ = kq.kq_quantize_mxfp4_dual(A, KX, d, layout=1)
+    for _ in range(2):
+        q1, s1, at1, _ = kq.kq_quantize_mxfp4_dual(A, KX, d, layout=1, workspace=workspace())
+        check_workspace_clean()
+        assert torch.equal(q0, q1) and torch.equal(s0[:nsf], s1[:nsf])
+        assert torch.equal(at0.view(torch.int16), at1.view(torch.int16))
+
+
+def test_workspace_in_cuda_graph():
+    """The FLUX FFN-down layer (4608 x 12288) quantized by a CUDA graph of
+    four launches sharing one workspace (the benchmark's launch form, with
+    programmatic dependent launch between them), replayed twice: every
+    output equals the fixed walk's and the counters end at zero."""
+    m, d = 4608, 12288
+    A = to_bf16(synth.activations(m, d, 2400, "flux"))
+    F, _ = lib_factors(d // 32, 2401)
+    KX = kq.kq_expand_blocks(dev(F), kq.KQ_K_BF16X3)
+    q0, s0, _ = kq.kq_quantize_mxfp4(A, d, K_expanded=KX, layout=1)
+    ws = workspace()
+    stream = torch.cuda.Stream()
+    outs = [(torch.empty_like(q0), torch.empty_like(s0)) for _ in range(4)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        kq.kq_quantize_mxfp4_ws(A, ws, d, K_expanded=KX, layout=1, q=outs[0][0], sf=outs[0][1],
+                                stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for q, sf in outs:
+            kq.kq_quantize_mxfp4_ws(A, ws, d, K_expanded=KX, layout=1, q=q, sf=sf, stream=stream)
+    nsf = kq.kq_sf_bytes(m, d, 1)
+    for _ in range(2):
+        for q, sf in outs:
+            q.zero_()
+            sf.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        for q, sf in outs:
+            assert torch.equal(q, q0) and torch.equal(sf[:nsf], s0[:nsf])
+        check_workspace_clean()
+
+
+# ------------------------------------------ a pipeline wait that runs out --
+
+STALL_LIMIT_NS = 20_000_000        # 20 ms: every normal wait ends in microseconds
+
+
+def tile_blocks(t, ncol, nb, m):
+    """(rows, blocks) of tile t of the tcgen05 kernel (128 rows x 2 blocks)."""
+    rt, ct = divmod(t, ncol)
+    rows = np.arange(rt * 128, min(rt * 128 + 128, m))
+    blocks = np.array([j for j in (2 * ct, 2 * ct + 1) if j < nb])
+    return rows, blocks
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_stalled_pipeline_marks_unfinished_blocks(layout):
+    """The error path of the fixed-walk kernel, made to run by a wait that
+    runs out (nothing faults): CTA 5's producer arms the ring stage of its
+    4th tile but never issues that tile's loads, and every wait gives up
+    after 20 ms.  The kernel must return; the blocks the CTA did not finish
+    get the E8M0 NaN byte 0xFF and zero codes, every other byte equals a
+    normal run.  With 6 ring stages and two MMA issuers taking alternate
+    tiles, the CTA finishes its tiles 0-2, 4, 6 and 8 (the other issuer's
+    tiles up to the one whose stage reuse waits on the skipped tile) and no
+    other."""
+    m, d = 4608, 3072                       # 36 x 48 tiles; CTA 5 owns 12 of them
+    nb = d // 32
+    A = to_bf16(synth.activations(m, d, 2500, "flux"))
+    F, _ = lib_factors(nb, 2501)
+    KX = kq.kq_expand_blocks(dev(F), kq.KQ_K_BF16X3)
+    q0, s0, _ = kq.kq_quantize_mxfp4(A, d, K_expanded=KX, layout=layout)
+    nsf = kq.kq_sf_bytes(m, d, layout)
+    ncol, ntiles, grid, cta = 48, 36 * 48, 152, 5
+    walk = list(range(cta, ntiles, grid))   # the CTA's tiles in order
+    assert len(walk) == 12
+    q1 = torch.full_like(q0, 0xA5)
+    s1 = torch.full_like(s0, 0xA5)
+    kq.kq_test_quantize_stall(A, KX, d, walk[3], STALL_LIMIT_NS, layout=layout, q=q1, sf=s1)
+    torch.cuda.synchronize()
+    want_q, want_s = np_(q0).copy(), np_(s0)[:nsf].copy()
+    for pos in (3, 5, 7, 9, 10, 11):
+        rows, blocks = tile_blocks(walk[pos], ncol, nb, m)
+        for j in blocks:
+            want_q[np.ix_(rows, np.arange(16 * j, 16 * j + 16))] = 0
+            off = (rows * nb + j) if layout == 0 else \
+                ((rows // 128) * ((nb + 3) // 4) + j // 4) * 512 + (rows % 32) * 16 + \
+                ((rows % 128) // 32) * 4 + j % 4
+            want_s[off] = 0xFF
+    got_q, got_s = np_(q1), np_(s1)[:nsf]
+    assert np.array_equal(got_s, want_s), int((got_s != want_s).sum())
+    assert np.array_equal(got_q, want_q), int((got_q != want_q).sum())
+    # the same hook with no tile skipped writes the normal bytes
+    kq.kq_test_quantize_stall(A, KX, d, -1, STALL_LIMIT_NS, layout=layout, q=q1, sf=s1)
+    torch.cuda.synchronize()
+    assert torch.equal(q1, q0) and torch.equal(s1[:nsf], s0[:nsf])
+
+
+def test_stalled_pipeline_with_workspace_schedule():
+    """The same stall under the counter schedule: the CTA that takes the
+    skipped tile stops, counts itself in workspace word 2 and lets the other
+    CTAs take every tile it did not; the counters end at zero.  Blocks that
+    differ from a normal run are those of a few tiles the stopped CTA held
+    (0xFF with zero codes where it knew the tile, the old bytes otherwise),
+    the skipped tile among them."""
+    m, d = 4608, 3072
+    nb = d // 32
+    A = to_bf16(synth.activations(m, d, 2600, "flux"))
+    F, _ = lib_factors(nb, 2601)
+    KX = kq.kq_expand_blocks(dev(F), kq.KQ_K_BF16X3)
+    q0, s0, _ = kq.kq_quantize_mxfp4(A, d, K_expanded=KX, layout=0)
+    ws = kq.sched_workspace("cuda")
+    skip = 1000
+    q1 = torch.full_like(q0, 0xA5)
+    s1 = torch.full_like(s0, 0xA5)
+    kq.kq_test_quantize_stall(A, KX, d, skip, STALL_LIMIT_NS, layout=0, q=q1, sf=s1, workspace=ws)
+    torch.cuda.synchronize()
+    assert np_(ws).tolist() == [0, 0, 1, 0]
+    ncol = nb // 2
+    bad_tiles = set()
+    g0, g1 = np_(s0)[:m * nb].reshape(m, nb), np_(s1)[:m * nb].reshape(m, nb)
+    c0, c1 = np_(q0).reshape(m, nb, 16), np_(q1).reshape(m, nb, 16)
+    for t in range(36 * ncol):
+        rows, blocks = tile_blocks(t, ncol, nb, m)
+        for j in blocks:
+            same = np.array_equal(g0[rows, j], g1[rows, j]) and np.array_equal(c0[rows, j], c1[rows, j])
+            if same:
+                continue
+            bad_tiles.add(t)
+            nan = (g1[rows, j] == 0xFF).all() and (c1[rows, j] == 0).all()
+            old = (g1[rows, j] == 0xA5).all() and (c1[rows, j] == 0xA5).all()
+            assert nan or old, (t, j)
+    assert skip in bad_tiles and len(bad_tiles) <= 12, sorted(bad_tiles)

@@ -146,6 +146,9 @@ void fill_quant_params(QuantParams &p, int64_t m, int64_t d, int64_t rows_per_ti
     p.y_debug = y_debug;
     p.shared_params = 0;
     p.in_f16 = 0;
+    p.tile_ctr = nullptr;
+    p.wait_limit_ns = kWaitLimitNs;
+    p.skip_tile = -1;
 }
 
 // ---------------------------------------------------------------------------
@@ -246,6 +249,92 @@ int grid_for(int64_t work, int threads)
 
 using namespace kq;
 
+namespace {
+
+// The quantizer entry points: argument checks, then the implementation
+// `variant` (0 butterfly, 2 identity, 3 tcgen05).  `extra` carries the
+// tcgen05 kernel's tile counters, wait limit and verification hook (its
+// other fields are filled here).
+kq_status quantize_variant(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                           const float *factors, const void *K_expanded, uint8_t *q, int64_t ldq,
+                           uint8_t *sf, kq_sf_layout sf_layout, float *y_debug, int variant,
+                           const QuantParams &extra, cudaStream_t stream)
+{
+    if (variant != 0 && variant != 2 && variant != 3) return KQ_ERR_LAYOUT;
+    kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
+    if (st != KQ_OK) return st;
+    if (variant == 0 && factors == nullptr) return KQ_ERR_NULL;
+    if (variant == 3 && K_expanded == nullptr) return KQ_ERR_NULL;
+    if (variant == 0 && !aligned16(factors)) return KQ_ERR_ALIGN;
+    if (variant == 3 && !aligned16(K_expanded)) return KQ_ERR_ALIGN;
+    if (m == 0) return KQ_OK;
+    DeviceInfo info;
+    if ((st = device_info(info)) != KQ_OK) return st;
+    QuantParams p;
+    fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
+    if (variant == 3) {
+        p.tile_ctr = extra.tile_ctr;
+        p.wait_limit_ns = extra.wait_limit_ns;
+        p.skip_tile = extra.skip_tile;
+        return launch_quant_umma(A, lda, K_expanded, p, nullptr, 0, stream);
+    }
+    if (variant == 0) {
+        p.factors = factors;
+        return launch_quant_tma(kKron, A, lda, p, stream);
+    }
+    return launch_quant_tma(kIdentity, A, lda, p, stream);
+}
+
+// The fastest implementation the arguments allow: tcgen05 on the expanded
+// blocks, else the butterfly on the raw factors, else identity.  With both
+// given, layers below 2^21 elements take the butterfly: there every kernel
+// is latency-bound and the tensor-core pipeline's longer first tile costs
+// more than its arithmetic saves (measured on GB300: butterfly faster up to
+// 1024 x 1152, tcgen05 from 1024 x 3072 on).
+int default_variant(int64_t m, int64_t d, const float *factors, const void *K_expanded)
+{
+    int variant = K_expanded != nullptr ? 3 : (factors != nullptr ? 0 : 2);
+    if (variant == 3 && factors != nullptr && m * d < (int64_t(1) << 21)) variant = 0;
+    return variant;
+}
+
+kq_status quantize_dual(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                        const void *K_expanded, uint8_t *q, int64_t ldq, uint8_t *sf,
+                        kq_sf_layout sf_layout, uint16_t *at, int64_t ldat, float *y_debug,
+                        uint32_t *workspace, cudaStream_t stream)
+{
+    kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
+    if (st != KQ_OK) return st;
+    if (ldat < d || ldat > (1LL << 38)) return KQ_ERR_SHAPE;
+    if (m == 0) return KQ_OK;
+    if (K_expanded == nullptr || at == nullptr) return KQ_ERR_NULL;
+    if (!aligned16(K_expanded) || !aligned16(at) || ldat % 8 != 0) return KQ_ERR_ALIGN;
+    QuantParams p;
+    fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
+    p.tile_ctr = workspace;
+    return launch_quant_umma(A, lda, K_expanded, p, at, ldat, stream);
+}
+
+// The tcgen05 kernel's scheduling fields: tile counters (or null for the
+// fixed walk), the default wait limit, no skipped tile.
+QuantParams sched_params(uint32_t *workspace)
+{
+    QuantParams p{};
+    p.tile_ctr = workspace;
+    p.wait_limit_ns = kWaitLimitNs;
+    p.skip_tile = -1;
+    return p;
+}
+
+kq_status check_workspace(const uint32_t *workspace)
+{
+    if (workspace == nullptr) return KQ_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(workspace) % 4 != 0) return KQ_ERR_ALIGN;
+    return KQ_OK;
+}
+
+}  // namespace
+
 // ---------------------------------------------------------------------------
 // C ABI
 
@@ -256,25 +345,8 @@ kq_status kq_quantize_mxfp4_variant(const uint16_t *A, int64_t m, int64_t d, int
                                     int64_t ldq, uint8_t *sf, kq_sf_layout sf_layout,
                                     float *y_debug, int variant, cudaStream_t stream)
 {
-    if (variant < 0 || variant > 3) return KQ_ERR_LAYOUT;
-    kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
-    if (st != KQ_OK) return st;
-    if (variant == 0 && factors == nullptr) return KQ_ERR_NULL;
-    if ((variant == 1 || variant == 3) && K_expanded == nullptr) return KQ_ERR_NULL;
-    if (variant == 0 && !aligned16(factors)) return KQ_ERR_ALIGN;
-    if ((variant == 1 || variant == 3) && !aligned16(K_expanded)) return KQ_ERR_ALIGN;
-    if (m == 0) return KQ_OK;
-    DeviceInfo info;
-    if ((st = device_info(info)) != KQ_OK) return st;
-    QuantParams p;
-    fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
-    if (variant == 1) return launch_quant_mma(A, lda, K_expanded, p, stream);
-    if (variant == 3) return launch_quant_umma(A, lda, K_expanded, p, nullptr, 0, stream);
-    if (variant == 0) {
-        p.factors = factors;
-        return launch_quant_tma(kKron, A, lda, p, stream);
-    }
-    return launch_quant_tma(kIdentity, A, lda, p, stream);
+    return quantize_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout, y_debug,
+                            variant, sched_params(nullptr), stream);
 }
 
 kq_status kq_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
@@ -282,16 +354,21 @@ kq_status kq_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda
                             uint8_t *sf, kq_sf_layout sf_layout, float *y_debug,
                             cudaStream_t stream)
 {
-    // the fastest implementation the arguments allow: tcgen05 on the
-    // expanded blocks, else the butterfly on the raw factors, else identity.
-    // With both given, layers below 2^21 elements take the butterfly: there
-    // every kernel is latency-bound and the tensor-core pipeline's longer
-    // first tile costs more than its arithmetic saves (measured on GB300:
-    // butterfly faster up to 1024 x 1152, tcgen05 from 1024 x 3072 on).
-    int variant = K_expanded != nullptr ? 3 : (factors != nullptr ? 0 : 2);
-    if (variant == 3 && factors != nullptr && m * d < (int64_t(1) << 21)) variant = 0;
-    return kq_quantize_mxfp4_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout,
-                                     y_debug, variant, stream);
+    return quantize_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout, y_debug,
+                            default_variant(m, d, factors, K_expanded), sched_params(nullptr),
+                            stream);
+}
+
+kq_status kq_quantize_mxfp4_ws(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                               const float *factors, const void *K_expanded, uint8_t *q,
+                               int64_t ldq, uint8_t *sf, kq_sf_layout sf_layout, float *y_debug,
+                               uint32_t *workspace, cudaStream_t stream)
+{
+    const kq_status st = check_workspace(workspace);
+    if (st != KQ_OK) return st;
+    return quantize_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout, y_debug,
+                            default_variant(m, d, factors, K_expanded), sched_params(workspace),
+                            stream);
 }
 
 kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
@@ -299,15 +376,33 @@ kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d, int64_
                                  kq_sf_layout sf_layout, uint16_t *at, int64_t ldat,
                                  float *y_debug, cudaStream_t stream)
 {
-    kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
+    return quantize_dual(A, m, d, lda, K_expanded, q, ldq, sf, sf_layout, at, ldat, y_debug,
+                         nullptr, stream);
+}
+
+kq_status kq_quantize_mxfp4_dual_ws(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                    const void *K_expanded, uint8_t *q, int64_t ldq, uint8_t *sf,
+                                    kq_sf_layout sf_layout, uint16_t *at, int64_t ldat,
+                                    float *y_debug, uint32_t *workspace, cudaStream_t stream)
+{
+    const kq_status st = check_workspace(workspace);
     if (st != KQ_OK) return st;
-    if (ldat < d || ldat > (1LL << 38)) return KQ_ERR_SHAPE;
-    if (m == 0) return KQ_OK;
-    if (K_expanded == nullptr || at == nullptr) return KQ_ERR_NULL;
-    if (!aligned16(K_expanded) || !aligned16(at) || ldat % 8 != 0) return KQ_ERR_ALIGN;
-    QuantParams p;
-    fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
-    return launch_quant_umma(A, lda, K_expanded, p, at, ldat, stream);
+    return quantize_dual(A, m, d, lda, K_expanded, q, ldq, sf, sf_layout, at, ldat, y_debug,
+                         workspace, stream);
+}
+
+kq_status kq_test_quantize_stall(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
+                                 const void *K_expanded, uint8_t *q, int64_t ldq, uint8_t *sf,
+                                 kq_sf_layout sf_layout, uint32_t *workspace, int64_t skip_tile,
+                                 uint64_t wait_limit_ns, cudaStream_t stream)
+{
+    if (wait_limit_ns < 1000000ull || wait_limit_ns > kWaitLimitNs) return KQ_ERR_SHAPE;
+    if (workspace != nullptr && check_workspace(workspace) != KQ_OK) return KQ_ERR_ALIGN;
+    QuantParams p = sched_params(workspace);
+    p.skip_tile = skip_tile;
+    p.wait_limit_ns = wait_limit_ns;
+    return quantize_variant(A, m, d, lda, nullptr, K_expanded, q, ldq, sf, sf_layout, nullptr,
+                            3, p, stream);
 }
 
 kq_status kq_fwht_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
@@ -488,7 +583,7 @@ kq_status kq_expand_blocks(const float *factors, int64_t nb, kq_kfmt fmt, void *
     DeviceInfo info;
     kq_status st = device_info(info);
     if (st != KQ_OK) return st;
-    if (fmt == KQ_K_BF16X3) return launch_mma_records(factors, nb, K_out, stream);
+    if (fmt == KQ_K_BF16X3) return launch_umma_records(factors, nb, K_out, stream);
     expand_kernel<<<grid_for(nb * 1024, 256), 256, 0, stream>>>(factors, nb, K_out);
     return check_launch();
 }

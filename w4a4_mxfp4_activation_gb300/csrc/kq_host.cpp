@@ -39,8 +39,7 @@ size_t kq_expanded_bytes(int64_t nb, kq_kfmt fmt)
 {
     if (nb <= 0) return 0;
     if (fmt == KQ_K_FP32) return static_cast<size_t>(nb) * 32 * 32 * 4;
-    if (fmt == KQ_K_BF16X3)      // two record sets
-        return static_cast<size_t>(nb) * (kq::kUmmaRecordBytes + kq::kMmaRecordBytes);
+    if (fmt == KQ_K_BF16X3) return static_cast<size_t>(nb) * kq::kUmmaRecordBytes;
     return 0;
 }
 

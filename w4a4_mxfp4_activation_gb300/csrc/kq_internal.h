@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "kq.h"
+#include "kq_testing.h"
 #include "kq_records.h"
 
 namespace kq {
@@ -36,6 +37,11 @@ struct QuantParams {
     float *y_debug;     // [m][d] or null
     int shared_params;  // 1: every block takes block 0's factors / operand records
     int in_f16;         // 1: A holds fp16 bit patterns (CUDA-core kernels), 0: bf16
+    // tcgen05 kernel only:
+    uint32_t *tile_ctr;     // null: fixed tile walk; else 3 words (next tile, CTAs done,
+                            // CTAs that stopped waiting) the CTAs take tiles from
+    uint64_t wait_limit_ns; // bound of every pipeline wait
+    int64_t skip_tile;      // verification hook: a tile whose loads are never issued (-1: none)
 };
 
 // Per-device facts the launchers need.
@@ -86,9 +92,8 @@ kq_status launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem,
 
 kq_status launch_quant_tma(Transform t, const uint16_t *A, int64_t lda, const QuantParams &p,
                            cudaStream_t stream);
-kq_status launch_quant_mma(const uint16_t *A, int64_t lda, const void *K_expanded,
-                           const QuantParams &p, cudaStream_t stream);
-kq_status launch_mma_records(const float *factors, int64_t nb, void *out, cudaStream_t stream);
+// The tcgen05 operand records of kq_expand_blocks (KQ_K_BF16X3).
+kq_status launch_umma_records(const float *factors, int64_t nb, void *out, cudaStream_t stream);
 // Full-row Walsh-Hadamard + MXFP4 (d a power of two, 128 <= d <= 16384).
 kq_status launch_quant_fwht(const uint16_t *A, int64_t lda, const QuantParams &p,
                             cudaStream_t stream);

@@ -6,10 +6,9 @@
 
 namespace kq {
 
-// Bytes of one block's operand record for the two tensor-core variants:
-// tcgen05 (dense K_j, three bf16 terms) and mma.sync (K'_j terms + G1).
-// K_expanded in KQ_K_BF16X3 holds nb tcgen05 records, then nb mma.sync ones.
+// Bytes of one block's operand record of the tcgen05 kernel: the dense K_j
+// as three bf16 terms (hi, mid, lo), laid out as the B operands of the
+// block's two K = 16 MMA steps.  K_expanded in KQ_K_BF16X3 holds nb records.
 constexpr int64_t kUmmaRecordBytes = 6144;
-constexpr int64_t kMmaRecordBytes = 1552;
 
 }  // namespace kq
