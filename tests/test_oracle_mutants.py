@@ -1,8 +1,13 @@
-"""Planted mistakes: each test compiles a copy of the C oracle with one
-plausible mistake and checks that the pins reject it.  This shows the pins
-are strong enough to catch that class of error in the oracle itself.
-The mistakes are planted only in temporary copies of the oracle, on the CPU.
+"""Planted mistakes: each test builds a copy of the oracle with one
+plausible mistake (the C arithmetic recompiled, or the Python layer-error
+code re-executed as a separate module) and checks that the pins reject it.
+This shows the pins are strong enough to catch that class of error in the
+oracle itself.  The mistakes are planted only in temporary copies of the
+oracle, on the CPU.
 """
+import inspect
+import types
+
 import pytest
 
 import test_oracle_pins as pins
@@ -56,3 +61,54 @@ def test_pins_catch_planted_mistake(tmp_path, oracle_lib, name, orig, mut, must_
         for pin in must_fail:
             with pytest.raises(AssertionError):
                 pin(kq_oracle)
+
+
+# Mistakes in the Python side of the oracle: eq. (2)'s layer error.
+# (name, original text, mutated text, pins that must fail)
+PY_MUTANTS = [
+    ("activations_not_transformed",
+     'qa = quantize_activations(A, d, "kron", factors, layout)',
+     'qa = quantize_activations(A, d, "identity", None, layout)',
+     [pins.test_layer_error_golden, pins.test_layer_error_exact_on_grid]),
+    ("weights_inverse_not_transposed",
+     "np.linalg.inv(K[j]).T for j", "np.linalg.inv(K[j]) for j",
+     [pins.test_layer_error_golden, pins.test_layer_error_exact_on_grid]),
+    ("weights_take_K",
+     'yw, bw = transform(W, d, "dense", inverse_transpose_blocks(factors))',
+     'yw, bw = transform(W, d, "kron", factors)',
+     [pins.test_layer_error_golden, pins.test_layer_error_exact_on_grid]),
+    ("weights_not_transformed",
+     'yw, bw = transform(W, d, "dense", inverse_transpose_blocks(factors))',
+     'yw, bw = transform(W, d, "identity")',
+     [pins.test_layer_error_golden, pins.test_layer_error_exact_on_grid]),
+    ("product_without_transpose", "E = Aq @ Wq.T - ref", "E = Aq @ Wq - ref",
+     [pins.test_layer_error_exact_on_grid]),
+    ("error_sign", "E = Aq @ Wq.T - ref", "E = Aq @ Wq.T + ref",
+     [pins.test_layer_error_golden, pins.test_layer_error_exact_on_grid]),
+    ("reference_from_quantized", "ref = a @ w.T", "ref = Aq @ Wq.T",
+     [pins.test_layer_error_golden]),
+    ("norms_swapped", "return float(np.linalg.norm(E)), float(np.linalg.norm(ref))",
+     "return float(np.linalg.norm(ref)), float(np.linalg.norm(E))",
+     [pins.test_layer_error_golden, pins.test_layer_error_exact_on_grid]),
+]
+
+
+def python_variant(src_text: str, name: str):
+    """The oracle's Python module re-executed from modified source, as a
+    separate module object (the shared C library is unchanged)."""
+    mod = types.ModuleType(f"kq_oracle_{name}")
+    mod.__file__ = kq_oracle.__file__
+    exec(compile(src_text, kq_oracle.__file__, "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name,orig,mut,must_fail", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_pins_catch_planted_layer_error_mistake(oracle_lib, name, orig, mut, must_fail):
+    src = inspect.getsource(kq_oracle)
+    assert src.count(orig) == 1, f"mutation anchor for {name} not found exactly once"
+    mutant = python_variant(src.replace(orig, mut), name)
+    # the unmodified source, run the same way, passes the same pins
+    for pin in must_fail:
+        pin(python_variant(src, "copy"))
+        with pytest.raises(AssertionError):
+            pin(mutant)

@@ -325,6 +325,120 @@ def test_layer_error_hadamard_vs_identity_sanity(oracle_lib):
         assert 0 < e < 0.5 * ref
 
 
+def _golden_layer_case():
+    """The hand-derived single-block case of tests/golden/layer_error.txt:
+    (A bits [1, 32], W bits [1, 32], factors [1, 5, 2, 2], ||E||_F, ||A W^T||_F)."""
+    g = {r[0]: r[1:] for r in read_golden("layer_error.txt")}
+    F = np.array([[float(v) for v in g[f"G{k}"]] for k in range(1, 6)]).reshape(1, 5, 2, 2)
+    a = np.zeros((1, 32))
+    w = np.zeros((1, 32))
+    a[0, :len(g["a"])] = [float(v) for v in g["a"]]
+    w[0, :len(g["w"])] = [float(v) for v in g["w"]]
+    return (synth.f64_to_bf16_bits(a), synth.f64_to_bf16_bits(w), F,
+            float(g["error_norm"][0]), float(g["reference_norm"][0]))
+
+
+def test_layer_error_golden(oracle_lib):
+    """eq. (2) on the hand-derived block: a shear factor G5 makes A T leave
+    the MXFP4 grid (one element on a rounding midpoint) while W T^{-T} stays
+    on it, so ||E||_F = 1.5 and ||A W^T||_F = 3.5 exactly.  A dropped
+    transform on either side, K^{-1} or K in place of K^{-T}, or a sign slip
+    in E gives another value."""
+    A, W, F, e_want, r_want = _golden_layer_case()
+    for layout in (0, 1):
+        e, ref = oracle_lib.layer_error(A, W, 32, F, layout=layout)
+        assert e == e_want and ref == r_want, (e, ref)
+
+
+# Monomial 2x2 factors with power-of-two entries and det 1 (signed
+# permutations times diagonal scalings): products and inverses are exact in
+# binary arithmetic, and none of P, Q is symmetric or orthogonal.
+_MONOMIAL = {
+    "I": [[1.0, 0.0], [0.0, 1.0]],
+    "P": [[0.0, 2.0], [-0.5, 0.0]],
+    "Q": [[0.0, -0.25], [4.0, 0.0]],
+    "D": [[2.0, 0.0], [0.0, 0.5]],
+    "S": [[0.0, 1.0], [-1.0, 0.0]],
+    "N": [[-1.0, 0.0], [0.0, -1.0]],
+}
+
+
+def _grid_rows(rng, rows, d):
+    """Rows whose every 32-block is E2M1 values x 2^e with block amax 4 or 6
+    times 2^e, i.e. exactly representable in MXFP4."""
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    v = grid[rng.integers(0, 8, (rows, d))] * rng.choice([-1.0, 1.0], (rows, d))
+    for j in range(d // 32):
+        pos = 32 * j + rng.integers(0, 32, rows)
+        v[np.arange(rows), pos] = rng.choice([-6.0, -4.0, 4.0, 6.0], rows)
+        v[:, 32 * j:32 * j + 32] *= np.ldexp(1.0, rng.integers(-4, 5, (rows, 1)))
+    return v
+
+
+def _kron_dense(G):
+    """Dense K = G1 (x) ... (x) G5 by nested numpy kron (a library routine;
+    G1 outermost, so it acts on bit 4 of the channel index)."""
+    K = np.array([[1.0]])
+    for k in range(5):
+        K = np.kron(K, G[k])
+    return K
+
+
+def _exact_zero_case(seed=11, m=3, d=64):
+    """A and W with A T and W T^{-T} exactly on the MXFP4 grid under monomial
+    factors: the quantizer is then exact on both sides and eq. (1) makes
+    Q(A T) Q(W T^{-T})^T equal A W^T exactly.  Returns (A bits, W bits,
+    factors, y = A T, z = W T^{-T}); W is square (o = d)."""
+    rng = np.random.default_rng(seed)
+    names = [["P", "I", "D", "S", "Q"], ["N", "Q", "I", "P", "D"]][: d // 32]
+    F = np.array([[_MONOMIAL[n] for n in blk] for blk in names])
+    y = _grid_rows(rng, m, d)
+    z = _grid_rows(rng, d, d)
+    A = np.zeros((m, d))
+    W = np.zeros((d, d))
+    for j in range(d // 32):
+        K = _kron_dense(F[j])
+        # K is monomial (one nonzero +-2^k per row and column), so its inverse
+        # is its transpose with every nonzero entry replaced by its reciprocal
+        assert ((K != 0).sum(0) == 1).all() and ((K != 0).sum(1) == 1).all()
+        Kinv = np.where(K != 0, 1.0 / np.where(K != 0, K, 1.0), 0.0).T
+        assert np.array_equal(K @ Kinv, np.eye(32))
+        sl = slice(32 * j, 32 * j + 32)
+        A[:, sl] = y[:, sl] @ Kinv                  # A T = y
+        W[:, sl] = z[:, sl] @ K.T                   # W T^{-T} = z
+    A_bits, W_bits = synth.f64_to_bf16_bits(A), synth.f64_to_bf16_bits(W)
+    assert np.array_equal(synth.bf16_bits_to_f32(A_bits), A)      # exact in bf16
+    assert np.array_equal(synth.bf16_bits_to_f32(W_bits), W)
+    return A_bits, W_bits, F, y, z
+
+
+def _exact_frobenius(y, z):
+    """||y z^T||_F from integer arithmetic on the dyadic entries (no floating
+    point in the sums)."""
+    from fractions import Fraction
+    sy = sz = 2 ** 12
+    Y = [[int(v * sy) for v in row] for row in y]
+    Z = [[int(v * sz) for v in row] for row in z]
+    assert np.array_equal(np.array(Y, float) / sy, y) and np.array_equal(np.array(Z, float) / sz, z)
+    tot = sum(sum(yi * zi for yi, zi in zip(r, c)) ** 2 for r in Y for c in Z)
+    return math.sqrt(float(Fraction(tot, (sy * sz) ** 2)))
+
+
+def test_layer_error_exact_on_grid(oracle_lib):
+    """eq. (1)-(2) with nothing left to round: signed-permutation-times-
+    power-of-two factors and activations / weights whose transformed blocks
+    lie on the E2M1 grid times 2^e.  The quantization error is zero, so
+    ||E||_F must be exactly 0 while ||A W^T||_F equals the exact integer
+    computation of ||y z^T||_F (y = A T, z = W T^{-T}).  Quantizing A without
+    T, using K^{-1} or K for K^{-T}, multiplying by W_q instead of W_q^T, or a
+    sign slip all give a nonzero error."""
+    A, W, F, y, z = _exact_zero_case()
+    for layout in (0, 1):
+        e, ref = oracle_lib.layer_error(A, W, 64, F, layout=layout)
+        assert e == 0.0, e
+        assert abs(ref - _exact_frobenius(y, z)) <= 1e-15 * ref and ref > 0
+
+
 # --- the 16-bit side output: fp64 -> bf16, round to nearest even ----------------
 
 def _bf16_decode(bits):
