@@ -147,6 +147,7 @@ void fill_quant_params(QuantParams &p, int64_t m, int64_t d, int64_t rows_per_ti
     p.shared_params = 0;
     p.in_f16 = 0;
     p.tile_ctr = nullptr;
+    p.sched_static = 0;
     p.wait_limit_ns = kWaitLimitNs;
     p.skip_tile = -1;
 }

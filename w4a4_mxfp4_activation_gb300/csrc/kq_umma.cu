@@ -74,6 +74,9 @@ constexpr int kBR = 128;                       // rows per tile (= MMA M)
 constexpr int kBlockCols = 96;                 // per block: 3 terms x 32 outputs
 constexpr int kAccCols = 2 * kBlockCols;       // fp32 columns per accumulator buffer
 constexpr int kTmemCols = 512;                 // 2 buffers (384 columns), power of two
+// Tiles per CTA taken from the counter at the end of a launch under the
+// counter schedule (the rest come from the fixed walk).
+constexpr int kSchedTail = 2;
 
 template <int STAGES>
 struct UCfg {
@@ -228,26 +231,34 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // The CTA's tiles.  Fixed walk (!DYN): tile blockIdx.x, then every
     // gridDim.x-th, each role walking its share itself (the producer all of
     // them, MMA issuer and epilogue group m those with it % 2 == m).  DYN:
-    // the producer takes the next unclaimed tile from the counter for each
-    // ring stage, so that CTAs that started late or stream slower take
-    // fewer; it writes the tile id beside the stage, the MMA issuer of the
-    // stage passes it on to its epilogue group, and the id -1 (one per
-    // issuer) ends the CTA's work.  Tile `it` of the CTA goes to ring stage
-    // it % STAGES.
+    // the producer takes its first p.sched_static tiles from the same fixed
+    // walk (tiles below sched_static * gridDim.x) and every later one from
+    // the counter, one unclaimed tile per ring stage, so that CTAs that
+    // started late or stream slower take fewer of the last tiles; it writes
+    // the tile id beside the stage, the MMA issuer of the stage passes it on
+    // to its epilogue group, and the id -1 (one per issuer) ends the CTA's
+    // work.  Tile `it` of the CTA goes to ring stage it % STAGES.
     TileWalk pw(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), ncol);
     int pit = 0;
     uint64_t pol = 0;
-    // The next tile (-1: none left).  A counter's value is only used when
-    // the tile is issued, so its round trip overlaps the wait for a stage.
-    auto fetch = [&]() -> int {
+    int taken = 0;        // DYN: tiles taken from the fixed walk
+    const uint32_t dyn_base = static_cast<uint32_t>(p.sched_static) * gridDim.x;
+    // The next tile as an unchecked index (>= ntiles: none left).  The
+    // counter's value is compared only when the tile is issued, after the
+    // wait for a free stage, so that its round trip overlaps that wait.
+    auto fetch = [&]() -> uint32_t {
         if (DYN) {
-            const uint32_t t = atomicAdd(p.tile_ctr, 1u);
-            return t < static_cast<uint32_t>(ntiles) ? static_cast<int>(t) : -1;
+            if (taken < p.sched_static)
+                return blockIdx.x + static_cast<uint32_t>(taken++) * gridDim.x;
+            return dyn_base + atomicAdd(p.tile_ctr, 1u);
         }
-        if (pw.rt >= p.nrow_tiles) return -1;
-        const int t = pw.rt * ncol + pw.ct;
+        if (pw.rt >= p.nrow_tiles) return 0xFFFFFFFFu;
+        const uint32_t t = static_cast<uint32_t>(pw.rt * ncol + pw.ct);
         pw.next();
         return t;
+    };
+    auto checked = [&](uint32_t t) -> int {
+        return t < static_cast<uint32_t>(ntiles) ? static_cast<int>(t) : -1;
     };
     auto issue_tile = [&](int t) {
         const int s = pit % STAGES;
@@ -274,8 +285,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                       rbytes, bar_full + 8 * s);
         }
     };
-    int pending = -1;     // the producer's next tile
-    int ends = 0;         // end markers issued (DYN)
+    uint32_t pending = 0xFFFFFFFFu;   // the producer's next tile, unchecked
+    int ends = 0;                     // end markers issued (DYN)
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);              // kernel parameters: no dependency on
@@ -300,8 +311,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         grid_dependency_wait();
         pol = l2_policy_evict_first();
         pending = fetch();
-        if (pending >= 0) {
-            issue_tile(pending);
+        if (checked(pending) >= 0) {
+            issue_tile(checked(pending));
             pending = fetch();
         } else if (DYN) {
             issue_tile(-1);
@@ -319,15 +330,16 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             for (;;) {
-                if (DYN ? ends == 2 : pending < 0) break;
+                if (DYN ? ends == 2 : pending == 0xFFFFFFFFu) break;
                 const int s = pit % STAGES;
                 const uint32_t ph = static_cast<uint32_t>((pit / STAGES) & 1);
                 if (pit >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1u, lim)) {
                     sts32(stall_flag, 1u);
                     break;
                 }
-                issue_tile(pending);
-                if (pending < 0)
+                const int t = checked(pending);
+                issue_tile(t);
+                if (t < 0)
                     ++ends;
                 else
                     pending = fetch();
@@ -703,6 +715,9 @@ kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, const CUt
     // one CTA per SM: each holds 256 of the SM's 512 TMEM columns
     const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, sm_count));
     if (!tiles_fit_int32(p, grid)) return KQ_ERR_SHAPE;
+    // under the counter schedule each CTA first takes all but the last
+    // kSchedTail tiles of its fixed share, then the rest one by one
+    p.sched_static = DYN ? static_cast<int>(std::max<int64_t>(p.ntiles / grid - kSchedTail, 0)) : 0;
     return launch_pdl(kern, grid, kThreadsU, Cfg::kSmemBytes, stream, map, mapq, mapat, p,
                       records);
 }
