@@ -77,9 +77,6 @@ def parse_args():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--variant", choices=("butterfly", "umma"), default="umma",
                     help="KroQuant kernel: tcgen05 (umma, default) or the CUDA-core butterfly")
-    ap.add_argument("--schedule", choices=("counter", "fixed"), default="counter",
-                    help="tile schedule of the tcgen05 kernel: taken from a workspace counter "
-                         "(kq_quantize_mxfp4_ws, default) or a fixed walk (kq_quantize_mxfp4)")
     ap.add_argument("--isolated", type=int, default=20,
                     help="single-launch measurements of the dominant layer (isolated_launch)")
     ap.add_argument("--no-baselines", action="store_true",
@@ -251,12 +248,35 @@ def recorded_traffic(workload: str):
     return None
 
 
+_NVML_POLLER = r"""
+import ctypes, sys, time
+uuid, path = sys.argv[1], sys.argv[2]
+L = ctypes.CDLL("libnvidia-ml.so.1")
+assert L.nvmlInit_v2() == 0
+h = ctypes.c_void_p()
+assert L.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+reasons = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+    L.nvmlDeviceGetCurrentClocksThrottleReasons
+mhz, mx, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+with open(path, "w", buffering=1) as f:
+    f.write("ready\n")
+    while True:
+        t = time.monotonic()
+        if (L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and
+                L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
+                reasons(h, ctypes.byref(bits)) == 0):
+            f.write(f"{t} {mhz.value} {mx.value} {bits.value}\n")
+        time.sleep(0.0002)
+"""
+
+
 class ClockSampler:
-    """SM clock and clock-event reasons of the benchmarked GPU, sampled in a
-    background thread while alive: read-only NVML queries in this process
-    (libnvidia-ml from the driver), else nvidia-smi writing to a file.
-    Samples carry host timestamps so that those inside a window (the timed
-    region) can be told from the rest."""
+    """SM clock and clock-event reasons of the benchmarked GPU, sampled while
+    alive by a child process that polls NVML (read-only queries of the
+    driver's libnvidia-ml) as fast as it answers; falls back to nvidia-smi
+    writing to a file.  Samples carry time.monotonic() stamps, so those inside
+    a window (the timed region) can be told from the rest; a separate process
+    keeps sampling while this one waits on the GPU."""
 
     # nvmlClocksEventReasons bits
     REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
@@ -266,91 +286,70 @@ class ClockSampler:
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, uuid: str | None, out_dir: str | None = None):
-        import threading
+        import tempfile
         self.uuid = uuid
-        self.samples = []            # (host time, sm MHz, max MHz, reason bits)
-        self.proc = None
-        self.path = None
-        self.stop_ev = threading.Event()
-        self.thread = None
+        self.samples = []            # (monotonic time or None, sm MHz, max MHz, reason bits)
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".txt", dir=out_dir)
+        os.close(fd)
         self.source = None
-        nv = self._nvml()
-        if nv is not None:
-            self.source = "nvml"
-            self.thread = threading.Thread(target=self._poll, args=nv, daemon=True)
-            self.thread.start()
-            return
-        try:
-            import tempfile
-            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv", dir=out_dir)
-            os.close(fd)
-            self.t0 = time.time()
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "20", "-f", self.path], stdout=subprocess.DEVNULL,
-                stderr=subprocess.DEVNULL)
-            self.source = "nvidia-smi"
-        except OSError:
-            self.proc = None
-
-    def _nvml(self):
-        import ctypes
-        try:
-            L = ctypes.CDLL("libnvidia-ml.so.1")
-            if L.nvmlInit_v2() != 0:
-                return None
-            h = ctypes.c_void_p()
-            if self.uuid is None or L.nvmlDeviceGetHandleByUUID(self.uuid.encode(),
-                                                                ctypes.byref(h)) != 0:
-                return None
-            reasons = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                L.nvmlDeviceGetCurrentClocksThrottleReasons
-            return L, h, reasons
-        except (OSError, AttributeError):
-            return None
-
-    def _poll(self, L, h, reasons):
-        import ctypes
-        mhz, mx, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
-        while not self.stop_ev.is_set():
-            t = time.perf_counter()
-            if (L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and
-                    L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
-                    reasons(h, ctypes.byref(bits)) == 0):
-                self.samples.append((t, float(mhz.value), float(mx.value), int(bits.value)))
-            self.stop_ev.wait(0.0002)
+        self.proc = None
+        if uuid:
+            try:
+                self.proc = subprocess.Popen([sys.executable, "-c", _NVML_POLLER, uuid, self.path],
+                                             stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+                self.source = "nvml"
+                for _ in range(100):                     # until its first line (<= 5 s)
+                    if self.proc.poll() is not None or os.path.getsize(self.path) > 0:
+                        break
+                    time.sleep(0.05)
+                if self.proc.poll() is not None:
+                    self.proc = None
+            except OSError:
+                self.proc = None
+        if self.proc is None:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                     "-lms", "20", "-f", self.path], stdout=subprocess.DEVNULL,
+                    stderr=subprocess.DEVNULL)
+                self.source = "nvidia-smi"
+            except OSError:
+                self.proc = None
 
     def stop(self):
-        if self.thread is not None:
-            self.stop_ev.set()
-            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+                self.proc.wait()
+        try:
+            with open(self.path) as f:
+                lines = f.read().splitlines()
+            os.unlink(self.path)
+        except OSError:
+            lines = []
+        for line in lines:
+            if self.source == "nvml":
+                fl = line.split()
+                if len(fl) == 4:
+                    self.samples.append((float(fl[0]), float(fl[1]), float(fl[2]), int(fl[3])))
+                continue
+            fl = [x.strip() for x in line.split(",")]
+            if len(fl) < 7 or (self.uuid and self.uuid not in fl[0] and fl[0] not in self.uuid):
+                continue
             try:
-                with open(self.path) as f:
-                    lines = f.read().splitlines()
-                os.unlink(self.path)
-            except OSError:
-                lines = []
-            for k, line in enumerate(lines):
-                fl = [x.strip() for x in line.split(",")]
-                if len(fl) < 7 or (self.uuid and self.uuid not in fl[0] and fl[0] not in self.uuid):
-                    continue
-                try:
-                    bits = sum(b for (name, b), v in zip(self.REASON_BITS.items(),
-                                                         (fl[6], fl[3], fl[5], fl[4]))
-                               if v.lower().startswith("active"))
-                    self.samples.append((None, float(fl[1]), float(fl[2]), bits))
-                except ValueError:
-                    continue
+                bits = sum(b for (name, b), v in zip(self.REASON_BITS.items(),
+                                                     (fl[6], fl[3], fl[5], fl[4]))
+                           if v.lower().startswith("active"))
+                self.samples.append((None, float(fl[1]), float(fl[2]), bits))
+            except ValueError:
+                continue
 
     def summary(self, window=None):
         """Median SM clock, max clock and the throttle reasons seen, over the
-        samples inside window = (t0, t1) (perf_counter seconds), or all."""
+        samples inside window = (t0, t1) (time.monotonic() seconds), or all."""
         pts = [x for x in self.samples
                if window is None or x[0] is None or window[0] <= x[0] <= window[1]]
         if not pts:
@@ -481,27 +480,19 @@ def run_ours(args, dist: Dist):
         KX.append(kq.kq_expand_blocks(F[-1], kq.KQ_K_BF16X3))
     torch.cuda.synchronize()
 
-    # the tcgen05 kernel's tile counters (one stream: its launches never overlap)
-    WS = kq.sched_workspace(dev)
-
     def launch(kind, li, s):
         _, m, d = LAYERS[li]
         if kind == "kroquant":
-            kind = args.variant if args.variant != "umma" else (
-                "umma_ws" if args.schedule == "counter" else "umma")
+            kind = args.variant
         if kind == "butterfly":
             kq.kq_quantize_mxfp4(A[li][s], d, factors=F[li], layout=layout, q=Q[li][s],
                                  sf=SF[li][s], variant=kq.VARIANT_BUTTERFLY, stream=stream)
         elif kind == "umma":
             kq.kq_quantize_mxfp4(A[li][s], d, K_expanded=KX[li], layout=layout, q=Q[li][s],
                                  sf=SF[li][s], stream=stream)
-        elif kind == "umma_ws":
-            kq.kq_quantize_mxfp4_ws(A[li][s], WS, d, K_expanded=KX[li], layout=layout,
-                                    q=Q[li][s], sf=SF[li][s], stream=stream)
         elif kind == "dual":
             kq.kq_quantize_mxfp4_dual(A[li][s], KX[li], d, layout=layout, q=Q[li][s],
-                                      sf=SF[li][s], at=AT[li][s], stream=stream,
-                                      workspace=WS if args.schedule == "counter" else None)
+                                      sf=SF[li][s], at=AT[li][s], stream=stream)
         elif kind == "diag":
             kq.kq_smooth_quantize_mxfp4(A[li][s], DIAG[li], d, layout=layout, q=Q[li][s],
                                         sf=SF[li][s], stream=stream)
@@ -576,12 +567,12 @@ def run_ours(args, dist: Dist):
             torch.cuda.synchronize()
             t0 = torch.cuda.Event(enable_timing=True)
             t1 = torch.cuda.Event(enable_timing=True)
-            h0 = time.perf_counter()
+            h0 = time.monotonic()
             t0.record(stream)
             counts = run_steps(g, steps, events)
             t1.record(stream)
             stream.synchronize()
-            h1 = time.perf_counter()
+            h1 = time.monotonic()
             dist.barrier()
             torch.cuda.synchronize()
         ms = t0.elapsed_time(t1)
@@ -608,10 +599,32 @@ def run_ours(args, dist: Dist):
                     out.append(a.elapsed_time(b))
         return statistics.median(out)
 
+    def launch_floor(n):
+        """The same single-launch measurement on a one-element kernel: the
+        time two events and a graph launch take with (almost) no work."""
+        tiny = torch.zeros(1, device=dev)
+        out = []
+        with torch.cuda.stream(stream):
+            tiny.add_(1.0)
+            stream.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                tiny.add_(1.0)
+            for k in range(n + 2):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                gr.replay()
+                b.record(stream)
+                b.synchronize()
+                if k >= 2:
+                    out.append(a.elapsed_time(b))
+        return statistics.median(out)
+
     W, K = args.warmup, args.steps
     clock = ClockSampler(device_uuid(dev), os.environ.get("TMPDIR"))
     ms, launch_ms, window, g_main = timed("kroquant", K, W, per_launch=True)
     iso_ms = isolated("kroquant", g_main, max(3, args.isolated))
+    floor_ms = launch_floor(max(3, args.isolated))
     del g_main
     ms_max = dist.max(ms)
     total_bytes = dist.sum(STEP_BYTES * K)
@@ -620,10 +633,8 @@ def run_ours(args, dist: Dist):
     dom_m, dom_d = LAYERS[DOMINANT][1], LAYERS[DOMINANT][2]
     dom_ms = statistics.mean(launch_ms) if launch_ms else float("nan")
     achieved = algo_bytes(dom_m, dom_d) / (dom_ms * 1e-3) / 1e9
-    kname = "umma_ws" if args.variant == "umma" and args.schedule == "counter" else args.variant
-    workload = f"kq_quantize_mxfp4{'_ws' if kname == 'umma_ws' else ''} {args.variant} " \
-               f"m={dom_m} d={dom_d}"
-    traffic = recorded_traffic(f"flux_ffn_down_{kname}")
+    workload = f"kq_quantize_mxfp4 {args.variant} m={dom_m} d={dom_d}"
+    traffic = recorded_traffic(f"flux_ffn_down_{args.variant}")
 
     # ---- the dual quantizer (MXFP4 + the bf16 side output A T of the
     #      low-rank branch) on the same step
@@ -653,13 +664,13 @@ def run_ours(args, dist: Dist):
     iso_diag_ms = None
     if not args.no_baselines:
         nb_steps = max(3, min(K, 4000))
-        others = [v for v in ("butterfly", "umma", "umma_ws") if v != kname]
+        others = [v for v in ("butterfly", "umma") if v != args.variant]
         for kind in (*others, "diag", "hadamard", "identity"):
             bms, _, _, g = timed(kind, nb_steps, W)
             if kind == "diag":
                 iso_diag_ms = isolated("diag", g, max(3, args.isolated))
             del g
-            name = f"kroquant_{kind}" if kind in ("butterfly", "umma", "umma_ws") else kind
+            name = f"kroquant_{kind}" if kind in ("butterfly", "umma") else kind
             baselines[name] = round(STEP_BYTES * nb_steps / (dist.max(bms) * 1e-3) / 1e9, 2)
     clock.stop()
     clocks = clock.summary(window)
@@ -757,8 +768,6 @@ def run_ours(args, dist: Dist):
             "data": "synthetic",
             "config": {"workload": "flux_layer_pair", "m": 4608, "d": [3072, 12288],
                        "transform": f"kroquant_{args.variant}", "input": "bf16",
-                       "schedule": ("tiles from a workspace counter (kq_quantize_mxfp4_ws)"
-                                    if kname == "umma_ws" else "fixed tile walk"),
                        "output": "mxfp4 (e2m1 codes + e8m0 scales, 128x4 tiled)",
                        "l2": f"{SETS} rotating input/output sets, "
                              f"{SETS * STEP_BYTES / 1e6:.0f} MB footprint > L2",
@@ -781,10 +790,12 @@ def run_ours(args, dist: Dist):
                 "us": round(iso_ms * 1e3, 3),
                 "gbs": round(algo_bytes(dom_m, dom_d) / (iso_ms * 1e-3) / 1e9, 2),
                 "frac": round(algo_bytes(dom_m, dom_d) / (iso_ms * 1e-3) / 1e9 / peak, 4),
+                "launch_floor_us": round(floor_ms * 1e3, 3),
                 "diag_us": round(iso_diag_ms * 1e3, 3) if iso_diag_ms else None,
                 "vs_diag_scale": round(iso_diag_ms / iso_ms, 4) if iso_diag_ms else None,
                 "how": "median over launches of one dominant-layer launch replayed alone as a "
-                       "one-launch CUDA graph between two events (no overlap with a neighbour)"},
+                       "one-launch CUDA graph between two events (no overlap with a neighbour); "
+                       "launch_floor_us is the same measurement of a one-element kernel"},
             "vs_diag_scale": round(value / dist.world / baselines["diag"], 4)
             if baselines.get("diag") else None,
             "baselines_gbs": baselines,
@@ -818,7 +829,6 @@ def run_profile_case(args):
           if args.variant == "umma" or args.profile == "dual" else None)
     at = torch.empty((m, d), dtype=torch.bfloat16, device="cuda") if args.profile == "dual" else None
     variant = {"butterfly": kq.VARIANT_BUTTERFLY, "umma": kq.VARIANT_UMMA}[args.variant]
-    ws = kq.sched_workspace("cuda") if args.schedule == "counter" else None
     if args.profile == "gemm":
         n = args.n
         qa, sfa, qw, sfw, _, _ = gemm_case(m, n, d, 9000, "cuda")
@@ -829,13 +839,11 @@ def run_profile_case(args):
         print(f"profile case done: gemm m={m} n={n} k={d} launches={args.launches}")
         return
     for _ in range(args.launches):
-        if args.profile == "kroquant" and variant == kq.VARIANT_UMMA and ws is not None:
-            kq.kq_quantize_mxfp4_ws(A, ws, d, K_expanded=KX, layout=layout, q=q, sf=sf)
-        elif args.profile == "kroquant":
+        if args.profile == "kroquant":
             kq.kq_quantize_mxfp4(A, d, factors=F if KX is None else None, K_expanded=KX,
                                  layout=layout, q=q, sf=sf, variant=variant)
         elif args.profile == "dual":
-            kq.kq_quantize_mxfp4_dual(A, KX, d, layout=layout, q=q, sf=sf, at=at, workspace=ws)
+            kq.kq_quantize_mxfp4_dual(A, KX, d, layout=layout, q=q, sf=sf, at=at)
         elif args.profile == "diag":
             kq.kq_smooth_quantize_mxfp4(A, s, d, layout=layout, q=q, sf=sf)
         elif args.profile == "hadamard":
@@ -858,7 +866,7 @@ TABLE_CONFIGS = (
     ("4", tuple((f"sweep_{m}x{d}", m, d, "flux") for m in (256, 1024, 4096, 16384, 65536)
                 for d in (1152, 3072, 12288))),
 )
-TABLE_KERNELS = ("umma_ws", "umma", "butterfly", "diag", "hadamard", "identity", "dual")
+TABLE_KERNELS = ("umma", "butterfly", "diag", "hadamard", "identity", "dual")
 
 
 def oracle_rate_shape(m: int, d: int, seconds: float):
@@ -930,7 +938,6 @@ def measure_shape(args, m, d, model, seed, kinds, peak):
           for _ in range(sets)]
     AT = ([torch.empty((m, d), dtype=torch.bfloat16, device=dev) for _ in range(sets)]
           if "dual" in kinds else None)
-    WS = kq.sched_workspace(dev)
     n_launch = max(sets, 32)
 
     def launch(kind, i):
@@ -938,15 +945,12 @@ def measure_shape(args, m, d, model, seed, kinds, peak):
         if kind == "umma":
             kq.kq_quantize_mxfp4(A[s], d, K_expanded=KX, layout=layout, q=Q[s], sf=SF[s],
                                  variant=kq.VARIANT_UMMA, stream=stream)
-        elif kind == "umma_ws":
-            kq.kq_quantize_mxfp4_ws(A[s], WS, d, K_expanded=KX, layout=layout, q=Q[s], sf=SF[s],
-                                    stream=stream)
         elif kind == "butterfly":
             kq.kq_quantize_mxfp4(A[s], d, factors=F, layout=layout, q=Q[s], sf=SF[s],
                                  variant=kq.VARIANT_BUTTERFLY, stream=stream)
         elif kind == "dual":
             kq.kq_quantize_mxfp4_dual(A[s], KX, d, layout=layout, q=Q[s], sf=SF[s], at=AT[s],
-                                      stream=stream, workspace=WS)
+                                      stream=stream)
         elif kind == "diag":
             kq.kq_smooth_quantize_mxfp4(A[s], S, d, layout=layout, q=Q[s], sf=SF[s],
                                         stream=stream)
@@ -1003,18 +1007,18 @@ def run_table(args):
         run_table3(args, peak)
         return
     print("| config | layer | m x d | sets | " + " | ".join(
-        f"{k} GB/s (% peak)" if k in ("umma_ws", "umma", "dual") else f"{k} GB/s"
-        for k in TABLE_KERNELS) + " | umma_ws / diag |")
+        f"{k} GB/s (% peak)" if k in ("umma", "dual") else f"{k} GB/s"
+        for k in TABLE_KERNELS) + " | umma / diag |")
     print("|" + "---|" * (len(TABLE_KERNELS) + 5))
     for cfg, layers in TABLE_CONFIGS:
         for name, m, d, model in layers:
             us, sets = measure_shape(args, m, d, model, synth_seed(cfg), TABLE_KERNELS, peak)
             gbs = {k: (algo_bytes_dual(m, d) if k == "dual" else algo_bytes(m, d)) / us[k] / 1e3
                    for k in TABLE_KERNELS}
-            cells = [f"{gbs[k]:.0f} ({100 * gbs[k] / peak:.0f} %)" if k in ("umma_ws", "umma", "dual")
+            cells = [f"{gbs[k]:.0f} ({100 * gbs[k] / peak:.0f} %)" if k in ("umma", "dual")
                      else f"{gbs[k]:.0f}" for k in TABLE_KERNELS]
             print(f"| {cfg} | {name} | {m}x{d} | {sets} | " + " | ".join(cells) +
-                  f" | {gbs['umma_ws'] / gbs['diag']:.2f} |", flush=True)
+                  f" | {gbs['umma'] / gbs['diag']:.2f} |", flush=True)
     run_table3(args, peak)
     # the oracle on the host cores: all of them, then one
     print()

@@ -156,39 +156,6 @@ KQ_API kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d,
                                  float *y_debug, cudaStream_t stream);
 
 /*
- * kq_quantize_mxfp4_ws / kq_quantize_mxfp4_dual_ws -- kq_quantize_mxfp4 and
- * kq_quantize_mxfp4_dual with a scheduling workspace: on the tensor-core
- * path the persistent CTAs take their 128-row x 64-channel tiles one at a
- * time from a counter in `workspace` instead of a fixed share, so that CTAs
- * that start late or stream slower take fewer tiles and the launch ends
- * sooner.  Every tile is computed the same way by whichever CTA takes it, so
- * the results equal those of the calls without workspace, byte for byte.
- * The other kernels the arguments may select ignore the workspace.
- *   workspace  device, KQ_SCHED_WORKSPACE_BYTES bytes, 4-byte aligned
- *              (KQ_ERR_NULL / KQ_ERR_ALIGN otherwise), owned by the caller.
- *              Words 0 and 1 must be zero before the first call (e.g. one
- *              cudaMemset); every call leaves them zero again when its kernel
- *              ends.  Word 2 counts the CTAs that found their pipeline
- *              stalled (see Errors above; the library never clears it): on
- *              this path the blocks of a tile taken by such a CTA keep their
- *              old bytes unless the CTA knew the tile when it stopped, in
- *              which case they get the scale byte 0xFF.  Calls that may run
- *              at the same time (different streams) need different
- *              workspaces.
- *   other arguments as kq_quantize_mxfp4 / kq_quantize_mxfp4_dual.
- */
-#define KQ_SCHED_WORKSPACE_BYTES 16
-KQ_API kq_status kq_quantize_mxfp4_ws(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
-                                      const float *factors, const void *K_expanded, uint8_t *q,
-                                      int64_t ldq, uint8_t *sf, kq_sf_layout sf_layout,
-                                      float *y_debug, uint32_t *workspace, cudaStream_t stream);
-KQ_API kq_status kq_quantize_mxfp4_dual_ws(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
-                                           const void *K_expanded, uint8_t *q, int64_t ldq,
-                                           uint8_t *sf, kq_sf_layout sf_layout, uint16_t *at,
-                                           int64_t ldat, float *y_debug, uint32_t *workspace,
-                                           cudaStream_t stream);
-
-/*
  * kq_quantize_mxfp4_shared -- kq_quantize_mxfp4 with one factor set shared
  * by every 32-channel block, K_j = K for all j ([KQ] Sec. 3.5.1 on K2: "many
  * column blocks share the same Kronecker factors", the case where storing

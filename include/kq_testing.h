@@ -57,24 +57,23 @@ KQ_API kq_status kq_test_encode_e2m1(uint32_t first, int64_t count, uint8_t *out
 
 /*
  * kq_test_quantize_stall -- the tensor-core quantizer (kq_quantize_mxfp4 on
- *   K_expanded, or kq_quantize_mxfp4_ws when workspace != NULL) with its
- *   pipeline made to stall on purpose: the producer of the CTA that takes
- *   tile `skip_tile` (row tile * column tiles + column tile, in 128-row x
- *   64-channel tiles; the tiled scale layout also counts its padding
- *   column tiles) arms that tile's ring stage but never issues its loads,
- *   and every wait of the kernel gives up after wait_limit_ns nanoseconds
- *   (1 ms to 1 s, KQ_ERR_SHAPE otherwise) instead of one second.  The kernel
- *   then takes the path a real stall would take: it returns, with the E8M0
- *   NaN byte 0xFF as the scale (and zero codes) of every block it did not
- *   finish, and with the workspace's word 2 counting the CTAs that stopped.
- *   Nothing faults: no access goes out of bounds and every wait ends.
- *   skip_tile = -1 runs the kernel normally with the given limit.
+ *   K_expanded) with its pipeline made to stall on purpose: the producer of
+ *   the CTA that owns tile `skip_tile` (row tile * column tiles + column
+ *   tile, in 128-row x 64-channel tiles; the tiled scale layout also counts
+ *   its padding column tiles; with G = min(tiles, SMs) CTAs, CTA c owns the
+ *   tiles c, c + G, c + 2G, ... in that order) arms that tile's ring stage
+ *   but never issues its loads, and every wait of the kernel gives up after
+ *   wait_limit_ns nanoseconds (1 ms to 1 s, KQ_ERR_SHAPE otherwise) instead
+ *   of one second.  The kernel then takes the path a real stall would take:
+ *   it returns, with the E8M0 NaN byte 0xFF as the scale (and zero codes) of
+ *   every block it did not finish.  Nothing faults: no access goes out of
+ *   bounds and every wait ends.  skip_tile = -1 runs the kernel normally
+ *   with the given limit.
  */
 KQ_API kq_status kq_test_quantize_stall(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
                                         const void *K_expanded, uint8_t *q, int64_t ldq,
-                                        uint8_t *sf, kq_sf_layout sf_layout, uint32_t *workspace,
-                                        int64_t skip_tile, uint64_t wait_limit_ns,
-                                        cudaStream_t stream);
+                                        uint8_t *sf, kq_sf_layout sf_layout, int64_t skip_tile,
+                                        uint64_t wait_limit_ns, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -250,34 +250,14 @@ def test_ex_argument_checks(L):
     assert f(A, 1, 0, 64, 64, 0, None, q, 32, sf, 0, None, None) == 0       # m = 0
 
 
-def test_workspace_argument_checks(L):
-    """kq_quantize_mxfp4_ws / kq_quantize_mxfp4_dual_ws: the workspace is
-    required and 4-byte aligned; the other checks are those of the plain
-    entry points.  Every call fails a check (or has m = 0): nothing launches."""
-    vp = ctypes.c_void_p
-    A, K, q, sf, at, ws = vp(4096), vp(8192), vp(12288), vp(16384), vp(20480), vp(24576)
-    f = L.kq_quantize_mxfp4_ws
-    assert f(A, 4, 64, 64, None, K, q, 32, sf, 0, None, None, None) == 1       # no workspace
-    assert f(A, 4, 64, 64, None, K, q, 32, sf, 0, None, vp(24578), None) == 3  # misaligned
-    assert f(A, 4, 60, 64, None, K, q, 32, sf, 0, None, ws, None) == 2         # d % 32
-    assert f(A, 4, 64, 64, None, vp(8200), q, 32, sf, 0, None, ws, None) == 3  # blocks alignment
-    assert f(A, 0, 64, 64, None, K, q, 32, sf, 0, None, ws, None) == 0         # m = 0
-    g = L.kq_quantize_mxfp4_dual_ws
-    assert g(A, 4, 64, 64, K, q, 32, sf, 0, at, 64, None, None, None) == 1     # no workspace
-    assert g(A, 4, 64, 64, K, q, 32, sf, 0, at, 64, None, vp(24577), None) == 3
-    assert g(A, 4, 64, 64, K, q, 32, sf, 0, at, 32, None, ws, None) == 2       # ldat < d
-    assert g(A, 4, 64, 64, None, q, 32, sf, 0, at, 64, None, ws, None) == 1    # no blocks
-    assert g(A, 0, 64, 64, K, q, 32, sf, 0, at, 64, None, ws, None) == 0       # m = 0
-
-
 def test_stall_hook_argument_checks(L):
     """kq_test_quantize_stall takes a wait limit between 1 ms and 1 s and the
     checks of the tensor-core path; nothing launches when one fails."""
     vp = ctypes.c_void_p
-    A, K, q, sf, ws = vp(4096), vp(8192), vp(12288), vp(16384), vp(24576)
+    A, K, q, sf = vp(4096), vp(8192), vp(12288), vp(16384)
     h = L.kq_test_quantize_stall
-    assert h(A, 4, 64, 64, K, q, 32, sf, 0, None, 0, 999_999, None) == 2          # limit < 1 ms
-    assert h(A, 4, 64, 64, K, q, 32, sf, 0, None, 0, 2_000_000_000, None) == 2    # limit > 1 s
-    assert h(A, 4, 64, 64, None, q, 32, sf, 0, None, 0, 10_000_000, None) == 1    # no blocks
-    assert h(A, 4, 64, 64, K, q, 32, sf, 0, vp(24578), 0, 10_000_000, None) == 3  # workspace
-    assert h(A, 0, 64, 64, K, q, 32, sf, 0, ws, 0, 10_000_000, None) == 0         # m = 0
+    assert h(A, 4, 64, 64, K, q, 32, sf, 0, 0, 999_999, None) == 2          # limit < 1 ms
+    assert h(A, 4, 64, 64, K, q, 32, sf, 0, 0, 2_000_000_000, None) == 2    # limit > 1 s
+    assert h(A, 4, 64, 64, None, q, 32, sf, 0, 0, 10_000_000, None) == 1    # no blocks
+    assert h(A, 4, 64, 64, vp(8200), q, 32, sf, 0, 0, 10_000_000, None) == 3  # blocks alignment
+    assert h(A, 0, 64, 64, K, q, 32, sf, 0, 0, 10_000_000, None) == 0       # m = 0

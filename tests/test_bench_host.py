@@ -49,11 +49,11 @@ def test_traffic_follows_the_launcher_and_the_compile_command(tmp_path, monkeypa
     for path in (csrc / "kq_api.cu", csrc.parent / "build.py"):
         h = bench.kernel_source_hash()
         (tmp_path / "profiles" / "traffic.txt").write_text(
-            f"flux_ffn_down_umma_ws    {h}  dram_bytes     122196480   115631616   6564864\n")
-        assert bench.recorded_traffic("flux_ffn_down_umma_ws") == 122196480.0
+            f"flux_ffn_down_umma    {h}  dram_bytes     122196480   115631616   6564864\n")
+        assert bench.recorded_traffic("flux_ffn_down_umma") == 122196480.0
         with open(path, "a") as f:
             f.write("\n# edited\n")
-        assert bench.recorded_traffic("flux_ffn_down_umma_ws") is None
+        assert bench.recorded_traffic("flux_ffn_down_umma") is None
 
 
 def test_round_structure_does_not_depend_on_steps():

@@ -52,36 +52,12 @@ def lib_factors(nb, seed, sign=+1):
         .astype(np.float32).astype(np.float64)
 
 
-_WS = {}
-
-
-def workspace():
-    """One scheduling workspace for the whole module (calls run one at a
-    time on the current stream); its words 0-1 must read zero after every
-    call and word 2 (CTAs that stopped waiting) must stay zero."""
-    if "ws" not in _WS:
-        _WS["ws"] = kq.sched_workspace("cuda")
-    return _WS["ws"]
-
-
-def check_workspace_clean():
-    torch.cuda.synchronize()
-    assert np_(workspace()).tolist() == [0, 0, 0, 0]
-
-
 def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None, q=None, sf=None):
     A = to_bf16(A_bits)
     if kind == "kron_umma":
         records = kq.kq_expand_blocks(dev(param_gpu), kq.KQ_K_BF16X3)
         return kq.kq_quantize_mxfp4(A, d, K_expanded=records, layout=layout, y_debug=y_debug,
                                     variant=kq.VARIANT_UMMA, q=q, sf=sf)
-    if kind == "kron_ws":
-        # the tensor-core kernel taking its tiles from the workspace counter
-        records = kq.kq_expand_blocks(dev(param_gpu), kq.KQ_K_BF16X3)
-        out = kq.kq_quantize_mxfp4_ws(A, workspace(), d, K_expanded=records, layout=layout,
-                                      y_debug=y_debug, q=q, sf=sf)
-        check_workspace_clean()
-        return out
     if kind == "kron":
         return kq.kq_quantize_mxfp4(A, d, factors=dev(param_gpu), layout=layout, y_debug=y_debug,
                                     variant=variant, q=q, sf=sf)
@@ -96,12 +72,12 @@ def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None
 
 
 def oracle_kind(kind):
-    return "kron" if kind in ("kron_ws", "kron_umma") else kind
+    return "kron" if kind == "kron_umma" else kind
 
 
 def params_for(kind, nb, d, seed):
     """(gpu param, oracle param) for a transform kind."""
-    if kind in ("kron", "kron_ws", "kron_umma"):
+    if kind in ("kron", "kron_umma"):
         return lib_factors(nb, seed)
     if kind == "diag":
         s = synth.smooth_scales(d)
@@ -157,7 +133,7 @@ CASES = synth.CONFIG0 + synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3
 
 
 @pytest.mark.parametrize("name,m,d,model,cfg", CASES, ids=[c[0] for c in CASES])
-@pytest.mark.parametrize("kind", ["kron", "kron_ws", "kron_umma", "diag", "hadamard", "identity"])
+@pytest.mark.parametrize("kind", ["kron", "kron_umma", "diag", "hadamard", "identity"])
 def test_config_parity(name, m, d, model, cfg, kind):
     """Configs 0-3 at full size, every row and block, both scale layouts
     (the oracle's result computed once and compared with both)."""
@@ -266,8 +242,8 @@ SWEEP = [(m, d) for m in synth.SWEEP_M for d in synth.SWEEP_D]
 
 @pytest.mark.parametrize("m,d", SWEEP, ids=[f"{m}x{d}" for m, d in SWEEP])
 def test_sweep_parity(m, d):
-    """Config 4: 4 layers' factor sets per point; KroQuant (butterfly, both
-    tensor-core schedules), diagonal and Hadamard quantizers.  Every row up
+    """Config 4: 4 layers' factor sets per point; KroQuant (butterfly and
+    tensor cores, two layers each), diagonal and Hadamard quantizers.  Every row up
     to m = 16384; at m = 65536 a seeded sample of 4096 rows (the first and
     last tiles always included)."""
     nb = d // 32
@@ -279,7 +255,7 @@ def test_sweep_parity(m, d):
                                          rng.choice(m, 4096, replace=False)]))
     for layer in range(4):
         Fg, Fo = lib_factors(nb, synth.SEED_FACTORS + 4 + layer)
-        kind = ("kron", "kron_umma", "kron_ws", "kron_umma")[layer]
+        kind = ("kron", "kron_umma", "kron", "kron_umma")[layer]
         q, sf, y = run_kind(kind, A_bits, d, layer % 2, Fg)
         res = parity.check(A_bits, d, "kron", Fo, layer % 2, np_(q), np_(sf), np_(y), rows)
         parity.record("config 4", f"sweep layer {layer}", m, d, kind, layer % 2, res)
@@ -299,7 +275,7 @@ EDGE_SHAPES = [(1, 32), (7, 96), (127, 160), (129, 64), (200, 5600), (3, 2240), 
 
 
 @pytest.mark.parametrize("m,d", EDGE_SHAPES, ids=[f"{m}x{d}" for m, d in EDGE_SHAPES])
-@pytest.mark.parametrize("kind", ["kron", "kron_ws", "kron_umma", "diag", "hadamard", "identity"])
+@pytest.mark.parametrize("kind", ["kron", "kron_umma", "diag", "hadamard", "identity"])
 def test_ragged_shapes_with_pitches_and_canaries(m, d, kind):
     """Ragged m and d (partial tiles and block-columns), lda > d, ldq > d/2,
     and guard bytes around every output that must stay untouched."""
@@ -356,7 +332,7 @@ def test_special_values():
     y_k[4] /= 2.0 ** 8
     bits_k = synth.f64_to_bf16_bits(y_k)
     Fg, Fo = lib_factors(1, 3)
-    for kind in ("kron", "kron_ws", "kron_umma"):
+    for kind in ("kron", "kron_umma"):
         q, sf, yd = run_kind(kind, bits_k, 32, 0, Fg)
         parity.check(bits_k, 32, "kron", Fo, 0, np_(q), np_(sf), np_(yd))
 
@@ -368,7 +344,7 @@ def test_raw_factor_interface():
     nb = d // 32
     A_bits = synth.activations(m, d, 9, "sana")
     F = synth.random_factors(nb, 12, scale=0.8)
-    for kind in ("kron", "kron_ws", "kron_umma"):
+    for kind in ("kron", "kron_umma"):
         q, sf, y = run_kind(kind, A_bits, d, 1, F)
         parity.check(A_bits, d, "kron", F.astype(np.float64), 1, np_(q), np_(sf), np_(y))
     Fg, Fo = lib_factors(nb, 13, sign=-1)
@@ -595,7 +571,7 @@ def test_identity_factors_reduce_to_bare_quantizer():
     for layout in (0, 1):
         nsf = kq.kq_sf_bytes(m, d, layout)
         q0, sf0, _ = run_kind("identity", A_bits, d, layout, y_debug=False)
-        for kind in ("kron", "kron_umma", "kron_ws"):
+        for kind in ("kron", "kron_umma"):
             q, sf, y = run_kind(kind, A_bits, d, layout, eye)
             assert torch.equal(q, q0) and torch.equal(sf[:nsf], sf0[:nsf]), kind
             assert np.array_equal(np_(y), synth.bf16_bits_to_f32(A_bits)), kind
@@ -889,88 +865,6 @@ def test_default_dispatch_with_both_factor_forms(m, d, expect):
     assert torch.equal(q, q2) and torch.equal(sf, sf2)
 
 
-# ------------------------------------------------ scheduling workspace --
-
-# (256, 5120): 160 tiles on 152 CTAs, so a CTA that starts late may take none
-WS_SHAPES = [(1, 64), (129, 96), (300, 1152), (256, 5120), (4096, 1152), (4608, 3072)]
-
-
-@pytest.mark.parametrize("m,d", WS_SHAPES, ids=[f"{m}x{d}" for m, d in WS_SHAPES])
-def test_workspace_schedule_matches_fixed_walk(m, d):
-    """kq_quantize_mxfp4_ws: the CTAs take tiles from the workspace counter;
-    every byte equals the fixed walk's (both scale layouts, with and without
-    the debug output), the counters are zero again after every call, and one
-    workspace serves calls back to back."""
-    A_bits = synth.activations(m, d, 2200 + m, "flux")
-    A = to_bf16(A_bits)
-    F, Fo = lib_factors(d // 32, 2201 + d)
-    KX = kq.kq_expand_blocks(dev(F), kq.KQ_K_BF16X3)
-    ws = workspace()
-    for layout in (0, 1):
-        nsf = kq.kq_sf_bytes(m, d, layout)       # the buffers may be longer (>= 16 bytes)
-        q0, s0, y0 = kq.kq_quantize_mxfp4(A, d, K_expanded=KX, layout=layout, y_debug=True)
-        for rep in range(3):
-            q1, s1, y1 = kq.kq_quantize_mxfp4_ws(A, ws, d, K_expanded=KX, layout=layout,
-                                                 y_debug=(rep == 0))
-            check_workspace_clean()
-            assert torch.equal(q0, q1) and torch.equal(s0[:nsf], s1[:nsf])
-            if rep == 0:
-                assert torch.equal(y0.view(torch.int32), y1.view(torch.int32))
-        if m * d <= 2_000_000:
-            parity.check(A_bits, d, "kron", Fo, layout, np_(q0), np_(s0), np_(y0))
-
-
-def test_dual_workspace_matches_fixed_walk():
-    """kq_quantize_mxfp4_dual_ws writes the same codes, scales and bf16 side
-    output as kq_quantize_mxfp4_dual, and leaves its workspace zero."""
-    m, d = 4608, 3072
-    A = to_bf16(synth.activations(m, d, 2300, "flux"))
-    F, _ = lib_factors(d // 32, 2301)
-    KX = kq.kq_expand_blocks(dev(F), kq.KQ_K_BF16X3)
-    nsf = kq.kq_sf_bytes(m, d, 1)
-    q0, s0, at0, _ = kq.kq_quantize_mxfp4_dual(A, KX, d, layout=1)
-    for _ in range(2):
-        q1, s1, at1, _ = kq.kq_quantize_mxfp4_dual(A, KX, d, layout=1, workspace=workspace())
-        check_workspace_clean()
-        assert torch.equal(q0, q1) and torch.equal(s0[:nsf], s1[:nsf])
-        assert torch.equal(at0.view(torch.int16), at1.view(torch.int16))
-
-
-def test_workspace_in_cuda_graph():
-    """The FLUX FFN-down layer (4608 x 12288) quantized by a CUDA graph of
-    four launches sharing one workspace (the benchmark's launch form, with
-    programmatic dependent launch between them), replayed twice: every
-    output equals the fixed walk's and the counters end at zero."""
-    m, d = 4608, 12288
-    A = to_bf16(synth.activations(m, d, 2400, "flux"))
-    F, _ = lib_factors(d // 32, 2401)
-    KX = kq.kq_expand_blocks(dev(F), kq.KQ_K_BF16X3)
-    q0, s0, _ = kq.kq_quantize_mxfp4(A, d, K_expanded=KX, layout=1)
-    ws = workspace()
-    stream = torch.cuda.Stream()
-    outs = [(torch.empty_like(q0), torch.empty_like(s0)) for _ in range(4)]
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        kq.kq_quantize_mxfp4_ws(A, ws, d, K_expanded=KX, layout=1, q=outs[0][0], sf=outs[0][1],
-                                stream=stream)
-    stream.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for q, sf in outs:
-            kq.kq_quantize_mxfp4_ws(A, ws, d, K_expanded=KX, layout=1, q=q, sf=sf, stream=stream)
-    nsf = kq.kq_sf_bytes(m, d, 1)
-    for _ in range(2):
-        for q, sf in outs:
-            q.zero_()
-            sf.zero_()
-        torch.cuda.synchronize()
-        g.replay()
-        torch.cuda.synchronize()
-        for q, sf in outs:
-            assert torch.equal(q, q0) and torch.equal(sf[:nsf], s0[:nsf])
-        check_workspace_clean()
-
-
 # ------------------------------------------ a pipeline wait that runs out --
 
 STALL_LIMIT_NS = 20_000_000        # 20 ms: every normal wait ends in microseconds
@@ -1025,40 +919,3 @@ def test_stalled_pipeline_marks_unfinished_blocks(layout):
     kq.kq_test_quantize_stall(A, KX, d, -1, STALL_LIMIT_NS, layout=layout, q=q1, sf=s1)
     torch.cuda.synchronize()
     assert torch.equal(q1, q0) and torch.equal(s1[:nsf], s0[:nsf])
-
-
-def test_stalled_pipeline_with_workspace_schedule():
-    """The same stall under the counter schedule: the CTA that takes the
-    skipped tile stops, counts itself in workspace word 2 and lets the other
-    CTAs take every tile it did not; the counters end at zero.  Blocks that
-    differ from a normal run are those of a few tiles the stopped CTA held
-    (0xFF with zero codes where it knew the tile, the old bytes otherwise),
-    the skipped tile among them."""
-    m, d = 4608, 3072
-    nb = d // 32
-    A = to_bf16(synth.activations(m, d, 2600, "flux"))
-    F, _ = lib_factors(nb, 2601)
-    KX = kq.kq_expand_blocks(dev(F), kq.KQ_K_BF16X3)
-    q0, s0, _ = kq.kq_quantize_mxfp4(A, d, K_expanded=KX, layout=0)
-    ws = kq.sched_workspace("cuda")
-    skip = 1000
-    q1 = torch.full_like(q0, 0xA5)
-    s1 = torch.full_like(s0, 0xA5)
-    kq.kq_test_quantize_stall(A, KX, d, skip, STALL_LIMIT_NS, layout=0, q=q1, sf=s1, workspace=ws)
-    torch.cuda.synchronize()
-    assert np_(ws).tolist() == [0, 0, 1, 0]
-    ncol = nb // 2
-    bad_tiles = set()
-    g0, g1 = np_(s0)[:m * nb].reshape(m, nb), np_(s1)[:m * nb].reshape(m, nb)
-    c0, c1 = np_(q0).reshape(m, nb, 16), np_(q1).reshape(m, nb, 16)
-    for t in range(36 * ncol):
-        rows, blocks = tile_blocks(t, ncol, nb, m)
-        for j in blocks:
-            same = np.array_equal(g0[rows, j], g1[rows, j]) and np.array_equal(c0[rows, j], c1[rows, j])
-            if same:
-                continue
-            bad_tiles.add(t)
-            nan = (g1[rows, j] == 0xFF).all() and (c1[rows, j] == 0).all()
-            old = (g1[rows, j] == 0xA5).all() and (c1[rows, j] == 0xA5).all()
-            assert nan or old, (t, j)
-    assert skip in bad_tiles and len(bad_tiles) <= 12, sorted(bad_tiles)

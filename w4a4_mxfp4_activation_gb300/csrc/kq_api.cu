@@ -146,8 +146,6 @@ void fill_quant_params(QuantParams &p, int64_t m, int64_t d, int64_t rows_per_ti
     p.y_debug = y_debug;
     p.shared_params = 0;
     p.in_f16 = 0;
-    p.tile_ctr = nullptr;
-    p.sched_static = 0;
     p.wait_limit_ns = kWaitLimitNs;
     p.skip_tile = -1;
 }
@@ -254,8 +252,8 @@ namespace {
 
 // The quantizer entry points: argument checks, then the implementation
 // `variant` (0 butterfly, 2 identity, 3 tcgen05).  `extra` carries the
-// tcgen05 kernel's tile counters, wait limit and verification hook (its
-// other fields are filled here).
+// tcgen05 kernel's wait limit and verification hook (its other fields are
+// filled here).
 kq_status quantize_variant(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
                            const float *factors, const void *K_expanded, uint8_t *q, int64_t ldq,
                            uint8_t *sf, kq_sf_layout sf_layout, float *y_debug, int variant,
@@ -274,7 +272,6 @@ kq_status quantize_variant(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
     QuantParams p;
     fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
     if (variant == 3) {
-        p.tile_ctr = extra.tile_ctr;
         p.wait_limit_ns = extra.wait_limit_ns;
         p.skip_tile = extra.skip_tile;
         return launch_quant_umma(A, lda, K_expanded, p, nullptr, 0, stream);
@@ -299,39 +296,13 @@ int default_variant(int64_t m, int64_t d, const float *factors, const void *K_ex
     return variant;
 }
 
-kq_status quantize_dual(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
-                        const void *K_expanded, uint8_t *q, int64_t ldq, uint8_t *sf,
-                        kq_sf_layout sf_layout, uint16_t *at, int64_t ldat, float *y_debug,
-                        uint32_t *workspace, cudaStream_t stream)
-{
-    kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
-    if (st != KQ_OK) return st;
-    if (ldat < d || ldat > (1LL << 38)) return KQ_ERR_SHAPE;
-    if (m == 0) return KQ_OK;
-    if (K_expanded == nullptr || at == nullptr) return KQ_ERR_NULL;
-    if (!aligned16(K_expanded) || !aligned16(at) || ldat % 8 != 0) return KQ_ERR_ALIGN;
-    QuantParams p;
-    fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
-    p.tile_ctr = workspace;
-    return launch_quant_umma(A, lda, K_expanded, p, at, ldat, stream);
-}
-
-// The tcgen05 kernel's scheduling fields: tile counters (or null for the
-// fixed walk), the default wait limit, no skipped tile.
-QuantParams sched_params(uint32_t *workspace)
+// The tcgen05 kernel's default wait limit and no skipped tile.
+QuantParams hook_params()
 {
     QuantParams p{};
-    p.tile_ctr = workspace;
     p.wait_limit_ns = kWaitLimitNs;
     p.skip_tile = -1;
     return p;
-}
-
-kq_status check_workspace(const uint32_t *workspace)
-{
-    if (workspace == nullptr) return KQ_ERR_NULL;
-    if (reinterpret_cast<uintptr_t>(workspace) % 4 != 0) return KQ_ERR_ALIGN;
-    return KQ_OK;
 }
 
 }  // namespace
@@ -347,7 +318,7 @@ kq_status kq_quantize_mxfp4_variant(const uint16_t *A, int64_t m, int64_t d, int
                                     float *y_debug, int variant, cudaStream_t stream)
 {
     return quantize_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout, y_debug,
-                            variant, sched_params(nullptr), stream);
+                            variant, hook_params(), stream);
 }
 
 kq_status kq_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
@@ -356,20 +327,7 @@ kq_status kq_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda
                             cudaStream_t stream)
 {
     return quantize_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout, y_debug,
-                            default_variant(m, d, factors, K_expanded), sched_params(nullptr),
-                            stream);
-}
-
-kq_status kq_quantize_mxfp4_ws(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
-                               const float *factors, const void *K_expanded, uint8_t *q,
-                               int64_t ldq, uint8_t *sf, kq_sf_layout sf_layout, float *y_debug,
-                               uint32_t *workspace, cudaStream_t stream)
-{
-    const kq_status st = check_workspace(workspace);
-    if (st != KQ_OK) return st;
-    return quantize_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout, y_debug,
-                            default_variant(m, d, factors, K_expanded), sched_params(workspace),
-                            stream);
+                            default_variant(m, d, factors, K_expanded), hook_params(), stream);
 }
 
 kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
@@ -377,29 +335,24 @@ kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d, int64_
                                  kq_sf_layout sf_layout, uint16_t *at, int64_t ldat,
                                  float *y_debug, cudaStream_t stream)
 {
-    return quantize_dual(A, m, d, lda, K_expanded, q, ldq, sf, sf_layout, at, ldat, y_debug,
-                         nullptr, stream);
-}
-
-kq_status kq_quantize_mxfp4_dual_ws(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
-                                    const void *K_expanded, uint8_t *q, int64_t ldq, uint8_t *sf,
-                                    kq_sf_layout sf_layout, uint16_t *at, int64_t ldat,
-                                    float *y_debug, uint32_t *workspace, cudaStream_t stream)
-{
-    const kq_status st = check_workspace(workspace);
+    kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
     if (st != KQ_OK) return st;
-    return quantize_dual(A, m, d, lda, K_expanded, q, ldq, sf, sf_layout, at, ldat, y_debug,
-                         workspace, stream);
+    if (ldat < d || ldat > (1LL << 38)) return KQ_ERR_SHAPE;
+    if (m == 0) return KQ_OK;
+    if (K_expanded == nullptr || at == nullptr) return KQ_ERR_NULL;
+    if (!aligned16(K_expanded) || !aligned16(at) || ldat % 8 != 0) return KQ_ERR_ALIGN;
+    QuantParams p;
+    fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
+    return launch_quant_umma(A, lda, K_expanded, p, at, ldat, stream);
 }
 
 kq_status kq_test_quantize_stall(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
                                  const void *K_expanded, uint8_t *q, int64_t ldq, uint8_t *sf,
-                                 kq_sf_layout sf_layout, uint32_t *workspace, int64_t skip_tile,
+                                 kq_sf_layout sf_layout, int64_t skip_tile,
                                  uint64_t wait_limit_ns, cudaStream_t stream)
 {
     if (wait_limit_ns < 1000000ull || wait_limit_ns > kWaitLimitNs) return KQ_ERR_SHAPE;
-    if (workspace != nullptr && check_workspace(workspace) != KQ_OK) return KQ_ERR_ALIGN;
-    QuantParams p = sched_params(workspace);
+    QuantParams p = hook_params();
     p.skip_tile = skip_tile;
     p.wait_limit_ns = wait_limit_ns;
     return quantize_variant(A, m, d, lda, nullptr, K_expanded, q, ldq, sf, sf_layout, nullptr,

@@ -38,10 +38,6 @@ struct QuantParams {
     int shared_params;  // 1: every block takes block 0's factors / operand records
     int in_f16;         // 1: A holds fp16 bit patterns (CUDA-core kernels), 0: bf16
     // tcgen05 kernel only:
-    uint32_t *tile_ctr;     // null: fixed tile walk; else 3 words (next tile, CTAs done,
-                            // CTAs that stopped waiting) the CTAs take tiles from
-    int sched_static;       // with tile_ctr: tiles each CTA takes from the fixed walk
-                            // before it takes the rest from the counter
     uint64_t wait_limit_ns; // bound of every pipeline wait
     int64_t skip_tile;      // verification hook: a tile whose loads are never issued (-1: none)
 };

@@ -51,9 +51,10 @@
 // shape and 128B swizzle), and one TMA store per tile sends it to HBM.  The
 // ring stage is then released by the epilogue, once that store has read it,
 // instead of by the MMA commit.
-// Every wait is bounded in time; a timed-out epilogue writes the E8M0 NaN
-// byte 0xFF as the scale of the blocks it could not finish (and bf16 NaNs
-// into the side output).
+// Every wait is bounded in time (one second, or the shorter limit of the
+// verification hook); a timed-out epilogue writes the E8M0 NaN byte 0xFF as
+// the scale of the blocks it could not finish (and bf16 NaNs into the side
+// output).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -74,9 +75,6 @@ constexpr int kBR = 128;                       // rows per tile (= MMA M)
 constexpr int kBlockCols = 96;                 // per block: 3 terms x 32 outputs
 constexpr int kAccCols = 2 * kBlockCols;       // fp32 columns per accumulator buffer
 constexpr int kTmemCols = 512;                 // 2 buffers (384 columns), power of two
-// Tiles per CTA taken from the counter at the end of a launch under the
-// counter schedule (the rest come from the fixed walk).
-constexpr int kSchedTail = 2;
 
 template <int STAGES>
 struct UCfg {
@@ -202,7 +200,7 @@ __device__ __forceinline__ void store_scale_u(const QuantParams &p, int64_t row,
     }
 }
 
-template <int STAGES, bool DEBUG, bool DUAL, bool DYN>
+template <int STAGES, bool DEBUG, bool DUAL>
 __global__ void __launch_bounds__(kThreadsU, 1)
     quant_umma_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmQ,
@@ -218,75 +216,49 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     const uint32_t bar_acc_full = bar + 16 * STAGES;      // [2]
     const uint32_t bar_acc_empty = bar_acc_full + 16;     // [2]
     const uint32_t tmem_slot = bar_acc_empty + 16;
-    const uint32_t stall_flag = tmem_slot + 4;            // a wait of this CTA ran out
-    // DYN: the tile ids handed from role to role
-    const uint32_t bar_acc_tid = tmem_slot + 16;          // [2] a buffer's tile id posted
-    const uint32_t acc_tile = bar_acc_tid + 16;           // [2] that tile id
-    const uint32_t stage_tile = acc_tile + 16;            // [STAGES] a stage's tile id
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ncol = static_cast<int>(p.ncol_tiles);
-    const int ntiles = static_cast<int>(p.ntiles);
+
     const uint64_t lim = p.wait_limit_ns;
 
-    // The CTA's tiles.  Fixed walk (!DYN): tile blockIdx.x, then every
-    // gridDim.x-th, each role walking its share itself (the producer all of
-    // them, MMA issuer and epilogue group m those with it % 2 == m).  DYN:
-    // the producer takes its first p.sched_static tiles from the same fixed
-    // walk (tiles below sched_static * gridDim.x) and every later one from
-    // the counter, one unclaimed tile per ring stage, so that CTAs that
-    // started late or stream slower take fewer of the last tiles; it writes
-    // the tile id beside the stage, the MMA issuer of the stage passes it on
-    // to its epilogue group, and the id -1 (one per issuer) ends the CTA's
-    // work.  Tile `it` of the CTA goes to ring stage it % STAGES.
-    TileWalk pw(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), ncol);
-    int pit = 0;
+    // The producer (thread 0) walks the CTA's tiles in order; it loads the
+    // activation box and the operand records of tile `it` into ring stage
+    // it % STAGES.  (Its work per tile sits on the pipeline's critical path:
+    // each stage is reissued as soon as its MMAs have read it, so the time
+    // from that release to the next load decides how much data is in
+    // flight.  Measured on GB300: a generic tile-index fetch with an integer
+    // division per tile made the FLUX FFN-down launch 13 % slower.)
+    TileWalk pw(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                static_cast<int>(p.ncol_tiles));
+    int64_t pit = 0;
     uint64_t pol = 0;
-    int taken = 0;        // DYN: tiles taken from the fixed walk
-    const uint32_t dyn_base = static_cast<uint32_t>(p.sched_static) * gridDim.x;
-    // The next tile as an unchecked index (>= ntiles: none left).  The
-    // counter's value is compared only when the tile is issued, after the
-    // wait for a free stage, so that its round trip overlaps that wait.
-    auto fetch = [&]() -> uint32_t {
-        if (DYN) {
-            if (taken < p.sched_static)
-                return blockIdx.x + static_cast<uint32_t>(taken++) * gridDim.x;
-            return dyn_base + atomicAdd(p.tile_ctr, 1u);
-        }
-        if (pw.rt >= p.nrow_tiles) return 0xFFFFFFFFu;
-        const uint32_t t = static_cast<uint32_t>(pw.rt * ncol + pw.ct);
-        pw.next();
-        return t;
-    };
-    auto checked = [&](uint32_t t) -> int {
-        return t < static_cast<uint32_t>(ntiles) ? static_cast<int>(t) : -1;
-    };
-    auto issue_tile = [&](int t) {
-        const int s = pit % STAGES;
+    // verification hook: the position in this CTA's walk of the tile whose
+    // loads are never issued (-1: none)
+    const int64_t skip_it =
+        (p.skip_tile >= 0 && p.skip_tile % gridDim.x == blockIdx.x) ? p.skip_tile / gridDim.x : -1;
+    auto issue_tile = [&]() {
+        const int s = static_cast<int>(pit % STAGES);
         const uint32_t dst = base + s * Cfg::kStageBytes;
-        ++pit;
-        if (DYN) sts32(stage_tile + 4 * s, static_cast<uint32_t>(t));
-        if (t < 0) {                                   // the end marker (DYN only)
-            mbar_arrive(bar_full + 8 * s);
-            return;
-        }
-        const int rt = t / ncol, ct = t - rt * ncol;
-        const int64_t left = p.nb - ct * 2;           // < 1 on padding tiles
+        const int64_t left = p.nb - pw.ct * 2;          // < 1 on padding tiles
         const uint32_t rbytes =
             static_cast<uint32_t>((left < 0 ? 0 : (left < 2 ? left : 2)) * Cfg::kRecBytes);
         mbar_arrive_expect_tx(bar_full + 8 * s, Cfg::kABytes + rbytes);
-        if (t == p.skip_tile) return;                  // verification hook: loads never issued
-        tma_load_2d(dst, &tmA, ct * 64, rt * kBR, bar_full + 8 * s, pol);
+        if (pit == skip_it) {                            // the stage stays armed, never filled
+            pw.next();
+            ++pit;
+            return;
+        }
+        tma_load_2d(dst, &tmA, pw.ct * 64, pw.rt * kBR, bar_full + 8 * s, pol);
         if (p.shared_params) {
             // one operand record for every block: a copy of it per block slot
             for (uint32_t off = 0; off < rbytes; off += Cfg::kRecBytes)
                 bulk_load(dst + Cfg::kBOff + off, records, Cfg::kRecBytes, bar_full + 8 * s);
         } else if (rbytes) {
-            bulk_load(dst + Cfg::kBOff, records + static_cast<int64_t>(ct) * 2 * Cfg::kRecBytes,
+            bulk_load(dst + Cfg::kBOff, records + static_cast<int64_t>(pw.ct) * 2 * Cfg::kRecBytes,
                       rbytes, bar_full + 8 * s);
         }
+        pw.next();
+        ++pit;
     };
-    uint32_t pending = 0xFFFFFFFFu;   // the producer's next tile, unchecked
-    int ends = 0;                     // end markers issued (DYN)
 
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);              // kernel parameters: no dependency on
@@ -299,9 +271,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_acc_full + 8 * a, 1);        // MMA commit
             mbar_init(bar_acc_empty + 8 * a, kEpiThreads / 2);
-            if (DYN) mbar_init(bar_acc_tid + 8 * a, 1);   // MMA issuer
         }
-        sts32(stall_flag, 0u);
         mbar_fence_init();
         // The first tile's loads go out before the CTA-wide setup barrier
         // (TMEM allocation), so its DRAM round trip overlaps it; every other
@@ -310,39 +280,24 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         // slower; one tile is faster on every shape tried.)
         grid_dependency_wait();
         pol = l2_policy_evict_first();
-        pending = fetch();
-        if (checked(pending) >= 0) {
-            issue_tile(checked(pending));
-            pending = fetch();
-        } else if (DYN) {
-            issue_tile(-1);
-            ++ends;
-        }
+        if (pw.rt < p.nrow_tiles) issue_tile();
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = lds32(tmem_slot);
+    uint32_t tmem_base;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(tmem_base) : "r"(tmem_slot) : "memory");
     grid_dependency_wait();
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            for (;;) {
-                if (DYN ? ends == 2 : pending == 0xFFFFFFFFu) break;
-                const int s = pit % STAGES;
+            while (pw.rt < p.nrow_tiles) {
+                const int s = static_cast<int>(pit % STAGES);
                 const uint32_t ph = static_cast<uint32_t>((pit / STAGES) & 1);
-                if (pit >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1u, lim)) {
-                    sts32(stall_flag, 1u);
-                    break;
-                }
-                const int t = checked(pending);
-                issue_tile(t);
-                if (t < 0)
-                    ++ends;
-                else
-                    pending = fetch();
+                if (pit >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1u, lim)) break;
+                issue_tile();
             }
             // The next grid may be scheduled once every CTA is this far: its
             // CTAs then take the SMs as this grid's CTAs exit, instead of
@@ -352,55 +307,30 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             // 12288 (162) +0.8 % and 65536 x 12288 (647) +3.2 %; the dual
             // kernel gained at 4 and lost 2-3 % from 45 on.
             if (p.ntiles < (DUAL ? 8 : 48) * static_cast<int64_t>(gridDim.x)) grid_dependents_launch();
-            for (int k = (pit > STAGES ? pit - STAGES : 0); k < pit; ++k)
-                (void)mbar_wait(bar_full + 8 * (k % STAGES), static_cast<uint32_t>((k / STAGES) & 1),
-                                lim);
+            const int64_t it = pit;
+            for (int64_t k = (it > STAGES ? it - STAGES : 0); k < it; ++k)
+                (void)mbar_wait(bar_full + 8 * static_cast<int>(k % STAGES),
+                                static_cast<uint32_t>((k / STAGES) & 1), lim);
         }
     } else if (warp < kFirstEpiWarp) {
         // ---------------- MMA issuers ----------------
         const int a = warp - 1;               // accumulator buffer; tiles with it % 2 == a
-        int it = a;
-        int last = -1;                        // the last tile whose MMAs were committed
-        bool ended = false;                   // DYN: the end marker was passed on
+        int64_t it = a;
+        bool ok = true;
         // the issuing lane, elected once (a commit tracks only the tcgen05
         // operations of its own thread)
         const bool leader = elect_one();
-        TileWalk tw(static_cast<int>(blockIdx.x + a * gridDim.x), static_cast<int>(2 * gridDim.x),
-                    ncol);
-        for (;; it += 2) {
-            if (!DYN && tw.rt >= p.nrow_tiles) break;
-            const int s = it % STAGES;
+        for (TileWalk tw(static_cast<int>(blockIdx.x + a * gridDim.x),
+                         static_cast<int>(2 * gridDim.x), static_cast<int>(p.ncol_tiles));
+             tw.rt < p.nrow_tiles && ok; tw.next(), it += 2) {
+            const int s = static_cast<int>(it % STAGES);
+            const int64_t ct = tw.ct;
+            const int64_t left = p.nb - ct * 2;
+            const int nblk = static_cast<int>(left < 0 ? 0 : (left < 2 ? left : 2));
             bool w = mbar_wait(bar_full + 8 * s, static_cast<uint32_t>((it / STAGES) & 1), lim);
-            int t = 0;
-            if (DYN && w) t = static_cast<int>(lds32(stage_tile + 4 * s));
             if (w && it >= 2)
                 w = mbar_wait(bar_acc_empty + 8 * a, static_cast<uint32_t>(((it >> 1) & 1) ^ 1), lim);
-            if (!__all_sync(0xffffffffu, w)) {
-                if (leader) sts32(stall_flag, 1u);
-                break;
-            }
-            int ct;
-            if (DYN) {
-                // the tile id to the epilogue group, posted before the MMAs
-                // (the group reads it after their commit); the end marker
-                // also completes the accumulator barrier the group waits on
-                if (leader) {
-                    sts32(acc_tile + 4 * a, static_cast<uint32_t>(t));
-                    mbar_arrive(bar_acc_tid + 8 * a);
-                    if (t < 0) mbar_arrive(bar_acc_full + 8 * a);
-                }
-                __syncwarp();
-                if (t < 0) {
-                    ended = true;
-                    break;
-                }
-                ct = t % ncol;
-            } else {
-                ct = tw.ct;
-                tw.next();
-            }
-            const int64_t left = p.nb - static_cast<int64_t>(ct) * 2;
-            const int nblk = static_cast<int>(left < 0 ? 0 : (left < 2 ? left : 2));
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             const uint32_t stage = base + s * Cfg::kStageBytes;
             tc_fence_after();
             if (leader) {
@@ -416,17 +346,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                     umma_commit(bar_empty + 8 * s);      // ring stage free once the MMAs read it
                 umma_commit(bar_acc_full + 8 * a);       // accumulators ready
             }
-            last = it;
             __syncwarp();
         }
         // Wait (bounded) for this warp's last MMAs before TMEM is released.
-        // After the end marker this is known: the marker was posted only
-        // once the epilogue had released the accumulators of the last tile,
-        // which it reads after those MMAs completed; and the marker itself
-        // completed one more phase of the accumulator barrier, so a wait on
-        // the last tile's parity would wait for a phase that never comes.
-        if (!ended && last >= 0)
-            (void)mbar_wait(bar_acc_full + 8 * a, static_cast<uint32_t>((last >> 1) & 1), lim);
+        if (it >= 2)
+            (void)mbar_wait(bar_acc_full + 8 * a, static_cast<uint32_t>(((it - 2) >> 1) & 1), lim);
     } else {
         // ---------------- epilogue ----------------
         const int e = warp - kFirstEpiWarp;
@@ -441,53 +365,21 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         // (measured on GB300: deferring the release by a tile, to overlap
         // the wait, costs more in ring depth than the wait itself)
         const bool at_leader = DUAL && (e & 7) == 4 && lane == 0;
-        const int a = grp;
         int it = grp;
         bool ok = true;
         TileWalk tw(static_cast<int>(blockIdx.x + grp * gridDim.x),
-                    static_cast<int>(2 * gridDim.x), ncol);
-        for (;; it += 2) {
-            int rt, ct;
-            if (DYN) {
-                // the accumulator first (its wait is the one that suspends),
-                // then the tile id, posted before the MMAs were issued.  The
-                // group decides together whether to go on (a timed-out wait
-                // may end differently in different warps, and the warps meet
-                // at named barriers below); after a wait ran out the tile
-                // ids are unknown, so the group stops after this tile.
-                bool wf = false, wt = false;
-                int t = -1;
-                if (ok) {
-                    wf = __all_sync(0xffffffffu, mbar_wait(bar_acc_full + 8 * a,
-                                                           static_cast<uint32_t>((it >> 1) & 1), lim));
-                    wt = __all_sync(0xffffffffu, mbar_wait(bar_acc_tid + 8 * a,
-                                                           static_cast<uint32_t>((it >> 1) & 1), lim));
-                    if (wt) t = static_cast<int>(lds32(acc_tile + 4 * a));
-                    if (!wt && lane == 0) sts32(stall_flag, 1u);
-                }
-                if (!named_barrier_and(11 + grp, kEpiThreads / 2, ok && wt && t >= 0)) break;
-                rt = t / ncol;
-                ct = t - rt * ncol;
-                ok = wf;
-                if (!wf && lane == 0) sts32(stall_flag, 1u);
-            } else {
-                if (tw.rt >= p.nrow_tiles) break;
-                rt = tw.rt;
-                ct = tw.ct;
-                tw.next();
-                if (ok) {
-                    ok = __all_sync(0xffffffffu,
-                                    mbar_wait(bar_acc_full + 8 * a, static_cast<uint32_t>((it >> 1) & 1),
-                                              lim));
-                    if (!ok && lane == 0) sts32(stall_flag, 1u);
-                }
-            }
+                    static_cast<int>(2 * gridDim.x), static_cast<int>(p.ncol_tiles));
+        for (; tw.rt < p.nrow_tiles; tw.next(), it += 2) {
+            const int a = grp;
+            const int rt = tw.rt, ct = tw.ct;
             const int j = ct * 2 + b;
             const int row = rt * kBR + r;
             const uint32_t stg = base + Cfg::kStgOff + (pair * Cfg::kStgBufs + slot) * Cfg::kStgBytes;
             const uint32_t sfstg = base + Cfg::kSfStgOff + (pair * Cfg::kStgBufs + slot) * 32;
             uint32_t sbyte = 0;       // this row's scale byte for block j (0: padding block)
             bool swrite = false;
+            if (ok) ok = __all_sync(0xffffffffu,
+                                    mbar_wait(bar_acc_full + 8 * a, static_cast<uint32_t>((it >> 1) & 1), lim));
             uint4 codes = make_uint4(0u, 0u, 0u, 0u);
             uint4 at_w[4];            // DUAL: the row's 32 bf16 of y (bf16 NaN if not computed)
             if (DUAL) {
@@ -612,18 +504,6 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
-    if (DYN && threadIdx.x == 0) {
-        // A CTA that stopped waiting is counted in word 2.  The last CTA to
-        // finish returns the tile counters to zero for the next call (every
-        // CTA has taken its last tile before it counts itself done).
-        if (lds32(stall_flag) != 0u) atomicAdd(p.tile_ctr + 2, 1u);
-        __threadfence();
-        if (atomicAdd(p.tile_ctr + 1, 1u) == gridDim.x - 1) {
-            __threadfence();
-            atomicExch(p.tile_ctr, 0u);
-            atomicExch(p.tile_ctr + 1, 0u);
-        }
-    }
 }
 
 // ---- operand records (kq_expand_blocks, KQ_K_BF16X3) ------------------------------
@@ -689,12 +569,12 @@ struct USlot {
     cudaError_t err[64] = {};
 };
 
-template <int STAGES, bool DEBUG, bool DUAL, bool DYN>
+template <int STAGES, bool DEBUG, bool DUAL>
 kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, const CUtensorMap &mapat,
                       QuantParams p, const uint8_t *records, int sm_count, cudaStream_t stream)
 {
     using Cfg = UCfg<STAGES>;
-    auto kern = quant_umma_kernel<STAGES, DEBUG, DUAL, DYN>;
+    auto kern = quant_umma_kernel<STAGES, DEBUG, DUAL>;
     static USlot slot;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
@@ -715,21 +595,8 @@ kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, const CUt
     // one CTA per SM: each holds 256 of the SM's 512 TMEM columns
     const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, sm_count));
     if (!tiles_fit_int32(p, grid)) return KQ_ERR_SHAPE;
-    // under the counter schedule each CTA first takes all but the last
-    // kSchedTail tiles of its fixed share, then the rest one by one
-    p.sched_static = DYN ? static_cast<int>(std::max<int64_t>(p.ntiles / grid - kSchedTail, 0)) : 0;
     return launch_pdl(kern, grid, kThreadsU, Cfg::kSmemBytes, stream, map, mapq, mapat, p,
                       records);
-}
-
-template <bool DEBUG, bool DUAL>
-kq_status launch_umma_sched(const CUtensorMap &map, const CUtensorMap &mapq,
-                            const CUtensorMap &mapat, const QuantParams &p, const uint8_t *records,
-                            int sm_count, cudaStream_t stream)
-{
-    if (p.tile_ctr != nullptr)
-        return launch_umma<6, DEBUG, DUAL, true>(map, mapq, mapat, p, records, sm_count, stream);
-    return launch_umma<6, DEBUG, DUAL, false>(map, mapq, mapat, p, records, sm_count, stream);
 }
 
 }  // namespace
@@ -757,14 +624,14 @@ kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expand
     const uint8_t *rec = static_cast<const uint8_t *>(K_expanded);
     const int sms = info.sm_count;
     if (at == nullptr) {
-        if (p.y_debug != nullptr) return launch_umma_sched<true, false>(map, mapq, map, p, rec, sms, stream);
-        return launch_umma_sched<false, false>(map, mapq, map, p, rec, sms, stream);
+        if (p.y_debug != nullptr) return launch_umma<6, true, false>(map, mapq, map, p, rec, sms, stream);
+        return launch_umma<6, false, false>(map, mapq, map, p, rec, sms, stream);
     }
     CUtensorMap mapat;
     st = make_tensor_map_2d_bf16(&mapat, at, p.m, p.d, ldat, 64, kBR);
     if (st != KQ_OK) return st;
-    if (p.y_debug != nullptr) return launch_umma_sched<true, true>(map, mapq, mapat, p, rec, sms, stream);
-    return launch_umma_sched<false, true>(map, mapq, mapat, p, rec, sms, stream);
+    if (p.y_debug != nullptr) return launch_umma<6, true, true>(map, mapq, mapat, p, rec, sms, stream);
+    return launch_umma<6, false, true>(map, mapq, mapat, p, rec, sms, stream);
 }
 
 }  // namespace kq

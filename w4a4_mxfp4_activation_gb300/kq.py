@@ -30,14 +30,13 @@ KQ_TRANSFORM = {"kron": 0, "diag": 1, "hadamard": 2, "identity": 3, "fwht": 4}
 VARIANT_BUTTERFLY = 0
 VARIANT_IDENTITY = 2
 VARIANT_UMMA = 3
-SCHED_WORKSPACE_BYTES = 16      # KQ_SCHED_WORKSPACE_BYTES
 
 # the functions include/kq.h declares, then those of include/kq_testing.h
 EXPORTS = (
     "kq_quantize_mxfp4", "kq_smooth_quantize_mxfp4", "kq_hadamard_quantize_mxfp4",
     "kq_expand_blocks", "kq_expanded_bytes", "kq_dequantize", "kq_sf_bytes",
     "kq_status_string", "kq_lu_to_factors", "kq_invert_transpose_factors",
-    "kq_quantize_mxfp4_dual", "kq_quantize_mxfp4_ws", "kq_quantize_mxfp4_dual_ws",
+    "kq_quantize_mxfp4_dual",
     "kq_fwht_quantize_mxfp4", "kq_w4a4_gemm", "kq_bf16_gemm",
     "kq_layer_error", "kq_quantize_mxfp4_shared", "kq_quantize_mxfp4_ex",
 )
@@ -77,13 +76,7 @@ def lib() -> ctypes.CDLL:
             L.kq_quantize_mxfp4_dual.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, st, vp, i64,
                                                  vp, vp]
             L.kq_quantize_mxfp4_dual.restype = st
-            L.kq_quantize_mxfp4_ws.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64, vp, st, vp, vp,
-                                               vp]
-            L.kq_quantize_mxfp4_ws.restype = st
-            L.kq_quantize_mxfp4_dual_ws.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, st, vp,
-                                                    i64, vp, vp, vp]
-            L.kq_quantize_mxfp4_dual_ws.restype = st
-            L.kq_test_quantize_stall.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, st, vp, i64,
+            L.kq_test_quantize_stall.argtypes = [vp, i64, i64, i64, vp, vp, i64, vp, st, i64,
                                                  ctypes.c_uint64, vp]
             L.kq_test_quantize_stall.restype = st
             L.kq_quantize_mxfp4_shared.argtypes = [vp, i64, i64, i64, vp, vp, vp, i64, vp, st, vp,
@@ -221,36 +214,11 @@ def kq_quantize_mxfp4(A, d: int | None = None, factors=None, K_expanded=None,
     return q, sf, y_debug
 
 
-def sched_workspace(device):
-    """A zeroed scheduling workspace for the *_ws entry points (one per set
-    of calls that never run at the same time).  Word 2 counts CTAs that
-    found their pipeline stalled."""
-    import torch
-    return torch.zeros(SCHED_WORKSPACE_BYTES // 4, dtype=torch.int32, device=device)
-
-
-def kq_quantize_mxfp4_ws(A, workspace, d: int | None = None, factors=None, K_expanded=None,
-                         layout: int = KQ_SF_ROWMAJOR, q=None, sf=None, y_debug=None,
-                         stream=None):
-    """kq_quantize_mxfp4 whose tensor-core path takes tiles from the counter
-    in ``workspace`` (from sched_workspace).  Returns (q, sf, y_debug)."""
-    A = _bf16_bits(A)
-    m, lda = A.shape
-    d = lda if d is None else d
-    q, sf, y_debug = _outputs(A, m, d, layout, q, sf, y_debug)
-    ldq = q.shape[1] if q.dim() == 2 else d // 2
-    _check(lib().kq_quantize_mxfp4_ws(_ptr(A), m, d, A.stride(0), _ptr(factors), _ptr(K_expanded),
-                                      _ptr(q), ldq, _ptr(sf), layout, _ptr(y_debug),
-                                      _ptr(workspace), _stream(stream)),
-           "kq_quantize_mxfp4_ws")
-    return q, sf, y_debug
-
-
 def kq_quantize_mxfp4_dual(A, K_expanded, d: int | None = None, layout: int = KQ_SF_ROWMAJOR,
-                           q=None, sf=None, at=None, y_debug=None, stream=None, workspace=None):
+                           q=None, sf=None, at=None, y_debug=None, stream=None):
     """Quantize A on the tensor-core path and also write the bf16 side output
     A T.  Returns (q, sf, at, y_debug); ``at`` is allocated as bf16 [m, d]
-    when not given.  With ``workspace`` the call is kq_quantize_mxfp4_dual_ws."""
+    when not given."""
     import torch
     A = _bf16_bits(A)
     m, lda = A.shape
@@ -260,19 +228,15 @@ def kq_quantize_mxfp4_dual(A, K_expanded, d: int | None = None, layout: int = KQ
         at = torch.empty((m, d), dtype=torch.bfloat16, device=A.device)
     ldq = q.shape[1] if q.dim() == 2 else d // 2
     ldat = at.stride(0) if at.dim() == 2 else d
-    args = (_ptr(A), m, d, A.stride(0), _ptr(K_expanded), _ptr(q), ldq, _ptr(sf), layout, _ptr(at),
-            ldat, _ptr(y_debug))
-    if workspace is None:
-        _check(lib().kq_quantize_mxfp4_dual(*args, _stream(stream)), "kq_quantize_mxfp4_dual")
-    else:
-        _check(lib().kq_quantize_mxfp4_dual_ws(*args, _ptr(workspace), _stream(stream)),
-               "kq_quantize_mxfp4_dual_ws")
+    _check(lib().kq_quantize_mxfp4_dual(_ptr(A), m, d, A.stride(0), _ptr(K_expanded), _ptr(q), ldq,
+                                        _ptr(sf), layout, _ptr(at), ldat, _ptr(y_debug),
+                                        _stream(stream)),
+           "kq_quantize_mxfp4_dual")
     return q, sf, at, y_debug
 
 
 def kq_test_quantize_stall(A, K_expanded, d: int, skip_tile: int, wait_limit_ns: int,
-                           layout: int = KQ_SF_ROWMAJOR, q=None, sf=None, workspace=None,
-                           stream=None):
+                           layout: int = KQ_SF_ROWMAJOR, q=None, sf=None, stream=None):
     """Verification hook: the tensor-core quantizer with tile ``skip_tile``'s
     loads never issued and every wait bounded by ``wait_limit_ns``.
     Returns (q, sf)."""
@@ -281,8 +245,8 @@ def kq_test_quantize_stall(A, K_expanded, d: int, skip_tile: int, wait_limit_ns:
     q, sf, _ = _outputs(A, m, d, layout, q, sf, None)
     ldq = q.shape[1] if q.dim() == 2 else d // 2
     _check(lib().kq_test_quantize_stall(_ptr(A), m, d, A.stride(0), _ptr(K_expanded), _ptr(q), ldq,
-                                        _ptr(sf), layout, _ptr(workspace), skip_tile,
-                                        wait_limit_ns, _stream(stream)),
+                                        _ptr(sf), layout, skip_tile, wait_limit_ns,
+                                        _stream(stream)),
            "kq_test_quantize_stall")
     return q, sf
 
