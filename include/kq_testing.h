@@ -22,8 +22,11 @@ extern "C" {
  *   implementation chosen explicitly: variant 0 = in-register butterfly
  *   from the raw factors (needs factors), 2 = identity, 3 = tcgen05 tensor
  *   cores with TMEM accumulators on the pre-expanded operand records (needs
- *   K_expanded).  Other values (including 1, the warp-level mma.sync
- *   variant, which is no longer built): KQ_ERR_LAYOUT.
+ *   K_expanded), 4 = the same tensor-core kernel with the records built in
+ *   the kernel from the raw factors ([KQ] Sec. 3.5.1 "K2": K_j constructed on
+ *   the fly from its Kronecker factors, no expanded blocks in memory; needs
+ *   factors).  Other values (including 1, the warp-level mma.sync variant,
+ *   which is no longer built): KQ_ERR_LAYOUT.
  */
 KQ_API kq_status kq_quantize_mxfp4_variant(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
                                            const float *factors, const void *K_expanded,

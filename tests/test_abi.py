@@ -134,7 +134,9 @@ def test_quantize_argument_checks(L):
     assert _q(L, f=FAKE + 4) == 3                 # factors misaligned
     assert _q(L, m=0) == 0                        # empty: no-op
     assert _q(L, m=0, A=None, q=None, sf=None) == 0
-    assert _q(L, variant=4) == 4
+    assert _q(L, variant=5) == 4
+    assert _q(L, variant=4, f=None) == 1          # K2 builds from the factors
+    assert _q(L, variant=4, f=FAKE + 4) == 3
     assert _q(L, variant=3, K=None) == 1
     assert _q(L, variant=1, K=FAKE) == 4         # the mma.sync variant is not built
     assert _q(L, variant=0, f=None) == 1

@@ -58,6 +58,10 @@ def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None
         records = kq.kq_expand_blocks(dev(param_gpu), kq.KQ_K_BF16X3)
         return kq.kq_quantize_mxfp4(A, d, K_expanded=records, layout=layout, y_debug=y_debug,
                                     variant=kq.VARIANT_UMMA, q=q, sf=sf)
+    if kind == "kron_k2":
+        # the tensor-core kernel building its operand records from the factors
+        return kq.kq_quantize_mxfp4(A, d, factors=dev(param_gpu), layout=layout, y_debug=y_debug,
+                                    variant=kq.VARIANT_K2, q=q, sf=sf)
     if kind == "kron":
         return kq.kq_quantize_mxfp4(A, d, factors=dev(param_gpu), layout=layout, y_debug=y_debug,
                                     variant=variant, q=q, sf=sf)
@@ -72,12 +76,12 @@ def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None
 
 
 def oracle_kind(kind):
-    return "kron" if kind == "kron_umma" else kind
+    return "kron" if kind in ("kron_umma", "kron_k2") else kind
 
 
 def params_for(kind, nb, d, seed):
     """(gpu param, oracle param) for a transform kind."""
-    if kind in ("kron", "kron_umma"):
+    if kind in ("kron", "kron_umma", "kron_k2"):
         return lib_factors(nb, seed)
     if kind == "diag":
         s = synth.smooth_scales(d)
@@ -133,7 +137,7 @@ CASES = synth.CONFIG0 + synth.CONFIG1 + synth.CONFIG2 + synth.CONFIG3
 
 
 @pytest.mark.parametrize("name,m,d,model,cfg", CASES, ids=[c[0] for c in CASES])
-@pytest.mark.parametrize("kind", ["kron", "kron_umma", "diag", "hadamard", "identity"])
+@pytest.mark.parametrize("kind", ["kron", "kron_umma", "kron_k2", "diag", "hadamard", "identity"])
 def test_config_parity(name, m, d, model, cfg, kind):
     """Configs 0-3 at full size, every row and block, both scale layouts
     (the oracle's result computed once and compared with both)."""
@@ -242,8 +246,9 @@ SWEEP = [(m, d) for m in synth.SWEEP_M for d in synth.SWEEP_D]
 
 @pytest.mark.parametrize("m,d", SWEEP, ids=[f"{m}x{d}" for m, d in SWEEP])
 def test_sweep_parity(m, d):
-    """Config 4: 4 layers' factor sets per point; KroQuant (butterfly and
-    tensor cores, two layers each), diagonal and Hadamard quantizers.  Every row up
+    """Config 4: 4 layers' factor sets per point; KroQuant (butterfly, the
+    tensor cores on expanded records for two layers, the tensor cores with
+    the records built in the kernel), diagonal and Hadamard quantizers.  Every row up
     to m = 16384; at m = 65536 a seeded sample of 4096 rows (the first and
     last tiles always included)."""
     nb = d // 32
@@ -255,7 +260,7 @@ def test_sweep_parity(m, d):
                                          rng.choice(m, 4096, replace=False)]))
     for layer in range(4):
         Fg, Fo = lib_factors(nb, synth.SEED_FACTORS + 4 + layer)
-        kind = ("kron", "kron_umma", "kron", "kron_umma")[layer]
+        kind = ("kron", "kron_umma", "kron_k2", "kron_umma")[layer]
         q, sf, y = run_kind(kind, A_bits, d, layer % 2, Fg)
         res = parity.check(A_bits, d, "kron", Fo, layer % 2, np_(q), np_(sf), np_(y), rows)
         parity.record("config 4", f"sweep layer {layer}", m, d, kind, layer % 2, res)
@@ -275,7 +280,7 @@ EDGE_SHAPES = [(1, 32), (7, 96), (127, 160), (129, 64), (200, 5600), (3, 2240), 
 
 
 @pytest.mark.parametrize("m,d", EDGE_SHAPES, ids=[f"{m}x{d}" for m, d in EDGE_SHAPES])
-@pytest.mark.parametrize("kind", ["kron", "kron_umma", "diag", "hadamard", "identity"])
+@pytest.mark.parametrize("kind", ["kron", "kron_umma", "kron_k2", "diag", "hadamard", "identity"])
 def test_ragged_shapes_with_pitches_and_canaries(m, d, kind):
     """Ragged m and d (partial tiles and block-columns), lda > d, ldq > d/2,
     and guard bytes around every output that must stay untouched."""
@@ -332,7 +337,7 @@ def test_special_values():
     y_k[4] /= 2.0 ** 8
     bits_k = synth.f64_to_bf16_bits(y_k)
     Fg, Fo = lib_factors(1, 3)
-    for kind in ("kron", "kron_umma"):
+    for kind in ("kron", "kron_umma", "kron_k2"):
         q, sf, yd = run_kind(kind, bits_k, 32, 0, Fg)
         parity.check(bits_k, 32, "kron", Fo, 0, np_(q), np_(sf), np_(yd))
 
@@ -344,7 +349,7 @@ def test_raw_factor_interface():
     nb = d // 32
     A_bits = synth.activations(m, d, 9, "sana")
     F = synth.random_factors(nb, 12, scale=0.8)
-    for kind in ("kron", "kron_umma"):
+    for kind in ("kron", "kron_umma", "kron_k2"):
         q, sf, y = run_kind(kind, A_bits, d, 1, F)
         parity.check(A_bits, d, "kron", F.astype(np.float64), 1, np_(q), np_(sf), np_(y))
     Fg, Fo = lib_factors(nb, 13, sign=-1)
@@ -571,7 +576,7 @@ def test_identity_factors_reduce_to_bare_quantizer():
     for layout in (0, 1):
         nsf = kq.kq_sf_bytes(m, d, layout)
         q0, sf0, _ = run_kind("identity", A_bits, d, layout, y_debug=False)
-        for kind in ("kron", "kron_umma"):
+        for kind in ("kron", "kron_umma", "kron_k2"):
             q, sf, y = run_kind(kind, A_bits, d, layout, eye)
             assert torch.equal(q, q0) and torch.equal(sf[:nsf], sf0[:nsf]), kind
             assert np.array_equal(np_(y), synth.bf16_bits_to_f32(A_bits)), kind
@@ -919,3 +924,24 @@ def test_stalled_pipeline_marks_unfinished_blocks(layout):
     kq.kq_test_quantize_stall(A, KX, d, -1, STALL_LIMIT_NS, layout=layout, q=q1, sf=s1)
     torch.cuda.synchronize()
     assert torch.equal(q1, q0) and torch.equal(s1[:nsf], s0[:nsf])
+
+
+
+def test_k2_matches_records_path_outside_flags():
+    """K2 builds K_j from the factors in fp32 (products rounded four times,
+    then split exactly into three bf16 terms); the records path expands it
+    in fp64.  Both are checked against the oracle elsewhere; here their codes
+    agree on every unflagged element of the FLUX FFN-down layer, and their
+    y differ by no more than the sum of the two 2^-16 allowances."""
+    m, d = 4608, 12288
+    A_bits = synth.activations(m, d, synth.SEED_A + 3, "flux")
+    Fg, Fo = lib_factors(d // 32, synth.SEED_FACTORS + 3)
+    qk, sk, yk = run_kind("kron_k2", A_bits, d, 1, Fg)
+    qr, sr, yr = run_kind("kron_umma", A_bits, d, 1, Fg)
+    rows = np.arange(0, m, 5)
+    ref = parity.reference(A_bits, d, "kron", Fo, rows)
+    strict = ref["flags"] == 0
+    ck, cr = parity.unpack(np_(qk)[rows], d), parity.unpack(np_(qr)[rows], d)
+    assert np.array_equal(ck[strict], cr[strict])
+    diff = np.abs(np_(yk)[rows].astype(np.float64) - np_(yr)[rows])
+    assert np.all(diff <= np.ldexp(ref["bound"], -15))

@@ -251,30 +251,33 @@ using namespace kq;
 namespace {
 
 // The quantizer entry points: argument checks, then the implementation
-// `variant` (0 butterfly, 2 identity, 3 tcgen05).  `extra` carries the
-// tcgen05 kernel's wait limit and verification hook (its other fields are
-// filled here).
+// `variant` (0 butterfly, 2 identity, 3 tcgen05 on the expanded records,
+// 4 tcgen05 building the records in the kernel from the raw factors, K2).
+// `extra` carries the tcgen05 kernel's wait limit and verification hook (its
+// other fields are filled here).
 kq_status quantize_variant(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
                            const float *factors, const void *K_expanded, uint8_t *q, int64_t ldq,
                            uint8_t *sf, kq_sf_layout sf_layout, float *y_debug, int variant,
                            const QuantParams &extra, cudaStream_t stream)
 {
-    if (variant != 0 && variant != 2 && variant != 3) return KQ_ERR_LAYOUT;
+    if (variant != 0 && variant != 2 && variant != 3 && variant != 4) return KQ_ERR_LAYOUT;
     kq_status st = validate_quant_args(A, m, d, lda, q, ldq, sf, sf_layout, y_debug);
     if (st != KQ_OK) return st;
-    if (variant == 0 && factors == nullptr) return KQ_ERR_NULL;
+    if ((variant == 0 || variant == 4) && factors == nullptr) return KQ_ERR_NULL;
     if (variant == 3 && K_expanded == nullptr) return KQ_ERR_NULL;
-    if (variant == 0 && !aligned16(factors)) return KQ_ERR_ALIGN;
+    if ((variant == 0 || variant == 4) && !aligned16(factors)) return KQ_ERR_ALIGN;
     if (variant == 3 && !aligned16(K_expanded)) return KQ_ERR_ALIGN;
     if (m == 0) return KQ_OK;
     DeviceInfo info;
     if ((st = device_info(info)) != KQ_OK) return st;
     QuantParams p;
     fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
-    if (variant == 3) {
+    if (variant == 3 || variant == 4) {
         p.wait_limit_ns = extra.wait_limit_ns;
         p.skip_tile = extra.skip_tile;
-        return launch_quant_umma(A, lda, K_expanded, p, nullptr, 0, stream);
+        if (variant == 4) p.factors = factors;
+        return launch_quant_umma(A, lda, variant == 3 ? K_expanded : nullptr, p, nullptr, 0,
+                                 stream);
     }
     if (variant == 0) {
         p.factors = factors;

@@ -95,7 +95,9 @@ kq_status launch_umma_records(const float *factors, int64_t nb, void *out, cudaS
 // Full-row Walsh-Hadamard + MXFP4 (d a power of two, 128 <= d <= 16384).
 kq_status launch_quant_fwht(const uint16_t *A, int64_t lda, const QuantParams &p,
                             cudaStream_t stream);
-// at != nullptr: also write the bf16 side output A T ([m][ldat], the DUAL kernel)
+// at != nullptr: also write the bf16 side output A T ([m][ldat], the DUAL kernel);
+// K_expanded == nullptr: the K2 form, building the operand records in the
+// kernel from p.factors (no side output)
 kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expanded,
                             const QuantParams &p, uint16_t *at, int64_t ldat, cudaStream_t stream);
 

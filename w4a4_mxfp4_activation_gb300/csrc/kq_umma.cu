@@ -71,6 +71,12 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kMmaWarps = 2;                   // one per accumulator buffer
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
 constexpr int kThreadsU = (kFirstEpiWarp + kEpiWarps) * 32;
+// K2 form: one more warp builds the tiles' operand records in the kernel
+// (a second one would put six warps on one SM sub-partition and cap every
+// thread at 80 registers, below what the epilogue needs)
+constexpr int kBuildWarps = 1;
+constexpr int kFirstBuildWarp = kFirstEpiWarp + kEpiWarps;
+constexpr int kThreadsK2 = kThreadsU + kBuildWarps * 32;
 constexpr int kBR = 128;                       // rows per tile (= MMA M)
 constexpr int kBlockCols = 96;                 // per block: 3 terms x 32 outputs
 constexpr int kAccCols = 2 * kBlockCols;       // fp32 columns per accumulator buffer
@@ -200,8 +206,55 @@ __device__ __forceinline__ void store_scale_u(const QuantParams &p, int64_t row,
     }
 }
 
-template <int STAGES, bool DEBUG, bool DUAL>
-__global__ void __launch_bounds__(kThreadsU, 1)
+// K2 (the tensor-core path without expanded records in memory): the three
+// bf16 terms of K_j for column c of one block, written into a tile's record
+// area in the MMA operand layout (see umma_records_kernel).  Entries by
+// eq. (12), K_j[r][c] = prod_k G_k[bit_{5-k}(r)][bit_{5-k}(c)], as fp32
+// products; each fp32 value splits exactly into hi + mid + lo (three 8-bit
+// significands).  Lane c of a warp writes, per 8-row group g, one 16-byte
+// row of a core matrix per term (conflict-free: the warp's 32 rows fill
+// 4 x 128 contiguous bytes).
+__device__ __forceinline__ void build_record_column(uint32_t rec, const float4 (&G)[5], int c)
+{
+    float col[5][2];            // G_k[row][bit_{4-k}(c)], k = 0..4 for G1..G5
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const int bit = (c >> (4 - k)) & 1;
+        col[k][0] = sel2x2(G[k], 0, bit);
+        col[k][1] = sel2x2(G[k], 1, bit);
+    }
+    float a[4], Q[8];           // r & 7 = i: G3[bit2(i)] G4[bit1(i)] G5[bit0(i)]
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = col[3][i >> 1] * col[4][i & 1];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) Q[i] = col[2][i >> 2] * a[i & 3];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {           // r = 8 g + i: bit 4 of r = g >> 1, bit 3 = g & 1
+        const float P = col[0][g >> 1] * col[1][g & 1];
+        uint32_t w[3][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float k0 = P * Q[2 * q], k1 = P * Q[2 * q + 1];
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(k0, k1);
+            const float2 hf = __bfloat1622float2(hi);
+            const float r0 = k0 - hf.x, r1 = k1 - hf.y;          // exact
+            const __nv_bfloat162 mid = __floats2bfloat162_rn(r0, r1);
+            const float2 mf = __bfloat1622float2(mid);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(r0 - mf.x, r1 - mf.y);
+            w[0][q] = *reinterpret_cast<const uint32_t *>(&hi);
+            w[1][q] = *reinterpret_cast<const uint32_t *>(&mid);
+            w[2][q] = *reinterpret_cast<const uint32_t *>(&lo);
+        }
+        // step h = g >> 1 (input channels 16 h..), core column g & 1, row c % 8
+        const uint32_t off = rec + (g >> 1) * 3072 + (g & 1) * 128 + (c & 7) * 16;
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+            sts128(off + ((32 * t + c) >> 3) * 256, make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]));
+    }
+}
+
+template <int STAGES, bool DEBUG, bool DUAL, bool K2>
+__global__ void __launch_bounds__(K2 ? kThreadsK2 : kThreadsU, 1)
     quant_umma_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmAT, const QuantParams p,
@@ -239,7 +292,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int s = static_cast<int>(pit % STAGES);
         const uint32_t dst = base + s * Cfg::kStageBytes;
         const int64_t left = p.nb - pw.ct * 2;          // < 1 on padding tiles
-        const uint32_t rbytes =
+        // K2: the records are built in the stage by the builder warps
+        const uint32_t rbytes = K2 ? 0u :
             static_cast<uint32_t>((left < 0 ? 0 : (left < 2 ? left : 2)) * Cfg::kRecBytes);
         mbar_arrive_expect_tx(bar_full + 8 * s, Cfg::kABytes + rbytes);
         if (pit == skip_it) {                            // the stage stays armed, never filled
@@ -248,7 +302,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             return;
         }
         tma_load_2d(dst, &tmA, pw.ct * 64, pw.rt * kBR, bar_full + 8 * s, pol);
-        if (p.shared_params) {
+        if (K2) {
+        } else if (p.shared_params) {
             // one operand record for every block: a copy of it per block slot
             for (uint32_t off = 0; off < rbytes; off += Cfg::kRecBytes)
                 bulk_load(dst + Cfg::kBOff + off, records, Cfg::kRecBytes, bar_full + 8 * s);
@@ -265,7 +320,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         tma_prefetch_desc(&tmQ);              // earlier grids
         if (DUAL) tma_prefetch_desc(&tmAT);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, K2 ? 2 : 1);     // K2: TMA bytes + the builder
             mbar_init(bar_empty + 8 * s, 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -351,6 +406,61 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         // Wait (bounded) for this warp's last MMAs before TMEM is released.
         if (it >= 2)
             (void)mbar_wait(bar_acc_full + 8 * a, static_cast<uint32_t>(((it - 2) >> 1) & 1), lim);
+    } else if (K2 && warp >= kFirstBuildWarp) {
+        // ---------------- K2: operand records built in the kernel ----------------
+        // The builder warp walks the CTA's tiles like the producer.  Per tile
+        // it waits until the stage's previous MMAs have read it, writes the
+        // three bf16 terms of the tile's two K_j from their raw factors
+        // (lane = output channel), makes the writes visible to the tensor
+        // cores and arrives on the stage's full barrier beside the producer's
+        // TMA bytes.  The next tile's factors (80 bytes per block) are
+        // prefetched into L1 one tile ahead.
+        int64_t it = 0;
+        TileWalk tw(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                    static_cast<int>(p.ncol_tiles));
+        auto factors_of = [&](int64_t j) {
+            return p.factors + ((p.shared_params || j >= p.nb) ? 0 : j) * 20;
+        };
+        // (the tile's up to 160 bytes span at most three 128-byte lines; the
+        // prefetched addresses stay inside the factor array)
+        const int64_t fbytes = (p.shared_params ? 1 : p.nb) * 80;
+        auto prefetch = [&](int ct) {
+            if (lane < 3) {
+                const int64_t j = 2 * static_cast<int64_t>(ct);
+                const int64_t first = (p.shared_params || j >= p.nb) ? 0 : j * 80;
+                const int64_t off = first + (lane == 2 ? 159 : 128 * lane);
+                const char *f = reinterpret_cast<const char *>(p.factors) +
+                                (off < fbytes ? off : fbytes - 1);
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(f));
+            }
+        };
+        if (tw.rt < p.nrow_tiles) prefetch(tw.ct);
+        while (tw.rt < p.nrow_tiles) {
+            const int ct = tw.ct;
+            tw.next();
+            if (tw.rt < p.nrow_tiles) prefetch(tw.ct);
+            const int s = static_cast<int>(it % STAGES);
+            if (it >= STAGES &&
+                !__all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * s,
+                                                   static_cast<uint32_t>(((it / STAGES) & 1) ^ 1),
+                                                   lim)))
+                break;
+            const uint32_t rec = base + s * Cfg::kStageBytes + Cfg::kBOff;
+#pragma unroll 1
+            for (int b = 0; b < 2; ++b) {
+                const int64_t j = 2 * static_cast<int64_t>(ct) + b;
+                if (j >= p.nb) break;
+                const float *g = factors_of(j);
+                float4 G[5];
+#pragma unroll
+                for (int k = 0; k < 5; ++k) G[k] = ldg_nc_f4(g + 4 * k);
+                build_record_column(rec + b * Cfg::kRecBytes, G, lane);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_full + 8 * s);
+            ++it;
+        }
     } else {
         // ---------------- epilogue ----------------
         const int e = warp - kFirstEpiWarp;
@@ -569,12 +679,13 @@ struct USlot {
     cudaError_t err[64] = {};
 };
 
-template <int STAGES, bool DEBUG, bool DUAL>
+template <int STAGES, bool DEBUG, bool DUAL, bool K2>
 kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, const CUtensorMap &mapat,
                       QuantParams p, const uint8_t *records, int sm_count, cudaStream_t stream)
 {
     using Cfg = UCfg<STAGES>;
-    auto kern = quant_umma_kernel<STAGES, DEBUG, DUAL>;
+    auto kern = quant_umma_kernel<STAGES, DEBUG, DUAL, K2>;
+    constexpr int threads = K2 ? kThreadsK2 : kThreadsU;
     static USlot slot;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
@@ -583,7 +694,7 @@ kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, const CUt
                                              Cfg::kSmemBytes);
         if (slot.err[dev] == cudaSuccess)
             slot.err[dev] = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &slot.occupancy[dev], kern, kThreadsU, Cfg::kSmemBytes);
+                &slot.occupancy[dev], kern, threads, Cfg::kSmemBytes);
     });
     if (slot.err[dev] != cudaSuccess || slot.occupancy[dev] < 1) return KQ_ERR_CUDA;
     // tiles of 64 channels (one TMA box); the tiled scale layout also needs
@@ -595,7 +706,7 @@ kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, const CUt
     // one CTA per SM: each holds 256 of the SM's 512 TMEM columns
     const int grid = static_cast<int>(std::min<int64_t>(p.ntiles, sm_count));
     if (!tiles_fit_int32(p, grid)) return KQ_ERR_SHAPE;
-    return launch_pdl(kern, grid, kThreadsU, Cfg::kSmemBytes, stream, map, mapq, mapat, p,
+    return launch_pdl(kern, grid, threads, Cfg::kSmemBytes, stream, map, mapq, mapat, p,
                       records);
 }
 
@@ -623,15 +734,24 @@ kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expand
     if (st != KQ_OK) return st;
     const uint8_t *rec = static_cast<const uint8_t *>(K_expanded);
     const int sms = info.sm_count;
+    if (K_expanded == nullptr) {
+        // K2: no records in memory, the kernel builds them from p.factors
+        if (at != nullptr || p.factors == nullptr) return KQ_ERR_NULL;
+        if (p.y_debug != nullptr)
+            return launch_umma<6, true, false, true>(map, mapq, map, p, nullptr, sms, stream);
+        return launch_umma<6, false, false, true>(map, mapq, map, p, nullptr, sms, stream);
+    }
     if (at == nullptr) {
-        if (p.y_debug != nullptr) return launch_umma<6, true, false>(map, mapq, map, p, rec, sms, stream);
-        return launch_umma<6, false, false>(map, mapq, map, p, rec, sms, stream);
+        if (p.y_debug != nullptr)
+            return launch_umma<6, true, false, false>(map, mapq, map, p, rec, sms, stream);
+        return launch_umma<6, false, false, false>(map, mapq, map, p, rec, sms, stream);
     }
     CUtensorMap mapat;
     st = make_tensor_map_2d_bf16(&mapat, at, p.m, p.d, ldat, 64, kBR);
     if (st != KQ_OK) return st;
-    if (p.y_debug != nullptr) return launch_umma<6, true, true>(map, mapq, mapat, p, rec, sms, stream);
-    return launch_umma<6, false, true>(map, mapq, mapat, p, rec, sms, stream);
+    if (p.y_debug != nullptr)
+        return launch_umma<6, true, true, false>(map, mapq, mapat, p, rec, sms, stream);
+    return launch_umma<6, false, true, false>(map, mapq, mapat, p, rec, sms, stream);
 }
 
 }  // namespace kq

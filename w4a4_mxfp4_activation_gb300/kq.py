@@ -30,6 +30,7 @@ KQ_TRANSFORM = {"kron": 0, "diag": 1, "hadamard": 2, "identity": 3, "fwht": 4}
 VARIANT_BUTTERFLY = 0
 VARIANT_IDENTITY = 2
 VARIANT_UMMA = 3
+VARIANT_K2 = 4          # tensor cores, operand records built in the kernel from the factors
 
 # the functions include/kq.h declares, then those of include/kq_testing.h
 EXPORTS = (
