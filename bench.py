@@ -258,12 +258,12 @@ assert L.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
 reasons = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
     L.nvmlDeviceGetCurrentClocksThrottleReasons
 mhz, mx, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+assert L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0
 with open(path, "w", buffering=1) as f:
     f.write("ready\n")
     while True:
         t = time.monotonic()
         if (L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0 and
-                L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 and
                 reasons(h, ctypes.byref(bits)) == 0):
             f.write(f"{t} {mhz.value} {mx.value} {bits.value}\n")
         time.sleep(0.0002)
@@ -561,6 +561,7 @@ def run_ours(args, dist: Dist):
         g = graphs_for(kind, round_lengths(steps) + round_lengths(warmup))
         events = [] if per_launch else None
         with torch.cuda.stream(stream):
+            hw = time.monotonic()
             run_steps(g, warmup, None)
             stream.synchronize()
             dist.barrier()
@@ -579,7 +580,7 @@ def run_ours(args, dist: Dist):
         # average duration of one dominant launch over the timed region
         launch_ms = ([sum(a.elapsed_time(b) for a, b in events) / sum(counts)]
                      if per_launch and events else [])
-        return ms, launch_ms, (h0, h1), g
+        return ms, launch_ms, (hw, h0, h1), g
 
     def isolated(kind, g, n):
         """Median CUDA-event time (ms) of one dominant-layer launch replayed
@@ -622,8 +623,9 @@ def run_ours(args, dist: Dist):
 
     W, K = args.warmup, args.steps
     clock = ClockSampler(device_uuid(dev), os.environ.get("TMPDIR"))
-    ms, launch_ms, window, g_main = timed("kroquant", K, W, per_launch=True)
+    ms, launch_ms, (hw, h0, h1), g_main = timed("kroquant", K, W, per_launch=True)
     iso_ms = isolated("kroquant", g_main, max(3, args.isolated))
+    h2 = time.monotonic()
     floor_ms = launch_floor(max(3, args.isolated))
     del g_main
     ms_max = dist.max(ms)
@@ -673,8 +675,15 @@ def run_ours(args, dist: Dist):
             name = f"kroquant_{kind}" if kind in ("butterfly", "umma") else kind
             baselines[name] = round(STEP_BYTES * nb_steps / (dist.max(bms) * 1e-3) / 1e9, 2)
     clock.stop()
-    clocks = clock.summary(window)
+    # NVML answers in tens of ms, so few samples fall inside a timed region of
+    # a millisecond: the reported window also holds the warm-up steps before
+    # it and the isolated launches after it (the same kernels, back to back)
+    clocks = dict(clock.summary((h0, h1)), window="timed region")
+    if clocks["samples"] < 3:
+        clocks = dict(clock.summary((hw, h2)), window="warm-up + timed region + isolated launches")
     run_clocks = clock.summary()
+    if clocks["samples"] < 3:
+        clocks = dict(run_clocks, window="whole run (no closer window holds 3 samples)")
 
     # ---- the consumer of the quantizer's output: the W4A4 product of the
     #      FFN-down layer (A_q: this step's quantized activations, 4608 x
@@ -866,7 +875,7 @@ TABLE_CONFIGS = (
     ("4", tuple((f"sweep_{m}x{d}", m, d, "flux") for m in (256, 1024, 4096, 16384, 65536)
                 for d in (1152, 3072, 12288))),
 )
-TABLE_KERNELS = ("umma", "butterfly", "diag", "hadamard", "identity", "dual")
+TABLE_KERNELS = ("umma", "k2", "butterfly", "diag", "hadamard", "identity", "dual")
 
 
 def oracle_rate_shape(m: int, d: int, seconds: float):
@@ -948,6 +957,9 @@ def measure_shape(args, m, d, model, seed, kinds, peak):
         elif kind == "butterfly":
             kq.kq_quantize_mxfp4(A[s], d, factors=F, layout=layout, q=Q[s], sf=SF[s],
                                  variant=kq.VARIANT_BUTTERFLY, stream=stream)
+        elif kind == "k2":
+            kq.kq_quantize_mxfp4(A[s], d, factors=F, layout=layout, q=Q[s], sf=SF[s],
+                                 variant=kq.VARIANT_K2, stream=stream)
         elif kind == "dual":
             kq.kq_quantize_mxfp4_dual(A[s], KX, d, layout=layout, q=Q[s], sf=SF[s], at=AT[s],
                                       stream=stream)
@@ -1046,15 +1058,16 @@ def run_table3(args, peak):
     # diagonal scale (Scale), the dense-block tensor-core kernel (tcgen05,
     # K1's form), the kernel built from the factors (butterfly, K2's input)
     # and the full-row Walsh-Hadamard transform (FWHT), all with MXFP4 output
-    kinds = ("identity", "diag", "umma", "butterfly", "fwht")
+    kinds = ("identity", "diag", "umma", "k2", "butterfly", "fwht")
     print()
-    print("| m | d | Q4 us | Scale us | tcgen05 us | butterfly us | FWHT us | Scale/tcgen05 | "
-          "Scale/butterfly | FWHT/tcgen05 | FWHT/butterfly |")
-    print("|" + "---|" * 11)
+    print("| m | d | Q4 us | Scale us | tcgen05 (K1 records) us | tcgen05 (K2) us | butterfly us | "
+          "FWHT us | Scale/tcgen05 | K1/K2 | Scale/butterfly | FWHT/tcgen05 | FWHT/butterfly |")
+    print("|" + "---|" * 13)
     for m, d in TABLE3_SHAPES:
         us, _ = measure_shape(args, m, d, "flux", synth_seed("3"), kinds, peak)
         print(f"| {m} | {d} | " + " | ".join(f"{us[k]:.2f}" for k in kinds) +
-              f" | {us['diag'] / us['umma']:.2f} | {us['diag'] / us['butterfly']:.2f} | "
+              f" | {us['diag'] / us['umma']:.2f} | {us['umma'] / us['k2']:.2f} | "
+              f"{us['diag'] / us['butterfly']:.2f} | "
               f"{us['fwht'] / us['umma']:.2f} | {us['fwht'] / us['butterfly']:.2f} |", flush=True)
     # the same with fp16 activations, the precision the pages time in: the
     # CUDA-core kernels (the tensor-core path reads bf16)
