@@ -71,12 +71,6 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kMmaWarps = 2;                   // one per accumulator buffer
 constexpr int kFirstEpiWarp = 1 + kMmaWarps;
 constexpr int kThreadsU = (kFirstEpiWarp + kEpiWarps) * 32;
-// K2 form: one more warp builds the tiles' operand records in the kernel
-// (a second one would put six warps on one SM sub-partition and cap every
-// thread at 80 registers, below what the epilogue needs)
-constexpr int kBuildWarps = 1;
-constexpr int kFirstBuildWarp = kFirstEpiWarp + kEpiWarps;
-constexpr int kThreadsK2 = kThreadsU + kBuildWarps * 32;
 constexpr int kBR = 128;                       // rows per tile (= MMA M)
 constexpr int kBlockCols = 96;                 // per block: 3 terms x 32 outputs
 constexpr int kAccCols = 2 * kBlockCols;       // fp32 columns per accumulator buffer
@@ -206,15 +200,15 @@ __device__ __forceinline__ void store_scale_u(const QuantParams &p, int64_t row,
     }
 }
 
-// K2 (the tensor-core path without expanded records in memory): the three
-// bf16 terms of K_j for column c of one block, written into a tile's record
-// area in the MMA operand layout (see umma_records_kernel).  Entries by
-// eq. (12), K_j[r][c] = prod_k G_k[bit_{5-k}(r)][bit_{5-k}(c)], as fp32
-// products; each fp32 value splits exactly into hi + mid + lo (three 8-bit
-// significands).  Lane c of a warp writes, per 8-row group g, one 16-byte
-// row of a core matrix per term (conflict-free: the warp's 32 rows fill
-// 4 x 128 contiguous bytes).
-__device__ __forceinline__ void build_record_column(uint32_t rec, const float4 (&G)[5], int c)
+// K2 (the tensor-core path without expanded records in memory): eight
+// entries of K_j -- rows 8 g .. 8 g + 7, column c -- as the three bf16 terms,
+// written into a tile's record area in the MMA operand layout (see
+// umma_records_kernel).  Entries by eq. (12), K_j[r][c] =
+// prod_k G_k[bit_{5-k}(r)][bit_{5-k}(c)], as fp32 products; each fp32 value
+// splits exactly into hi + mid + lo (three 8-bit significands).  The eight
+// entries of a term form one 16-byte row of a core matrix; a warp with
+// c = lane fills 4 x 128 contiguous bytes per term (no bank conflicts).
+__device__ __forceinline__ void build_record_rows(uint32_t rec, const float4 (&G)[5], int c, int g)
 {
     float col[5][2];            // G_k[row][bit_{4-k}(c)], k = 0..4 for G1..G5
 #pragma unroll
@@ -223,38 +217,33 @@ __device__ __forceinline__ void build_record_column(uint32_t rec, const float4 (
         col[k][0] = sel2x2(G[k], 0, bit);
         col[k][1] = sel2x2(G[k], 1, bit);
     }
-    float a[4], Q[8];           // r & 7 = i: G3[bit2(i)] G4[bit1(i)] G5[bit0(i)]
+    // r = 8 g + i: bit 4 of r = g >> 1, bit 3 = g & 1, bits 2..0 = i (g is a
+    // run-time value: selects, not an indexed array, keep col in registers)
+    const float P = ((g >> 1) ? col[0][1] : col[0][0]) * ((g & 1) ? col[1][1] : col[1][0]);
+    uint32_t w[3][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] = col[3][i >> 1] * col[4][i & 1];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) Q[i] = col[2][i >> 2] * a[i & 3];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {           // r = 8 g + i: bit 4 of r = g >> 1, bit 3 = g & 1
-        const float P = col[0][g >> 1] * col[1][g & 1];
-        uint32_t w[3][4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float k0 = P * Q[2 * q], k1 = P * Q[2 * q + 1];
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(k0, k1);
-            const float2 hf = __bfloat1622float2(hi);
-            const float r0 = k0 - hf.x, r1 = k1 - hf.y;          // exact
-            const __nv_bfloat162 mid = __floats2bfloat162_rn(r0, r1);
-            const float2 mf = __bfloat1622float2(mid);
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(r0 - mf.x, r1 - mf.y);
-            w[0][q] = *reinterpret_cast<const uint32_t *>(&hi);
-            w[1][q] = *reinterpret_cast<const uint32_t *>(&mid);
-            w[2][q] = *reinterpret_cast<const uint32_t *>(&lo);
-        }
-        // step h = g >> 1 (input channels 16 h..), core column g & 1, row c % 8
-        const uint32_t off = rec + (g >> 1) * 3072 + (g & 1) * 128 + (c & 7) * 16;
-#pragma unroll
-        for (int t = 0; t < 3; ++t)
-            sts128(off + ((32 * t + c) >> 3) * 256, make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]));
+    for (int q = 0; q < 4; ++q) {
+        const float k0 = P * (col[2][q >> 1] * (col[3][q & 1] * col[4][0]));
+        const float k1 = P * (col[2][q >> 1] * (col[3][q & 1] * col[4][1]));
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(k0, k1);
+        const float2 hf = __bfloat1622float2(hi);
+        const float r0 = k0 - hf.x, r1 = k1 - hf.y;              // exact
+        const __nv_bfloat162 mid = __floats2bfloat162_rn(r0, r1);
+        const float2 mf = __bfloat1622float2(mid);
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(r0 - mf.x, r1 - mf.y);
+        w[0][q] = *reinterpret_cast<const uint32_t *>(&hi);
+        w[1][q] = *reinterpret_cast<const uint32_t *>(&mid);
+        w[2][q] = *reinterpret_cast<const uint32_t *>(&lo);
     }
+    // step h = g >> 1 (input channels 16 h..), core column g & 1, row c % 8
+    const uint32_t off = rec + (g >> 1) * 3072 + (g & 1) * 128 + (c & 7) * 16;
+#pragma unroll
+    for (int t = 0; t < 3; ++t)
+        sts128(off + ((32 * t + c) >> 3) * 256, make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]));
 }
 
 template <int STAGES, bool DEBUG, bool DUAL, bool K2>
-__global__ void __launch_bounds__(K2 ? kThreadsK2 : kThreadsU, 1)
+__global__ void __launch_bounds__(kThreadsU, 1)
     quant_umma_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmAT, const QuantParams p,
@@ -292,7 +281,7 @@ __global__ void __launch_bounds__(K2 ? kThreadsK2 : kThreadsU, 1)
         const int s = static_cast<int>(pit % STAGES);
         const uint32_t dst = base + s * Cfg::kStageBytes;
         const int64_t left = p.nb - pw.ct * 2;          // < 1 on padding tiles
-        // K2: the records are built in the stage by the builder warps
+        // K2: the records are built in the stage by the epilogue warps
         const uint32_t rbytes = K2 ? 0u :
             static_cast<uint32_t>((left < 0 ? 0 : (left < 2 ? left : 2)) * Cfg::kRecBytes);
         mbar_arrive_expect_tx(bar_full + 8 * s, Cfg::kABytes + rbytes);
@@ -320,7 +309,7 @@ __global__ void __launch_bounds__(K2 ? kThreadsK2 : kThreadsU, 1)
         tma_prefetch_desc(&tmQ);              // earlier grids
         if (DUAL) tma_prefetch_desc(&tmAT);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, K2 ? 2 : 1);     // K2: TMA bytes + the builder
+            mbar_init(bar_full + 8 * s, K2 ? 2 : 1);     // K2: TMA bytes + the record builders
             mbar_init(bar_empty + 8 * s, 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -406,61 +395,6 @@ __global__ void __launch_bounds__(K2 ? kThreadsK2 : kThreadsU, 1)
         // Wait (bounded) for this warp's last MMAs before TMEM is released.
         if (it >= 2)
             (void)mbar_wait(bar_acc_full + 8 * a, static_cast<uint32_t>(((it - 2) >> 1) & 1), lim);
-    } else if (K2 && warp >= kFirstBuildWarp) {
-        // ---------------- K2: operand records built in the kernel ----------------
-        // The builder warp walks the CTA's tiles like the producer.  Per tile
-        // it waits until the stage's previous MMAs have read it, writes the
-        // three bf16 terms of the tile's two K_j from their raw factors
-        // (lane = output channel), makes the writes visible to the tensor
-        // cores and arrives on the stage's full barrier beside the producer's
-        // TMA bytes.  The next tile's factors (80 bytes per block) are
-        // prefetched into L1 one tile ahead.
-        int64_t it = 0;
-        TileWalk tw(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
-                    static_cast<int>(p.ncol_tiles));
-        auto factors_of = [&](int64_t j) {
-            return p.factors + ((p.shared_params || j >= p.nb) ? 0 : j) * 20;
-        };
-        // (the tile's up to 160 bytes span at most three 128-byte lines; the
-        // prefetched addresses stay inside the factor array)
-        const int64_t fbytes = (p.shared_params ? 1 : p.nb) * 80;
-        auto prefetch = [&](int ct) {
-            if (lane < 3) {
-                const int64_t j = 2 * static_cast<int64_t>(ct);
-                const int64_t first = (p.shared_params || j >= p.nb) ? 0 : j * 80;
-                const int64_t off = first + (lane == 2 ? 159 : 128 * lane);
-                const char *f = reinterpret_cast<const char *>(p.factors) +
-                                (off < fbytes ? off : fbytes - 1);
-                asm volatile("prefetch.global.L1 [%0];" ::"l"(f));
-            }
-        };
-        if (tw.rt < p.nrow_tiles) prefetch(tw.ct);
-        while (tw.rt < p.nrow_tiles) {
-            const int ct = tw.ct;
-            tw.next();
-            if (tw.rt < p.nrow_tiles) prefetch(tw.ct);
-            const int s = static_cast<int>(it % STAGES);
-            if (it >= STAGES &&
-                !__all_sync(0xffffffffu, mbar_wait(bar_empty + 8 * s,
-                                                   static_cast<uint32_t>(((it / STAGES) & 1) ^ 1),
-                                                   lim)))
-                break;
-            const uint32_t rec = base + s * Cfg::kStageBytes + Cfg::kBOff;
-#pragma unroll 1
-            for (int b = 0; b < 2; ++b) {
-                const int64_t j = 2 * static_cast<int64_t>(ct) + b;
-                if (j >= p.nb) break;
-                const float *g = factors_of(j);
-                float4 G[5];
-#pragma unroll
-                for (int k = 0; k < 5; ++k) G[k] = ldg_nc_f4(g + 4 * k);
-                build_record_column(rec + b * Cfg::kRecBytes, G, lane);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_full + 8 * s);
-            ++it;
-        }
     } else {
         // ---------------- epilogue ----------------
         const int e = warp - kFirstEpiWarp;
@@ -479,9 +413,51 @@ __global__ void __launch_bounds__(K2 ? kThreadsK2 : kThreadsU, 1)
         bool ok = true;
         TileWalk tw(static_cast<int>(blockIdx.x + grp * gridDim.x),
                     static_cast<int>(2 * gridDim.x), static_cast<int>(p.ncol_tiles));
+        // K2: the group also builds the operand records of its tiles in their
+        // ring stages.  A tile's stage is free for its records once the MMAs
+        // of the tile STAGES positions earlier -- the group's own tile three
+        // steps back -- have completed, which the group sees when it reads
+        // that tile's accumulators; so, after finishing tile it, the group
+        // builds tile it + STAGES into the same stage (the first STAGES / 2
+        // of its tiles before the loop).  Warp (e & 7) writes block
+        // (e & 7) >> 2, rows 8 ((e & 7) & 3) .. + 7, lane = output channel.
+        // The group then arrives on the stage's full barrier beside the
+        // producer's TMA bytes -- unless a wait ran out in one of its warps
+        // (the stage might then still be read), in which case no warp
+        // arrives and the tile's MMAs time out in turn.
+        TileWalk bwk = tw;                    // the next tile whose records to build
+        const int bb = (e & 7) >> 2, bg = (e & 7) & 3;
+        auto build = [&](int ct, int s, bool can) {
+            const int64_t j = 2 * static_cast<int64_t>(ct) + bb;
+            if (can && j < p.nb) {
+                const float *g = p.factors + (p.shared_params ? 0 : j * 20);
+                float4 G[5];
+#pragma unroll
+                for (int k = 0; k < 5; ++k) G[k] = ldg_nc_f4(g + 4 * k);
+                build_record_rows(base + s * Cfg::kStageBytes + Cfg::kBOff + bb * Cfg::kRecBytes, G,
+                                  lane, bg);
+            }
+            fence_proxy_async_smem();
+            if (named_barrier_and(9 + grp, kEpiThreads / 2, can) && (e & 7) == 0 && lane == 0)
+                mbar_arrive(bar_full + 8 * s);
+        };
+        if (K2) {
+            for (int k = 0; k < STAGES / 2 && bwk.rt < p.nrow_tiles; ++k, bwk.next())
+                build(bwk.ct, grp + 2 * k, true);
+        }
         for (; tw.rt < p.nrow_tiles; tw.next(), it += 2) {
             const int a = grp;
             const int rt = tw.rt, ct = tw.ct;
+            if (K2 && lane < 2 && bwk.rt < p.nrow_tiles) {
+                // this iteration's record build reads 80 bytes of factors:
+                // fetch them into L1 now, under the tile's epilogue
+                const int64_t j = 2 * static_cast<int64_t>(bwk.ct) + bb;
+                if (j < p.nb) {
+                    const char *f = reinterpret_cast<const char *>(
+                        p.factors + (p.shared_params ? 0 : j * 20));
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(f + 79 * lane));
+                }
+            }
             const int j = ct * 2 + b;
             const int row = rt * kBR + r;
             const uint32_t stg = base + Cfg::kStgOff + (pair * Cfg::kStgBufs + slot) * Cfg::kStgBytes;
@@ -603,6 +579,10 @@ __global__ void __launch_bounds__(K2 ? kThreadsK2 : kThreadsU, 1)
                 }
             }
             slot = slot == Cfg::kStgBufs - 1 ? 0 : slot + 1;
+            if (K2 && bwk.rt < p.nrow_tiles) {
+                build(bwk.ct, static_cast<int>(it % STAGES), ok);
+                bwk.next();
+            }
         }
         if (b == 0 && lane == 0) bulk_wait_group_all();
         if (at_leader) bulk_wait_group_all();
@@ -685,7 +665,7 @@ kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, const CUt
 {
     using Cfg = UCfg<STAGES>;
     auto kern = quant_umma_kernel<STAGES, DEBUG, DUAL, K2>;
-    constexpr int threads = K2 ? kThreadsK2 : kThreadsU;
+    constexpr int threads = kThreadsU;
     static USlot slot;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KQ_ERR_CUDA;
