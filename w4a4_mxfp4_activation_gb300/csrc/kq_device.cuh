@@ -170,22 +170,6 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// Barrier over `count` threads (whole, converged warps) with id `id` that
-// also returns, to every participant, whether v was true in all of them.
-__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool v)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %3, 0;\n\t"
-        "bar.red.and.pred p, %1, %2, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(id), "r"(count), "r"(static_cast<uint32_t>(v))
-        : "memory");
-    return r != 0;
-}
-
 // L2 policy for data read exactly once (the activations): evict first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {

@@ -204,36 +204,42 @@ __device__ __forceinline__ void store_scale_u(const QuantParams &p, int64_t row,
 // entries of K_j -- rows 8 g .. 8 g + 7, column c -- as the three bf16 terms,
 // written into a tile's record area in the MMA operand layout (see
 // umma_records_kernel).  Entries by eq. (12), K_j[r][c] =
-// prod_k G_k[bit_{5-k}(r)][bit_{5-k}(c)], as fp32 products; each fp32 value
-// splits exactly into hi + mid + lo (three 8-bit significands).  The eight
-// entries of a term form one 16-byte row of a core matrix; a warp with
-// c = lane fills 4 x 128 contiguous bytes per term (no bank conflicts).
-__device__ __forceinline__ void build_record_rows(uint32_t rec, const float4 (&G)[5], int c, int g)
+// prod_k G_k[bit_{5-k}(r)][bit_{5-k}(c)], as fp32 products.  Each fp32 value
+// k splits exactly into three bf16 terms by truncation: hi = the top 16 bits
+// of k, mid = the top 16 bits of k - hi (exact), lo = k - hi - mid (exact,
+// and at most 8 significant bits, so exact in bf16).  The eight entries of a
+// term form one 16-byte row of a core matrix; a warp with c = lane fills
+// 4 x 128 contiguous bytes per term (no bank conflicts).
+__device__ __forceinline__ void build_record_rows(uint32_t rec, const float *__restrict__ f, int c,
+                                                  int g)
 {
-    float col[5][2];            // G_k[row][bit_{4-k}(c)], k = 0..4 for G1..G5
+    // the ten factor entries column c needs: G_k[row][bit_{4-k}(c)], k = 0..4
+    // for G1..G5 (f holds the block's raw factors, [5][2][2])
+    float col[5][2];
 #pragma unroll
     for (int k = 0; k < 5; ++k) {
         const int bit = (c >> (4 - k)) & 1;
-        col[k][0] = sel2x2(G[k], 0, bit);
-        col[k][1] = sel2x2(G[k], 1, bit);
+        col[k][0] = __ldg(f + 4 * k + bit);
+        col[k][1] = __ldg(f + 4 * k + 2 + bit);
     }
     // r = 8 g + i: bit 4 of r = g >> 1, bit 3 = g & 1, bits 2..0 = i (g is a
     // run-time value: selects, not an indexed array, keep col in registers)
     const float P = ((g >> 1) ? col[0][1] : col[0][0]) * ((g & 1) ? col[1][1] : col[1][0]);
+    const float2 P2 = make_float2(P, P), c4 = make_float2(col[4][0], col[4][1]);
     uint32_t w[3][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float k0 = P * (col[2][q >> 1] * (col[3][q & 1] * col[4][0]));
-        const float k1 = P * (col[2][q >> 1] * (col[3][q & 1] * col[4][1]));
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(k0, k1);
-        const float2 hf = __bfloat1622float2(hi);
-        const float r0 = k0 - hf.x, r1 = k1 - hf.y;              // exact
-        const __nv_bfloat162 mid = __floats2bfloat162_rn(r0, r1);
-        const float2 mf = __bfloat1622float2(mid);
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(r0 - mf.x, r1 - mf.y);
-        w[0][q] = *reinterpret_cast<const uint32_t *>(&hi);
-        w[1][q] = *reinterpret_cast<const uint32_t *>(&mid);
-        w[2][q] = *reinterpret_cast<const uint32_t *>(&lo);
+    for (int q = 0; q < 4; ++q) {       // entries i = 2q, 2q + 1: bit 0 of i = G5's row
+        const float s = col[2][q >> 1] * col[3][q & 1];
+        const float2 kv = __fmul2_rn(P2, __fmul2_rn(make_float2(s, s), c4));
+        const uint32_t b0 = __float_as_uint(kv.x), b1 = __float_as_uint(kv.y);
+        const float2 hi = make_float2(__uint_as_float(b0 & 0xffff0000u), __uint_as_float(b1 & 0xffff0000u));
+        const float2 r = __fadd2_rn(kv, make_float2(-hi.x, -hi.y));                 // exact
+        const uint32_t m0 = __float_as_uint(r.x) & 0xffff0000u, m1 = __float_as_uint(r.y) & 0xffff0000u;
+        const float2 lo = __fadd2_rn(r, make_float2(-__uint_as_float(m0), -__uint_as_float(m1)));  // exact
+        // element 2q in the low half of each word
+        w[0][q] = __byte_perm(b0, b1, 0x7632);
+        w[1][q] = __byte_perm(m0, m1, 0x7632);
+        w[2][q] = __byte_perm(__float_as_uint(lo.x), __float_as_uint(lo.y), 0x7632);
     }
     // step h = g >> 1 (input channels 16 h..), core column g & 1, row c % 8
     const uint32_t off = rec + (g >> 1) * 3072 + (g & 1) * 128 + (c & 7) * 16;
@@ -309,7 +315,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         tma_prefetch_desc(&tmQ);              // earlier grids
         if (DUAL) tma_prefetch_desc(&tmAT);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, K2 ? 2 : 1);     // K2: TMA bytes + the record builders
+            // K2: the producer's TMA bytes and the 8 record-building warps
+            mbar_init(bar_full + 8 * s, K2 ? 1 + kEpiWarps / 2 : 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -421,30 +428,26 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         // builds tile it + STAGES into the same stage (the first STAGES / 2
         // of its tiles before the loop).  Warp (e & 7) writes block
         // (e & 7) >> 2, rows 8 ((e & 7) & 3) .. + 7, lane = output channel.
-        // The group then arrives on the stage's full barrier beside the
-        // producer's TMA bytes -- unless a wait ran out in one of its warps
-        // (the stage might then still be read), in which case no warp
-        // arrives and the tile's MMAs time out in turn.
+        // Each warp then arrives on the stage's full barrier (which counts
+        // the producer and these 8 warps) -- unless one of its own waits ran
+        // out (the stage might then still be read), in which case the phase
+        // never completes and the tile's MMAs time out in turn.
         TileWalk bwk = tw;                    // the next tile whose records to build
         const int bb = (e & 7) >> 2, bg = (e & 7) & 3;
         auto build = [&](int ct, int s, bool can) {
             const int64_t j = 2 * static_cast<int64_t>(ct) + bb;
-            if (can && j < p.nb) {
-                const float *g = p.factors + (p.shared_params ? 0 : j * 20);
-                float4 G[5];
-#pragma unroll
-                for (int k = 0; k < 5; ++k) G[k] = ldg_nc_f4(g + 4 * k);
-                build_record_rows(base + s * Cfg::kStageBytes + Cfg::kBOff + bb * Cfg::kRecBytes, G,
-                                  lane, bg);
-            }
+            if (can && j < p.nb)
+                build_record_rows(base + s * Cfg::kStageBytes + Cfg::kBOff + bb * Cfg::kRecBytes,
+                                  p.factors + (p.shared_params ? 0 : j * 20), lane, bg);
             fence_proxy_async_smem();
-            if (named_barrier_and(9 + grp, kEpiThreads / 2, can) && (e & 7) == 0 && lane == 0)
-                mbar_arrive(bar_full + 8 * s);
+            __syncwarp();
+            if (can && lane == 0) mbar_arrive(bar_full + 8 * s);
         };
         if (K2) {
             for (int k = 0; k < STAGES / 2 && bwk.rt < p.nrow_tiles; ++k, bwk.next())
                 build(bwk.ct, grp + 2 * k, true);
         }
+
         for (; tw.rt < p.nrow_tiles; tw.next(), it += 2) {
             const int a = grp;
             const int rt = tw.rt, ct = tw.ct;
