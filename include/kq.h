@@ -116,14 +116,15 @@ typedef enum {
  *   K_expanded device, output of kq_expand_blocks(..., KQ_K_BF16X3, ...), or
  *              NULL.  With K_expanded != NULL the transform runs on the
  *              tensor cores (tcgen05.mma, fp32 accumulation in TMEM) against
- *              the dense 32x32 K_j as three bf16 terms -- the fastest path
- *              (when factors are given as well, layers of fewer than 2^21
- *              elements take the butterfly below, faster there);
- *              otherwise, with factors != NULL, the five 2x2 factors are
- *              applied as an in-register butterfly on the CUDA cores; with
- *              both NULL the transform is the identity (the bare quantizer,
- *              "Q4" of [KQ] Tables 3 and 4).  Both paths compute y to about
- *              fp32 precision (|error| <= 2^-16 * sum_r |a_r K_rc|).
+ *              the dense 32x32 K_j as three bf16 terms -- the fastest path.
+ *              Otherwise, with factors != NULL, the same tensor-core kernel
+ *              builds the three bf16 terms of each K_j itself, from the raw
+ *              factors (eq. 12 as fp32 products, [KQ] Sec. 3.5.1 "K2": no
+ *              expanded blocks in memory); with both NULL the transform is
+ *              the identity (the bare quantizer, "Q4" of [KQ] Tables 3 and
+ *              4).  Both paths compute y to about fp32 precision (|error| <=
+ *              2^-16 * sum_r |a_r K_rc|); the CUDA-core butterfly on the raw
+ *              factors is kq_quantize_mxfp4_ex(..., KQ_TRANSFORM_KRON, ...).
  *   q, ldq     device, packed codes [m][ldq] (written)
  *   sf         device, scales in sf_layout (written; kq_sf_bytes() bytes)
  *   y_debug    device fp32 [m][d] or NULL: if given, receives y = a . K_j
@@ -163,8 +164,9 @@ KQ_API kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d,
  *   factors     device fp32 [5][2][2]: the shared G1..G5, or NULL
  *   K_expanded  device, kq_expand_blocks(factors, 1, KQ_K_BF16X3, ...)
  *               (kq_expanded_bytes(1, KQ_K_BF16X3) bytes), or NULL; with it
- *               the transform runs on the tensor cores, otherwise the
- *               butterfly applies `factors`.  One of the two is required
+ *               the tensor cores read that record for every block,
+ *               otherwise they build it from `factors` (the K2 form of
+ *               kq_quantize_mxfp4).  One of the two is required
  *               (KQ_ERR_NULL).
  *   other arguments as kq_quantize_mxfp4; the result equals
  *   kq_quantize_mxfp4 given the set repeated d/32 times.

@@ -63,8 +63,10 @@ def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None
         return kq.kq_quantize_mxfp4(A, d, factors=dev(param_gpu), layout=layout, y_debug=y_debug,
                                     variant=kq.VARIANT_K2, q=q, sf=sf)
     if kind == "kron":
+        # the CUDA-core butterfly (the default from raw factors is K2)
         return kq.kq_quantize_mxfp4(A, d, factors=dev(param_gpu), layout=layout, y_debug=y_debug,
-                                    variant=variant, q=q, sf=sf)
+                                    variant=kq.VARIANT_BUTTERFLY if variant is None else variant,
+                                    q=q, sf=sf)
     if kind == "identity":
         return kq.kq_quantize_mxfp4(A, d, layout=layout, y_debug=y_debug, q=q, sf=sf)
     if kind == "diag":
@@ -773,13 +775,14 @@ def test_w4a4_gemm_variants_agree_on_quantizer_output():
 SHARED_SHAPES = [(256, 1152), (300, 2240), (7, 96), (129, 5600)]
 
 
-@pytest.mark.parametrize("path", ["umma", "butterfly"])
+@pytest.mark.parametrize("path", ["umma", "k2"])
 @pytest.mark.parametrize("layout", [0, 1])
 @pytest.mark.parametrize("m,d", SHARED_SHAPES, ids=[f"{m}x{d}" for m, d in SHARED_SHAPES])
 def test_shared_factors(m, d, layout, path):
     """One factor set for every block: parity with the oracle given the set
     repeated d/32 times (rules i-iii), and the same bytes as the per-block
-    entry point given that repeated set."""
+    entry point given that repeated set (the expanded record, or the raw
+    factors the K2 kernel builds it from)."""
     nb = d // 32
     A_bits = synth.activations(m, d, 1700 + m, "sana")
     lu = synth.lu_params(1, 1701)
@@ -797,7 +800,7 @@ def test_shared_factors(m, d, layout, path):
         q, sf, y = kq.kq_quantize_mxfp4_shared(A, d, factors=dev(F1[0]), layout=layout, y_debug=True)
         Frep = np.ascontiguousarray(np.broadcast_to(F1, (nb, 5, 2, 2)))
         q2, sf2, _ = kq.kq_quantize_mxfp4(A, d, factors=dev(Frep), layout=layout,
-                                          variant=kq.VARIANT_BUTTERFLY)
+                                          variant=kq.VARIANT_K2)
     nbytes = kq.kq_sf_bytes(m, d, layout)
     assert np.array_equal(np_(q), np_(q2)) and np.array_equal(np_(sf)[:nbytes], np_(sf2)[:nbytes])
     parity.check(A_bits, d, "kron", np.ascontiguousarray(Fo), layout, np_(q), np_(sf), np_(y))
@@ -853,21 +856,22 @@ def test_ex_bf16_matches_entry_points():
         assert torch.equal(q1, q2) and torch.equal(s1, s2)
 
 
-@pytest.mark.parametrize("m,d,expect", [(256, 1152, "butterfly"), (1024, 1152, "butterfly"),
-                                        (1024, 3072, "umma")])
-def test_default_dispatch_with_both_factor_forms(m, d, expect):
-    """kq_quantize_mxfp4 given the raw factors and the expanded blocks runs
-    the butterfly below 2^21 elements and the tensor cores above: its bytes
-    equal those of that variant called explicitly."""
+@pytest.mark.parametrize("m,d", [(256, 1152), (1024, 1152), (1024, 3072), (4608, 3072)])
+def test_default_dispatch(m, d):
+    """kq_quantize_mxfp4 runs the records path whenever the expanded blocks
+    are given (with or without the raw factors), and K2 when only the raw
+    factors are: its bytes equal those of that variant called explicitly."""
     A_bits = synth.activations(m, d, 2100 + m, "flux")
     A = to_bf16(A_bits)
     F, _ = lib_factors(d // 32, 2101)
     Fd = dev(F)
     KX = kq.kq_expand_blocks(Fd, kq.KQ_K_BF16X3)
-    q, sf, _ = kq.kq_quantize_mxfp4(A, d, factors=Fd, K_expanded=KX, layout=1)
-    v = kq.VARIANT_BUTTERFLY if expect == "butterfly" else kq.VARIANT_UMMA
-    q2, sf2, _ = kq.kq_quantize_mxfp4(A, d, factors=Fd, K_expanded=KX, layout=1, variant=v)
-    assert torch.equal(q, q2) and torch.equal(sf, sf2)
+    want_r = kq.kq_quantize_mxfp4(A, d, K_expanded=KX, layout=1, variant=kq.VARIANT_UMMA)
+    want_k2 = kq.kq_quantize_mxfp4(A, d, factors=Fd, layout=1, variant=kq.VARIANT_K2)
+    for got, want in ((kq.kq_quantize_mxfp4(A, d, factors=Fd, K_expanded=KX, layout=1), want_r),
+                      (kq.kq_quantize_mxfp4(A, d, K_expanded=KX, layout=1), want_r),
+                      (kq.kq_quantize_mxfp4(A, d, factors=Fd, layout=1), want_k2)):
+        assert torch.equal(got[0], want[0]) and torch.equal(got[1], want[1])
 
 
 # ------------------------------------------ a pipeline wait that runs out --

@@ -287,16 +287,14 @@ kq_status quantize_variant(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
 }
 
 // The fastest implementation the arguments allow: tcgen05 on the expanded
-// blocks, else the butterfly on the raw factors, else identity.  With both
-// given, layers below 2^21 elements take the butterfly: there every kernel
-// is latency-bound and the tensor-core pipeline's longer first tile costs
-// more than its arithmetic saves (measured on GB300: butterfly faster up to
-// 1024 x 1152, tcgen05 from 1024 x 3072 on).
-int default_variant(int64_t m, int64_t d, const float *factors, const void *K_expanded)
+// blocks, else tcgen05 building the blocks from the raw factors (K2), else
+// identity.  Measured on GB300 (steady state, FLUX-shaped activations): the
+// records path is the fastest on every shape from 256 x 1152 to 65536 x
+// 12288; from the raw factors alone, K2 beats the CUDA-core butterfly from
+// 1024 x 3072 up (32.0 against 36.2 us at 4608 x 12288) and ties it below.
+int default_variant(const float *factors, const void *K_expanded)
 {
-    int variant = K_expanded != nullptr ? 3 : (factors != nullptr ? 0 : 2);
-    if (variant == 3 && factors != nullptr && m * d < (int64_t(1) << 21)) variant = 0;
-    return variant;
+    return K_expanded != nullptr ? 3 : (factors != nullptr ? 4 : 2);
 }
 
 // The tcgen05 kernel's default wait limit and no skipped tile.
@@ -330,7 +328,7 @@ kq_status kq_quantize_mxfp4(const uint16_t *A, int64_t m, int64_t d, int64_t lda
                             cudaStream_t stream)
 {
     return quantize_variant(A, m, d, lda, factors, K_expanded, q, ldq, sf, sf_layout, y_debug,
-                            default_variant(m, d, factors, K_expanded), hook_params(), stream);
+                            default_variant(factors, K_expanded), hook_params(), stream);
 }
 
 kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d, int64_t lda,
@@ -448,9 +446,10 @@ kq_status kq_quantize_mxfp4_shared(const uint16_t *A, int64_t m, int64_t d, int6
     QuantParams p;
     fill_quant_params(p, m, d, 128, q, ldq, sf, sf_layout, y_debug);
     p.shared_params = 1;
-    if (K_expanded != nullptr) return launch_quant_umma(A, lda, K_expanded, p, nullptr, 0, stream);
     p.factors = factors;
-    return launch_quant_tma(kKron, A, lda, p, stream);
+    // the records path on the record, else K2 building every block's
+    // records from the one factor set
+    return launch_quant_umma(A, lda, K_expanded, p, nullptr, 0, stream);
 }
 
 kq_status kq_quantize_mxfp4_ex(const uint16_t *A, kq_in_format in_format, int64_t m, int64_t d,
