@@ -75,8 +75,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=40000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--variant", choices=("butterfly", "umma"), default="umma",
-                    help="KroQuant kernel: tcgen05 (umma, default) or the CUDA-core butterfly")
+    ap.add_argument("--variant", choices=("butterfly", "umma", "k2"), default="umma",
+                    help="KroQuant kernel: tcgen05 on expanded records (umma, default), "
+                         "tcgen05 building the records from the raw factors (k2), or the "
+                         "CUDA-core butterfly")
     ap.add_argument("--isolated", type=int, default=20,
                     help="single-launch measurements of the dominant layer (isolated_launch)")
     ap.add_argument("--no-baselines", action="store_true",
@@ -490,6 +492,9 @@ def run_ours(args, dist: Dist):
         elif kind == "umma":
             kq.kq_quantize_mxfp4(A[li][s], d, K_expanded=KX[li], layout=layout, q=Q[li][s],
                                  sf=SF[li][s], stream=stream)
+        elif kind == "k2":
+            kq.kq_quantize_mxfp4(A[li][s], d, factors=F[li], layout=layout, q=Q[li][s],
+                                 sf=SF[li][s], variant=kq.VARIANT_K2, stream=stream)
         elif kind == "dual":
             kq.kq_quantize_mxfp4_dual(A[li][s], KX[li], d, layout=layout, q=Q[li][s],
                                       sf=SF[li][s], at=AT[li][s], stream=stream)
@@ -666,13 +671,13 @@ def run_ours(args, dist: Dist):
     iso_diag_ms = None
     if not args.no_baselines:
         nb_steps = max(3, min(K, 4000))
-        others = [v for v in ("butterfly", "umma") if v != args.variant]
+        others = [v for v in ("butterfly", "umma", "k2") if v != args.variant]
         for kind in (*others, "diag", "hadamard", "identity"):
             bms, _, _, g = timed(kind, nb_steps, W)
             if kind == "diag":
                 iso_diag_ms = isolated("diag", g, max(3, args.isolated))
             del g
-            name = f"kroquant_{kind}" if kind in ("butterfly", "umma") else kind
+            name = f"kroquant_{kind}" if kind in ("butterfly", "umma", "k2") else kind
             baselines[name] = round(STEP_BYTES * nb_steps / (dist.max(bms) * 1e-3) / 1e9, 2)
     clock.stop()
     # NVML answers in tens of ms, so few samples fall inside a timed region of
@@ -837,7 +842,8 @@ def run_profile_case(args):
     KX = (kq.kq_expand_blocks(F, kq.KQ_K_BF16X3)
           if args.variant == "umma" or args.profile == "dual" else None)
     at = torch.empty((m, d), dtype=torch.bfloat16, device="cuda") if args.profile == "dual" else None
-    variant = {"butterfly": kq.VARIANT_BUTTERFLY, "umma": kq.VARIANT_UMMA}[args.variant]
+    variant = {"butterfly": kq.VARIANT_BUTTERFLY, "umma": kq.VARIANT_UMMA,
+               "k2": kq.VARIANT_K2}[args.variant]
     if args.profile == "gemm":
         n = args.n
         qa, sfa, qw, sfw, _, _ = gemm_case(m, n, d, 9000, "cuda")
