@@ -53,7 +53,7 @@ def lib_factors(nb, seed, sign=+1):
 
 
 def run_kind(kind, A_bits, d, layout, param_gpu=None, y_debug=True, variant=None, q=None, sf=None):
-    A = to_bf16(A_bits)
+    A = A_bits if isinstance(A_bits, torch.Tensor) else to_bf16(A_bits)
     if kind == "kron_umma":
         records = kq.kq_expand_blocks(dev(param_gpu), kq.KQ_K_BF16X3)
         return kq.kq_quantize_mxfp4(A, d, K_expanded=records, layout=layout, y_debug=y_debug,
@@ -313,6 +313,88 @@ def test_ragged_shapes_with_pitches_and_canaries(m, d, kind):
             off = ((i // 128) * ncb + kb // 4) * 512 + (i % 32) * 16 + ((i % 128) // 32) * 4 + kb % 4
             full[off.ravel()] = True
             assert (np_(sf)[~full] == 0).all()
+
+
+# ------------------------------------------------------------ maximum sizes --
+
+MAX_ROWS = 0x7FFFFFFF          # the largest m the entry points accept
+PERIOD = 4096                  # rows of the seeded base that every row repeats
+
+
+@pytest.fixture(scope="module")
+def max_rows_input():
+    """A bf16 [2^31 - 1, 32] input (137 GB) whose row r is row r % 4096 of a
+    seeded base, built on the device."""
+    d = 32
+    free, _ = torch.cuda.mem_get_info()
+    if free < 200e9:
+        pytest.skip(f"needs about 190 GB of free device memory, {free / 1e9:.0f} GB free")
+    base_bits = synth.activations(PERIOD, d, 9100, "flux")
+    A = to_bf16(base_bits).repeat(-(-MAX_ROWS // PERIOD), 1)[:MAX_ROWS]
+    yield base_bits, A
+    del A
+    torch.cuda.empty_cache()
+
+
+def _periodic_equal(got, pattern, what):
+    """got (1-D uint8 device tensor) equals pattern repeated, chunk by chunk."""
+    reps = max(1, (256 << 20) // pattern.numel())
+    ref = pattern.repeat(reps)
+    step = ref.numel()
+    for s in range(0, got.numel(), step):
+        e = min(got.numel(), s + step)
+        assert torch.equal(got[s:e], ref[:e - s]), f"{what}: bytes {s}..{e} differ from the base"
+
+
+MAX_ROW_CASES = [("kron_umma", 0), ("kron_umma", 1), ("kron_k2", 0), ("kron_k2", 1), ("kron", 0),
+                 ("kron", 1), ("diag", 0), ("diag", 1), ("hadamard", 0), ("identity", 1)]
+
+
+@pytest.mark.parametrize("kind,layout", MAX_ROW_CASES, ids=[f"{k}-{l}" for k, l in MAX_ROW_CASES])
+def test_maximum_rows(max_rows_input, kind, layout):
+    """m = 2^31 - 1 rows, the entry points' upper limit (row offsets past
+    2^31 bytes in every output, 2^24 row tiles).  The 4096-row base is
+    checked against the oracle under rules i-iii; every row of the full
+    launch must then equal the base launch's output for row r % 4096, bit
+    for bit, and in the tiled scale layout the padding row of the last
+    128-row tile must read 0."""
+    base_bits, A = max_rows_input
+    d, nb = 32, 1
+    pg, po = params_for(kind, nb, d, 9101)
+    qb, sfb, yb = run_kind(kind, base_bits, d, layout, pg)
+    parity.check(base_bits, d, oracle_kind(kind), po, layout, np_(qb), np_(sfb), np_(yb))
+    q, sf, _ = run_kind(kind, A, d, layout, pg, y_debug=None)
+    torch.cuda.synchronize()
+    _periodic_equal(q.view(-1), qb.view(-1), "codes")
+    if layout == 0:
+        _periodic_equal(sf.view(-1), sfb.view(-1), "scales")
+    else:
+        # 512 bytes per 128-row tile; the base spans 32 tiles, the launch
+        # 2^24, the last of which holds 127 rows and one padding row
+        assert sf.numel() == (MAX_ROWS + 1) // 128 * 512
+        _periodic_equal(sf.view(-1)[:-512], sfb.view(-1), "scales")
+        last = sfb.view(-1)[-512:].clone()
+        last[31 * 16 + 3 * 4] = 0                  # row 127 of the tile, block 0
+        assert torch.equal(sf.view(-1)[-512:], last)
+    del q, sf
+    torch.cuda.empty_cache()
+
+
+WIDE = (300, (1 << 20) + 96)   # 2^20 + 96 channels: 32771 blocks (odd, not a multiple of 4)
+
+
+@pytest.mark.parametrize("kind", ["kron_umma", "kron_k2", "kron", "diag", "hadamard", "identity"])
+def test_widest_rows(kind):
+    """Rows of 2^20 + 96 channels (column coordinates past 2^20, 32771
+    blocks, 201 MB of operand records), every element against the oracle in
+    both scale layouts."""
+    m, d = WIDE
+    A_bits = synth.activations(m, d, 9200, "flux")
+    pg, po = params_for(kind, d // 32, d, 9201)
+    ref = parity.reference(A_bits, d, oracle_kind(kind), po)
+    for layout in (0, 1):
+        q, sf, y = run_kind(kind, A_bits, d, layout, pg)
+        parity.check(A_bits, d, oracle_kind(kind), po, layout, np_(q), np_(sf), np_(y), ref=ref)
 
 
 def test_special_values():
