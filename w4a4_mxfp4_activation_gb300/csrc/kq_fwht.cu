@@ -9,22 +9,24 @@
 // couples every channel of a row with every other, so a row must be complete
 // on chip before any output block is known.
 //
-// Layout of the work: a persistent CTA of 512 threads transforms 16384
-// elements per iteration (16384 / d rows).  The butterfly stages of H_d act on
-// one bit of the channel index each and commute, so they run in the order
-// that keeps shared-memory traffic lowest:
-//   1. the iteration's rows arrive by 16-byte cp.async copies into a bf16
-//      staging tile in natural order (consecutive threads, consecutive
-//      chunks), issued during the previous iteration;
-//   2. the stages with pairs 32 apart and more run as passes: a thread
-//      gathers r values at the pass's stride (lanes at consecutive channels,
-//      so every access is conflict-free), applies log2(r) stages in registers
-//      and writes them to a shared fp32 buffer padded to 36 floats per 32 --
-//      the first pass reads the bf16 staging tile, a second one (d > 1024)
-//      the fp32 buffer;
-//   3. each thread then reads one 32-channel block of a row, applies the five
-//      stages with pairs 1..16 apart in registers, multiplies by 1/sqrt(d),
-//      quantizes and stores 16 bytes of codes and one scale byte.
+// Layout of the work: a persistent CTA of 512 threads (two per SM)
+// transforms 16384 elements per iteration (16384 / d rows).  Bit b of an
+// element's index within the iteration is bit b of its channel for b < log2 d
+// and a row bit above; the butterfly stages of H_d act on one channel bit
+// each and commute, so they run in three register phases, 32 values per
+// thread, joined by two exchanges through a shared fp32 buffer (padded to 36
+// floats per 32, so every access pattern below is free of bank conflicts):
+//   A. channel bits 0 and 10..13: the thread reads 16 adjacent bf16 (or fp16)
+//      pairs 1024 elements apart from the staging tile (the iteration's rows,
+//      copied in natural order by 16-byte cp.async during the previous
+//      iteration), applies those stages and stores the 16 pairs;
+//   B. bits 5..9: 32 values 32 apart (a warp reads 32 consecutive floats);
+//   C. bits 1..4, then the quantizer: the thread's own 32-channel block, read
+//      as 8 float4; it scales by 1/sqrt(d), quantizes and stores 16 bytes of
+//      codes and one scale byte.
+// Values travel as fp32 pairs, so every stage whose partner is not the other
+// half of a pair is one packed fp32x2 add and one packed fused multiply-add
+// (x + y, x - y) for two butterflies.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -39,8 +41,8 @@ namespace {
 constexpr int kFThreads = 512;
 constexpr int kFElems = 16384;                       // elements per iteration
 constexpr int kFSmemFloats = kFElems + kFElems / 8;  // padded: 36 floats per 32
-// bf16 staging of the next iteration's rows, natural order: element e of the
-// iteration (row_local * d + channel) at byte 2 e
+// 16-bit staging of the next iteration's rows, natural order: element e of
+// the iteration (row_local * d + channel) at byte 2 e
 constexpr int kFStageOff = kFSmemFloats * 4;
 constexpr int kFSmemBytes = kFStageOff + kFElems * 2;
 
@@ -53,60 +55,25 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 __device__ __forceinline__ int pad(int e) { return e + 4 * (e >> 5); }
 
-// In-place unnormalised Walsh-Hadamard transform of n = 2^k values (Sylvester
-// order): butterflies (x, y) -> (x + y, x - y) over pairs h = 1, 2, ..., n/2 apart.
+// Butterflies (x, y) -> (x + y, x - y) on two pairs at once.
+__device__ __forceinline__ void bfly2(float2 &a, float2 &b)
+{
+    const float2 x = a;
+    a = __fadd2_rn(x, b);
+    b = __ffma2_rn(b, make_float2(-1.0f, -1.0f), x);
+}
+
+// Butterfly stages on the pair-index bits h = 1, 2, 4, ... < N of v[0..N)
+// that are set in `mask` (a compile-time constant at every call).
 template <int N>
-__device__ __forceinline__ void wht_regs(float (&v)[32])
+__device__ __forceinline__ void bfly_stages(float2 *v, int mask)
 {
 #pragma unroll
     for (int h = 1; h < N; h *= 2)
+        if (mask & h)
 #pragma unroll
-        for (int j = 0; j < N; ++j)
-            if ((j & h) == 0) {
-                const float x = v[j], z = v[j + h];
-                v[j] = x + z;
-                v[j + h] = x - z;
-            }
-}
-
-// One pass over the stages with pairs S, 2S, ..., (R/2)S apart: groups of R
-// values at stride S; group g of a row = (lo, hi) with lo = g % S (the lanes
-// of a warp take consecutive lo, i.e. consecutive channels) and base
-// lo + hi * S * R.  FROM_STAGING: the values come from the 16-bit staging
-// tile (bf16, or fp16 when f16); they always go to the padded fp32 buffer.
-template <int D, int S, int R, bool FROM_STAGING>
-__device__ __forceinline__ void wht_pass(float *buf, const uint16_t *stg, int row_local, int tr,
-                                         bool f16)
-{
-    static_assert(S % 32 == 0, "pass strides are multiples of 32");
-    constexpr int kThreadsPerRow = D / 32;
-    constexpr int kGroupsPerThread = (D / R) / kThreadsPerRow;
-    static_assert(kGroupsPerThread >= 1, "every thread takes at least one group");
-#pragma unroll 1
-    for (int q = 0; q < kGroupsPerThread; ++q) {
-        const int g = tr + q * kThreadsPerRow;
-        const int e0 = row_local * D + (g % S) + (g / S) * S * R;
-        // S is a multiple of 32, so the padded index of e0 + k S is
-        // pad(e0) + k (S + S / 8)
-        float *pb = buf + pad(e0);
-        float v[32];
-        if constexpr (FROM_STAGING) {
-            const uint16_t *sb = stg + e0;
-            if (f16) {
-#pragma unroll
-                for (int k = 0; k < R; ++k) v[k] = __half2float(__ushort_as_half(sb[k * S]));
-            } else {
-#pragma unroll
-                for (int k = 0; k < R; ++k) v[k] = __uint_as_float(static_cast<uint32_t>(sb[k * S]) << 16);
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < R; ++k) v[k] = pb[k * (S + S / 8)];
-        }
-        wht_regs<R>(v);
-#pragma unroll
-        for (int k = 0; k < R; ++k) pb[k * (S + S / 8)] = v[k];
-    }
+            for (int k = 0; k < N; ++k)
+                if ((k & h) == 0) bfly2(v[k], v[k + h]);
 }
 
 template <int LOGD, bool DEBUG>
@@ -115,14 +82,15 @@ __global__ void __launch_bounds__(kFThreads, 2) fwht_quant_kernel(const uint16_t
 {
     constexpr int D = 1 << LOGD;
     constexpr int kRows = kFElems / D;               // rows per iteration
-    constexpr int kThreadsPerRow = D / 32;
-    constexpr int kChunksPerRow = D / 8;             // 16-byte chunks of a bf16 row
-    extern __shared__ float fbuf[];
-    uint16_t *stg = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(fbuf) + kFStageOff);
+    constexpr int kChunksPerRow = D / 8;             // 16-byte chunks of a 16-bit row
+    // which of the phase's index bits are channel bits (stages to apply):
+    // A: pair index k bit i = channel bit 10 + i; B: bit i = channel bit 5 + i
+    constexpr int kMaskA = LOGD >= 14 ? 15 : (LOGD > 10 ? (1 << (LOGD - 10)) - 1 : 0);
+    constexpr int kMaskB = LOGD >= 10 ? 31 : (1 << (LOGD - 5)) - 1;
+    extern __shared__ __align__(16) float fbuf[];
+    const uint8_t *stg = reinterpret_cast<const uint8_t *>(fbuf) + kFStageOff;
     grid_dependency_wait();
-    const int t = threadIdx.x;
-    const int row_local = t / kThreadsPerRow, tr = t % kThreadsPerRow;
-    const int b = tr;                                // the thread's 32-channel block in step 3
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const bool f16 = p.in_f16 != 0;
     const float inv = 1.0f / sqrtf(static_cast<float>(D));   // exact when d = 4^k
     const int64_t groups = (p.m_rows + kRows - 1) / kRows;
@@ -145,39 +113,65 @@ __global__ void __launch_bounds__(kFThreads, 2) fwht_quant_kernel(const uint16_t
         }
         cp_async_commit();
     };
+    const int ea = 2 * lane + 64 * warp;             // phase A: elements ea + 1024 k (+ 0, 1)
+    const int eb = lane + 1024 * warp;               // phase B: elements eb + 32 j
+    const int ec = 32 * t;                           // phase C: elements ec .. ec + 31
+    const int64_t row_c = ec >> LOGD;                // row of the thread's block in the tile
+    const int b = (ec & (D - 1)) >> 5;               // the block
     issue(blockIdx.x);
     for (int64_t grp = blockIdx.x; grp < groups; grp += gridDim.x) {
-        const int64_t row = grp * kRows + row_local;
         cp_async_wait_all();
-        __syncthreads();                             // every chunk of the tile has landed
-        // stages with pairs 32 apart and more: the first pass reads the staging tile
-        if constexpr (LOGD > 10) {
-            wht_pass<D, 1024, (1 << (LOGD - 10)), true>(fbuf, stg, row_local, tr, f16);   // 1024..8192
-            __syncthreads();
-            issue(grp + gridDim.x);                  // staging consumed: next tile in flight
-            wht_pass<D, 32, 32, false>(fbuf, stg, row_local, tr, f16);                    // 32..512
-        } else {
-            wht_pass<D, 32, (1 << (LOGD - 5)), true>(fbuf, stg, row_local, tr, f16);
-            __syncthreads();
-            issue(grp + gridDim.x);
-        }
-        __syncthreads();
-        // the thread's own block: stages with pairs 1..16 apart, then quantize
-        const int own = pad(row_local * D + b * 32);   // a multiple of 36: 16-byte aligned
-        const float4 *own4 = reinterpret_cast<const float4 *>(fbuf + own);
-        float v[32];
+        __syncthreads();   // the tile has landed; the last iteration's phase C is done with fbuf
+        // ---- phase A: channel bits 0, 10..13
+        {
+            const uint32_t *st32 = reinterpret_cast<const uint32_t *>(stg);
+            float2 v[16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float4 w = own4[k];
-            v[4 * k] = w.x;
-            v[4 * k + 1] = w.y;
-            v[4 * k + 2] = w.z;
-            v[4 * k + 3] = w.w;
+            for (int k = 0; k < 16; ++k) {
+                const uint32_t w = st32[(ea + 1024 * k) >> 1];
+                v[k] = f16 ? make_float2(f16_lo(w), f16_hi(w)) : make_float2(bf16_lo(w), bf16_hi(w));
+                v[k] = make_float2(v[k].x + v[k].y, v[k].x - v[k].y);          // bit 0
+            }
+            bfly_stages<16>(v, kMaskA);
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                *reinterpret_cast<float2 *>(fbuf + pad(ea + 1024 * k)) = v[k];
         }
-        wht_regs<32>(v);
+        __syncthreads();   // phase A's values are in fbuf; the staging tile is free
+        issue(grp + gridDim.x);                      // next tile in flight during B and C
+        // ---- phase B: channel bits 5..9 (pairs j, j + 16: bit 9 inside a pair)
+        {
+            float2 v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                v[j] = make_float2(fbuf[pad(eb + 32 * j)], fbuf[pad(eb + 32 * (j + 16))]);
+            bfly_stages<16>(v, kMaskB & 15);
+            if (kMaskB & 16) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = make_float2(v[j].x + v[j].y, v[j].x - v[j].y);
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                fbuf[pad(eb + 32 * j)] = v[j].x;
+                fbuf[pad(eb + 32 * (j + 16))] = v[j].y;
+            }
+        }
+        __syncthreads();   // phase B's values are in fbuf
+        // ---- phase C: channel bits 1..4 of the thread's block, then quantize
         float2 Y[16];
+        {
+            const float4 *own4 = reinterpret_cast<const float4 *>(fbuf + pad(ec));
 #pragma unroll
-        for (int k = 0; k < 16; ++k) Y[k] = make_float2(v[2 * k] * inv, v[2 * k + 1] * inv);
+            for (int k = 0; k < 8; ++k) {
+                const float4 w = own4[k];
+                Y[2 * k] = make_float2(w.x, w.y);
+                Y[2 * k + 1] = make_float2(w.z, w.w);
+            }
+            bfly_stages<16>(Y, 15);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) Y[k] = __fmul2_rn(Y[k], make_float2(inv, inv));
+        }
+        const int64_t row = grp * kRows + row_c;
         if (row < p.m_rows) {
             if (DEBUG && row < p.m) {
                 float *yd = p.y_debug + row * p.d + b * 32;
@@ -195,7 +189,6 @@ __global__ void __launch_bounds__(kFThreads, 2) fwht_quant_kernel(const uint16_t
                 p.sf[sf_blocked_offset(row, b, p.ncb)] = static_cast<uint8_t>(byte);
             }
         }
-        __syncthreads();                             // the buffer is reused next iteration
     }
     cp_async_wait_all();
 }
