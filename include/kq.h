@@ -158,8 +158,8 @@ KQ_API kq_status kq_quantize_mxfp4_dual(const uint16_t *A, int64_t m, int64_t d,
 
 /*
  * kq_quantize_mxfp4_shared -- kq_quantize_mxfp4 with one factor set shared
- * by every 32-channel block, K_j = K for all j ([KQ] Sec. 3.5.1 on K2: "many
- * column blocks share the same Kronecker factors", the case where storing
+ * by every 32-channel block, K_j = K for all j ([KQ] Sec. 3.5.1 on K2: the case where
+ * several column blocks use one set of Kronecker factors, so that storing
  * the transform per block is wasted).
  *   factors     device fp32 [5][2][2]: the shared G1..G5, or NULL
  *   K_expanded  device, kq_expand_blocks(factors, 1, KQ_K_BF16X3, ...)

@@ -418,7 +418,7 @@ KQO_EXPORT void kqo_encode_e2m1_array(const double *v, int64_t n, uint8_t *codes
 
 /* fp64 -> bf16 bit pattern, round to nearest with ties to even.  This is the
  * cast of the transformed activations to the 16-bit input dtype: [KQ] Sec.
- * 3.5.1 (K1 stores y "after casting to the input dtype") and App. D
+ * 3.5.1 (K1 writes y back in the 16-bit type of its input) and App. D
  * "Quantization" (the activations that feed the low-rank branch of eq. (11)
  * stay in 16 bits; bf16 for SANA and FLUX).
  * bf16: 1 sign, 8 exponent, 7 fraction bits.  A finite magnitude is
