@@ -321,11 +321,12 @@ MAX_ROWS = 0x7FFFFFFF          # the largest m the entry points accept
 PERIOD = 4096                  # rows of the seeded base that every row repeats
 
 
-@pytest.fixture(scope="module")
+@pytest.fixture
 def max_rows_input():
     """A bf16 [2^31 - 1, 32] input (137 GB) whose row r is row r % 4096 of a
     seeded base, built on the device."""
     d = 32
+    torch.cuda.empty_cache()              # blocks the previous case released
     free, _ = torch.cuda.mem_get_info()
     if free < 200e9:
         pytest.skip(f"needs about 190 GB of free device memory, {free / 1e9:.0f} GB free")
@@ -377,6 +378,48 @@ def test_maximum_rows(max_rows_input, kind, layout):
         last[31 * 16 + 3 * 4] = 0                  # row 127 of the tile, block 0
         assert torch.equal(sf.view(-1)[-512:], last)
     del q, sf
+    torch.cuda.empty_cache()
+
+
+LARGE_ROWS = (1 << 28) - 3      # at d = 128: 68.7 GB of bf16 input, 2^35 input bytes past 2^31
+
+
+@pytest.mark.parametrize("kind", ["fwht", "dual"])
+def test_large_rows_whole_row_and_dual(kind):
+    """The full-row FWHT and the dual kernel (codes, scales and the bf16 side
+    output A T) at 2^28 - 3 rows of 128 channels, a ragged last tile.  Every
+    row repeats row r % 4096 of a seeded base: the base launch is checked
+    against the oracle, and every row of the large launch must equal the
+    base launch's row bit for bit."""
+    m, d = LARGE_ROWS, 128
+    torch.cuda.empty_cache()
+    free, _ = torch.cuda.mem_get_info()
+    need = m * d * (2 + 0.5 + (2 if kind == "dual" else 0)) + m * 4 + 4e9
+    if free < need:
+        pytest.skip(f"needs about {need / 1e9:.0f} GB of free device memory, {free / 1e9:.0f} GB free")
+    base_bits = synth.activations(PERIOD, d, 9300, "flux")
+    base = to_bf16(base_bits)
+    A = base.repeat(-(-m // PERIOD), 1)[:m]
+    if kind == "fwht":
+        qb, sfb, yb = kq.kq_fwht_quantize_mxfp4(base, d, y_debug=True)
+        parity.check(base_bits, d, "fwht", None, 0, np_(qb), np_(sfb), np_(yb))
+        q, sf, _ = kq.kq_fwht_quantize_mxfp4(A, d)
+        pairs = [(q, qb), (sf, sfb)]
+    else:
+        pg, po = lib_factors(d // 32, 9301)
+        records = kq.kq_expand_blocks(dev(pg), kq.KQ_K_BF16X3)
+        qb, sfb, atb, yb = kq.kq_quantize_mxfp4_dual(base, records, d, y_debug=True)
+        parity.check(base_bits, d, "kron", po, 0, np_(qb), np_(sfb), np_(yb))
+        parity.check_side_output(base_bits, d, "kron", po,
+                                 np_(atb.view(torch.int16)).view(np.uint16), np_(yb))
+        q, sf, at, _ = kq.kq_quantize_mxfp4_dual(A, records, d)
+        pairs = [(q, qb), (sf, sfb), (at.view(torch.uint8), atb.view(torch.uint8))]
+    torch.cuda.synchronize()
+    for name, (got, ref) in zip(("codes", "scales", "side output"), pairs):
+        _periodic_equal(got.reshape(-1)[:m * ref.numel() // PERIOD], ref.reshape(-1), name)
+    del A, q, sf, pairs
+    if kind == "dual":
+        del at
     torch.cuda.empty_cache()
 
 
