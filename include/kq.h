@@ -287,8 +287,8 @@ KQ_API kq_status kq_layer_error(const float *c, int64_t ldc, const float *c_ref,
                                 int64_t m, int64_t n, double *out, cudaStream_t stream);
 
 /*
- * kq_expand_blocks -- [KQ] Sec. 3.5.1 K1 ("each 32x32 block K_j is
- * materialized"): expand the raw factors into dense blocks by eq. (12),
+ * kq_expand_blocks -- [KQ] Sec. 3.5.1 K1 (the dense 32x32 blocks are kept
+ * in device memory): expand the raw factors into dense blocks by eq. (12),
  * computed in fp64 and then rounded to the requested format.
  *   factors  device fp32 [nb][5][2][2]
  *   nb       number of 32-channel blocks (> 0)
