@@ -517,6 +517,33 @@ def test_expand_blocks_fp32():
     assert np.array_equal(K.view(np.uint32), ref.view(np.uint32))
 
 
+def bf16_bits_to_f64(b):
+    return (np.asarray(b, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def test_expand_blocks_bf16x3_records():
+    """The tensor-core operand records (KQ_K_BF16X3), decoded from their
+    documented layout, hold for every entry of the oracle's fp64 K_j
+    (eq. 12) the three bf16 terms hi = RN(K), mid = RN(K - hi), lo = RN(K -
+    hi - mid), bit for bit (the oracle's fp64 -> bf16 rounding)."""
+    nb = 70
+    Fg, Fo = lib_factors(nb, 32)
+    rec = np_(kq.kq_expand_blocks(dev(Fg), kq.KQ_K_BF16X3))
+    assert rec.size == nb * 6144
+    body = rec.view(np.uint16).reshape(nb, 3072)
+    t, r, c = np.meshgrid(np.arange(3), np.arange(32), np.arange(32), indexing="ij")
+    h, k, n = r // 16, r % 16, 32 * t + c
+    off = h * 3072 + (n // 8) * 256 + (k // 8) * 128 + (n % 8) * 16 + (k % 8) * 2
+    got = body[:, off // 2]                                  # [nb][term][row][col]
+    K = O.expand_blocks(Fg.astype(np.float64))
+    rem = K.copy()
+    for term in range(3):
+        want = O.round_bf16(rem)
+        assert np.array_equal(got[:, term], want), term
+        rem = rem - bf16_bits_to_f64(want)
+    assert np.all(np.abs(rem) <= 2.0 ** -24 * np.abs(K))
+
+
 def test_blocked_layout_against_library_gemm():
     """P8: the 128x4 scale tiles, handed to a library's block-scaled GEMM,
     give the fp64 product of our own dequantized operands: the library's

@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         if (K2) {
         } else if (p.shared_params) {
             // one operand record for every block: a copy of it per block slot
-            for (uint32_t off = 0; off < rbytes; off += Cfg::kRecBytes)
+            for (uint32_t off = 0; off + Cfg::kRecBytes <= rbytes; off += Cfg::kRecBytes)
                 bulk_load(dst + Cfg::kBOff + off, records, Cfg::kRecBytes, bar_full + 8 * s);
         } else if (rbytes) {
             bulk_load(dst + Cfg::kBOff, records + static_cast<int64_t>(pw.ct) * 2 * Cfg::kRecBytes,
@@ -614,18 +614,6 @@ __device__ __forceinline__ double kron_tail(const float *f, int r, int c)
     return x;
 }
 
-__device__ __forceinline__ uint16_t bf16_term(double x, int t)
-{
-    // term t of the three-term bf16 split x = hi + mid + lo
-    double rem = x;
-    __nv_bfloat16 v = __double2bfloat16(rem);
-    for (int i = 0; i < t; ++i) {
-        rem -= static_cast<double>(__bfloat162float(v));
-        v = __double2bfloat16(rem);
-    }
-    return __bfloat16_as_ushort(v);
-}
-
 // Records of the tcgen05 variant: per block, the dense K_j = G1 (x) K'_j
 // (entries in fp64, eq. 12) as three bf16 terms, arranged as the B operands
 // of the block's two K = 16 steps.  Step h (input channels 16 h .. 16 h + 15)
@@ -636,23 +624,34 @@ __device__ __forceinline__ uint16_t bf16_term(double x, int t)
 __global__ void umma_records_kernel(const float *__restrict__ factors, int64_t nb,
                                     uint8_t *__restrict__ out)
 {
-    constexpr int kWords = static_cast<int>(kUmmaRecordBytes / 4);   // element pairs
-    const int64_t n = nb * kWords;
+    // one thread per block j, K = 16 step h, output channel c and input
+    // channel pair kp: the entries K_j[16 h + 2 kp][c] and K_j[16 h + 2 kp + 1][c]
+    // in fp64, each split into its three bf16 terms in turn (term t = the
+    // remainder after terms 0 .. t-1, rounded to nearest), one word per term
+    const int64_t n = nb * 512;
     for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
          idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t j = idx / kWords;
-        const int w = static_cast<int>(idx % kWords);
+        const int64_t j = idx >> 9;
+        const int w = static_cast<int>(idx & 511);
+        const int h = w >> 8, c = (w >> 3) & 31, kp = w & 7;
+        const int k0 = 2 * kp, r0 = 16 * h + k0;
         const float *f = factors + j * 20;
         uint8_t *rec = out + j * kUmmaRecordBytes;
-        const int h = w / 768, nn = (w / 8) % 96, kp = w % 8;
-        const int t = nn / 32, c = nn % 32, k0 = 2 * kp, r0 = 16 * h + k0;
         // K_j[r][c] = G1[bit4(r)][bit4(c)] * K'_j[r % 16][c % 16]
         const double g0 = static_cast<double>(f[((r0 >> 4) & 1) * 2 + ((c >> 4) & 1)]);
-        const uint16_t e0 = bf16_term(g0 * kron_tail(f, r0 & 15, c & 15), t);
-        const uint16_t e1 = bf16_term(g0 * kron_tail(f, (r0 + 1) & 15, c & 15), t);
-        const int off = h * 3072 + (nn >> 3) * 256 + (k0 >> 3) * 128 + (nn & 7) * 16 + (k0 & 7) * 2;
-        *reinterpret_cast<uint32_t *>(rec + off) = static_cast<uint32_t>(e0) |
-                                                   (static_cast<uint32_t>(e1) << 16);
+        double x0 = g0 * kron_tail(f, r0 & 15, c & 15);
+        double x1 = g0 * kron_tail(f, (r0 + 1) & 15, c & 15);
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+            const __nv_bfloat16 v0 = __double2bfloat16(x0), v1 = __double2bfloat16(x1);
+            x0 -= static_cast<double>(__bfloat162float(v0));
+            x1 -= static_cast<double>(__bfloat162float(v1));
+            const int nn = 32 * t + c;
+            const int off = h * 3072 + (nn >> 3) * 256 + (k0 >> 3) * 128 + (nn & 7) * 16 + (k0 & 7) * 2;
+            *reinterpret_cast<uint32_t *>(rec + off) =
+                static_cast<uint32_t>(__bfloat16_as_ushort(v0)) |
+                (static_cast<uint32_t>(__bfloat16_as_ushort(v1)) << 16);
+        }
     }
 }
 
@@ -697,7 +696,7 @@ kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, const CUt
 
 kq_status launch_umma_records(const float *factors, int64_t nb, void *out, cudaStream_t stream)
 {
-    const int64_t work = nb * (kUmmaRecordBytes / 4);
+    const int64_t work = nb * 512;
     umma_records_kernel<<<static_cast<int>(std::min<int64_t>((work + 255) / 256, 4096)), 256, 0,
                           stream>>>(factors, nb, static_cast<uint8_t *>(out));
     return check_launch();
