@@ -819,6 +819,24 @@ def test_w4a4_gemm_flux_ffn_down_sampled():
     print("max error / bound:", check_product(got[rows], Aq, Wq, k))
 
 
+@pytest.mark.parametrize("variant", ["mxf4_narrow", "mxf4_wide"])
+def test_w4a4_gemm_many_tiles_ragged(variant):
+    """Several tiles per CTA (2 to 4 on 152 SMs) with ragged m and n and an
+    odd block count (k = 1120: a partial last stage with a padding block),
+    so that the accumulators, stage ring and barrier phases run on across
+    tile boundaries; all columns of 160 sampled rows against the oracle."""
+    m, n, k = 4096 + 33, 1280 + 8, 1120
+    qa, sfa_rm, sfa = mx_operand(m, k, 601)
+    qw, _, sfw = mx_operand(n, k, 602)
+    got = np_(kq.kq_w4a4_gemm(dev(qa), dev(sfa), dev(qw), dev(sfw), m, n, k,
+                              variant=GEMM_VARIANTS[variant]))
+    rows = np.unique(np.concatenate([np.arange(48), np.arange(m - 48, m),
+                                     np.random.default_rng(603).choice(m, 64, replace=False)]))
+    Aq = O.dequantize(qa[rows], O.sf_place(sfa_rm[rows], 1), 1, len(rows), k)
+    Wq = O.dequantize(qw, sfw, 1, n, k)
+    print("max error / bound:", check_product(got[rows], Aq, Wq, k))
+
+
 BF16_GEMM_SHAPES = [(256, 384, 1152), (300, 129, 100), (1, 1, 8), (129, 257, 3072)]
 
 

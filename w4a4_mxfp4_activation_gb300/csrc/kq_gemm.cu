@@ -370,13 +370,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
 //   32x128b.warpx4 puts tile row r -- the scales of rows r, r + 32, r + 64,
 //   r + 96 -- into lane r of every lane quarter; an N = 256 instruction reads
 //   W rows 128-255 from the 4 columns after rows 0-127).
-// The SM issues tcgen05 instructions at a bounded rate (tens of nanoseconds
-// each, a commit several times that), so the design keeps them per flop low:
-// N = 256 instructions, stages released in pairs by one commit, the scale
-// copies issued by the MMA thread itself (in-order, no commit between them
-// and the MMAs), and the issuing warp kept converged with its operands
-// warp-uniform, one elected lane issuing (an issue loop inside a one-lane
-// branch ran the copies at half the rate).
+// A kind::mxf4 M = 128, K = 64 instruction occupies the tensor pipe for 128
+// cycles at N = 128 and N = 256 alike, so the tile is as wide as one
+// instruction allows (N = 256).  The pipe holds little work ahead of the
+// issuing thread: every cycle that thread spends between two stages' MMAs
+// (waits, address arithmetic, loop control) is a cycle the pipe may idle.  So
+// a full stage is issued from straight-line code (loops with run-time bounds
+// cost a quarter more per stage), a stage's scale copies are issued ahead of
+// its four MMAs, by the MMA thread itself (in-order, no commit between them
+// and the MMAs), each stage is released by its own commit, and the issuing
+// warp is kept converged with its operands warp-uniform, one elected lane
+// issuing.
 // Roles: warp 0 producer, warp 1 scale copies + MMAs, 4 NH epilogue warps:
 // NH per TMEM lane quarter, 128 columns each, read their part of the
 // accumulator into registers and release it before they store, so the next
@@ -394,7 +398,6 @@ struct XCfg {
     static constexpr int kBN = 128 * NH;                  // tile width (C columns, W rows)
     static constexpr int kBK = MX ? 256 : 64;             // K elements per stage
     static constexpr int kStages = 4;
-    static constexpr bool kPairs = kStages % 2 == 0;       // stages released in pairs
     static constexpr int kEpiWarps = 4 * NH;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA, epilogue
     static constexpr int kAccBufs = NH == 1 ? 2 : 1;
@@ -511,11 +514,8 @@ __global__ void __launch_bounds__(XCfg<NH, MX>::kThreads, 1)
                 const int64_t mt = t / g.ntiles, nt = t % g.ntiles;
                 for (int64_t ks = 0; ks < g.ksteps; ++ks, ++kk) {
                     const int s = static_cast<int>(kk % kXStages);
-                    // stages are released in pairs (s, s + 1 for even s): one
-                    // commit per pair, on the pair's barrier
                     if (kk >= kXStages &&
-                        !mbar_wait(empty + 8 * (C::kPairs ? s >> 1 : s),
-                                   static_cast<uint32_t>(((kk / kXStages) - 1) & 1))) {
+                        !mbar_wait(empty + 8 * s, static_cast<uint32_t>(((kk / kXStages) - 1) & 1))) {
                         ok = false;
                         break;
                     }
@@ -555,17 +555,25 @@ __global__ void __launch_bounds__(XCfg<NH, MX>::kThreads, 1)
         // addresses are warp-uniform values; one elected lane issues a
         // stage's scale copies (A tile, then W's halves, per scale tile at)
         // and its MMAs -- in order from one thread, the copies need no
-        // commit before the MMAs that read them.  An odd block count leaves
-        // one padding block inside the last instruction: the warp first sets
-        // its scale bytes to 2^0 (lane r: row r of each tile).
+        // commit before the MMAs that read them.  The wait for a stage's data
+        // closes the previous stage (the first stage of a tile: at the top of
+        // the tile).  An odd block count leaves one padding block inside the
+        // last instruction: the warp first sets its scale bytes to 2^0 (lane
+        // r: row r of each tile).
         int64_t kk = 0, tc = 0;
         bool ok = true;
         const bool pad_fix = MX && (g.nb & 1) != 0;
         // the issuing lane, elected once: a commit tracks only the tcgen05
         // operations of its own thread, so one lane issues everything
         const bool leader = elect_one();
-        constexpr uint32_t id0 = x_idesc(0), id2 = x_idesc(2);
         constexpr uint32_t kIdN = static_cast<uint32_t>((NH - 1) * (128 >> 3)) << 17;  // N += 128
+        constexpr uint32_t id0 = x_idesc(0) + kIdN, id2 = x_idesc(2) + kIdN;
+        // stages whose four K = 64 instructions all lie inside k
+        const int64_t full_steps = MX ? g.k / kXBK : 0;
+        auto wait_full = [&](int64_t q) {
+            return __all_sync(0xffffffffu, mbar_wait(full + 8 * static_cast<int>(q % kXStages),
+                                                     static_cast<uint32_t>((q / kXStages) & 1)));
+        };
         for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tc) {
             // accumulator buffer b of tile tc is free once the epilogue has
             // read tile tc - kAccBufs from it
@@ -575,16 +583,13 @@ __global__ void __launch_bounds__(XCfg<NH, MX>::kThreads, 1)
                 ok = __all_sync(0xffffffffu,
                                 mbar_wait(acc_empty + 8 * b, static_cast<uint32_t>((use - 1) & 1)));
             const uint32_t acc = tmem_base + 128 * b;
+            if (ok) ok = wait_full(kk);
             for (int64_t ks = 0; ks < g.ksteps && ok; ++ks, ++kk) {
                 const int s = static_cast<int>(kk % kXStages);
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(full + 8 * s, static_cast<uint32_t>((kk / kXStages) & 1)));
-                if (!ok) break;
-                const int64_t rem = (g.k - ks * kXBK + 63) / 64;
-                const int nmma = rem < 4 ? static_cast<int>(rem) : 4;
+                const bool last = ks == g.ksteps - 1;
                 const uint32_t st = base + s * kXStageBytes;
                 const uint32_t sfa_s = st + kXSfaOff, sfw_s = st + kXSfwOff;
-                if (pad_fix && ks == g.ksteps - 1) {
+                if (pad_fix && last) {
                     const int kb = static_cast<int>(g.nb - 8 * ks);     // padding block, local index
                     const uint32_t off = static_cast<uint32_t>((kb >> 2) * 512 + 16 * lane + (kb & 3));
 #pragma unroll
@@ -609,35 +614,56 @@ __global__ void __launch_bounds__(XCfg<NH, MX>::kThreads, 1)
                 const uint32_t sft = tmem_base + kXSfCol + kXSfStride * s;
                 const uint64_t da = g_desc(st), db = g_desc(st + kXACodeBytes);
                 const uint64_t dsa = x_desc_noswz(sfa_s, 128), dsw = x_desc_noswz(sfw_s, 128);
-                if (leader && !MX) {
-                    // kind::f16: four K = 16 steps of 32 bytes; zero fill past k
-                    constexpr uint32_t kIdF16 = (1u << 4) | (1u << 7) | (1u << 10) |
-                                                ((static_cast<uint32_t>(kXBN) >> 3) << 17) |
-                                                ((128u >> 4) << 24);
-                    for (int j = 0; j < 4; ++j)
-                        g_mma_id(acc, da + 2 * j, db + 2 * j, kIdF16, (ks > 0 || j > 0) ? 1u : 0u);
-                    if (!C::kPairs)
-                        g_commit(empty + 8 * s);
-                    else if (kk & 1)
-                        g_commit(empty + 8 * (s >> 1));
-                    if (ks == g.ksteps - 1) g_commit(acc_full + 8 * b);
-                }
-                if (leader && MX) {
-                    for (int at = 0; at < (nmma + 1) / 2; ++at) {
-                        x_cp_sf(sft + 4 * at, dsa + 32 * at);
+                const uint32_t a0 = ks > 0 ? 1u : 0u;           // accumulate into D
+                auto copies = [&](int at) {
+                    x_cp_sf(sft + 4 * at, dsa + 32 * at);
 #pragma unroll
-                        for (int hh = 0; hh < NH; ++hh)
-                            x_cp_sf(sft + 8 + 4 * (NH * at + hh), dsw + 64 * hh + 32 * at);
-                        for (int j = 2 * at; j < 2 * at + 2 && j < nmma; ++j)
-                            x_mma(acc, da + 2 * j, db + 2 * j, ((j & 1) ? id2 : id0) + kIdN, sft + 4 * at,
-                                  sft + 8 + 4 * (NH * at), (ks > 0 || j > 0) ? 1u : 0u);
-                    }
-                    if (!C::kPairs)
+                    for (int hh = 0; hh < NH; ++hh)
+                        x_cp_sf(sft + 8 + 4 * (NH * at + hh), dsw + 64 * hh + 32 * at);
+                };
+                bool next = true;
+                if (MX && ks < full_steps) {
+                    // the copies first: an MMA issued right behind a copy
+                    // waits for it, and four MMAs in a row leave the pipe
+                    // more work queued while the warp does its bookkeeping
+                    if (leader) {
+                        copies(0);
+                        copies(1);
+                        x_mma(acc, da, db, id0, sft, sft + 8, a0);
+                        x_mma(acc, da + 2, db + 2, id2, sft, sft + 8, 1u);
+                        x_mma(acc, da + 4, db + 4, id0, sft + 4, sft + 8 + 4 * NH, 1u);
+                        x_mma(acc, da + 6, db + 6, id2, sft + 4, sft + 8 + 4 * NH, 1u);
                         g_commit(empty + 8 * s);
-                    else if (kk & 1)
-                        g_commit(empty + 8 * (s >> 1));
-                    if (ks == g.ksteps - 1) g_commit(acc_full + 8 * b);
+                        if (last) g_commit(acc_full + 8 * b);
+                    }
+                    if (!last) next = wait_full(kk + 1);
+                } else {
+                    if (leader && !MX) {
+                        // kind::f16: four K = 16 steps of 32 bytes; zero fill past k
+                        constexpr uint32_t kIdF16 = (1u << 4) | (1u << 7) | (1u << 10) |
+                                                    ((static_cast<uint32_t>(kXBN) >> 3) << 17) |
+                                                    ((128u >> 4) << 24);
+                        for (int j = 0; j < 4; ++j)
+                            g_mma_id(acc, da + 2 * j, db + 2 * j, kIdF16, (ks > 0 || j > 0) ? 1u : 0u);
+                    }
+                    if (leader && MX) {
+                        // the last stage of a k that is not a multiple of 256
+                        const int64_t rem = (g.k - ks * kXBK + 63) / 64;
+                        const int nmma = rem < 4 ? static_cast<int>(rem) : 4;
+                        for (int at = 0; at < (nmma + 1) / 2; ++at) {
+                            copies(at);
+                            for (int j = 2 * at; j < 2 * at + 2 && j < nmma; ++j)
+                                x_mma(acc, da + 2 * j, db + 2 * j, (j & 1) ? id2 : id0, sft + 4 * at,
+                                      sft + 8 + 4 * (NH * at), (ks > 0 || j > 0) ? 1u : 0u);
+                        }
+                    }
+                    if (leader) {
+                        g_commit(empty + 8 * s);
+                        if (last) g_commit(acc_full + 8 * b);
+                    }
+                    if (!last) next = wait_full(kk + 1);
                 }
+                ok = next;
                 __syncwarp();
             }
         }
