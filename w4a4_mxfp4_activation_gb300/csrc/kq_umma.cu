@@ -51,6 +51,11 @@
 // shape and 128B swizzle), and one TMA store per tile sends it to HBM.  The
 // ring stage is then released by the epilogue, once that store has read it,
 // instead of by the MMA commit.
+// With K2 ("KroQuant ...", Sec. 3.5.1 K2 and App. B), no operand records come
+// from memory: the epilogue groups write them into the ring stages from the
+// raw factors (build_record_rows).  With PAIR, the CTA walks its tiles by
+// pairs of row tiles of one column, which share one set of records built
+// once (PairWalk).
 // Every wait is bounded in time (one second, or the shorter limit of the
 // verification hook); a timed-out epilogue writes the E8M0 NaN byte 0xFF as
 // the scale of the blocks it could not finish (and bf16 NaNs into the side
@@ -200,6 +205,32 @@ __device__ __forceinline__ void store_scale_u(const QuantParams &p, int64_t row,
     }
 }
 
+// Walk over a CTA's tiles by pairs of row tiles: super tile (rtp, ct) in
+// row-major order over ceil(nrow / 2) x ncol, the CTA's super tiles first,
+// first + step, ...; within one, rows 2 rtp + h.  half >= 0 walks that half
+// only, half < 0 both halves in turn (h = 0, then 1).  Neighbouring CTAs
+// still read neighbouring columns of the same rows, as the row-major walk.
+struct PairWalk {
+    TileWalk sw;
+    int h, rt, ct;
+    bool fixed;
+    __device__ __forceinline__ PairWalk(int first, int step, int ncol, int half)
+        : sw(first, step, ncol), h(half < 0 ? 0 : half), rt(2 * sw.rt + h), ct(sw.ct), fixed(half >= 0)
+    {
+    }
+    __device__ __forceinline__ void next()
+    {
+        if (!fixed && h == 0) {
+            h = 1;
+        } else {
+            if (!fixed) h = 0;
+            sw.next();
+        }
+        rt = 2 * sw.rt + h;
+        ct = sw.ct;
+    }
+};
+
 // K2 (the tensor-core path without expanded records in memory): eight
 // entries of K_j -- rows 8 g .. 8 g + 7, column c -- as the three bf16 terms,
 // written into a tile's record area in the MMA operand layout (see
@@ -248,7 +279,7 @@ __device__ __forceinline__ void build_record_rows(uint32_t rec, const float *__r
         sts128(off + ((32 * t + c) >> 3) * 256, make_uint4(w[t][0], w[t][1], w[t][2], w[t][3]));
 }
 
-template <int STAGES, bool DEBUG, bool DUAL, bool K2>
+template <int STAGES, bool DEBUG, bool DUAL, bool K2, bool PAIR>
 __global__ void __launch_bounds__(kThreadsU, 1)
     quant_umma_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmQ,
@@ -256,6 +287,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                       const uint8_t *__restrict__ records)
 {
     using Cfg = UCfg<STAGES>;
+    static_assert(!PAIR || (K2 && !DUAL), "tile pairs share the records K2 builds");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     const uint32_t bar = base + Cfg::kBarOff;
@@ -268,6 +300,32 @@ __global__ void __launch_bounds__(kThreadsU, 1)
 
     const uint64_t lim = p.wait_limit_ns;
 
+    // PAIR (K2 only): the CTA walks its tiles by pairs of row tiles of one
+    // column, tile it = 2 P + h; the pair shares one set of operand records,
+    // built once into the ring stage of its first tile, 2 P % STAGES (an
+    // even stage; the odd stages hold no records).  A pair of an odd row
+    // count's last row is completed by a tile past the last row: its loads
+    // fill with zeros and its stores are clipped or skipped.
+    const int nrp = static_cast<int>((p.nrow_tiles + 1) / 2);
+    auto valid = [&](const auto &w) {
+        if constexpr (PAIR) return w.sw.rt < nrp;
+        else return w.rt < p.nrow_tiles;
+    };
+    // this CTA's tiles (half < 0: all of them in order; else tiles it % 2 ==
+    // half, in order)
+    auto walker = [&](int half) {
+        if constexpr (PAIR) {
+            return PairWalk(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                            static_cast<int>(p.ncol_tiles), half);
+        } else if (half < 0) {
+            return TileWalk(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                            static_cast<int>(p.ncol_tiles));
+        } else {
+            return TileWalk(static_cast<int>(blockIdx.x + half * gridDim.x),
+                            static_cast<int>(2 * gridDim.x), static_cast<int>(p.ncol_tiles));
+        }
+    };
+
     // The producer (thread 0) walks the CTA's tiles in order; it loads the
     // activation box and the operand records of tile `it` into ring stage
     // it % STAGES.  (Its work per tile sits on the pipeline's critical path:
@@ -275,8 +333,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // from that release to the next load decides how much data is in
     // flight.  Measured on GB300: a generic tile-index fetch with an integer
     // division per tile made the FLUX FFN-down launch 13 % slower.)
-    TileWalk pw(static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
-                static_cast<int>(p.ncol_tiles));
+    auto pw = walker(-1);
     int64_t pit = 0;
     uint64_t pol = 0;
     // verification hook: the position in this CTA's walk of the tile whose
@@ -316,8 +373,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         if (DUAL) tma_prefetch_desc(&tmAT);
         for (int s = 0; s < STAGES; ++s) {
             // K2: the producer's TMA bytes and the 8 record-building warps
-            mbar_init(bar_full + 8 * s, K2 ? 1 + kEpiWarps / 2 : 1);
-            mbar_init(bar_empty + 8 * s, 1);
+            // (PAIR: on the even stages only, which hold a pair's records
+            // and are released by the MMAs of both its tiles)
+            const bool rec = K2 && (!PAIR || s % 2 == 0);
+            mbar_init(bar_full + 8 * s, rec ? 1 + kEpiWarps / 2 : 1);
+            mbar_init(bar_empty + 8 * s, PAIR && s % 2 == 0 ? 2 : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(bar_acc_full + 8 * a, 1);        // MMA commit
@@ -331,7 +391,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         // slower; one tile is faster on every shape tried.)
         grid_dependency_wait();
         pol = l2_policy_evict_first();
-        if (pw.rt < p.nrow_tiles) issue_tile();
+        if (valid(pw)) issue_tile();
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
@@ -344,7 +404,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            while (pw.rt < p.nrow_tiles) {
+            while (valid(pw)) {
                 const int s = static_cast<int>(pit % STAGES);
                 const uint32_t ph = static_cast<uint32_t>((pit / STAGES) & 1);
                 if (pit >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1u, lim)) break;
@@ -371,18 +431,23 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         // the issuing lane, elected once (a commit tracks only the tcgen05
         // operations of its own thread)
         const bool leader = elect_one();
-        for (TileWalk tw(static_cast<int>(blockIdx.x + a * gridDim.x),
-                         static_cast<int>(2 * gridDim.x), static_cast<int>(p.ncol_tiles));
-             tw.rt < p.nrow_tiles && ok; tw.next(), it += 2) {
+        for (auto tw = walker(a); valid(tw) && ok; tw.next(), it += 2) {
             const int s = static_cast<int>(it % STAGES);
+            // PAIR: the second tile of a pair takes the records from the
+            // first tile's stage, so it also waits for that stage's phase
+            // (which cannot move on before this tile's own commit below)
+            const int sr = PAIR && a == 1 ? static_cast<int>((it - 1) % STAGES) : s;
             const int64_t ct = tw.ct;
             const int64_t left = p.nb - ct * 2;
             const int nblk = static_cast<int>(left < 0 ? 0 : (left < 2 ? left : 2));
             bool w = mbar_wait(bar_full + 8 * s, static_cast<uint32_t>((it / STAGES) & 1), lim);
+            if (PAIR && a == 1 && w)
+                w = mbar_wait(bar_full + 8 * sr, static_cast<uint32_t>(((it - 1) / STAGES) & 1), lim);
             if (w && it >= 2)
                 w = mbar_wait(bar_acc_empty + 8 * a, static_cast<uint32_t>(((it >> 1) & 1) ^ 1), lim);
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             const uint32_t stage = base + s * Cfg::kStageBytes;
+            const uint32_t rstage = base + sr * Cfg::kStageBytes;
             tc_fence_after();
             if (leader) {
                 const uint32_t d0 = tmem_base + a * kAccCols;
@@ -390,11 +455,13 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                     for (int h = 0; h < 2; ++h)       // input half h: K = 16 step
                         umma_bf16(d0 + b * kBlockCols,
                                   smem_desc(stage + 64 * b + 32 * h, 16, 1024, 2),
-                                  smem_desc(stage + Cfg::kBOff + b * Cfg::kRecBytes + h * 3072,
+                                  smem_desc(rstage + Cfg::kBOff + b * Cfg::kRecBytes + h * 3072,
                                             128, 256, 0),
                                   static_cast<uint32_t>(h));
                 if (!DUAL)
                     umma_commit(bar_empty + 8 * s);      // ring stage free once the MMAs read it
+                if (PAIR && a == 1)
+                    umma_commit(bar_empty + 8 * sr);     // and the pair's records
                 umma_commit(bar_acc_full + 8 * a);       // accumulators ready
             }
             __syncwarp();
@@ -418,8 +485,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const bool at_leader = DUAL && (e & 7) == 4 && lane == 0;
         int it = grp;
         bool ok = true;
-        TileWalk tw(static_cast<int>(blockIdx.x + grp * gridDim.x),
-                    static_cast<int>(2 * gridDim.x), static_cast<int>(p.ncol_tiles));
+        auto tw = walker(grp);
         // K2: the group also builds the operand records of its tiles in their
         // ring stages.  A tile's stage is free for its records once the MMAs
         // of the tile STAGES positions earlier -- the group's own tile three
@@ -432,7 +498,16 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         // the producer and these 8 warps) -- unless one of its own waits ran
         // out (the stage might then still be read), in which case the phase
         // never completes and the tile's MMAs time out in turn.
-        TileWalk bwk = tw;                    // the next tile whose records to build
+        // PAIR: the records of pair P are built once, by group P % 2, into
+        // stage 2 P % STAGES, which is free once both tiles of pair P - 3
+        // (the pair STAGES / 2 earlier in the same stage) have been read by
+        // their MMAs: the group waits on the stage's empty barrier, which
+        // counts the two MMA warps' commits.  So each group builds after every
+        // other tile, half the work of the unpaired walk.
+        TileWalk bwk(static_cast<int>(blockIdx.x), static_cast<int>(PAIR ? gridDim.x : 2 * gridDim.x),
+                     static_cast<int>(p.ncol_tiles));   // the next tile (PAIR: pair) whose records to build
+        if constexpr (!PAIR) bwk = TileWalk(static_cast<int>(blockIdx.x + grp * gridDim.x),
+                                            static_cast<int>(2 * gridDim.x), static_cast<int>(p.ncol_tiles));
         const int bb = (e & 7) >> 2, bg = (e & 7) & 3;
         auto build = [&](int ct, int s, bool can) {
             const int64_t j = 2 * static_cast<int64_t>(ct) + bb;
@@ -443,15 +518,28 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             __syncwarp();
             if (can && lane == 0) mbar_arrive(bar_full + 8 * s);
         };
-        if (K2) {
-            for (int k = 0; k < STAGES / 2 && bwk.rt < p.nrow_tiles; ++k, bwk.next())
+        // bwk's next position is the one this group builds (unpaired), or
+        // the pair to build after this iteration, if the group's (PAIR)
+        auto bwk_valid = [&]() {
+            if constexpr (PAIR) return bwk.rt < nrp;
+            else return bwk.rt < p.nrow_tiles;
+        };
+        if (K2 && !PAIR) {
+            for (int k = 0; k < STAGES / 2 && bwk_valid(); ++k, bwk.next())
                 build(bwk.ct, grp + 2 * k, true);
         }
+        if (PAIR) {
+            for (int P = 0; P < STAGES / 2 && bwk_valid(); ++P, bwk.next())
+                if (P % 2 == grp) build(bwk.ct, (2 * P) % STAGES, true);
+        }
 
-        for (; tw.rt < p.nrow_tiles; tw.next(), it += 2) {
+        for (; valid(tw); tw.next(), it += 2) {
             const int a = grp;
             const int rt = tw.rt, ct = tw.ct;
-            if (K2 && lane < 2 && bwk.rt < p.nrow_tiles) {
+            // PAIR: this iteration is pair Q = it / 2; after it the group
+            // builds pair Q + 3 if that pair is its own
+            const bool builds = K2 && bwk_valid() && (!PAIR || ((it / 2 + STAGES / 2) % 2) == grp);
+            if (builds && lane < 2) {
                 // this iteration's record build reads 80 bytes of factors:
                 // fetch them into L1 now, under the tile's epilogue
                 const int64_t j = 2 * static_cast<int64_t>(bwk.ct) + bb;
@@ -557,7 +645,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
             }
             fence_proxy_async_smem();
             named_barrier(1 + pair, 64);
-            if (tiled && b == 0) {
+            if (tiled && b == 0 && (!PAIR || row < p.m_rows)) {     // PAIR: rows past the last tile
                 uint32_t partner;
                 asm volatile("ld.shared.u8 %0, [%1];" : "=r"(partner) : "r"(sfstg + lane) : "memory");
                 *reinterpret_cast<uint16_t *>(p.sf + sf_blocked_offset(row, ct * 2, p.ncb)) =
@@ -582,8 +670,20 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                 }
             }
             slot = slot == Cfg::kStgBufs - 1 ? 0 : slot + 1;
-            if (K2 && bwk.rt < p.nrow_tiles) {
+            if (K2 && !PAIR && bwk_valid()) {
                 build(bwk.ct, static_cast<int>(it % STAGES), ok);
+                bwk.next();
+            }
+            if (PAIR && bwk_valid()) {
+                if (builds) {
+                    // pair Q + 3 goes into pair Q's stage once both of pair
+                    // Q's tiles have been read
+                    const int64_t q0 = it - grp;                 // pair Q's first tile
+                    const int s2 = static_cast<int>(q0 % STAGES);
+                    const bool can = __all_sync(0xffffffffu,
+                        ok && mbar_wait(bar_empty + 8 * s2, static_cast<uint32_t>((q0 / STAGES) & 1), lim));
+                    build(bwk.ct, s2, can);
+                }
                 bwk.next();
             }
         }
@@ -661,12 +761,12 @@ struct USlot {
     cudaError_t err[64] = {};
 };
 
-template <int STAGES, bool DEBUG, bool DUAL, bool K2>
+template <int STAGES, bool DEBUG, bool DUAL, bool K2, bool PAIR = false>
 kq_status launch_umma(const CUtensorMap &map, const CUtensorMap &mapq, const CUtensorMap &mapat,
                       QuantParams p, const uint8_t *records, int sm_count, cudaStream_t stream)
 {
     using Cfg = UCfg<STAGES>;
-    auto kern = quant_umma_kernel<STAGES, DEBUG, DUAL, K2>;
+    auto kern = quant_umma_kernel<STAGES, DEBUG, DUAL, K2, PAIR>;
     constexpr int threads = kThreadsU;
     static USlot slot;
     int dev = 0;
@@ -717,8 +817,18 @@ kq_status launch_quant_umma(const uint16_t *A, int64_t lda, const void *K_expand
     const uint8_t *rec = static_cast<const uint8_t *>(K_expanded);
     const int sms = info.sm_count;
     if (K_expanded == nullptr) {
-        // K2: no records in memory, the kernel builds them from p.factors
+        // K2: no records in memory, the kernel builds them from p.factors.
+        // With at least four tiles per CTA the tiles go by pairs of one
+        // column, which share their records (half the building); below
+        // that, pairs would leave SMs idle.
         if (at != nullptr || p.factors == nullptr) return KQ_ERR_NULL;
+        const int64_t ncol = p.sf_layout == KQ_SF_ROWMAJOR ? (p.nb + 1) / 2 : 2 * p.ncb;
+        const int64_t ntiles = (p.m_rows + kBR - 1) / kBR * ncol;
+        if (ntiles >= 4 * static_cast<int64_t>(sms)) {
+            if (p.y_debug != nullptr)
+                return launch_umma<6, true, false, true, true>(map, mapq, map, p, nullptr, sms, stream);
+            return launch_umma<6, false, false, true, true>(map, mapq, map, p, nullptr, sms, stream);
+        }
         if (p.y_debug != nullptr)
             return launch_umma<6, true, false, true>(map, mapq, map, p, nullptr, sms, stream);
         return launch_umma<6, false, false, true>(map, mapq, map, p, nullptr, sms, stream);
