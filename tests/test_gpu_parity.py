@@ -315,6 +315,35 @@ def test_ragged_shapes_with_pitches_and_canaries(m, d, kind):
             assert (np_(sf)[~full] == 0).all()
 
 
+@pytest.mark.parametrize("m", [2907, 4347])
+def test_k2_tile_pairs(m):
+    """K2 with enough tiles per CTA to walk them by pairs of row tiles of one
+    column, sharing the pair's records: an odd row-tile count (23, the last
+    ragged), whose last pair is completed by a tile past the last row that
+    must write nothing, and an even one (34, the last ragged: 17 pairs);
+    lda > d, ldq > d/2, guard bytes around every output, every row against
+    the oracle, both scale layouts."""
+    d = 12288
+    nb = d // 32
+    lda, ldq = d + 64, d // 2 + 32
+    A_bits = synth.activations(m, d, 3100 + m, "flux", lda=lda)
+    pg, po = params_for("kron_k2", nb, d, 3200)
+    for layout in (0, 1):
+        sfb = kq.kq_sf_bytes(m, d, layout)
+        q_store = torch.full((m + 2, ldq), 0xA5, dtype=torch.uint8, device="cuda")
+        sf_store = torch.full((sfb + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
+        q = q_store[1:m + 1]
+        sf = sf_store[16:16 + sfb]
+        qq, ssf, y = run_kind("kron_k2", A_bits, d, layout, pg, q=q, sf=sf)
+        qs = np_(q_store)
+        assert (qs[0] == 0xA5).all() and (qs[m + 1] == 0xA5).all()
+        assert (qs[1:m + 1, d // 2:] == 0xA5).all(), "row padding of q overwritten"
+        ss = np_(sf_store)
+        assert (ss[:16] == 0xA5).all() and (ss[16 + sfb:] == 0xA5).all(), "bytes past the scales written"
+        parity.check(np.ascontiguousarray(A_bits[:, :d]), d, "kron", po, layout,
+                     np_(q)[:, :d // 2], np_(sf), np_(y))
+
+
 # ------------------------------------------------------------ maximum sizes --
 
 MAX_ROWS = 0x7FFFFFFF          # the largest m the entry points accept
